@@ -1,0 +1,163 @@
+/*
+ * mla.h - C ABI of the GB300 (sm_103a) library for multi-head latent attention
+ * (MLA) decode over a paged latent KV cache.
+ *
+ * Every pointer argument named "device" must point to memory the current CUDA
+ * device can access (for example a torch CUDA tensor); "host" pointers are
+ * ordinary CPU memory. The caller owns every buffer. Entry points validate
+ * their arguments on the host, enqueue kernels on `stream` (a cudaStream_t;
+ * NULL = the legacy default stream) and return without synchronising; they
+ * never allocate memory. A non-zero return means nothing was enqueued, except
+ * MLA_ERR_CUDA, which reports a failed launch.
+ *
+ * Cache geometry. Each cached token is one row of the paged pool:
+ *   MLA_CACHE_BF16_576       1152 bytes: latent c[0:512] then k_pe[0:64], bf16.
+ *                            ("sabi-mla-vllm" README: intro paragraph and "What
+ *                            the plugin does": 512-d latent plus one shared
+ *                            64-d rotary key, 576 values per token, paged bf16.)
+ *   MLA_CACHE_FP8_DS_MLA_656 656 bytes: [0,512) e4m3 codes of c / scale_j,
+ *                            [512,528) four fp32 scales scale_j = absmax_j/448
+ *                            over the 128-value blocks j = d/128 (1.0 for an
+ *                            all-zero block), [528,656) the 64 bf16 k_pe values.
+ *                            (vLLM PR #55543, commits 3.1+3.2 and 5.1-5.4, PR
+ *                            description "Approach" and "Memory tradeoff".)
+ * The pool is addressed as [num_slots, row_bytes]; token j of request b lives
+ * in slot block_table[b][j / page_size] * page_size + j % page_size. Every
+ * offset is formed in 64-bit arithmetic, so slots above 2^31 / 576 =
+ * 3,728,270 are read correctly ("sabi-mla-vllm" README, "B300 fix (0.2.0)").
+ */
+#ifndef MLA_GB300_H_
+#define MLA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = -1,  /* bad size, null or misaligned pointer */
+    MLA_ERR_UNSUPPORTED = -2,  /* valid request this build does not handle */
+    MLA_ERR_WORKSPACE = -3,    /* workspace too small */
+    MLA_ERR_CUDA = -4          /* a CUDA runtime call or launch failed */
+} mla_status;
+
+enum { MLA_CACHE_BF16_576 = 0, MLA_CACHE_FP8_DS_MLA_656 = 1 };
+enum { MLA_OUT_BF16 = 0, MLA_OUT_F32 = 1 };
+
+/* Bytes of one cached row for a cache kind (1152 or 656), or 0 if unknown. */
+MLA_API int mla_row_bytes(int cache_kind);
+
+/*
+ * mla_cache_write - scatter new tokens into the paged pool.
+ * Follows vLLM PR #55543 commit 3.1+3.2 (concat_and_cache_mla: rows are
+ * concat(latent, k_pe) with kv_lora_rank 512 and pe_dim 64; 656-byte rows for
+ * fp8_ds_mla) and commit 5.1-5.4 (NoPE bytes are a per-128-block fp8
+ * quantisation; rope bytes are the bf16 k_pe).
+ *   latent        device, bf16 [num_tokens, 512], row stride latent_stride
+ *                 elements (multiple of 8, base 16-byte aligned).
+ *   k_pe          device, bf16 [num_tokens, 64], row stride k_pe_stride
+ *                 elements (multiple of 8, base 16-byte aligned).
+ *   slot_mapping  device, int64 [num_tokens]; a negative entry skips the token.
+ *   cache         device, [num_slots, mla_row_bytes(cache_kind)] bytes, 16-byte
+ *                 aligned. Rows not named by slot_mapping are left unchanged.
+ * fp8 rows: scale_j = absmax_j / 448 by IEEE fp32 division, each code is the
+ * round-to-nearest-even, saturating e4m3 encoding of the fp32 quotient x /
+ * scale_j. Two tokens mapped to the same slot race (the last write is
+ * unspecified). Slots >= num_slots are undefined behaviour (not checked on
+ * the device). Returns MLA_ERR_INVALID_ARG on bad sizes, pointers or strides.
+ */
+MLA_API int mla_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
+                    const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots,
+                    int cache_kind, void* stream);
+
+/*
+ * mla_decode_workspace_bytes - bytes of device workspace mla_decode needs.
+ *   B, q_len, Hq   as for mla_decode.
+ *   num_ctas       the value that will be passed to mla_decode (0 = one CTA per
+ *                  SM of the current device).
+ * The workspace holds a 256-byte header (word 0: device-side status, see
+ * mla_decode) and fp32 partial results of requests split across CTAs.
+ * Returns 0 for invalid sizes.
+ */
+MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas);
+
+/*
+ * mla_decode - absorbed MLA decode over the paged latent cache.
+ * For request b, query token t < q_len and head h, the row is
+ * r = (b * q_len + t) * Hq + h and the visible tokens are j = 0 ..
+ * seq_lens[b] - q_len + t (the q_len new tokens are already in the cache; each
+ * sees itself and its past, as in the multi-token verify step of "qwen-mla-vllm"
+ * README, "Speculative decoding (MTP)", which reads the latent once per
+ * request). With c_j = row[0:512], k_pe_j = row[512:576] (fp8 rows:
+ * c_j[d] = e4m3(code) * scale_{d/128}):
+ *   s_j      = scale * (q_lat[r] . c_j + q_pe[r] . k_pe_j)
+ *   out[r]   = sum_j softmax_j(s) c_j          (softmax over the tokens)
+ *   lse[r]   = ln sum_j exp(s_j)
+ * A row with no visible token gets out = 0 and lse = -inf (vLLM PR #55543
+ * commit 5.1-5.4: all-invalid rows neutralise to (0, -inf)).
+ *   q_lat        device, bf16 [B*q_len, Hq, 512], contiguous, 16-byte aligned.
+ *   q_pe         device, bf16 [B*q_len, Hq, 64], contiguous, 16-byte aligned.
+ *   cache        device, the pool written by mla_cache_write, 16-byte aligned,
+ *                num_slots rows of mla_row_bytes(cache_kind) bytes.
+ *   page_size    tokens per page, >= 1.
+ *   block_table  device, int32 [B, block_table_stride]; entries past
+ *                ceil(seq_lens[b] / page_size) are never read.
+ *   seq_lens     device, int32 [B], each >= 0; read on the device only, so the
+ *                call does not synchronise.
+ *   scale        softmax scale applied to the dot products.
+ *   out          device, [B*q_len, Hq, 512], bf16 or fp32 per out_dtype.
+ *   lse          device, fp32 [B*q_len, Hq], natural log.
+ *   workspace    device, at least mla_decode_workspace_bytes(B, q_len, Hq,
+ *                num_ctas) bytes, 256-byte aligned. Its first int32 is set to
+ *                0 at the start of the call and afterwards holds device-side
+ *                status bits: 1 = a bounded internal wait gave up (the kernel
+ *                returned early, outputs are invalid), 2 = a block-table entry
+ *                pointed outside the pool (page 0 was read instead).
+ *   num_ctas     CTAs sharing the token stream (0 = one per SM). The tokens of
+ *                all requests are cut into 128-token tiles and dealt out as
+ *                equal contiguous ranges; requests cut across CTAs are merged
+ *                from fp32 partials by a second kernel.
+ * Limits: Hq * q_len rows are processed in groups of at most 64. Returns
+ * MLA_ERR_UNSUPPORTED on a device other than sm_103 / sm_100 family.
+ */
+MLA_API int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache_kind, int64_t num_slots,
+               int page_size, const int32_t* block_table, int64_t block_table_stride, const int32_t* seq_lens,
+               int B, int q_len, int Hq, float scale, void* out, int out_dtype, float* lse, void* workspace,
+               size_t workspace_bytes, int num_ctas, void* stream);
+
+/*
+ * mla_merge_lse - combine S partial results of the same N rows computed over
+ * disjoint token sets (flash-decoding split-KV / decode context parallel
+ * combine; vLLM PR #55543 commit 5.1-5.4 "(0, -inf) per the DCP merge
+ * contract"):
+ *   L      = ln sum_i exp(part_lse[i][n])
+ *   out[n] = sum_i exp(part_lse[i][n] - L) * part_out[i][n]
+ *   lse[n] = L;   rows whose partials are all -inf give (0, -inf).
+ *   part_out  device, fp32 [S, N, 512], contiguous.
+ *   part_lse  device, fp32 [S, N].
+ *   out       device, [N, 512] bf16 or fp32 per out_dtype.
+ *   lse       device, fp32 [N] (may be NULL).
+ */
+MLA_API int mla_merge_lse(const float* part_out, const float* part_lse, int S, int64_t N, void* out, int out_dtype,
+                  float* lse, void* stream);
+
+/* Number of SMs of the current device (what num_ctas = 0 means), or < 0. */
+MLA_API int mla_num_sms(void);
+
+/* Static English text for a status code. */
+MLA_API const char* mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H_ */

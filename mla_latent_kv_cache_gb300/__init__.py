@@ -1,0 +1,168 @@
+"""Paged MLA decode for GB300 (sm_103a): Python binding of the C ABI.
+
+The compute path lives in ``_lib/libmla_gb300.so`` (built from ``csrc/`` by
+``mla_latent_kv_cache_gb300.build``). This module only marshals arguments:
+torch tensors -> device pointers, the current CUDA stream, and status codes ->
+exceptions. There is no fallback: if the library is missing, every call
+raises.
+
+Entry points mirror ``include/mla.h``:
+  mla_cache_write, mla_decode_workspace_bytes, mla_decode, mla_merge_lse,
+  mla_num_sms, mla_row_bytes, mla_status_string.
+``decode(...)`` is a convenience wrapper that allocates the outputs and the
+workspace with torch and calls ``mla_decode``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmla_gb300.so")
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA = 0, -1, -2, -3, -4
+MLA_CACHE_BF16_576, MLA_CACHE_FP8_DS_MLA_656 = 0, 1
+MLA_OUT_BF16, MLA_OUT_F32 = 0, 1
+STATUS_WAIT_TIMEOUT, STATUS_BAD_BLOCK = 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {mla_status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with `python -m mla_latent_kv_cache_gb300.build` "
+                    "(there is no CPU fallback)")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+            lib.mla_row_bytes.argtypes = [i32]
+            lib.mla_row_bytes.restype = i32
+            lib.mla_status_string.argtypes = [i32]
+            lib.mla_status_string.restype = ctypes.c_char_p
+            lib.mla_num_sms.argtypes = []
+            lib.mla_num_sms.restype = i32
+            lib.mla_cache_write.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp]
+            lib.mla_cache_write.restype = i32
+            lib.mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            lib.mla_decode_workspace_bytes.restype = sz
+            lib.mla_decode.argtypes = [vp, vp, vp, i32, i64, i32, vp, i64, vp, i32, i32, i32, f32, vp, i32, vp,
+                                       vp, sz, i32, vp]
+            lib.mla_decode.restype = i32
+            lib.mla_merge_lse.argtypes = [vp, vp, i32, i64, vp, i32, vp, vp]
+            lib.mla_merge_lse.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != MLA_OK:
+        raise MlaError(status, where)
+
+
+def mla_status_string(status: int) -> str:
+    try:
+        return load().mla_status_string(status).decode()
+    except ImportError:
+        return f"status {status}"
+
+
+def mla_row_bytes(cache_kind: int) -> int:
+    return load().mla_row_bytes(cache_kind)
+
+
+def mla_num_sms() -> int:
+    return load().mla_num_sms()
+
+
+def mla_cache_write(latent: torch.Tensor, k_pe: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor,
+                    cache_kind: int = MLA_CACHE_BF16_576, stream=None) -> None:
+    """latent [T,512] bf16, k_pe [T,64] bf16 (row-strided views allowed),
+    slot_mapping [T] int64 (-1 = skip), cache [num_slots, row_bytes] (any dtype
+    viewable as bytes). Scatters rows in place."""
+    assert latent.dtype == torch.bfloat16 and k_pe.dtype == torch.bfloat16
+    assert latent.stride(-1) == 1 and k_pe.stride(-1) == 1 and slot_mapping.dtype == torch.int64
+    T = slot_mapping.numel()
+    nbytes = cache.numel() * cache.element_size()
+    rb = mla_row_bytes(cache_kind)
+    _check(load().mla_cache_write(latent.data_ptr(), latent.stride(0) if latent.dim() == 2 else 512,
+                                  k_pe.data_ptr(), k_pe.stride(0) if k_pe.dim() == 2 else 64,
+                                  slot_mapping.data_ptr(), T, cache.data_ptr(), nbytes // rb, cache_kind,
+                                  _stream(stream)), "mla_cache_write")
+
+
+def mla_decode_workspace_bytes(B: int, q_len: int, Hq: int, num_ctas: int = 0) -> int:
+    n = load().mla_decode_workspace_bytes(B, q_len, Hq, num_ctas)
+    if n == 0:
+        raise MlaError(MLA_ERR_INVALID_ARG, "mla_decode_workspace_bytes")
+    return n
+
+
+def mla_decode(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens, q_len, scale, out, lse,
+               workspace, num_ctas: int = 0, stream=None) -> None:
+    """Raw entry point: every buffer is caller-allocated (see include/mla.h)."""
+    B = seq_lens.numel()
+    Hq = q_lat.shape[-2]
+    assert q_lat.is_contiguous() and q_pe.is_contiguous() and block_table.dtype == torch.int32
+    assert seq_lens.dtype == torch.int32 and lse.dtype == torch.float32
+    out_dtype = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
+    nbytes = cache.numel() * cache.element_size()
+    rb = mla_row_bytes(cache_kind)
+    _check(load().mla_decode(q_lat.data_ptr(), q_pe.data_ptr(), cache.data_ptr(), cache_kind, nbytes // rb,
+                             page_size, block_table.data_ptr(), block_table.stride(0), seq_lens.data_ptr(), B, q_len,
+                             Hq, float(scale), out.data_ptr(), out_dtype, lse.data_ptr(), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), num_ctas, _stream(stream)),
+           "mla_decode")
+
+
+def mla_merge_lse(part_out: torch.Tensor, part_lse: torch.Tensor, out: torch.Tensor, lse=None, stream=None) -> None:
+    """part_out [S,N,512] fp32, part_lse [S,N] fp32 -> out [N,512] (bf16/fp32), lse [N]."""
+    S, N = part_lse.shape
+    assert part_out.is_contiguous() and part_lse.is_contiguous() and part_out.dtype == torch.float32
+    out_dtype = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
+    _check(load().mla_merge_lse(part_out.data_ptr(), part_lse.data_ptr(), S, N, out.data_ptr(), out_dtype,
+                                lse.data_ptr() if lse is not None else None, _stream(stream)), "mla_merge_lse")
+
+
+def decode(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens, q_len, scale,
+           out_dtype=torch.bfloat16, num_ctas: int = 0, workspace=None, stream=None):
+    """Allocate out/lse (and the workspace unless given) and run mla_decode.
+    Returns (out [B*q_len, Hq, 512], lse [B*q_len, Hq], workspace)."""
+    B = seq_lens.numel()
+    Hq = q_lat.shape[-2]
+    dev = q_lat.device
+    out = torch.empty((B * q_len, Hq, 512), dtype=out_dtype, device=dev)
+    lse = torch.empty((B * q_len, Hq), dtype=torch.float32, device=dev)
+    need = mla_decode_workspace_bytes(B, q_len, Hq, num_ctas)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    mla_decode(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens, q_len, scale, out, lse, workspace,
+               num_ctas, stream)
+    return out, lse, workspace
+
+
+def device_status(workspace: torch.Tensor) -> int:
+    """Device-side status word of the last mla_decode that used `workspace`
+    (0 = ok; bit 1 = a bounded wait gave up; bit 2 = bad block id)."""
+    return int(workspace[:4].view(torch.int32).item())

@@ -1,0 +1,213 @@
+// C ABI entry points (declared in include/mla.h): host-side validation,
+// launch planning and TMA descriptor set-up. No entry point allocates memory
+// or synchronises.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mla.h"
+#include "launch.cuh"
+#include "mla_common.cuh"
+
+namespace {
+
+constexpr size_t kWsHeader = 256;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DevInfo {
+    int sms = -1;
+    int major = 0, minor = 0;
+};
+
+DevInfo dev_info(int dev) {
+    static std::mutex mu;
+    static DevInfo cache[64];
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64) return DevInfo{};
+    if (cache[dev].sms < 0) {
+        DevInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DevInfo{};
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cache[dev] = d;
+    }
+    return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int gcd_int(int a, int b) {
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+int rows_padded(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
+
+size_t decode_ws_bytes(int B, int HQ, int G) {
+    const size_t GY = (static_cast<size_t>(HQ) + 63) / 64;
+    const size_t slots = GY * static_cast<size_t>(G + B) * 64;
+    const size_t lse_bytes = (slots * sizeof(float) + 255) / 256 * 256;
+    return kWsHeader + lse_bytes + slots * 512 * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_row_bytes(int cache_kind) {
+    return cache_kind == MLA_CACHE_BF16_576 ? mla::kRowBf16 : cache_kind == MLA_CACHE_FP8_DS_MLA_656 ? mla::kRowFp8 : 0;
+}
+
+const char* mla_status_string(int status) {
+    switch (status) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case MLA_ERR_WORKSPACE: return "workspace too small";
+        case MLA_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int mla_num_sms(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev_info(dev).sms;
+}
+
+int mla_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
+                    const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots, int cache_kind,
+                    void* stream) {
+    if (num_tokens < 0 || num_slots < 0) return MLA_ERR_INVALID_ARG;
+    if (cache_kind != MLA_CACHE_BF16_576 && cache_kind != MLA_CACHE_FP8_DS_MLA_656) return MLA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MLA_OK;
+    if (!latent || !k_pe || !slot_mapping || !cache) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(latent) || !aligned16(k_pe) || !aligned16(cache)) return MLA_ERR_INVALID_ARG;
+    if (latent_stride < mla::kD || latent_stride % 8 || k_pe_stride < mla::kP || k_pe_stride % 8)
+        return MLA_ERR_INVALID_ARG;
+    cudaError_t e = mla::launch_cache_write(latent, latent_stride, k_pe, k_pe_stride, slot_mapping, num_tokens, cache,
+                                            cache_kind, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas) {
+    if (B <= 0 || q_len <= 0 || Hq <= 0 || num_ctas < 0) return 0;
+    int G = num_ctas;
+    if (G == 0) {
+        G = mla_num_sms();
+        if (G <= 0) return 0;
+    }
+    return decode_ws_bytes(B, Hq * q_len, G);
+}
+
+int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache_kind, int64_t num_slots,
+               int page_size, const int32_t* block_table, int64_t block_table_stride, const int32_t* seq_lens, int B,
+               int q_len, int Hq, float scale, void* out, int out_dtype, float* lse, void* workspace,
+               size_t workspace_bytes, int num_ctas, void* stream) {
+    if (B <= 0 || q_len <= 0 || Hq <= 0 || page_size <= 0 || num_slots <= 0 || num_ctas < 0)
+        return MLA_ERR_INVALID_ARG;
+    if (num_slots > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+    if (cache_kind != MLA_CACHE_BF16_576 && cache_kind != MLA_CACHE_FP8_DS_MLA_656) return MLA_ERR_INVALID_ARG;
+    if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_F32) return MLA_ERR_INVALID_ARG;
+    if (!q_lat || !q_pe || !cache || !block_table || !seq_lens || !out || !lse || !workspace)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MLA_ERR_INVALID_ARG;
+    if (block_table_stride < 1) return MLA_ERR_INVALID_ARG;
+    const int64_t HQ64 = static_cast<int64_t>(Hq) * q_len;
+    if (HQ64 > (1 << 20)) return MLA_ERR_UNSUPPORTED;
+    const int HQ = static_cast<int>(HQ64);
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    const DevInfo di = dev_info(dev);
+    if (di.sms <= 0) return MLA_ERR_CUDA;
+    if (di.major != 10) return MLA_ERR_UNSUPPORTED;
+    const int G = num_ctas > 0 ? num_ctas : di.sms;
+    if (workspace_bytes < decode_ws_bytes(B, HQ, G)) return MLA_ERR_WORKSPACE;
+    const int GY = (HQ + 63) / 64;
+    if (GY > 65535) return MLA_ERR_UNSUPPORTED;
+
+    const bool lsu = cache_kind == MLA_CACHE_FP8_DS_MLA_656 || (page_size % 8) != 0;
+    CUtensorMap tmap;
+    std::memset(&tmap, 0, sizeof(tmap));
+    if (!lsu) {
+        auto enc = encode_fn();
+        if (!enc) return MLA_ERR_CUDA;
+        const int br = gcd_int(page_size, 128);
+        cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(num_slots)};
+        cuuint64_t gstride[1] = {static_cast<cuuint64_t>(mla::kRowBf16)};
+        cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(br)};
+        cuuint32_t estride[2] = {1u, 1u};
+        CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box,
+                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t slots = static_cast<size_t>(GY) * (G + B) * 64;
+    const size_t lse_bytes = (slots * sizeof(float) + 255) / 256 * 256;
+    if (cudaMemsetAsync(ws, 0, 16, s) != cudaSuccess) return MLA_ERR_CUDA;
+
+    mla::DecodeParams p;
+    p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+    p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+    p.cache = static_cast<const uint8_t*>(cache);
+    p.num_slots = num_slots;
+    p.block_table = block_table;
+    p.bt_stride = block_table_stride;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.lse = lse;
+    p.status = reinterpret_cast<int*>(ws);
+    p.part_lse = reinterpret_cast<float*>(ws + kWsHeader);
+    p.part_o = reinterpret_cast<float*>(ws + kWsHeader + lse_bytes);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.page_size = page_size;
+    p.run_rows = gcd_int(page_size, 128);
+    p.B = B;
+    p.Qt = q_len;
+    p.Hq = Hq;
+    p.HQ = HQ;
+    p.out_f32 = out_dtype == MLA_OUT_F32;
+    p.SPG = G + B;
+    const int NP = rows_padded(HQ < 64 ? HQ : 64);
+    cudaError_t e = mla::launch_decode(tmap, p, NP, lsu, cache_kind, G, GY, s);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_merge_lse(const float* part_out, const float* part_lse, int S, int64_t N, void* out, int out_dtype,
+                  float* lse, void* stream) {
+    if (S < 0 || N < 0) return MLA_ERR_INVALID_ARG;
+    if (out_dtype != MLA_OUT_BF16 && out_dtype != MLA_OUT_F32) return MLA_ERR_INVALID_ARG;
+    if (N == 0) return MLA_OK;
+    if ((S > 0 && (!part_out || !part_lse)) || !out) return MLA_ERR_INVALID_ARG;
+    if ((S > 0 && !aligned16(part_out)) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+    cudaError_t e = mla::launch_merge_lse(part_out, part_lse, S, N, out, out_dtype == MLA_OUT_F32, lse,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // extern "C"

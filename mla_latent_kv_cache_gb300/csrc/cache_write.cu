@@ -1,0 +1,101 @@
+// Cache write: scatter new tokens' rows into the paged latent pool.
+//
+// bf16 rows (1152 B) are concat(latent[0:512], k_pe[0:64]) ("sabi-mla-vllm"
+// README, "What the plugin does"; vLLM PR #55543 commit 3.1+3.2,
+// concat_and_cache_mla). fp8_ds_mla rows (656 B) hold the e4m3 codes of the
+// latent divided by a per-128-block scale absmax/448, the four fp32 scales and
+// the bf16 k_pe (vLLM PR #55543 commit 5.1-5.4 and PR description "Approach").
+//
+// One warp per token; every row offset is slot * row_bytes in 64-bit.
+#include "launch.cuh"
+#include "mla_common.cuh"
+
+namespace mla {
+
+__global__ void __launch_bounds__(256) cache_write_bf16_kernel(const __nv_bfloat16* __restrict__ latent,
+                                                               int64_t latent_stride,
+                                                               const __nv_bfloat16* __restrict__ k_pe,
+                                                               int64_t k_pe_stride,
+                                                               const int64_t* __restrict__ slot_mapping,
+                                                               int64_t num_tokens, uint8_t* __restrict__ cache) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= num_tokens) return;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;
+    uint8_t* row = cache + slot * static_cast<int64_t>(kRowBf16);
+    const uint4* src_l = reinterpret_cast<const uint4*>(latent + t * latent_stride);
+    const uint4* src_r = reinterpret_cast<const uint4*>(k_pe + t * k_pe_stride);
+    uint4* dst = reinterpret_cast<uint4*>(row);
+    // 72 units of 16 bytes: 64 of latent, then 8 of k_pe
+    const uint4 a = __ldg(src_l + lane);
+    const uint4 b = __ldg(src_l + lane + 32);
+    dst[lane] = a;
+    dst[lane + 32] = b;
+    if (lane < 8) dst[64 + lane] = __ldg(src_r + lane);
+}
+
+__global__ void __launch_bounds__(256) cache_write_fp8_kernel(const __nv_bfloat16* __restrict__ latent,
+                                                              int64_t latent_stride,
+                                                              const __nv_bfloat16* __restrict__ k_pe,
+                                                              int64_t k_pe_stride,
+                                                              const int64_t* __restrict__ slot_mapping,
+                                                              int64_t num_tokens, uint8_t* __restrict__ cache) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= num_tokens) return;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;
+    uint8_t* row = cache + slot * static_cast<int64_t>(kRowFp8);
+    // lane owns latent values [16*lane, 16*lane+16); lanes 8j..8j+7 form block j
+    const uint4* src = reinterpret_cast<const uint4*>(latent + t * latent_stride) + 2 * lane;
+    uint4 raw[2] = {__ldg(src), __ldg(src + 1)};
+    const __nv_bfloat16* xv = reinterpret_cast<const __nv_bfloat16*>(raw);
+    float x[16];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        x[i] = __bfloat162float(xv[i]);
+        amax = fmaxf(amax, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float scale = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+    uint32_t packed[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float q = __fdiv_rn(x[4 * w + k], scale);
+            const uint32_t code = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
+            v |= code << (8 * k);
+        }
+        packed[w] = v;
+    }
+    reinterpret_cast<uint4*>(row)[lane] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    if ((lane & 7) == 0) reinterpret_cast<float*>(row + 512)[lane >> 3] = scale;
+    if (lane < 8) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(k_pe + t * k_pe_stride) + lane);
+        reinterpret_cast<uint4*>(row + 528)[lane] = r;
+    }
+}
+
+cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
+                               const int64_t* slot_mapping, int64_t num_tokens, void* cache, int kind,
+                               cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int64_t blocks = (num_tokens + 7) / 8;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    if (kind == 0)
+        cache_write_bf16_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(latent), latent_stride,
+                                                          static_cast<const __nv_bfloat16*>(k_pe), k_pe_stride,
+                                                          slot_mapping, num_tokens, static_cast<uint8_t*>(cache));
+    else
+        cache_write_fp8_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(latent), latent_stride,
+                                                         static_cast<const __nv_bfloat16*>(k_pe), k_pe_stride,
+                                                         slot_mapping, num_tokens, static_cast<uint8_t*>(cache));
+    return cudaGetLastError();
+}
+
+}  // namespace mla

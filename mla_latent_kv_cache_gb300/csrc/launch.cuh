@@ -1,0 +1,40 @@
+// Internal launch interface shared by the C ABI layer and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+// Everything a decode launch needs; passed by value as a kernel parameter.
+struct DecodeParams {
+    const __nv_bfloat16* q_lat;
+    const __nv_bfloat16* q_pe;
+    const uint8_t* cache;
+    int64_t num_slots;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    const int32_t* seq_lens;
+    void* out;
+    float* lse;
+    int* status;       // device status word (workspace header)
+    float* part_o;     // [GY][SPG][64][512] fp32 partial outputs
+    float* part_lse;   // [GY][SPG][64] fp32 partial LSEs
+    float scale_log2;  // softmax scale * log2(e)
+    int page_size;
+    int run_rows;      // TMA box height: gcd(page_size, 128)
+    int B, Qt, Hq, HQ; // HQ = Hq * Qt rows per request
+    int out_f32;
+    int SPG;           // partial slots per row group = gridDim.x + B
+};
+
+cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
+                               const int64_t* slot_mapping, int64_t num_tokens, void* cache, int kind,
+                               cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap& tmap, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,
+                          cudaStream_t stream);
+cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, int64_t N, void* out, int out_f32,
+                             float* lse, cudaStream_t stream);
+
+}  // namespace mla

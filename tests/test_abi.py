@@ -1,0 +1,75 @@
+"""The C-ABI library loads and exports what include/mla.h declares; host-side
+argument checks reject bad calls before any GPU work (no device needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_latent_kv_cache_gb300 as m
+from mla_latent_kv_cache_gb300 import build as mbuild
+
+HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return m.load()
+
+
+def declared_functions():
+    txt = open(HDR).read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["mla_cache_write", "mla_decode", "mla_merge_lse", "mla_decode_workspace_bytes"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings(lib):
+    assert m.mla_status_string(0) == "ok"
+    assert "invalid" in m.mla_status_string(-1)
+    assert m.mla_row_bytes(0) == 1152 and m.mla_row_bytes(1) == 656 and m.mla_row_bytes(7) == 0
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    # every one of these is rejected on the host before any CUDA call
+    assert lib.mla_cache_write(None, 512, None, 64, None, -1, None, 10, 0, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_cache_write(None, 512, None, 64, None, 0, None, 10, 0, None) == m.MLA_OK  # nothing to do
+    assert lib.mla_cache_write(16, 512, 16, 64, 16, 4, 16, 10, 5, None) == m.MLA_ERR_INVALID_ARG  # kind
+    assert lib.mla_cache_write(16, 500, 16, 64, 16, 4, 16, 10, 0, None) == m.MLA_ERR_INVALID_ARG  # stride
+    assert lib.mla_cache_write(8, 512, 16, 64, 16, 4, 16, 10, 0, None) == m.MLA_ERR_INVALID_ARG   # alignment
+    args = [16, 16, 16, 0, 100, 16, 16, 4, 16, 2, 1, 8, 0.1, 16, 0, 16, 256, 1 << 20, 0, None]
+    bad = list(args)
+    bad[9] = 0                                                     # B = 0
+    assert lib.mla_decode(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[5] = 0                                                     # page_size = 0
+    assert lib.mla_decode(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[16] = 264                                                  # workspace not 256-aligned
+    assert lib.mla_decode(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[3] = 9                                                     # cache kind
+    assert lib.mla_decode(*bad) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_lse(16, 16, -1, 4, 16, 0, 16, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge_lse(16, 16, 2, 0, 16, 0, 16, None) == m.MLA_OK
+
+
+def test_workspace_size_formula(lib):
+    # header + [groups][ctas + B][64] lse + [groups][ctas + B][64][512] partial outputs
+    for B, q, H, G in [(2, 1, 8, 152), (64, 1, 16, 152), (128, 4, 16, 152), (3, 1, 80, 7)]:
+        gy = -(-(H * q) // 64)
+        slots = gy * (G + B) * 64
+        lse_b = -(-(slots * 4) // 256) * 256
+        assert m.mla_decode_workspace_bytes(B, q, H, G) == 256 + lse_b + slots * 512 * 4
+    assert lib.mla_decode_workspace_bytes(0, 1, 8, 4) == 0
