@@ -672,10 +672,18 @@ __global__ void __launch_bounds__(LSU ? 384 : 256, 1)
 // Merge `nseg` partials of one row: out = sum_i w_i o_i with
 // w_i = exp(lse_i - L), L = ln sum exp(lse_i); all -inf -> (0, -inf).
 // One warp; lane owns dims 4*lane + 128*k, k = 0..3.
+// CTA g of G got tiles [g*tot/G, (g+1)*tot/G); with more CTAs than tiles some
+// ranges are empty and wrote no partial. tot == 0 means "all partials live".
+__device__ __forceinline__ bool seg_live(long long tot, int G, long long g) {
+    return tot == 0 || (g * tot / G) < ((g + 1) * tot / G);
+}
+
 __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, const float* pl, int64_t l_stride,
-                                          int nseg, void* out, int out_f32, float* lse_out, int lane) {
+                                          int nseg, void* out, int out_f32, float* lse_out, int lane,
+                                          long long tot = 0, int G = 1, long long g0 = 0) {
     float mx = -INFINITY;
-    for (int s = lane; s < nseg; s += 32) mx = fmaxf(mx, pl[s * l_stride]);
+    for (int s = lane; s < nseg; s += 32)
+        if (seg_live(tot, G, g0 + s)) mx = fmaxf(mx, pl[s * l_stride]);
     mx = warp_max(mx);
     float4 acc[4];
 #pragma unroll
@@ -684,12 +692,14 @@ __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, con
     if (mx != -INFINITY) {
         float ws = 0.f;
         for (int s = lane; s < nseg; s += 32) {
+            if (!seg_live(tot, G, g0 + s)) continue;
             const float v = pl[s * l_stride];
             if (v != -INFINITY) ws += expf(v - mx);
         }
         ws = warp_sum(ws);
         L = mx + logf(ws);
         for (int s = 0; s < nseg; ++s) {
+            if (!seg_live(tot, G, g0 + s)) continue;
             const float v = pl[s * l_stride];
             if (v == -INFINITY) continue;
             const float w = expf(v - L);
@@ -758,7 +768,8 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
     for (int n = warp; n < HQg; n += 8) {
         const int64_t row = static_cast<int64_t>(b) * p.HQ + gy * 64 + n;
         merge_row(p.part_o + (slot0 * 64 + n) * kD, 64 * kD, p.part_lse + slot0 * 64 + n, 64, nseg,
-                  static_cast<uint8_t*>(p.out) + row * kD * (p.out_f32 ? 4 : 2), p.out_f32, p.lse + row, lane);
+                  static_cast<uint8_t*>(p.out) + row * kD * (p.out_f32 ? 4 : 2), p.out_f32, p.lse + row, lane,
+                  tot, G, g0);
     }
 }
 
