@@ -1,0 +1,411 @@
+"""Benchmark: paged MLA decode latent-cache bandwidth on GB300.
+
+One step = the hot path over one batch: write the step's new cache rows
+(mla_cache_write) and decode every request against the paged latent cache
+(mla_decode, which includes the split merge). Metric: latent-cache GB/s =
+(sum of context tokens x row bytes) / step time, each request's rows counted
+once; also decode steps/s and context tokens/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config batched|long|mtp|fp8|tiny]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream, with L2 flushed (a 256 MiB write) before every step
+outside the events; barrier + synchronize around the timed region; the max
+over ranks is reported. Under torchrun every rank runs an independent replica
+(its own seeded batch): requests are independent, so there is no collective
+on the data path and scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA paged decode latent-cache HBM GB/s (% of GB300 peak) and decode steps/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SRC = os.path.join(ROOT, "mla_latent_kv_cache_gb300", "csrc", "decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+CONFIG_TEXT = {
+    "tiny": "B=2 Hq=8 seq {37,200} page 16 bf16",
+    "batched": "B=64 Hq=16 seq U{1024..8192} page 16 bf16",
+    "long": "B=4 Hq=32 seq 262144 page 64 bf16",
+    "mtp": "B=128 Hq=16 Qt=4 causal, 9.8M-slot pool above slot 3,728,270, seq 0/1/U{2048..100000}, page 16 bf16",
+    "fp8": "B=64 Hq=64 seq 32768 page 64 fp8_ds_mla (656 B rows)",
+}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_over_ranks(values, op):
+    """values: list of floats on this rank -> reduced over ranks ("max"/"sum")."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return t.cpu().tolist()
+
+
+def aggregate(bytes_per_step, ms_per_step):
+    """Whole-job throughput: bytes of all ranks / the slowest rank's time."""
+    tot_bytes = reduce_over_ranks([bytes_per_step], "sum")[0]
+    ms = reduce_over_ranks([ms_per_step], "max")[0]
+    return tot_bytes, ms
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    return hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()[:16]
+
+
+def traffic_for(config):
+    """DRAM bytes per decode launch from a committed ncu capture, if it was
+    taken on the current decode kernel source; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    d = json.load(open(TRAFFIC_FILE))
+    e = d.get(config)
+    if not e or e.get("kernel_src_sha") != kernel_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, out_path: str | None):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.out_path = out_path
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        if self.out_path:
+            with open(self.out_path, "w") as f:
+                f.write(self.Q + "\n" + "\n".join(self.lines) + "\n")
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+
+    from mla_latent_kv_cache_gb300 import build as mbuild
+    mbuild.build()
+    import mla_latent_kv_cache_gb300 as m
+    from mla_latent_kv_cache_gb300 import workloads as W
+
+    wl = W.CONFIGS[args.config](device=dev, seed={"tiny": 1, "batched": 2, "long": 3, "mtp": 4, "fp8": 5}[args.config] + 1000 * rank)
+    # the fp8 pool is written once (the step then writes only the last token per request)
+    if wl.kind == 1:
+        m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+        last = []
+        sl = wl.seq_lens.tolist()
+        start = 0
+        for T in sl:
+            if T:
+                last.append(start + T - 1)
+            start += T
+        idx = torch.tensor(last, device=dev, dtype=torch.int64)
+        wl.w_latent, wl.w_k_pe, wl.w_slots = wl.w_latent[idx].contiguous(), wl.w_k_pe[idx].contiguous(), wl.w_slots[idx].contiguous()
+        torch.cuda.synchronize()
+
+    cache_bytes = wl.cache_bytes()
+    ctx_tokens = wl.context_tokens()
+    B, Qt, Hq = wl.B, wl.Qt, wl.Hq
+    out = torch.empty((B * Qt, Hq, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B * Qt, Hq), dtype=torch.float32, device=dev)
+    wsb = m.mla_decode_workspace_bytes(B, Qt, Hq, 0)
+    workspace = torch.empty((wsb,), dtype=torch.uint8, device=dev)
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+        m.mla_decode(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens, Qt,
+                     wl.scale, out, lse, workspace)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    assert m.device_status(workspace) == 0, "device-side status after warm-up"
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_bench_{args.config}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    if ws_ > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+        evd[i][0].record(stream)
+        m.mla_decode(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens, Qt,
+                     wl.scale, out, lse, workspace)
+        evd[i][1].record(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if ws_ > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    dec_ms = sum(a.elapsed_time(b) for a, b in evd) / K
+    assert m.device_status(workspace) == 0, "device-side status after the timed steps"
+
+    # ---- end to end through the public API with host buffers
+    host_in = {k: v.cpu().pin_memory() for k, v in dict(q_lat=wl.q_lat, q_pe=wl.q_pe, w_latent=wl.w_latent,
+                                                          w_k_pe=wl.w_k_pe, w_slots=wl.w_slots,
+                                                          block_table=wl.block_table, seq_lens=wl.seq_lens).items()}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    Ke = max(3, min(K, 200))
+    eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+    for i in range(Ke + 3):
+        flush.fill_(1)
+        if i >= 3:
+            eve[i - 3][0].record(stream)
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        m.mla_cache_write(dev_in["w_latent"], dev_in["w_k_pe"], dev_in["w_slots"], wl.pool, wl.kind)
+        m.mla_decode(dev_in["q_lat"], dev_in["q_pe"], wl.pool, wl.kind, wl.page_size, dev_in["block_table"],
+                     dev_in["seq_lens"], Qt, wl.scale, out, lse, workspace)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+        if i >= 3:
+            eve[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eve) / Ke
+
+    tot_bytes, step_ms_max = aggregate(cache_bytes, step_ms)
+    _, dec_ms_max = aggregate(cache_bytes, dec_ms)
+    _, e2e_ms_max = aggregate(cache_bytes, e2e_ms)
+    if rank != 0:
+        if ws_ > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = measured_peaks()
+    value = tot_bytes / (step_ms_max * 1e-3) / 1e9
+    achieved = cache_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = traffic_for(args.config)
+    cpu = cpu_baseline(args.config, wl) if ws_ == 1 and not args.no_cpu else None
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws_, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.kind == 0 else "e4m3+bf16",
+        "data": "synthetic (seeded N(0,1) bf16 rows, shuffled block tables, NaN-filled free slots)",
+        "config": {"workload": args.config, "shape": CONFIG_TEXT[args.config], "context_tokens": ctx_tokens,
+                   "cache_bytes_per_step": cache_bytes, "row_bytes": wl.row_bytes,
+                   "l2": "flushed before every step (256 MiB write, outside the timed events)",
+                   "step": "mla_cache_write of the step's new rows + mla_decode (decode + split merge)",
+                   "parallelism": f"replicas x{ws_} (requests are independent)"},
+        "decode_steps_per_s": round(1e3 / step_ms_max, 1),
+        "ctx_tokens_per_s": round(ctx_tokens * ws_ / (step_ms_max * 1e-3), 1),
+        "pct_of_8TBps": round(100 * value / ws_ / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * value / ws_ / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "mla_decode call (decode kernel + split-merge kernel), CUDA events",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: copy, read+write)",
+                     "algorithmic_bytes_per_launch": cache_bytes},
+        "e2e": {"value": round(tot_bytes / (e2e_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms_max, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def _oracle_request(wl, b, cap=None):
+    """Run the oracle on request b (its first `cap` tokens when given);
+    returns (bytes, seconds)."""
+    import oracle
+    from mla_latent_kv_cache_gb300 import workloads as W
+    c = W.compact(wl, [b])
+    pool = c["pool"].copy()
+    oracle.cache_write(c["w_latent"], c["w_k_pe"], c["w_slots"], pool, wl.kind)
+    sl = c["seq_lens"].copy()
+    if cap is not None:
+        sl[0] = min(int(sl[0]), int(cap))
+    t0 = time.perf_counter()
+    oracle.decode(c["q_lat"], c["q_pe"], pool, wl.kind, wl.page_size, c["block_table"], sl, 1, wl.Qt, wl.Hq,
+                  wl.scale)
+    return int(sl[0]) * wl.row_bytes, time.perf_counter() - t0
+
+
+def oracle_sample(config, wl, budget_s=15.0):
+    """Time the oracle on whole requests of the workload (middle lengths
+    first) until about `budget_s` of CPU work; returns (bytes, seconds,
+    requests, threads)."""
+    import oracle
+    sl = wl.seq_lens.cpu().numpy()
+    order = [int(b) for b in sorted(range(wl.B), key=lambda b: sl[b]) if sl[b] > 0]
+    order = order[len(order) // 2:] + order[:len(order) // 2]
+    done_bytes, secs, used = 0, 0.0, []
+    for b in order:
+        nb, dt = _oracle_request(wl, b)
+        done_bytes += nb
+        secs += dt
+        used.append(b)
+        if secs >= budget_s:
+            break
+    return done_bytes, secs, used, oracle.num_threads()
+
+
+def cpu_baseline(config, wl):
+    b, s, used, th = oracle_sample(config, wl)
+    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": th, "kind": "oracle",
+            "sample": f"{len(used)} whole request(s) of the '{config}' workload ({b // wl.row_bytes} context tokens, "
+                      f"{s:.1f} s), fp64 C oracle with OpenMP over (request, query, head)"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    same workload (one request, cut to a token budget so the whole run takes
+    about a minute of CPU time) on the host cores; rank 0 only."""
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import torch
+    from mla_latent_kv_cache_gb300 import workloads as W
+    wl = W.CONFIGS[args.config](device="cuda" if torch.cuda.is_available() else "cpu")
+    sl = wl.seq_lens.cpu().numpy()
+    live = [int(b) for b in range(wl.B) if sl[b] > 0]
+    # calibrate tokens per second on a short piece of one request
+    nb, dt = _oracle_request(wl, live[0], cap=256)
+    rate = (nb / wl.row_bytes) / max(dt, 1e-6)
+    per_step = max(0.02, 60.0 / (args.steps + args.warmup))
+    cap = max(16, int(rate * per_step))
+    tb, ts = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        nb, dt = _oracle_request(wl, live[i % len(live)], cap=cap)
+        if i >= args.warmup:
+            tb += nb
+            ts += dt
+    v = tb / ts / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * ts / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.config, "shape": CONFIG_TEXT[args.config]},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"each step: one request of the '{args.config}' workload, first {cap} context "
+                                   f"tokens, all {wl.Hq * wl.Qt} query rows"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="batched", choices=sorted(CONFIG_TEXT))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -82,8 +82,8 @@ MLA_API int mla_cache_write(const void* latent, int64_t latent_stride, const voi
 /*
  * mla_decode_workspace_bytes - bytes of device workspace mla_decode needs.
  *   B, q_len, Hq   as for mla_decode.
- *   num_ctas       the value that will be passed to mla_decode (0 = one CTA per
- *                  SM of the current device).
+ *   num_ctas       the value that will be passed to mla_decode (0 = as many
+ *                  CTAs as fit on the current device).
  * The workspace holds a 256-byte header (word 0: device-side status, see
  * mla_decode) and fp32 partial results of requests split across CTAs.
  * Returns 0 for invalid sizes.
@@ -122,10 +122,13 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *                status bits: 1 = a bounded internal wait gave up (the kernel
  *                returned early, outputs are invalid), 2 = a block-table entry
  *                pointed outside the pool (page 0 was read instead).
- *   num_ctas     CTAs sharing the token stream (0 = one per SM). The tokens of
- *                all requests are cut into 128-token tiles and dealt out as
- *                equal contiguous ranges; requests cut across CTAs are merged
- *                from fp32 partials by a second kernel.
+ *   num_ctas     CTAs sharing the token stream (0 = as many as fit on the
+ *                device, one per SM). CTAs work in clusters of two that split
+ *                each token's 576 dims between them, so num_ctas / 2 clusters
+ *                run. The tokens of all requests are cut into 128-token tiles
+ *                dealt out as equal contiguous ranges, one per cluster;
+ *                requests cut across clusters are merged from fp32 partials by
+ *                a second kernel.
  * Limits: Hq * q_len rows are processed in groups of at most 64. Returns
  * MLA_ERR_UNSUPPORTED on a device other than sm_103 / sm_100 family.
  */

@@ -27,8 +27,11 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
+
+
 def _flags(extra=()):
-    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+    return ARCH + ["-I", INCLUDE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                    "--expt-relaxed-constexpr", *extra]
 
 

@@ -7,7 +7,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/mla.h"
+#include "mla.h"
 #include "launch.cuh"
 #include "mla_common.cuh"
 
@@ -62,6 +62,7 @@ int gcd_int(int a, int b) {
 
 int rows_padded(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
 
+// G = clusters of the decode grid (2 CTAs each).
 size_t decode_ws_bytes(int B, int HQ, int G) {
     const size_t GY = (static_cast<size_t>(HQ) + 63) / 64;
     const size_t slots = GY * static_cast<size_t>(G + B) * 64;
@@ -111,12 +112,13 @@ int mla_cache_write(const void* latent, int64_t latent_stride, const void* k_pe,
 
 size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas) {
     if (B <= 0 || q_len <= 0 || Hq <= 0 || num_ctas < 0) return 0;
-    int G = num_ctas;
-    if (G == 0) {
-        G = mla_num_sms();
-        if (G <= 0) return 0;
+    int G = num_ctas / 2;  // clusters of 2 CTAs
+    if (num_ctas == 0) {
+        const int sms = mla_num_sms();
+        if (sms <= 0) return 0;
+        G = sms / 2;
     }
-    return decode_ws_bytes(B, Hq * q_len, G);
+    return decode_ws_bytes(B, Hq * q_len, G < 1 ? 1 : G);
 }
 
 int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache_kind, int64_t num_slots,
@@ -143,25 +145,36 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     const DevInfo di = dev_info(dev);
     if (di.sms <= 0) return MLA_ERR_CUDA;
     if (di.major != 10) return MLA_ERR_UNSUPPORTED;
-    const int G = num_ctas > 0 ? num_ctas : di.sms;
-    if (workspace_bytes < decode_ws_bytes(B, HQ, G)) return MLA_ERR_WORKSPACE;
     const int GY = (HQ + 63) / 64;
     if (GY > 65535) return MLA_ERR_UNSUPPORTED;
-
+    const int NP = rows_padded(HQ < 64 ? HQ : 64);
     const bool lsu = cache_kind == MLA_CACHE_FP8_DS_MLA_656 || (page_size % 8) != 0;
-    CUtensorMap tmap;
-    std::memset(&tmap, 0, sizeof(tmap));
+    const int G = mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
+    if (G <= 0) return MLA_ERR_CUDA;
+    if (workspace_bytes < decode_ws_bytes(B, HQ, G)) return MLA_ERR_WORKSPACE;
+
+    // Two TMA descriptors over the pool [num_slots, 576] bf16: 64-dim latent
+    // chunks (128-byte swizzle) and 32-dim rope halves (64-byte swizzle), both
+    // gcd(page_size, 128) rows high so a box never crosses a page.
+    CUtensorMap tmap_lat, tmap_rope;
+    std::memset(&tmap_lat, 0, sizeof(tmap_lat));
+    std::memset(&tmap_rope, 0, sizeof(tmap_rope));
     if (!lsu) {
         auto enc = encode_fn();
         if (!enc) return MLA_ERR_CUDA;
         const int br = gcd_int(page_size, 128);
         cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(num_slots)};
         cuuint64_t gstride[1] = {static_cast<cuuint64_t>(mla::kRowBf16)};
-        cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(br)};
         cuuint32_t estride[2] = {1u, 1u};
-        CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box,
-                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        cuuint32_t box_lat[2] = {64u, static_cast<cuuint32_t>(br)};
+        cuuint32_t box_rope[2] = {32u, static_cast<cuuint32_t>(br)};
+        CUresult r = enc(&tmap_lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride,
+                         box_lat, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+        r = enc(&tmap_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box_rope,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
     }
 
@@ -169,7 +182,7 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const size_t slots = static_cast<size_t>(GY) * (G + B) * 64;
     const size_t lse_bytes = (slots * sizeof(float) + 255) / 256 * 256;
-    if (cudaMemsetAsync(ws, 0, 16, s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, kWsHeader, s) != cudaSuccess) return MLA_ERR_CUDA;
 
     mla::DecodeParams p;
     p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
@@ -193,8 +206,7 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     p.HQ = HQ;
     p.out_f32 = out_dtype == MLA_OUT_F32;
     p.SPG = G + B;
-    const int NP = rows_padded(HQ < 64 ? HQ : 64);
-    cudaError_t e = mla::launch_decode(tmap, p, NP, lsu, cache_kind, G, GY, s);
+    cudaError_t e = mla::launch_decode(tmap_lat, tmap_rope, p, NP, lsu, cache_kind, G, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -9,80 +9,112 @@
 //   lse = ln sum_j exp(s_j), over the tokens each query row may see.
 //
 // Work split ("stream-K" over 128-token tiles). The tiles of all requests are
-// concatenated and gridDim.x CTAs (one per SM) each take an equal contiguous
-// range, so every SM streams the same number of cache bytes whatever the
-// request lengths. A CTA walks its range tile by tile; the tiles of one
-// request inside a range form a segment. A segment that covers its whole
-// request writes the final output; otherwise it writes an fp32 partial
-// (out, lse) that a second kernel merges. Rows (query token x head) are
-// processed NP at a time (NP = 16, 32 or 64, padded); gridDim.y covers more.
+// concatenated and the clusters (one per SM pair) each take an equal
+// contiguous range, so every SM streams the same number of cache bytes
+// whatever the request lengths. The tiles of one request inside a range form
+// a segment; a segment covering its whole request writes the final output,
+// otherwise an fp32 partial (out, lse) that a second kernel merges. Query rows
+// (query token x head) are processed NP at a time (NP = 16, 32 or 64,
+// padded); gridDim.y covers more.
 //
-// Per tile, all query rows share one read of the cache (the pages' point that
-// a verify step must read the latent once per request):
-//   S^T[128 tok, NP] = C[128, 576] . Q^T            (UMMA M=128, K=576)
-//   P = exp2(S*scale*log2e - m)  (bf16, in smem)
-//   O^T[512, NP]    += C[128, 0:512]^T . P^T         (4 UMMAs of M=128, K=128)
-// C stays in shared memory in the 128-byte-swizzled layout that serves as the
-// K-major A operand of the first product and the MN-major A operand of the
-// second. S and O live in tensor memory.
+// Two CTAs per tile (a cluster of 2 on neighbouring SMs) split the 576 cached
+// dims: CTA r holds latent dims [256r, 256r+256) and rope dims
+// [512+32r, 512+32r+32), i.e. 72 KB of each 128-token tile, so two or more
+// tiles fit in shared memory and loads overlap compute. Per tile:
+//   S_r^T[128 tok, NP] = C_r[128, 288] . Q_r^T        (UMMA M=128, into TMEM)
+//   S = S_0 + S_1       (each CTA sends its partial to the other through
+//                        distributed shared memory)
+//   P = exp2(S*scale*log2e - m)   (bf16, identical in both CTAs)
+//   O_r^T[256, NP] += C_r[128, 0:256]^T . P^T          (2 UMMAs of M=128)
+// C stays in shared memory in the 128-byte-swizzled layout that is the K-major
+// A operand of the first product and the MN-major A operand of the second.
+// All query rows share one read of the cache (the pages' point that a verify
+// step must read the latent once per request).
 //
-// Warp roles (one CTA per SM):
-//   warp 0      : TMEM allocation; one lane issues every tcgen05.mma
+// Warp roles in each CTA:
+//   warp 0      : TMEM allocation; lane 0 issues the S = C.Q^T MMAs
 //   warp 1      : TMA producer (bf16 pools, page_size % 8 == 0)
 //   warp 2      : tile-range scan at start
+//   warp 3      : lane 0 issues the O += C^T.P MMAs
 //   warps 4..7  : softmax, P, output epilogue (thread t <-> token t <-> TMEM lane t)
 //   warps 8..11 : load/convert producers (fp8 pools or odd page sizes)
 //
-// Online softmax with a lazily updated maximum: m is raised only when a score
-// exceeds it by more than 2^8 (in log2 units), so P <= 256 and rescaling of O
-// is rare; l is kept per thread and reduced once per segment.
+// Online softmax with a lazily raised maximum: m moves only when a score
+// exceeds it by more than 2^8 (log2 units), so P <= 256 and rescaling O is
+// rare; l is kept per thread and reduced once per segment.
 #include <climits>
+#include <cstddef>
 
 #include "launch.cuh"
 #include "mla_common.cuh"
 
 namespace mla {
 
+// Pipeline timeline for development builds (-DMLA_TRACE): %globaltimer at
+// hand-off points for the first 8 CTAs and 64 tiles, read back by the host
+// through mla_trace_dump(). Compiles to nothing otherwise.
+enum TraceEvent : int {
+    kTrProdStart = 0, kTrProdIssued, kTrSPair0, kTrSAllIn, kTrPvIssue, kTrSmSFull, kTrSmXFull, kTrSmPArrive,
+    kTrSIssued = 8, kTrSmTmemLd, kTrSmXFree, kTrSmSent, kTrSmMath, kTrSmBarOr, kTrSmExp, kTrSmPStore, kTrPvIssued,
+    kTrSmXRead, kTrSmExpLoop, kTrEvents = 19
+};
+#ifdef MLA_TRACE
+__device__ unsigned long long g_trace[8][64][kTrEvents];
+#define MLA_TRACE_POINT(i, e)                                                                     \
+    do {                                                                                          \
+        if (blockIdx.y == 0 && blockIdx.x < 8 && (i) < 64) g_trace[blockIdx.x][(i)][(e)] = globaltimer_ns(); \
+    } while (0)
+#else
+#define MLA_TRACE_POINT(i, e) \
+    do {                      \
+    } while (0)
+#endif
+
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kPrefetchTiles = 2;          // L2 lookahead of the load/convert producers
 
 template <int NP>
 struct Cfg {
     static_assert(NP == 16 || NP == 32 || NP == 64, "NP");
-    static constexpr int kPairBytes = 2 * 128 * 128;  // two 64-dim chunks of a 128-token tile
-    static constexpr int kRopeBytes = 128 * 128;
-    static constexpr bool kPInRope = (NP == 64);  // P reuses the tile's rope buffer
-    static constexpr int kRL = (NP == 64) ? 4 : 5;
-    static constexpr int kRR = (NP == 16) ? 2 : 1;
-    static constexpr int kQBytes = 9 * NP * 128;
-    static constexpr int kPBytes = kPInRope ? 0 : 128 * NP * 2;
+    static constexpr int kPairBytes = 2 * 128 * 128;  // 2 x (64 dims x 128 tokens), 128-B swizzled
+    static constexpr int kRopeBytes = 128 * 64;       // 32 rope dims x 128 tokens, 64-B swizzled
+    static constexpr int kRL = (NP == 16) ? 5 : 4;    // pair slots (2 per tile)
+    static constexpr int kRR = (NP == 64) ? 1 : 3;    // rope slots (1 per tile; freed right after S)
+    static constexpr int kQBytes = NP * (4 * 128 + 64);
+    static constexpr int kXBytes = 128 * NP * 4;      // the peer's partial S of one tile
+    static constexpr int kPBufs = (NP == 64) ? 1 : 2; // P (bf16) buffers
+    static constexpr int kPBytes = 128 * NP * 2;
     static constexpr int kOffRope = kRL * kPairBytes;
     static constexpr int kOffQ = kOffRope + kRR * kRopeBytes;
-    static constexpr int kOffP = kOffQ + kQBytes;
-    static constexpr int kOffCtrl = kOffP + kPBytes;
-    static constexpr int kSmemBytes = kOffCtrl + 4096 + 1024;  // + alignment slack
-    static constexpr int kTmemCols = (5 * NP <= 128) ? 128 : (5 * NP <= 256) ? 256 : 512;
-    static constexpr int kColS = 4 * NP;
-    // P operand: MN-major rows of NP bf16, swizzle span = row width
+    static constexpr int kOffX = (kOffQ + kQBytes + 1023) / 1024 * 1024;
+    static constexpr int kOffP = kOffX + kXBytes;
+    static constexpr int kOffCtrl = kOffP + kPBufs * kPBytes;
+    static constexpr int kSmemBytes = kOffCtrl + 2048 + 1024;  // + control block, alignment slack
+    static constexpr int kTmemCols = 4 * NP;                   // O: 2 x NP, S: 2 buffers x NP
+    static constexpr int kColS = 2 * NP;
     static constexpr uint32_t kPSwizzle = NP == 16 ? kSw32 : NP == 32 ? kSw64 : kSw128;
     static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kTmemCols >= 32, "tmem");
 };
 
 struct Ctrl {
     uint64_t pair_full[5], pair_empty[5];
-    uint64_t rope_full[2], rope_empty[2];
-    uint64_t s_full, p_full, o_done, q_full;
+    uint64_t rope_full[3], rope_empty[3];
+    uint64_t s_full[2], s_free[2], p_full, o_done[2], q_full;
+    uint64_t xfull;          // the peer's partial S landed (st.async transactions + 1 local arrive)
+    uint64_t xfree;          // the peer has read this CTA's last partial S (1 remote arrive)
     uint32_t tmem_base;
     int abort;
     int t_begin, t_end, b0, j0;
-    int colvis[64];       // query row -> how many trailing tokens it may not see
-    float m[64];          // running max per row (log2 units)
-    float alpha[64];
-    float red[4][64];
+    int colvis[64];                  // query row -> trailing tokens it may not see
+    alignas(16) float m[64];         // running max per row (log2 units); read as float4
+    alignas(16) float alpha[64];
+    alignas(16) float red[4][64];
 };
+static_assert(sizeof(Ctrl) <= 2048, "control block");
+static_assert(offsetof(Ctrl, m) % 16 == 0 && offsetof(Ctrl, alpha) % 16 == 0, "vector loads of m / alpha");
 
-// Column c of this row group may see token `tok` of a request of length T iff
-// tok + colvis[c] < T; padded columns never see anything.
 __device__ __forceinline__ int swz_p(int row, uint32_t mode) {
     return mode == kSw128 ? (row & 7) : mode == kSw64 ? ((row >> 1) & 3) : ((row >> 2) & 1);
 }
@@ -125,42 +157,68 @@ __device__ __forceinline__ void tmem_ld_np(uint32_t taddr, uint32_t (&r)[NP]) {
     else if constexpr (NP == 32) tmem_ld_x32(taddr, r);
     else tmem_ld_x64(taddr, r);
 }
-template <int NP>
-__device__ __forceinline__ void tmem_st_np(uint32_t taddr, const uint32_t (&r)[NP]) {
-    if constexpr (NP == 16) tmem_st_x16(taddr, r);
-    else if constexpr (NP == 32) tmem_st_x32(taddr, r);
-    else tmem_st_x64(taddr, r);
-}
 
-__device__ __forceinline__ void fail(const DecodeParams& p, Ctrl* ctrl, int code) {
+// Wait sites, recorded with the first failure (workspace header words 1..3:
+// site, tile index within the CTA's range, linear block index).
+enum WaitSite : int {
+    kSiteQFull = 1, kSiteSFree, kSitePairFull, kSiteRopeFull, kSitePFull, kSiteTmaPairEmpty, kSiteTmaRopeEmpty,
+    kSiteLsuPairEmpty, kSiteLsuRopeEmpty, kSiteSFull, kSiteXFree, kSiteXFull, kSiteOEpi, kSiteORescale, kSiteOPbuf,
+    kSiteOFinal
+};
+
+__device__ __forceinline__ void fail(const DecodeParams& p, Ctrl* ctrl, int code, int site = 0, int tile = 0) {
     atomicOr(p.status, code);
+    if (site && atomicCAS(p.status + 1, 0, site) == 0) {
+        p.status[2] = tile;
+        p.status[3] = blockIdx.y * gridDim.x + blockIdx.x;
+    }
     ctrl->abort = 1;
 }
 
 // Every softmax thread waits, then the 128 threads agree on the outcome, so a
 // timeout seen by some of them cannot strand the rest at a named barrier.
-__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, const DecodeParams& p, Ctrl* ctrl) {
-    const bool ok = mbar_wait(bar, parity, &ctrl->abort);
+// When a role leaves its loop on a failed wait it records where it was
+// waiting: header word 4 + role = (site << 24) | tile (first CTA to fail only).
+enum Role : int { kRoleS = 0, kRolePV, kRoleSoftmax, kRoleTma, kRoleLsu0 };
+
+__device__ __forceinline__ void report(const DecodeParams& p, int role, int site, int idx) {
+    if (p.status[3] == static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x))
+        p.status[4 + role] = (site << 24) | (idx & 0xFFFFFF);
+}
+
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, const DecodeParams& p, Ctrl* ctrl,
+                                           int site, int tile, bool cluster_scope = false) {
+    bool ok = !ctrl->abort;
+    if (ok) ok = cluster_scope ? mbar_wait_cluster(bar, parity, &ctrl->abort) : mbar_wait(bar, parity, &ctrl->abort);
     const bool all = named_bar_and(3, 128, ok ? 1 : 0) != 0;
-    if (!ok) fail(p, ctrl, kErrWaitTimeout);
+    if (!ok) fail(p, ctrl, kErrWaitTimeout, site, tile);
+    if (!all && threadIdx.x == 128) report(p, kRoleSoftmax, site, tile);
     return all;
 }
 
-// Load the NP query rows of request b (row group gy) into the K-major,
-// 128-byte-swizzled B operand: chunk k (64 dims) at k*NP*128, row n at n*128.
+// This CTA's half of the NP query rows of request b (row group gy), as the
+// B operands of S: latent chunks 0..3 (dims 256*rank + 64k) K-major with
+// 128-B swizzle at k*NP*128, then the rope half (32 dims) K-major with 64-B
+// swizzle at 4*NP*128.
 template <int NP>
-__device__ void load_q(const DecodeParams& p, int b, int gy, uint8_t* qs, int tid) {
-    for (int q = tid; q < NP * 72; q += 128) {
-        const int n = q / 72, u = q - n * 72;
+__device__ void load_q(const DecodeParams& p, int b, int gy, int rank, uint8_t* qs, int tid) {
+    constexpr int kUnits = 4 * 8 + 4;  // 16-byte units per row: 32 latent + 4 rope
+    for (int q = tid; q < NP * kUnits; q += 128) {
+        const int n = q / kUnits, u = q - n * kUnits;
         const int r = gy * 64 + n;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (r < p.HQ) {
             const int64_t row = static_cast<int64_t>(b) * p.HQ + r;
-            v = (u < 64) ? __ldg(reinterpret_cast<const uint4*>(p.q_lat + row * kD) + u)
-                         : __ldg(reinterpret_cast<const uint4*>(p.q_pe + row * kP) + (u - 64));
+            v = (u < 32) ? __ldg(reinterpret_cast<const uint4*>(p.q_lat + row * kD + 256 * rank) + u)
+                         : __ldg(reinterpret_cast<const uint4*>(p.q_pe + row * kP + 32 * rank) + (u - 32));
         }
-        const int chunk = u >> 3, uu = u & 7;
-        *reinterpret_cast<uint4*>(qs + chunk * NP * 128 + n * 128 + ((uu ^ (n & 7)) << 4)) = v;
+        if (u < 32) {
+            const int chunk = u >> 3, uu = u & 7;
+            *reinterpret_cast<uint4*>(qs + chunk * NP * 128 + n * 128 + ((uu ^ (n & 7)) << 4)) = v;
+        } else {
+            const int uu = u - 32;
+            *reinterpret_cast<uint4*>(qs + 4 * NP * 128 + n * 64 + ((uu ^ ((n >> 1) & 3)) << 4)) = v;
+        }
     }
 }
 
@@ -173,6 +231,25 @@ __device__ __forceinline__ int64_t token_slot(const DecodeParams& p, const int32
         return tok % p.page_size;  // page 0: in bounds, flagged
     }
     return page * ps + tok % p.page_size;
+}
+
+// Ask L2 for the cache rows of tile t, one bulk prefetch per run of tokens
+// sharing a page (their rows are contiguous); runs alternate between the two
+// CTAs of the cluster.
+__device__ __forceinline__ void prefetch_tile(const DecodeParams& p, const TileIt& t, int row_bytes, int rank) {
+    const int valid = min(kTile, t.T - t.j * kTile);
+    const int32_t* btr = p.block_table + static_cast<int64_t>(t.b) * p.bt_stride;
+    bool bad = false;
+    int tok = t.j * kTile, k = 0;
+    const int end = tok + valid;
+    while (tok < end) {
+        const int run = min(end, (tok / p.page_size + 1) * p.page_size) - tok;
+        if ((k++ & 1) == rank) {
+            const int64_t slot = token_slot(p, btr, tok, bad);
+            if (!bad) prefetch_l2_bulk(p.cache + slot * row_bytes, static_cast<uint32_t>(run * row_bytes));
+        }
+        tok += run;
+    }
 }
 
 // e4m3 x16 (one uint4) times scale -> 16 bf16 (two uint4).
@@ -193,27 +270,37 @@ __device__ __forceinline__ void dequant16(uint4 codes, float scale, uint4& lo, u
 }
 
 template <int NP, bool LSU, int KIND>
-__global__ void __launch_bounds__(LSU ? 384 : 256, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmap_lat, const __grid_constant__ CUtensorMap tmap_rope,
+                      const DecodeParams p) {
     using C = Cfg<NP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* pair_ring = smem;
     uint8_t* rope_ring = smem + C::kOffRope;
     uint8_t* qs = smem + C::kOffQ;
-    uint8_t* pbuf = smem + C::kOffP;
+    uint8_t* xbuf = smem + C::kOffX;
+    uint8_t* pbufs = smem + C::kOffP;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + C::kOffCtrl);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.x, G = gridDim.x, gy = blockIdx.y;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int g = blockIdx.x >> 1, G = gridDim.x >> 1, gy = blockIdx.y;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kRL; ++i) { mbar_init(&ctrl->pair_full[i], 1); mbar_init(&ctrl->pair_empty[i], 1); }
-        for (int i = 0; i < C::kRR; ++i) { mbar_init(&ctrl->rope_full[i], 1); mbar_init(&ctrl->rope_empty[i], 1); }
-        mbar_init(&ctrl->s_full, 1);
+        // TMA: one expect_tx arrival per fill; load/convert warps: one arrival per
+        // warp that writes part of the fill (2 per pair, 4 per rope slot)
+        for (int i = 0; i < C::kRL; ++i) { mbar_init(&ctrl->pair_full[i], LSU ? 2 : 1); mbar_init(&ctrl->pair_empty[i], 1); }
+        for (int i = 0; i < C::kRR; ++i) { mbar_init(&ctrl->rope_full[i], LSU ? 4 : 1); mbar_init(&ctrl->rope_empty[i], 1); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctrl->s_full[i], 1);
+            mbar_init(&ctrl->s_free[i], 1);
+            mbar_init(&ctrl->o_done[i], 1);
+        }
         mbar_init(&ctrl->p_full, 1);
-        mbar_init(&ctrl->o_done, 1);
         mbar_init(&ctrl->q_full, 1);
+        mbar_init(&ctrl->xfull, 1);
+        mbar_init(&ctrl->xfree, 1);
         ctrl->abort = 0;
         fence_mbar_init();
     }
@@ -222,9 +309,12 @@ __global__ void __launch_bounds__(LSU ? 384 : 256, 1)
         tmem_relinquish();
         tc_fence_before();
     }
-    if (!LSU && warp == 1 && lane == 0) prefetch_tensormap(&tmap);
+    if (!LSU && warp == 1 && lane == 0) {
+        prefetch_tensormap(&tmap_lat);
+        prefetch_tensormap(&tmap_rope);
+    }
     if (warp == 2) {
-        // tiles per request, their total, and where this CTA's range starts
+        // tiles per request, their total, and where this cluster's range starts
         long long total = 0;
         for (int base = 0; base < p.B; base += 32) {
             const int b = base + lane;
@@ -273,228 +363,296 @@ __global__ void __launch_bounds__(LSU ? 384 : 256, 1)
         ctrl->m[c] = -INFINITY;
     }
     __syncthreads();
+    cluster_sync_all();  // the peer's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
     const int ntiles = ctrl->t_end - ctrl->t_begin;
 
     if (ntiles > 0) {
         if (warp == 0 && lane == 0) {
-            // ------------------------------------------------------ MMA issuer
+            // -------------------------------------------------- S issuer
+            // S(i) into TMEM buffer i%2 as soon as tile i is in shared memory
+            // and the softmax has read S(i-2) from that buffer.
             TileIt it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint32_t idS = idesc_bf16(128, NP, false, false);
-            const uint32_t idPV = idesc_bf16(128, NP, true, true);
-            const uint32_t q_addr = smem_u32(qs);
-            const uint32_t tS = tmem + C::kColS;
+            const uint64_t dq = smem_desc(smem_u32(qs), 16, 1024, kSw128);
+            const uint64_t dqr = smem_desc(smem_u32(qs) + 4 * NP * 128, 16, 512, kSw64);
             int seg = 0;
             for (int i = 0; i < ntiles; ++i) {
-                const bool new_seg = (i == 0) || (it.j == 0);
-                if (new_seg) {
-                    if (!mbar_wait(&ctrl->q_full, seg & 1, &ctrl->abort)) { fail(p, ctrl, kErrWaitTimeout); break; }
+                if (i == 0 || it.j == 0) {
+                    if (!mbar_wait(&ctrl->q_full, seg & 1, &ctrl->abort)) {
+                        fail(p, ctrl, kErrWaitTimeout, kSiteQFull, i);
+                        report(p, kRoleS, kSiteQFull, i);
+                        break;
+                    }
                     ++seg;
                 }
+                if (i >= 2 && !mbar_wait(&ctrl->s_free[i & 1], ((i - 2) >> 1) & 1, &ctrl->abort)) {
+                    fail(p, ctrl, kErrWaitTimeout, kSiteSFree, i);
+                    report(p, kRoleS, kSiteSFree, i);
+                    break;
+                }
+                const uint32_t tS = tmem + C::kColS + (i & 1) * NP;
                 bool ok = true;
-                for (int pp = 0; pp < 4 && ok; ++pp) {
-                    const int u = 4 * i + pp, slot = u % C::kRL;
+                int site = kSitePairFull;
+                for (int pp = 0; pp < 2 && ok; ++pp) {
+                    const int u = 2 * i + pp, slot = u % C::kRL;
                     if (!mbar_wait(&ctrl->pair_full[slot], (u / C::kRL) & 1, &ctrl->abort)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t base = smem_u32(pair_ring + slot * C::kPairBytes);
+                    if (pp == 0) MLA_TRACE_POINT(i, kTrSPair0);
+                    const uint64_t da = smem_desc(smem_u32(pair_ring + slot * C::kPairBytes), 16, 1024, kSw128);
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = smem_desc(base + c * 16384 + kk * 32, 16, 1024, kSw128);
-                            const uint64_t bq = smem_desc(q_addr + (2 * pp + c) * NP * 128 + kk * 32, 16, 1024, kSw128);
-                            umma_bf16(tS, a, bq, idS, (pp | c | kk) != 0);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_bf16(tS, da + ((c * 16384 + kk * 32) >> 4), dq + (((2 * pp + c) * NP * 128 + kk * 32) >> 4),
+                                      idS, (pp | c | kk) != 0);
                 }
                 const int rr = i % C::kRR;
-                if (ok && !mbar_wait(&ctrl->rope_full[rr], (i / C::kRR) & 1, &ctrl->abort)) ok = false;
-                if (!ok) { fail(p, ctrl, kErrWaitTimeout); break; }
-                tc_fence_after();
-                const uint32_t rbase = smem_u32(rope_ring + rr * C::kRopeBytes);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a = smem_desc(rbase + kk * 32, 16, 1024, kSw128);
-                    const uint64_t bq = smem_desc(q_addr + 8 * NP * 128 + kk * 32, 16, 1024, kSw128);
-                    umma_bf16(tS, a, bq, idS, 1u);
+                if (ok && !mbar_wait(&ctrl->rope_full[rr], (i / C::kRR) & 1, &ctrl->abort)) {
+                    ok = false;
+                    site = kSiteRopeFull;
                 }
-                umma_commit(&ctrl->s_full);
-                if (!C::kPInRope) umma_commit(&ctrl->rope_empty[rr]);
-
-                if (!mbar_wait(&ctrl->p_full, i & 1, &ctrl->abort)) { fail(p, ctrl, kErrWaitTimeout); break; }
-                tc_fence_after();
-                const uint32_t paddr = C::kPInRope ? rbase : smem_u32(pbuf);
-                constexpr uint32_t p_sbo = 8 * NP * 2;
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
-                    const int slot = (4 * i + mt) % C::kRL;
-                    const uint32_t base = smem_u32(pair_ring + slot * C::kPairBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = smem_desc(base + kk * 2048, 16384, 1024, kSw128);
-                        const uint64_t bp = smem_desc(paddr + kk * 16 * NP * 2, p_sbo, p_sbo, C::kPSwizzle);
-                        umma_bf16(tmem + mt * NP, a, bp, idPV, (new_seg && kk == 0) ? 0u : 1u);
-                    }
-                    umma_commit(&ctrl->pair_empty[slot]);
+                if (!ok) {
+                    fail(p, ctrl, kErrWaitTimeout, site, i);
+                    report(p, kRoleS, site, i);
+                    break;
                 }
-                if (C::kPInRope) umma_commit(&ctrl->rope_empty[rr]);
-                umma_commit(&ctrl->o_done);
+                tc_fence_after();
+                MLA_TRACE_POINT(i, kTrSAllIn);
+                const uint64_t dr = smem_desc(smem_u32(rope_ring + rr * C::kRopeBytes), 16, 512, kSw64);
+                umma_bf16(tS, dr, dqr, idS, 1u);
+                umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
+                umma_commit(&ctrl->s_full[i & 1]);
+                umma_commit(&ctrl->rope_empty[rr]);
+                MLA_TRACE_POINT(i, kTrSIssued);
                 it.next(p.seq_lens, p.B);
             }
-        } else if (!LSU && warp == 1 && lane == 0) {
+        } else if (warp == 3 && lane == 0) {
+            // ------------------------------------------------- PV issuer
+            TileIt it;
+            it.init(p.seq_lens, ctrl->b0, ctrl->j0);
+            const uint32_t idPV = idesc_bf16(128, NP, true, true);
+            constexpr uint32_t p_sbo = 8 * NP * 2;
+            for (int i = 0; i < ntiles; ++i) {
+                const bool new_seg = (i == 0) || (it.j == 0);
+                if (!mbar_wait(&ctrl->p_full, i & 1, &ctrl->abort)) {
+                    fail(p, ctrl, kErrWaitTimeout, kSitePFull, i);
+                    report(p, kRolePV, kSitePFull, i);
+                    break;
+                }
+                tc_fence_after();
+                MLA_TRACE_POINT(i, kTrPvIssue);
+                const uint64_t dp = smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), p_sbo, p_sbo, C::kPSwizzle);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int slot = (2 * i + mt) % C::kRL;
+                    const uint64_t da = smem_desc(smem_u32(pair_ring + slot * C::kPairBytes), 16384, 1024, kSw128);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16(tmem + mt * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
+                                  (new_seg && kk == 0) ? 0u : 1u);
+                    umma_commit(&ctrl->pair_empty[slot]);
+                }
+                umma_commit(&ctrl->o_done[i & 1]);
+                MLA_TRACE_POINT(i, kTrPvIssued);
+                it.next(p.seq_lens, p.B);
+            }
+        } else if (!LSU && warp == 1) {
             // ------------------------------------------------- TMA producer
+            // Lane r owns run r of the tile (a page-contiguous run of BR rows).
             TileIt it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint64_t pol = l2_policy_evict_first();
             const int BR = p.run_rows;
             bool bad = false, ok = true;
+            int fsite = 0, ftile = 0;
             for (int i = 0; i < ntiles && ok; ++i) {
                 const int valid = min(kTile, it.T - it.j * kTile);
                 const int nruns = (valid + BR - 1) / BR;
                 const int32_t* btr = p.block_table + static_cast<int64_t>(it.b) * p.bt_stride;
-                int ys[16];
-                for (int r = 0; r < nruns; ++r)
-                    ys[r] = static_cast<int>(token_slot(p, btr, it.j * kTile + r * BR, bad));
-                const uint32_t bytes = static_cast<uint32_t>(nruns * BR * 128);
-                for (int pp = 0; pp < 4; ++pp) {
-                    const int u = 4 * i + pp, slot = u % C::kRL;
-                    if (u >= C::kRL && !mbar_wait(&ctrl->pair_empty[slot], ((u / C::kRL) - 1) & 1, &ctrl->abort)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&ctrl->pair_full[slot], 2 * bytes);
-                    uint8_t* dst = pair_ring + slot * C::kPairBytes;
-                    for (int r = 0; r < nruns; ++r)
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            tma_load_2d(dst + c * 16384 + r * BR * 128, &tmap, &ctrl->pair_full[slot],
-                                        128 * pp + 64 * c, ys[r], pol);
-                }
-                if (!ok) break;
-                const int rr = i % C::kRR;
-                if (i >= C::kRR && !mbar_wait(&ctrl->rope_empty[rr], ((i / C::kRR) - 1) & 1, &ctrl->abort)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&ctrl->rope_full[rr], bytes);
-                for (int r = 0; r < nruns; ++r)
-                    tma_load_2d(rope_ring + rr * C::kRopeBytes + r * BR * 128, &tmap, &ctrl->rope_full[rr], 512,
-                                ys[r], pol);
-                it.next(p.seq_lens, p.B);
-            }
-            if (!ok) fail(p, ctrl, kErrWaitTimeout);
-            if (bad) atomicOr(p.status, kErrBadBlock);
-        } else if (LSU && warp >= 8) {
-            // ------------------------------------- load/convert producers
-            const int pw = warp - 8;
-            TileIt it;
-            it.init(p.seq_lens, ctrl->b0, ctrl->j0);
-            int ti = 0;
-            bool bad = false, ok = true;
-            const int rb = KIND == 0 ? kRowBf16 : kRowFp8;
-            for (int f = pw; f < ntiles * 5 && ok; f += 4) {
-                const int i = f / 5, k = f - 5 * (f / 5);
-                while (ti < i) { it.next(p.seq_lens, p.B); ++ti; }
-                const int valid = min(kTile, it.T - it.j * kTile);
-                const int32_t* btr = p.block_table + static_cast<int64_t>(it.b) * p.bt_stride;
-                uint64_t* full;
-                uint8_t* dst;
-                if (k < 4) {
-                    const int u = 4 * i + k, slot = u % C::kRL;
+                const int y = lane < nruns ? static_cast<int>(token_slot(p, btr, it.j * kTile + lane * BR, bad)) : 0;
+                const uint32_t chunk_bytes = static_cast<uint32_t>(nruns * BR * 128);
+                if (lane == 0) MLA_TRACE_POINT(i, kTrProdStart);
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int u = 2 * i + pp, slot = u % C::kRL;
                     if (u >= C::kRL &&
                         !__all_sync(0xffffffffu, mbar_wait(&ctrl->pair_empty[slot], ((u / C::kRL) - 1) & 1, &ctrl->abort))) {
                         ok = false;
+                        fsite = kSiteTmaPairEmpty;
+                        ftile = i;
                         break;
                     }
-                    full = &ctrl->pair_full[slot];
-                    dst = pair_ring + slot * C::kPairBytes;
-                    if (KIND == 0) {
-                        // 16 units of 16 B per token: dims [128k, 128k+128)
-                        for (int q0 = 0; q0 < valid * 16; q0 += 128) {
-                            uint4 v[4];
-                            int tl[4], uu[4];
+                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->pair_full[slot], 2 * chunk_bytes);
+                    __syncwarp();
+                    if (lane < nruns) {
+                        uint8_t* dst = pair_ring + slot * C::kPairBytes + lane * BR * 128;
 #pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                const int q = q0 + s * 32 + lane;
-                                tl[s] = q >> 4;
-                                uu[s] = q & 15;
-                                if (tl[s] < valid) {
-                                    const int64_t slot64 = token_slot(p, btr, it.j * kTile + tl[s], bad);
-                                    v[s] = __ldg(reinterpret_cast<const uint4*>(p.cache + slot64 * rb + k * 256) + uu[s]);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_2d(dst + c * 16384, &tmap_lat, &ctrl->pair_full[slot], 256 * rank + 128 * pp + 64 * c,
+                                        y, pol);
+                    }
+                }
+                if (!ok) break;
+                const int rr = i % C::kRR;
+                if (i >= C::kRR &&
+                    !__all_sync(0xffffffffu, mbar_wait(&ctrl->rope_empty[rr], ((i / C::kRR) - 1) & 1, &ctrl->abort))) {
+                    ok = false;
+                    fsite = kSiteTmaRopeEmpty;
+                    ftile = i;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], chunk_bytes / 2);
+                __syncwarp();
+                if (lane < nruns)
+                    tma_load_2d(rope_ring + rr * C::kRopeBytes + lane * BR * 64, &tmap_rope, &ctrl->rope_full[rr],
+                                512 + 32 * rank, y, pol);
+                if (lane == 0) MLA_TRACE_POINT(i, kTrProdIssued);
+                it.next(p.seq_lens, p.B);
+            }
+            if (!ok && lane == 0) {
+                fail(p, ctrl, kErrWaitTimeout, fsite, ftile);
+                report(p, kRoleTma, fsite, ftile);
+            }
+            if (bad) atomicOr(p.status, kErrBadBlock);
+        } else if (LSU && warp >= 8) {
+            // ------------------------------------- load/convert producers
+            // Each warp keeps a fixed, in-order share of every tile: warps 8/9 the
+            // two 64-row halves of pair 0, warps 10/11 those of pair 1, and each a
+            // 32-row quarter of the rope half. Walking the tiles in order, a warp
+            // never waits on a slot more than one phase ahead of its release.
+            // Rows past the request are left stale (the softmax clears them).
+            const int pw = warp - 8;
+            const int pk = pw >> 1, half = pw & 1;
+            TileIt it;
+            it.init(p.seq_lens, ctrl->b0, ctrl->j0);
+            TileIt pf = it;
+            int pf_i = 0;
+            bool bad = false, ok = true;
+            const int rb = KIND == 0 ? kRowBf16 : kRowFp8;
+            int fsite = 0, ftile = 0;
+            if (pw == 0 && lane == 0) prefetch_tile(p, pf, rb, rank);
+            for (int i = 0; i < ntiles && ok; ++i) {
+                if (pw == 0 && lane == 0) {
+                    while (pf_i < i + kPrefetchTiles && pf_i + 1 < ntiles) {
+                        pf.next(p.seq_lens, p.B);
+                        ++pf_i;
+                        prefetch_tile(p, pf, rb, rank);
+                    }
+                }
+                const int valid = min(kTile, it.T - it.j * kTile);
+                const int32_t* btr = p.block_table + static_cast<int64_t>(it.b) * p.bt_stride;
+                // ---- pair pk, rows [64*half, 64*half + 64)
+                {
+                    const int u = 2 * i + pk, slot = u % C::kRL;
+                    if (u >= C::kRL &&
+                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->pair_empty[slot], ((u / C::kRL) - 1) & 1, &ctrl->abort))) {
+                        ok = false;
+                        fsite = kSiteLsuPairEmpty;
+                        ftile = i;
+                        break;
+                    }
+                    uint8_t* dst = pair_ring + slot * C::kPairBytes;
+                    const int r0 = 64 * half, r1 = min(64 * half + 64, valid);
+                    if (KIND == 0) {
+                        // 16 units of 16 B per token: dims 256*rank + 128*pk + [0, 128)
+                        for (int q0 = r0 * 16; q0 < r1 * 16; q0 += 256) {
+                            uint4 v[8];
+                            int tl[8], uu[8];
+#pragma unroll
+                            for (int s8 = 0; s8 < 8; ++s8) {
+                                const int q = q0 + s8 * 32 + lane;
+                                tl[s8] = q >> 4;
+                                uu[s8] = q & 15;
+                                if (tl[s8] < r1) {
+                                    const int64_t slot64 = token_slot(p, btr, it.j * kTile + tl[s8], bad);
+                                    v[s8] = __ldg(reinterpret_cast<const uint4*>(p.cache + slot64 * rb + 512 * rank + pk * 256) + uu[s8]);
                                 }
                             }
 #pragma unroll
-                            for (int s = 0; s < 4; ++s)
-                                if (tl[s] < valid) {
-                                    const int c = uu[s] >> 3, un = uu[s] & 7;
-                                    *reinterpret_cast<uint4*>(dst + c * 16384 + tl[s] * 128 + ((un ^ (tl[s] & 7)) << 4)) = v[s];
+                            for (int s8 = 0; s8 < 8; ++s8)
+                                if (tl[s8] < r1) {
+                                    const int c = uu[s8] >> 3, un = uu[s8] & 7;
+                                    *reinterpret_cast<uint4*>(dst + c * 16384 + tl[s8] * 128 + ((un ^ (tl[s8] & 7)) << 4)) = v[s8];
                                 }
                         }
                     } else {
-                        // 8 units of 16 codes per token, block scale k
-                        for (int q0 = 0; q0 < valid * 8; q0 += 128) {
-                            uint4 v[4];
-                            float sc[4];
-                            int tl[4], uu[4];
+                        // quant block 2*rank + pk: 8 units of 16 codes per token and its scale
+                        const int qb = 2 * rank + pk;
+                        for (int q0 = r0 * 8; q0 < r1 * 8; q0 += 256) {
+                            uint4 v[8];
+                            float sc[8];
+                            int tl[8], uu[8];
 #pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                const int q = q0 + s * 32 + lane;
-                                tl[s] = q >> 3;
-                                uu[s] = q & 7;
-                                if (tl[s] < valid) {
-                                    const int64_t slot64 = token_slot(p, btr, it.j * kTile + tl[s], bad);
+                            for (int s8 = 0; s8 < 8; ++s8) {
+                                const int q = q0 + s8 * 32 + lane;
+                                tl[s8] = q >> 3;
+                                uu[s8] = q & 7;
+                                if (tl[s8] < r1) {
+                                    const int64_t slot64 = token_slot(p, btr, it.j * kTile + tl[s8], bad);
                                     const uint8_t* row = p.cache + slot64 * rb;
-                                    v[s] = __ldg(reinterpret_cast<const uint4*>(row + k * 128) + uu[s]);
-                                    sc[s] = __ldg(reinterpret_cast<const float*>(row + 512) + k);
+                                    v[s8] = __ldg(reinterpret_cast<const uint4*>(row + qb * 128) + uu[s8]);
+                                    sc[s8] = __ldg(reinterpret_cast<const float*>(row + 512) + qb);
                                 }
                             }
 #pragma unroll
-                            for (int s = 0; s < 4; ++s)
-                                if (tl[s] < valid) {
+                            for (int s8 = 0; s8 < 8; ++s8)
+                                if (tl[s8] < r1) {
                                     uint4 lo, hi;
-                                    dequant16(v[s], sc[s], lo, hi);
-                                    const int c = uu[s] >> 2, un = (uu[s] & 3) * 2;
-                                    uint8_t* rowp = dst + c * 16384 + tl[s] * 128;
-                                    *reinterpret_cast<uint4*>(rowp + ((un ^ (tl[s] & 7)) << 4)) = lo;
-                                    *reinterpret_cast<uint4*>(rowp + (((un + 1) ^ (tl[s] & 7)) << 4)) = hi;
+                                    dequant16(v[s8], sc[s8], lo, hi);
+                                    const int c = uu[s8] >> 2, un = (uu[s8] & 3) * 2;
+                                    uint8_t* rowp = dst + c * 16384 + tl[s8] * 128;
+                                    *reinterpret_cast<uint4*>(rowp + ((un ^ (tl[s8] & 7)) << 4)) = lo;
+                                    *reinterpret_cast<uint4*>(rowp + (((un + 1) ^ (tl[s8] & 7)) << 4)) = hi;
                                 }
                         }
                     }
-                } else {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctrl->pair_full[slot]);
+                }
+                // ---- rope half, rows [32*pw, 32*pw + 32)
+                {
                     const int rr = i % C::kRR;
                     if (i >= C::kRR &&
                         !__all_sync(0xffffffffu, mbar_wait(&ctrl->rope_empty[rr], ((i / C::kRR) - 1) & 1, &ctrl->abort))) {
                         ok = false;
+                        fsite = kSiteLsuRopeEmpty;
+                        ftile = i;
                         break;
                     }
-                    full = &ctrl->rope_full[rr];
-                    dst = rope_ring + rr * C::kRopeBytes;
-                    const int roff = KIND == 0 ? 1024 : 528;
-                    for (int q0 = 0; q0 < valid * 8; q0 += 128) {
+                    uint8_t* dst = rope_ring + rr * C::kRopeBytes;
+                    const int roff = (KIND == 0 ? 1024 : 528) + 64 * rank;
+                    const int r0 = 32 * pw, r1 = min(32 * pw + 32, valid);
+                    for (int q0 = r0 * 4; q0 < r1 * 4; q0 += 128) {
                         uint4 v[4];
                         int tl[4], uu[4];
 #pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            const int q = q0 + s * 32 + lane;
-                            tl[s] = q >> 3;
-                            uu[s] = q & 7;
-                            if (tl[s] < valid) {
-                                const int64_t slot64 = token_slot(p, btr, it.j * kTile + tl[s], bad);
-                                v[s] = __ldg(reinterpret_cast<const uint4*>(p.cache + slot64 * rb + roff) + uu[s]);
+                        for (int s4 = 0; s4 < 4; ++s4) {
+                            const int q = q0 + s4 * 32 + lane;
+                            tl[s4] = q >> 2;
+                            uu[s4] = q & 3;
+                            if (tl[s4] < r1) {
+                                const int64_t slot64 = token_slot(p, btr, it.j * kTile + tl[s4], bad);
+                                v[s4] = __ldg(reinterpret_cast<const uint4*>(p.cache + slot64 * rb + roff) + uu[s4]);
                             }
                         }
 #pragma unroll
-                        for (int s = 0; s < 4; ++s)
-                            if (tl[s] < valid)
-                                *reinterpret_cast<uint4*>(dst + tl[s] * 128 + ((uu[s] ^ (tl[s] & 7)) << 4)) = v[s];
+                        for (int s4 = 0; s4 < 4; ++s4)
+                            if (tl[s4] < r1)
+                                *reinterpret_cast<uint4*>(dst + tl[s4] * 64 + ((uu[s4] ^ ((tl[s4] >> 1) & 3)) << 4)) = v[s4];
                     }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctrl->rope_full[rr]);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full);
+                it.next(p.seq_lens, p.B);
             }
-            if (!ok && lane == 0) fail(p, ctrl, kErrWaitTimeout);
+            if (!ok && lane == 0) {
+                fail(p, ctrl, kErrWaitTimeout, fsite, ftile);
+                report(p, kRoleLsu0 + pw, fsite, ftile);
+            }
             if (bad) atomicOr(p.status, kErrBadBlock);
         } else if (warp >= 4 && warp < 8) {
             // ------------------------------------------ softmax + epilogue
@@ -502,6 +660,14 @@ __global__ void __launch_bounds__(LSU ? 384 : 256, 1)
             const int sw = warp - 4;
             const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
             const int HQg = min(64, p.HQ - gy * 64);
+            const int peer = rank ^ 1;
+            const uint32_t x_local = smem_u32(xbuf);
+            const uint32_t x_peer = mapa_shared(x_local, peer);
+            const uint32_t xfull_peer = mapa_shared(smem_u32(&ctrl->xfull), peer);
+            constexpr uint32_t kXferBytes = 128 * NP * 4;
+            const uint32_t xfree_peer = mapa_shared(smem_u32(&ctrl->xfree), peer);
+            // 16-byte unit swizzle of the exchange rows (NP/4 units per row)
+            const int xs = (NP == 16) ? ((st >> 1) & 3) : (st & 7);
             TileIt it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             float l[NP];
@@ -509,38 +675,135 @@ __global__ void __launch_bounds__(LSU ? 384 : 256, 1)
             for (int c = 0; c < NP; ++c) l[c] = 0.f;
             int seg_start_j = it.j;
             bool seg_has_pv = false;
-            load_q<NP>(p, it.b, gy, qs, st);
+            // the segment whose output is still in TMEM: written once its last PV is done
+            bool epi_pending = false;
+            bool epi_final = false;
+            int epi_b = 0;
+
+            auto epilogue = [&]() {
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    const float v = warp_sum(l[c]);
+                    if (lane == 0) ctrl->red[sw][c] = v;
+                }
+                named_bar_sync(1, 128);
+                const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + epi_b;
+                __syncwarp();
+#pragma unroll 1
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int d = 256 * rank + mt * 128 + st;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < NP && c0 < HQg; c0 += 16) {
+                        uint32_t o[16];
+                        tmem_ld_x16(tmem + lane_base + mt * NP + c0, o);
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc) {
+                            const int c = c0 + cc;
+                            if (c >= HQg) break;
+                            const float lt = ctrl->red[0][c] + ctrl->red[1][c] + ctrl->red[2][c] + ctrl->red[3][c];
+                            const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
+                            if (epi_final) {
+                                const int64_t idx = (static_cast<int64_t>(epi_b) * p.HQ + gy * 64 + c) * kD + d;
+                                if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
+                                else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+                            } else {
+                                p.part_o[(pslot * 64 + c) * kD + d] = v;
+                            }
+                        }
+                    }
+                }
+                if (rank == 0 && st < HQg) {
+                    const float lt = ctrl->red[0][st] + ctrl->red[1][st] + ctrl->red[2][st] + ctrl->red[3][st];
+                    const float lv = lt > 0.f ? (ctrl->m[st] + log2f(lt)) * kLn2 : -INFINITY;
+                    if (epi_final) p.lse[static_cast<int64_t>(epi_b) * p.HQ + gy * 64 + st] = lv;
+                    else p.part_lse[pslot * 64 + st] = lv;
+                }
+                tc_fence_before();
+                named_bar_sync(1, 128);
+                if (st < NP) ctrl->m[st] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < NP; ++c) l[c] = 0.f;
+                named_bar_sync(1, 128);
+            };
+
+            load_q<NP>(p, it.b, gy, rank, qs, st);
             fence_proxy_async_smem();
             named_bar_sync(1, 128);
             if (st == 0) mbar_arrive(&ctrl->q_full);
+            bool alive = true;
             for (int i = 0; i < ntiles; ++i) {
                 const int b = it.b, j = it.j, T = it.T;
                 const bool last_of_seg = (j == it.tiles - 1) || (i == ntiles - 1);
-                if (!group_wait(&ctrl->s_full, i & 1, p, ctrl)) break;
+                if (epi_pending) {
+                    // the previous segment ended with tile i-1: write it out once its PV is done
+                    if (!group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteOEpi, i)) { alive = false; break; }
+                    tc_fence_after();
+                    epilogue();
+                    epi_pending = false;
+                    seg_has_pv = false;
+                }
+                if (!group_wait(&ctrl->s_full[i & 1], (i >> 1) & 1, p, ctrl, kSiteSFull, i)) { alive = false; break; }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmSFull);
                 tc_fence_after();
                 __syncwarp();
                 uint32_t sr[NP];
-                tmem_ld_np<NP>(tmem + lane_base + C::kColS, sr);
+                tmem_ld_np<NP>(tmem + lane_base + C::kColS + (i & 1) * NP, sr);
+                tc_fence_before();
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmTmemLd);
                 if (last_of_seg && i + 1 < ntiles) {
-                    // S of this tile is complete, so Q may be replaced by the next request's
+                    // S(i) is complete, so Q may be replaced by the next request's
                     TileIt nx = it;
                     nx.next(p.seq_lens, p.B);
-                    load_q<NP>(p, nx.b, gy, qs, st);
+                    load_q<NP>(p, nx.b, gy, rank, qs, st);
                     fence_proxy_async_smem();
                     named_bar_sync(1, 128);
                     if (st == 0) mbar_arrive(&ctrl->q_full);
                 }
+                // send this CTA's partial scores once the peer has read the last ones
+                if (i > 0 && !group_wait(&ctrl->xfree, (i - 1) & 1, p, ctrl, kSiteXFree, i, true)) { alive = false; break; }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmXFree);
+                // (every thread has read S(i) from TMEM: the buffer may be reused)
+                if (st == 0) mbar_arrive(&ctrl->s_free[i & 1]);
+#pragma unroll
+                for (int u = 0; u < NP / 4; ++u)
+                    st_async_v4(x_peer + st * NP * 4 + ((u ^ xs) << 4), sr[4 * u], sr[4 * u + 1], sr[4 * u + 2],
+                                sr[4 * u + 3], xfull_peer);
+                if (st == 0) mbar_arrive_expect_tx(&ctrl->xfull, kXferBytes);
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmSent);
+                if (!group_wait(&ctrl->xfull, i & 1, p, ctrl, kSiteXFull, i, true)) { alive = false; break; }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmXFull);
+                float x[NP];
+#pragma unroll
+                for (int u = 0; u < NP / 4; ++u) {
+                    const float4 v = *reinterpret_cast<const float4*>(xbuf + st * NP * 4 + ((u ^ xs) << 4));
+                    x[4 * u] = __uint_as_float(sr[4 * u]) + v.x;
+                    x[4 * u + 1] = __uint_as_float(sr[4 * u + 1]) + v.y;
+                    x[4 * u + 2] = __uint_as_float(sr[4 * u + 2]) + v.z;
+                    x[4 * u + 3] = __uint_as_float(sr[4 * u + 3]) + v.w;
+                }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmXRead);
+
                 const int tok = j * kTile + st;
                 const bool all_vis = (j * kTile + kTile + p.Qt - 1) <= T;
-                float x[NP];
+                const float4* m4 = reinterpret_cast<const float4*>(ctrl->m);
                 int need = 0;
 #pragma unroll
-                for (int c = 0; c < NP; ++c) {
-                    const bool v = all_vis ? (c < HQg) : (tok + ctrl->colvis[c] < T);
-                    x[c] = v ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-                    need |= (x[c] > ctrl->m[c] + kRescaleThreshold) ? 1 : 0;
+                for (int u = 0; u < NP / 4; ++u) {
+                    const float4 mv = m4[u];
+                    const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = 4 * u + k;
+                        const bool v = all_vis ? (c < HQg) : (tok + ctrl->colvis[c] < T);
+                        x[c] = v ? x[c] * p.scale_log2 : -INFINITY;
+                        need |= (x[c] > mm[k] + kRescaleThreshold) ? 1 : 0;
+                    }
                 }
+                // (also: every thread has read the exchange buffer; hand it back to the peer)
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmMath);
                 need = named_bar_or(2, 128, need);
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmBarOr);
+                if (st == 0) mbar_arrive_remote(xfree_peer);
                 if (need) {
 #pragma unroll
                     for (int c = 0; c < NP; ++c) {
@@ -560,29 +823,50 @@ __global__ void __launch_bounds__(LSU ? 384 : 256, 1)
 #pragma unroll
                     for (int c = 0; c < NP; ++c) l[c] *= ctrl->alpha[c];
                     if (seg_has_pv) {
-                        // O holds earlier tiles of this segment: wait for the last PV, rescale
-                        if (!group_wait(&ctrl->o_done, (i - 1) & 1, p, ctrl)) break;
+                        // O holds earlier tiles of this segment: wait for their PV, rescale
+                        if (!group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i)) { alive = false; break; }
                         tc_fence_after();
                         __syncwarp();
 #pragma unroll 1
-                        for (int mt = 0; mt < 4; ++mt) {
-                            uint32_t o[NP];
-                            tmem_ld_np<NP>(tmem + lane_base + mt * NP, o);
+                        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll 1
+                            for (int c0 = 0; c0 < NP; c0 += 16) {
+                                uint32_t o[16];
+                                tmem_ld_x16(tmem + lane_base + mt * NP + c0, o);
 #pragma unroll
-                            for (int c = 0; c < NP; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * ctrl->alpha[c]);
-                            tmem_st_np<NP>(tmem + lane_base + mt * NP, o);
-                        }
+                                for (int cc = 0; cc < 16; ++cc)
+                                    o[cc] = __float_as_uint(__uint_as_float(o[cc]) * ctrl->alpha[c0 + cc]);
+                                tmem_st_x16(tmem + lane_base + mt * NP + c0, o);
+                            }
                         tmem_wait_st();
                     }
                 }
 #pragma unroll
-                for (int c = 0; c < NP; ++c) {
-                    const float pc = (x[c] == -INFINITY) ? 0.f : ex2(x[c] - ctrl->m[c]);
-                    l[c] += pc;
-                    x[c] = pc;
+                for (int u = 0; u < NP / 4; ++u) {
+                    const float4 mv = m4[u];
+                    const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = 4 * u + k;
+                        const float pc = (x[c] == -INFINITY) ? 0.f : ex2(x[c] - mm[k]);
+                        l[c] += pc;
+                        x[c] = pc;
+                    }
                 }
-                // P row `st`: NP bf16, MN-major, swizzled like the MMA reads it
-                uint8_t* prow = (C::kPInRope ? rope_ring + (i % C::kRR) * C::kRopeBytes : pbuf) + st * NP * 2;
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmExpLoop);
+                // The P buffer of this tile was last read by PV(i - kPBufs). Each warp
+                // writes its own 32 rows, so one lane per warp waits; on a timeout the
+                // warp carries on to the next group barrier, which then fails for all.
+                if (i >= C::kPBufs) {
+                    const int jp = i - C::kPBufs;
+                    bool okp = true;
+                    if (lane == 0) okp = !ctrl->abort && mbar_wait(&ctrl->o_done[jp & 1], (jp >> 1) & 1, &ctrl->abort);
+                    okp = __shfl_sync(0xffffffffu, okp ? 1 : 0, 0) != 0;
+                    if (!okp && lane == 0) fail(p, ctrl, kErrWaitTimeout, kSiteOPbuf, i);
+                }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmExp);
+                // P row `st`: NP bf16, MN-major, swizzled as the MMA reads it
+                uint8_t* prow = pbufs + (i % C::kPBufs) * C::kPBytes + st * NP * 2;
                 const int sz = swz_p(st, C::kPSwizzle);
 #pragma unroll
                 for (int u = 0; u < NP / 8; ++u) {
@@ -591,75 +875,45 @@ __global__ void __launch_bounds__(LSU ? 384 : 256, 1)
                     *reinterpret_cast<uint4*>(prow + ((u ^ sz) << 4)) = v;
                 }
                 if (tok >= T) {
-                    // rows past the request hold stale data (possibly NaN); P is 0
-                    // there, but 0 * NaN would still poison O, so clear them
+                    // rows past the request hold stale data (maybe NaN); P is 0 there,
+                    // but 0 * NaN would still poison O, so clear them
                     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                    for (int pp = 0; pp < 4; ++pp) {
-                        uint8_t* ps = pair_ring + ((4 * i + pp) % C::kRL) * C::kPairBytes + st * 128;
+                    for (int pp = 0; pp < 2; ++pp) {
+                        uint8_t* ps = pair_ring + ((2 * i + pp) % C::kRL) * C::kPairBytes + st * 128;
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
 #pragma unroll
                             for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(ps + c * 16384 + u * 16) = z;
                     }
                 }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmPStore);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(1, 128);
-                if (st == 0) mbar_arrive(&ctrl->p_full);
+                if (st == 0) {
+                    MLA_TRACE_POINT(i, kTrSmPArrive);
+                    mbar_arrive(&ctrl->p_full);
+                }
                 seg_has_pv = true;
-
                 if (last_of_seg) {
-                    // ------------------------------------------- epilogue
-                    if (!group_wait(&ctrl->o_done, i & 1, p, ctrl)) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < NP; ++c) {
-                        const float v = warp_sum(l[c]);
-                        if (lane == 0) ctrl->red[sw][c] = v;
-                    }
-                    named_bar_sync(1, 128);
-                    const bool final_seg = (seg_start_j == 0) && (j == it.tiles - 1);
-                    __syncwarp();
-                    const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + b;
-#pragma unroll 1
-                    for (int mt = 0; mt < 4; ++mt) {
-                        uint32_t o[NP];
-                        tmem_ld_np<NP>(tmem + lane_base + mt * NP, o);
-                        const int d = mt * 128 + st;
-#pragma unroll
-                        for (int c = 0; c < NP; ++c) {
-                            if (c >= HQg) break;
-                            const float lt = ctrl->red[0][c] + ctrl->red[1][c] + ctrl->red[2][c] + ctrl->red[3][c];
-                            const float v = lt > 0.f ? __uint_as_float(o[c]) / lt : 0.f;
-                            if (final_seg) {
-                                const int64_t idx = (static_cast<int64_t>(b) * p.HQ + gy * 64 + c) * kD + d;
-                                if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
-                                else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
-                            } else {
-                                p.part_o[(pslot * 64 + c) * kD + d] = v;
-                            }
-                        }
-                    }
-                    if (st < HQg) {
-                        const float lt = ctrl->red[0][st] + ctrl->red[1][st] + ctrl->red[2][st] + ctrl->red[3][st];
-                        const float lv = lt > 0.f ? (ctrl->m[st] + log2f(lt)) * kLn2 : -INFINITY;
-                        if (final_seg) p.lse[static_cast<int64_t>(b) * p.HQ + gy * 64 + st] = lv;
-                        else p.part_lse[pslot * 64 + st] = lv;
-                    }
-                    tc_fence_before();
-                    named_bar_sync(1, 128);
-                    if (st < NP) ctrl->m[st] = -INFINITY;
-#pragma unroll
-                    for (int c = 0; c < NP; ++c) l[c] = 0.f;
-                    named_bar_sync(1, 128);
-                    seg_has_pv = false;
+                    epi_pending = true;
+                    epi_final = (seg_start_j == 0) && (j == it.tiles - 1);
+                    epi_b = b;
                     seg_start_j = 0;
                 }
                 it.next(p.seq_lens, p.B);
             }
+            if (alive && epi_pending) {
+                const int il = ntiles - 1;
+                if (group_wait(&ctrl->o_done[il & 1], (il >> 1) & 1, p, ctrl, kSiteOFinal, il)) {
+                    tc_fence_after();
+                    epilogue();
+                }
+            }
         }
     }
     __syncthreads();
+    cluster_sync_all();  // no remote traffic into this CTA after here
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
@@ -669,15 +923,15 @@ __global__ void __launch_bounds__(LSU ? 384 : 256, 1)
 
 // ---------------------------------------------------------------- merging
 
-// Merge `nseg` partials of one row: out = sum_i w_i o_i with
-// w_i = exp(lse_i - L), L = ln sum exp(lse_i); all -inf -> (0, -inf).
-// One warp; lane owns dims 4*lane + 128*k, k = 0..3.
-// CTA g of G got tiles [g*tot/G, (g+1)*tot/G); with more CTAs than tiles some
-// ranges are empty and wrote no partial. tot == 0 means "all partials live".
+// Cluster g of G got tiles [g*tot/G, (g+1)*tot/G); with more clusters than
+// tiles some ranges are empty and wrote no partial. tot == 0: all live.
 __device__ __forceinline__ bool seg_live(long long tot, int G, long long g) {
     return tot == 0 || (g * tot / G) < ((g + 1) * tot / G);
 }
 
+// Merge `nseg` partials of one row: out = sum_i w_i o_i with
+// w_i = exp(lse_i - L), L = ln sum exp(lse_i); all -inf -> (0, -inf).
+// One warp; lane owns dims 4*lane + 128*k, k = 0..3.
 __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, const float* pl, int64_t l_stride,
                                           int nseg, void* out, int out_f32, float* lse_out, int lane,
                                           long long tot = 0, int G = 1, long long g0 = 0) {
@@ -728,7 +982,7 @@ __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, con
 }
 
 // Per request b (blockIdx.x) and row group (blockIdx.y): merge the partials
-// of a request cut across CTAs, and write (0, -inf) for empty requests.
+// of a request cut across clusters, and write (0, -inf) for empty requests.
 __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParams p, int G) {
     const int b = blockIdx.x, gy = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -759,10 +1013,10 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
         }
         return;
     }
-    // CTA holding tile t: the largest g with floor(g * tot / G) <= t
+    // cluster holding tile t: the largest g with floor(g * tot / G) <= t
     const long long g0 = ((pre + 1) * G - 1) / tot;
     const long long g1 = ((pre + tiles_b) * G - 1) / tot;
-    if (g0 == g1) return;  // one CTA held the whole request and wrote the output
+    if (g0 == g1) return;  // one cluster held the whole request and wrote the output
     const int nseg = static_cast<int>(g1 - g0 + 1);
     const int64_t slot0 = static_cast<int64_t>(gy) * p.SPG + g0 + b;
     for (int n = warp; n < HQg; n += 8) {
@@ -787,37 +1041,63 @@ __global__ void __launch_bounds__(256) mla_merge_lse_kernel(const float* __restr
 // ------------------------------------------------------------------ launch
 
 template <int NP, bool LSU, int KIND>
-static cudaError_t launch_variant(const CUtensorMap& tmap, const DecodeParams& p, int G, int GY, cudaStream_t stream) {
-    using C = Cfg<NP>;
-    auto kern = mla_decode_kernel<NP, LSU, KIND>;
-    static int attr_done[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = 1;
+struct Variant {
+    static constexpr int kThreads = LSU ? 384 : 256;
+
+    // Set the shared-memory attribute (once per device) and return how many
+    // clusters of 2 fit on the device at once.
+    static int max_clusters() {
+        static int done[64] = {0};
+        static int clusters[64] = {0};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return -1;
+        if (!done[dev]) {
+            auto k = mla_decode_kernel<NP, LSU, KIND>;
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NP>::kSmemBytes) != cudaSuccess)
+                return -1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2, 1, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = Cfg<NP>::kSmemBytes;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) return -1;
+            clusters[dev] = n;
+            done[dev] = 1;
+        }
+        return clusters[dev];
     }
-    kern<<<dim3(G, GY), LSU ? 384 : 256, C::kSmemBytes, stream>>>(tmap, p);
-    return cudaGetLastError();
+
+    static cudaError_t launch(const CUtensorMap& tl, const CUtensorMap& tr, const DecodeParams& p, int G, int GY,
+                              cudaStream_t stream) {
+        mla_decode_kernel<NP, LSU, KIND><<<dim3(2 * G, GY), kThreads, Cfg<NP>::kSmemBytes, stream>>>(tl, tr, p);
+        return cudaGetLastError();
+    }
+};
+
+template <typename V>
+static int pick_clusters(int requested_ctas) {
+    const int mx = V::max_clusters();
+    if (mx <= 0) return -1;
+    if (requested_ctas <= 0) return mx;
+    return max(1, requested_ctas / 2);
 }
 
-cudaError_t launch_decode(const CUtensorMap& tmap, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,
-                          cudaStream_t stream) {
-    cudaError_t e;
-    if (kind == 1) {
-        e = NP == 16 ? launch_variant<16, true, 1>(tmap, p, G, GY, stream)
-          : NP == 32 ? launch_variant<32, true, 1>(tmap, p, G, GY, stream)
-                     : launch_variant<64, true, 1>(tmap, p, G, GY, stream);
-    } else if (lsu) {
-        e = NP == 16 ? launch_variant<16, true, 0>(tmap, p, G, GY, stream)
-          : NP == 32 ? launch_variant<32, true, 0>(tmap, p, G, GY, stream)
-                     : launch_variant<64, true, 0>(tmap, p, G, GY, stream);
-    } else {
-        e = NP == 16 ? launch_variant<16, false, 0>(tmap, p, G, GY, stream)
-          : NP == 32 ? launch_variant<32, false, 0>(tmap, p, G, GY, stream)
-                     : launch_variant<64, false, 0>(tmap, p, G, GY, stream);
-    }
+#define MLA_DISPATCH(NPV, EXPR)                                                                         \
+    (kind == 1 ? (NPV == 16 ? EXPR(16, true, 1) : NPV == 32 ? EXPR(32, true, 1) : EXPR(64, true, 1)) \
+     : lsu     ? (NPV == 16 ? EXPR(16, true, 0) : NPV == 32 ? EXPR(32, true, 0) : EXPR(64, true, 0)) \
+               : (NPV == 16 ? EXPR(16, false, 0) : NPV == 32 ? EXPR(32, false, 0) : EXPR(64, false, 0)))
+
+int decode_clusters(int NP, bool lsu, int kind, int requested_ctas) {
+#define MLA_PICK(a, b, c) pick_clusters<Variant<a, b, c>>(requested_ctas)
+    return MLA_DISPATCH(NP, MLA_PICK);
+#undef MLA_PICK
+}
+
+cudaError_t launch_decode(const CUtensorMap& tl, const CUtensorMap& tr, const DecodeParams& p, int NP, bool lsu,
+                          int kind, int G, int GY, cudaStream_t stream) {
+#define MLA_LAUNCH(a, b, c) Variant<a, b, c>::launch(tl, tr, p, G, GY, stream)
+    cudaError_t e = MLA_DISPATCH(NP, MLA_LAUNCH);
+#undef MLA_LAUNCH
     if (e != cudaSuccess) return e;
     mla_decode_merge_kernel<<<dim3(p.B, GY), 256, 0, stream>>>(p, G);
     return cudaGetLastError();
@@ -833,3 +1113,9 @@ cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, 
 }
 
 }  // namespace mla
+
+#ifdef MLA_TRACE
+extern "C" __attribute__((visibility("default"))) int mla_trace_dump(void* host) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, mla::g_trace, sizeof(mla::g_trace)));
+}
+#endif

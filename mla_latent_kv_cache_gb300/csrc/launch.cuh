@@ -26,14 +26,17 @@ struct DecodeParams {
     int run_rows;      // TMA box height: gcd(page_size, 128)
     int B, Qt, Hq, HQ; // HQ = Hq * Qt rows per request
     int out_f32;
-    int SPG;           // partial slots per row group = gridDim.x + B
+    int SPG;           // partial slots per row group = clusters + B
 };
 
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
                                const int64_t* slot_mapping, int64_t num_tokens, void* cache, int kind,
                                cudaStream_t stream);
-cudaError_t launch_decode(const CUtensorMap& tmap, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,
-                          cudaStream_t stream);
+// Clusters (of 2 CTAs) the decode kernel variant runs with: the number that
+// fit on the current device at once, or requested_ctas / 2 when given.
+int decode_clusters(int NP, bool lsu, int kind, int requested_ctas);
+cudaError_t launch_decode(const CUtensorMap& tmap_lat, const CUtensorMap& tmap_rope, const DecodeParams& p, int NP,
+                          bool lsu, int kind, int G, int GY, cudaStream_t stream);
 cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, int64_t N, void* out, int out_f32,
                              float* lse, cudaStream_t stream);
 

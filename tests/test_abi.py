@@ -66,10 +66,11 @@ def test_host_validation_rejects_bad_arguments(lib):
 
 
 def test_workspace_size_formula(lib):
-    # header + [groups][ctas + B][64] lse + [groups][ctas + B][64][512] partial outputs
+    # header + [groups][clusters + B][64] lse + [groups][clusters + B][64][512]
+    # partial outputs, with clusters = ctas / 2
     for B, q, H, G in [(2, 1, 8, 152), (64, 1, 16, 152), (128, 4, 16, 152), (3, 1, 80, 7)]:
         gy = -(-(H * q) // 64)
-        slots = gy * (G + B) * 64
+        slots = gy * (max(1, G // 2) + B) * 64
         lse_b = -(-(slots * 4) // 256) * 256
         assert m.mla_decode_workspace_bytes(B, q, H, G) == 256 + lse_b + slots * 512 * 4
     assert lib.mla_decode_workspace_bytes(0, 1, 8, 4) == 0
