@@ -64,9 +64,27 @@ __device__ unsigned long long g_trace[8][64][kTrEvents];
     do {                                                                                          \
         if (blockIdx.y == 0 && blockIdx.x < 8 && (i) < 64) g_trace[blockIdx.x][(i)][(e)] = globaltimer_ns(); \
     } while (0)
+// whole-kernel points per CTA (row group 0): entry, setup done, softmax
+// done, exit; and entry/exit of each merge block
+__device__ unsigned long long g_ktrace[512][4];
+__device__ unsigned long long g_mtrace[512][2];
+#define MLA_KTRACE(e)                                                                  \
+    do {                                                                               \
+        if (blockIdx.y == 0 && blockIdx.x < 512) g_ktrace[blockIdx.x][(e)] = globaltimer_ns(); \
+    } while (0)
+#define MLA_MTRACE(e)                                                                   \
+    do {                                                                                \
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.x < 512) g_mtrace[blockIdx.x][(e)] = globaltimer_ns(); \
+    } while (0)
 #else
 #define MLA_TRACE_POINT(i, e) \
     do {                      \
+    } while (0)
+#define MLA_KTRACE(e) \
+    do {              \
+    } while (0)
+#define MLA_MTRACE(e) \
+    do {              \
     } while (0)
 #endif
 
@@ -186,14 +204,17 @@ __device__ __forceinline__ void report(const DecodeParams& p, int role, int site
         p.status[4 + role] = (site << 24) | (idx & 0xFFFFFF);
 }
 
+// Softmax-group wait. A thread whose wait fails raises the abort flag and
+// carries on (its results no longer matter); the group leaves its tile loop
+// together after the tile's last barrier, where every thread reads the flag.
 __device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, const DecodeParams& p, Ctrl* ctrl,
                                            int site, int tile, bool cluster_scope = false) {
-    bool ok = !ctrl->abort;
-    if (ok) ok = cluster_scope ? mbar_wait_cluster(bar, parity, &ctrl->abort) : mbar_wait(bar, parity, &ctrl->abort);
-    const bool all = named_bar_and(3, 128, ok ? 1 : 0) != 0;
-    if (!ok) fail(p, ctrl, kErrWaitTimeout, site, tile);
-    if (!all && threadIdx.x == 128) report(p, kRoleSoftmax, site, tile);
-    return all;
+    const bool ok = cluster_scope ? mbar_wait_cluster(bar, parity, &ctrl->abort) : mbar_wait(bar, parity, &ctrl->abort);
+    if (!ok) {
+        fail(p, ctrl, kErrWaitTimeout, site, tile);
+        report(p, kRoleSoftmax, site, tile);
+    }
+    return ok;
 }
 
 // This CTA's half of the NP query rows of request b (row group gy), as the
@@ -275,7 +296,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                       const DecodeParams p) {
     using C = Cfg<NP>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // align by offset from the shared array so every derived pointer stays a
+    // shared-space pointer (ld/st.shared rather than generic accesses)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* pair_ring = smem;
     uint8_t* rope_ring = smem + C::kOffRope;
     uint8_t* qs = smem + C::kOffQ;
@@ -286,6 +309,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = static_cast<int>(cluster_ctarank());
     const int g = blockIdx.x >> 1, G = gridDim.x >> 1, gy = blockIdx.y;
+    if (threadIdx.x == 0) MLA_KTRACE(0);
 
     if (threadIdx.x == 0) {
         // TMA: one expect_tx arrival per fill; load/convert warps: one arrival per
@@ -364,6 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
     }
     __syncthreads();
     cluster_sync_all();  // the peer's barriers exist before any remote arrive
+    if (threadIdx.x == 0) MLA_KTRACE(1);
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
     const int ntiles = ctrl->t_end - ctrl->t_begin;
@@ -736,13 +761,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 const bool last_of_seg = (j == it.tiles - 1) || (i == ntiles - 1);
                 if (epi_pending) {
                     // the previous segment ended with tile i-1: write it out once its PV is done
-                    if (!group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteOEpi, i)) { alive = false; break; }
+                    group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteOEpi, i);
                     tc_fence_after();
                     epilogue();
                     epi_pending = false;
                     seg_has_pv = false;
                 }
-                if (!group_wait(&ctrl->s_full[i & 1], (i >> 1) & 1, p, ctrl, kSiteSFull, i)) { alive = false; break; }
+                group_wait(&ctrl->s_full[i & 1], (i >> 1) & 1, p, ctrl, kSiteSFull, i);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmSFull);
                 tc_fence_after();
                 __syncwarp();
@@ -760,17 +785,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                     if (st == 0) mbar_arrive(&ctrl->q_full);
                 }
                 // send this CTA's partial scores once the peer has read the last ones
-                if (i > 0 && !group_wait(&ctrl->xfree, (i - 1) & 1, p, ctrl, kSiteXFree, i, true)) { alive = false; break; }
+                if (i > 0) group_wait(&ctrl->xfree, (i - 1) & 1, p, ctrl, kSiteXFree, i, true);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFree);
-                // (every thread has read S(i) from TMEM: the buffer may be reused)
-                if (st == 0) mbar_arrive(&ctrl->s_free[i & 1]);
 #pragma unroll
                 for (int u = 0; u < NP / 4; ++u)
                     st_async_v4(x_peer + st * NP * 4 + ((u ^ xs) << 4), sr[4 * u], sr[4 * u + 1], sr[4 * u + 2],
                                 sr[4 * u + 3], xfull_peer);
                 if (st == 0) mbar_arrive_expect_tx(&ctrl->xfull, kXferBytes);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmSent);
-                if (!group_wait(&ctrl->xfull, i & 1, p, ctrl, kSiteXFull, i, true)) { alive = false; break; }
+                group_wait(&ctrl->xfull, i & 1, p, ctrl, kSiteXFull, i, true);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFull);
                 float x[NP];
 #pragma unroll
@@ -786,24 +809,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 const int tok = j * kTile + st;
                 const bool all_vis = (j * kTile + kTile + p.Qt - 1) <= T;
                 const float4* m4 = reinterpret_cast<const float4*>(ctrl->m);
+                if (all_vis) {
+                    // every real row sees every token of the tile
+#pragma unroll
+                    for (int c = 0; c < NP; ++c) x[c] = (c < HQg) ? x[c] * p.scale_log2 : -INFINITY;
+                } else {
+                    // tail of a request: per-row causal limit and the end of the request
+#pragma unroll
+                    for (int c = 0; c < NP; ++c)
+                        x[c] = (tok + ctrl->colvis[c] < T) ? x[c] * p.scale_log2 : -INFINITY;
+                }
                 int need = 0;
 #pragma unroll
                 for (int u = 0; u < NP / 4; ++u) {
                     const float4 mv = m4[u];
-                    const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = 4 * u + k;
-                        const bool v = all_vis ? (c < HQg) : (tok + ctrl->colvis[c] < T);
-                        x[c] = v ? x[c] * p.scale_log2 : -INFINITY;
-                        need |= (x[c] > mm[k] + kRescaleThreshold) ? 1 : 0;
-                    }
+                    need |= (x[4 * u] > mv.x + kRescaleThreshold) | (x[4 * u + 1] > mv.y + kRescaleThreshold) |
+                            (x[4 * u + 2] > mv.z + kRescaleThreshold) | (x[4 * u + 3] > mv.w + kRescaleThreshold);
                 }
                 // (also: every thread has read the exchange buffer; hand it back to the peer)
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmMath);
                 need = named_bar_or(2, 128, need);
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmBarOr);
-                if (st == 0) mbar_arrive_remote(xfree_peer);
+                if (st == 0) {
+                    MLA_TRACE_POINT(i, kTrSmBarOr);
+                    // every thread has read S(i) from TMEM (fenced before the barrier)
+                    // and has used the peer's scores read from the exchange buffer
+                    mbar_arrive(&ctrl->s_free[i & 1]);
+                    mbar_arrive_remote_relaxed(xfree_peer);
+                }
                 if (need) {
 #pragma unroll
                     for (int c = 0; c < NP; ++c) {
@@ -824,7 +856,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                     for (int c = 0; c < NP; ++c) l[c] *= ctrl->alpha[c];
                     if (seg_has_pv) {
                         // O holds earlier tiles of this segment: wait for their PV, rescale
-                        if (!group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i)) { alive = false; break; }
+                        group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i);
                         tc_fence_after();
                         __syncwarp();
 #pragma unroll 1
@@ -847,8 +879,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                     const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
+                        // masked entries are -inf: ex2(-inf - finite) = 0 exactly; a row
+                        // with no visible token yet has m = -inf, replaced by 0 here
                         const int c = 4 * u + k;
-                        const float pc = (x[c] == -INFINITY) ? 0.f : ex2(x[c] - mm[k]);
+                        const float mk = (mm[k] == -INFINITY) ? 0.f : mm[k];
+                        const float pc = ex2(x[c] - mk);
                         l[c] += pc;
                         x[c] = pc;
                     }
@@ -890,6 +925,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(1, 128);
+                if (ctrl->abort) { alive = false; break; }  // same value in every thread after the barrier
                 if (st == 0) {
                     MLA_TRACE_POINT(i, kTrSmPArrive);
                     mbar_arrive(&ctrl->p_full);
@@ -905,15 +941,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
             }
             if (alive && epi_pending) {
                 const int il = ntiles - 1;
-                if (group_wait(&ctrl->o_done[il & 1], (il >> 1) & 1, p, ctrl, kSiteOFinal, il)) {
+                group_wait(&ctrl->o_done[il & 1], (il >> 1) & 1, p, ctrl, kSiteOFinal, il);
+                named_bar_sync(1, 128);
+                if (!ctrl->abort) {  // same value in every thread after the barrier
                     tc_fence_after();
                     epilogue();
                 }
             }
+            if (st == 0) MLA_KTRACE(2);
         }
     }
     __syncthreads();
     cluster_sync_all();  // no remote traffic into this CTA after here
+    if (threadIdx.x == 0) MLA_KTRACE(3);
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
@@ -986,6 +1026,7 @@ __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, con
 __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParams p, int G) {
     const int b = blockIdx.x, gy = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    MLA_MTRACE(0);
     __shared__ long long red_pre[8], red_tot[8];
     long long pre = 0, tot = 0;
     for (int i = tid; i < p.B; i += 256) {
@@ -1025,6 +1066,7 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
                   static_cast<uint8_t*>(p.out) + row * kD * (p.out_f32 ? 4 : 2), p.out_f32, p.lse + row, lane,
                   tot, G, g0);
     }
+    MLA_MTRACE(1);
 }
 
 // Public split-KV combine: part_o [S, N, 512], part_lse [S, N]. One warp per row.
@@ -1117,5 +1159,11 @@ cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, 
 #ifdef MLA_TRACE
 extern "C" __attribute__((visibility("default"))) int mla_trace_dump(void* host) {
     return static_cast<int>(cudaMemcpyFromSymbol(host, mla::g_trace, sizeof(mla::g_trace)));
+}
+extern "C" __attribute__((visibility("default"))) int mla_ktrace_dump(void* host) {
+    cudaError_t e = cudaMemcpyFromSymbol(host, mla::g_ktrace, sizeof(mla::g_ktrace));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    return static_cast<int>(cudaMemcpyFromSymbol(static_cast<char*>(host) + sizeof(mla::g_ktrace), mla::g_mtrace,
+                                                 sizeof(mla::g_mtrace)));
 }
 #endif

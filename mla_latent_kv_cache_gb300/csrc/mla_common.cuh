@@ -147,10 +147,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
         : "memory");
 }
 
-// Arrive on an mbarrier in another CTA of the cluster, releasing this
-// thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Arrive on an mbarrier in another CTA of the cluster without ordering this
+// thread's earlier memory operations (a release at cluster scope would wait
+// for its in-flight remote stores, about a microsecond). Used only to hand a
+// buffer back after reads whose values have already been consumed.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
