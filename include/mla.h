@@ -85,7 +85,8 @@ MLA_API int mla_cache_write(const void* latent, int64_t latent_stride, const voi
  *   num_ctas       the value that will be passed to mla_decode (0 = as many
  *                  CTAs as fit on the current device).
  * The workspace holds a 256-byte header (word 0: device-side status, see
- * mla_decode) and fp32 partial results of requests split across CTAs.
+ * mla_decode), one 64-byte status record per CTA, and fp32 partial results of
+ * requests split across CTAs, each part rounded up to 256 bytes.
  * Returns 0 for invalid sizes.
  */
 MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas);
@@ -117,11 +118,14 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *   out          device, [B*q_len, Hq, 512], bf16 or fp32 per out_dtype.
  *   lse          device, fp32 [B*q_len, Hq], natural log.
  *   workspace    device, at least mla_decode_workspace_bytes(B, q_len, Hq,
- *                num_ctas) bytes, 256-byte aligned. Its first int32 is set to
- *                0 at the start of the call and afterwards holds device-side
- *                status bits: 1 = a bounded internal wait gave up (the kernel
- *                returned early, outputs are invalid), 2 = a block-table entry
- *                pointed outside the pool (page 0 was read instead).
+ *                num_ctas) bytes, 256-byte aligned; needs no initialisation.
+ *                Once the call's work has run, its first int32 holds
+ *                device-side status bits: 1 = a bounded internal wait gave up
+ *                (the kernel returned early, outputs are invalid), 2 = a
+ *                block-table entry pointed outside the pool (page 0 was read
+ *                instead). Words 1..3: wait site, tile and CTA of the lowest
+ *                failing CTA; words 4..11 where each of its roles gave up.
+ *                Calls sharing a workspace must be ordered on one stream.
  *   num_ctas     CTAs sharing the token stream (0 = as many as fit on the
  *                device, one per SM). CTAs work in clusters of two that split
  *                each token's 576 dims between them, so num_ctas / 2 clusters

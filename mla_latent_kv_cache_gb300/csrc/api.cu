@@ -63,12 +63,26 @@ int gcd_int(int a, int b) {
 int rows_padded(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
 
 // G = clusters of the decode grid (2 CTAs each).
-size_t decode_ws_bytes(int B, int HQ, int G) {
+// Workspace: [header 256 B][per-CTA status records][partial LSEs][partial outputs],
+// each part 256-byte aligned.
+struct WsLayout {
+    size_t rec_off, lse_off, o_off, total;
+};
+
+WsLayout decode_ws_layout(int B, int HQ, int G) {
     const size_t GY = (static_cast<size_t>(HQ) + 63) / 64;
     const size_t slots = GY * static_cast<size_t>(G + B) * 64;
+    const size_t rec_bytes = (2 * static_cast<size_t>(G) * GY * mla::kStatusRecWords * sizeof(int) + 255) / 256 * 256;
     const size_t lse_bytes = (slots * sizeof(float) + 255) / 256 * 256;
-    return kWsHeader + lse_bytes + slots * 512 * sizeof(float);
+    WsLayout l;
+    l.rec_off = kWsHeader;
+    l.lse_off = l.rec_off + rec_bytes;
+    l.o_off = l.lse_off + lse_bytes;
+    l.total = l.o_off + slots * 512 * sizeof(float);
+    return l;
 }
+
+size_t decode_ws_bytes(int B, int HQ, int G) { return decode_ws_layout(B, HQ, G).total; }
 
 }  // namespace
 
@@ -147,6 +161,8 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     if (di.major != 10) return MLA_ERR_UNSUPPORTED;
     const int GY = (HQ + 63) / 64;
     if (GY > 65535) return MLA_ERR_UNSUPPORTED;
+    // TMA row coordinates of the queries are 32-bit
+    if (static_cast<int64_t>(B) * HQ + 64 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
     const int NP = rows_padded(HQ < 64 ? HQ : 64);
     const bool lsu = cache_kind == MLA_CACHE_FP8_DS_MLA_656 || (page_size % 8) != 0;
     const int G = mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
@@ -156,12 +172,32 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     // Two TMA descriptors over the pool [num_slots, 576] bf16: 64-dim latent
     // chunks (128-byte swizzle) and 32-dim rope halves (64-byte swizzle), both
     // gcd(page_size, 128) rows high so a box never crosses a page.
-    CUtensorMap tmap_lat, tmap_rope;
-    std::memset(&tmap_lat, 0, sizeof(tmap_lat));
-    std::memset(&tmap_rope, 0, sizeof(tmap_rope));
+    mla::DecodeMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    CUtensorMap& tmap_lat = maps.lat;
+    CUtensorMap& tmap_rope = maps.rope;
+    auto enc = encode_fn();
+    if (!enc) return MLA_ERR_CUDA;
+    {
+        // queries: q_lat [B*HQ, 512] and q_pe [B*HQ, 64] bf16, NP-row boxes
+        const cuuint64_t rows = static_cast<cuuint64_t>(B) * HQ;
+        cuuint64_t gq[2] = {static_cast<cuuint64_t>(mla::kD), rows};
+        cuuint64_t sq[1] = {static_cast<cuuint64_t>(mla::kD * 2)};
+        cuuint64_t gp[2] = {64u, rows};
+        cuuint64_t sp[1] = {128u};
+        cuuint32_t estride[2] = {1u, 1u};
+        cuuint32_t bq[2] = {64u, static_cast<cuuint32_t>(NP)};
+        cuuint32_t bp[2] = {32u, static_cast<cuuint32_t>(NP)};
+        CUresult r = enc(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_lat), gq, sq, bq, estride,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+        r = enc(&maps.qpe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_pe), gp, sp, bp, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+    }
     if (!lsu) {
-        auto enc = encode_fn();
-        if (!enc) return MLA_ERR_CUDA;
         const int br = gcd_int(page_size, 128);
         cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(num_slots)};
         cuuint64_t gstride[1] = {static_cast<cuuint64_t>(mla::kRowBf16)};
@@ -180,9 +216,7 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const size_t slots = static_cast<size_t>(GY) * (G + B) * 64;
-    const size_t lse_bytes = (slots * sizeof(float) + 255) / 256 * 256;
-    if (cudaMemsetAsync(ws, 0, kWsHeader, s) != cudaSuccess) return MLA_ERR_CUDA;
+    const WsLayout wl = decode_ws_layout(B, HQ, G);
 
     mla::DecodeParams p;
     p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
@@ -195,8 +229,9 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     p.out = out;
     p.lse = lse;
     p.status = reinterpret_cast<int*>(ws);
-    p.part_lse = reinterpret_cast<float*>(ws + kWsHeader);
-    p.part_o = reinterpret_cast<float*>(ws + kWsHeader + lse_bytes);
+    p.rec = reinterpret_cast<int*>(ws + wl.rec_off);
+    p.part_lse = reinterpret_cast<float*>(ws + wl.lse_off);
+    p.part_o = reinterpret_cast<float*>(ws + wl.o_off);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.page_size = page_size;
     p.run_rows = gcd_int(page_size, 128);
@@ -206,7 +241,7 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     p.HQ = HQ;
     p.out_f32 = out_dtype == MLA_OUT_F32;
     p.SPG = G + B;
-    cudaError_t e = mla::launch_decode(tmap_lat, tmap_rope, p, NP, lsu, cache_kind, G, GY, s);
+    cudaError_t e = mla::launch_decode(maps, p, NP, lsu, cache_kind, G, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

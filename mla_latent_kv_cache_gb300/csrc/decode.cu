@@ -56,7 +56,7 @@ namespace mla {
 enum TraceEvent : int {
     kTrProdStart = 0, kTrProdIssued, kTrSPair0, kTrSAllIn, kTrPvIssue, kTrSmSFull, kTrSmXFull, kTrSmPArrive,
     kTrSIssued = 8, kTrSmTmemLd, kTrSmXFree, kTrSmSent, kTrSmMath, kTrSmBarOr, kTrSmExp, kTrSmPStore, kTrPvIssued,
-    kTrSmXRead, kTrSmExpLoop, kTrEvents = 19
+    kTrSmXRead, kTrSmExpLoop, kTrEpiStart, kTrEpiRed, kTrEpiStored, kTrEpiEnd, kTrEpiHalf, kTrEvents = 24
 };
 #ifdef MLA_TRACE
 __device__ unsigned long long g_trace[8][64][kTrEvents];
@@ -67,10 +67,21 @@ __device__ unsigned long long g_trace[8][64][kTrEvents];
 // whole-kernel points per CTA (row group 0): entry, setup done, softmax
 // done, exit; and entry/exit of each merge block
 __device__ unsigned long long g_ktrace[512][4];
+// per CTA (row group 0) and tile: when the softmax handed P to the PV issuer
+__device__ unsigned long long g_ttrace[512][1024];
+__device__ unsigned int g_ksm[512][4];  // smid, tiles, segments
 __device__ unsigned long long g_mtrace[512][2];
 #define MLA_KTRACE(e)                                                                  \
     do {                                                                               \
         if (blockIdx.y == 0 && blockIdx.x < 512) g_ktrace[blockIdx.x][(e)] = globaltimer_ns(); \
+    } while (0)
+#define MLA_TTRACE(i)                                                                            \
+    do {                                                                                         \
+        if (blockIdx.y == 0 && blockIdx.x < 512 && (i) < 1024) g_ttrace[blockIdx.x][(i)] = globaltimer_ns(); \
+    } while (0)
+#define MLA_KSM(k, v)                                             \
+    do {                                                          \
+        if (blockIdx.y == 0 && blockIdx.x < 512) g_ksm[blockIdx.x][(k)] = (v); \
     } while (0)
 #define MLA_MTRACE(e)                                                                   \
     do {                                                                                \
@@ -84,6 +95,12 @@ __device__ unsigned long long g_mtrace[512][2];
     do {              \
     } while (0)
 #define MLA_MTRACE(e) \
+    do {              \
+    } while (0)
+#define MLA_TTRACE(i) \
+    do {              \
+    } while (0)
+#define MLA_KSM(k, v) \
     do {              \
     } while (0)
 #endif
@@ -108,9 +125,12 @@ struct Cfg {
     static constexpr int kOffX = (kOffQ + kQBytes + 1023) / 1024 * 1024;
     static constexpr int kOffP = kOffX + kXBytes;
     static constexpr int kOffCtrl = kOffP + kPBufs * kPBytes;
-    static constexpr int kSmemBytes = kOffCtrl + 2048 + 1024;  // + control block, alignment slack
-    static constexpr int kTmemCols = 4 * NP;                   // O: 2 x NP, S: 2 buffers x NP
-    static constexpr int kColS = 2 * NP;
+    static constexpr int kSmemBytes = kOffCtrl + 3072 + 1024;  // + control block, alignment slack
+    // TMEM: two O accumulators of 2 x NP columns (one per alternating
+    // segment, so a finished segment drains while the next accumulates),
+    // then two S buffers of NP columns
+    static constexpr int kTmemCols = NP == 16 ? 128 : NP == 32 ? 256 : 512;
+    static constexpr int kColS = 4 * NP;
     static constexpr uint32_t kPSwizzle = NP == 16 ? kSw32 : NP == 32 ? kSw64 : kSw128;
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(kTmemCols >= 32, "tmem");
@@ -129,8 +149,10 @@ struct Ctrl {
     alignas(16) float m[64];         // running max per row (log2 units); read as float4
     alignas(16) float alpha[64];
     alignas(16) float red[4][64];
+    float dlt[64];                   // row sums of the segment being written out
+    float dm[64];                    // and its row maxima
 };
-static_assert(sizeof(Ctrl) <= 2048, "control block");
+static_assert(sizeof(Ctrl) <= 3072, "control block");
 static_assert(offsetof(Ctrl, m) % 16 == 0 && offsetof(Ctrl, alpha) % 16 == 0, "vector loads of m / alpha");
 
 __device__ __forceinline__ int swz_p(int row, uint32_t mode) {
@@ -158,6 +180,26 @@ struct TileIt {
     }
 };
 
+// L2 prefetch of what the first tiles of request b read besides the cache:
+// its query rows of row group gy and its block-table row (whole 16-byte
+// units inside the row only).
+__device__ __forceinline__ void prefetch_request(const DecodeParams& p, int b, int gy) {
+    const int HQg = min(64, p.HQ - gy * 64);
+    const int64_t row0 = static_cast<int64_t>(b) * p.HQ + gy * 64;
+    prefetch_l2_bulk(p.q_lat + row0 * kD, static_cast<uint32_t>(HQg * kD * 2));
+    prefetch_l2_bulk(p.q_pe + row0 * kP, static_cast<uint32_t>(HQg * kP * 2));
+    const int T = max(__ldg(p.seq_lens + b), 0);
+    const int64_t pages = (static_cast<int64_t>(T) + p.page_size - 1) / p.page_size;
+    uintptr_t a0 = reinterpret_cast<uintptr_t>(p.block_table + static_cast<int64_t>(b) * p.bt_stride);
+    uintptr_t a1 = a0 + static_cast<uintptr_t>(pages) * 4;
+    a0 = (a0 + 15) & ~static_cast<uintptr_t>(15);
+    a1 &= ~static_cast<uintptr_t>(15);
+    if (a1 > a0) {
+        const uintptr_t n = a1 - a0;
+        prefetch_l2_bulk(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(n < (1u << 20) ? n : (1u << 20)));
+    }
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -184,24 +226,27 @@ enum WaitSite : int {
     kSiteOFinal
 };
 
+// This CTA's status record; zeroed by the CTA itself at launch and folded
+// into the workspace header by the merge step.
+__device__ __forceinline__ int* status_rec(const DecodeParams& p) {
+    return p.rec + static_cast<int64_t>(blockIdx.y * gridDim.x + blockIdx.x) * kStatusRecWords;
+}
+
 __device__ __forceinline__ void fail(const DecodeParams& p, Ctrl* ctrl, int code, int site = 0, int tile = 0) {
-    atomicOr(p.status, code);
-    if (site && atomicCAS(p.status + 1, 0, site) == 0) {
-        p.status[2] = tile;
-        p.status[3] = blockIdx.y * gridDim.x + blockIdx.x;
-    }
+    int* r = status_rec(p);
+    atomicOr(r, code);
+    if (site && atomicCAS(r + 1, 0, site) == 0) r[2] = tile;
     ctrl->abort = 1;
 }
 
 // Every softmax thread waits, then the 128 threads agree on the outcome, so a
 // timeout seen by some of them cannot strand the rest at a named barrier.
 // When a role leaves its loop on a failed wait it records where it was
-// waiting: header word 4 + role = (site << 24) | tile (first CTA to fail only).
+// waiting: record word 4 + role = (site << 24) | tile.
 enum Role : int { kRoleS = 0, kRolePV, kRoleSoftmax, kRoleTma, kRoleLsu0 };
 
 __device__ __forceinline__ void report(const DecodeParams& p, int role, int site, int idx) {
-    if (p.status[3] == static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x))
-        p.status[4 + role] = (site << 24) | (idx & 0xFFFFFF);
+    status_rec(p)[4 + role] = (site << 24) | (idx & 0xFFFFFF);
 }
 
 // Softmax-group wait. A thread whose wait fails raises the abort flag and
@@ -215,32 +260,6 @@ __device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, const
         report(p, kRoleSoftmax, site, tile);
     }
     return ok;
-}
-
-// This CTA's half of the NP query rows of request b (row group gy), as the
-// B operands of S: latent chunks 0..3 (dims 256*rank + 64k) K-major with
-// 128-B swizzle at k*NP*128, then the rope half (32 dims) K-major with 64-B
-// swizzle at 4*NP*128.
-template <int NP>
-__device__ void load_q(const DecodeParams& p, int b, int gy, int rank, uint8_t* qs, int tid) {
-    constexpr int kUnits = 4 * 8 + 4;  // 16-byte units per row: 32 latent + 4 rope
-    for (int q = tid; q < NP * kUnits; q += 128) {
-        const int n = q / kUnits, u = q - n * kUnits;
-        const int r = gy * 64 + n;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < p.HQ) {
-            const int64_t row = static_cast<int64_t>(b) * p.HQ + r;
-            v = (u < 32) ? __ldg(reinterpret_cast<const uint4*>(p.q_lat + row * kD + 256 * rank) + u)
-                         : __ldg(reinterpret_cast<const uint4*>(p.q_pe + row * kP + 32 * rank) + (u - 32));
-        }
-        if (u < 32) {
-            const int chunk = u >> 3, uu = u & 7;
-            *reinterpret_cast<uint4*>(qs + chunk * NP * 128 + n * 128 + ((uu ^ (n & 7)) << 4)) = v;
-        } else {
-            const int uu = u - 32;
-            *reinterpret_cast<uint4*>(qs + 4 * NP * 128 + n * 64 + ((uu ^ ((n >> 1) & 3)) << 4)) = v;
-        }
-    }
 }
 
 // 64-bit slot of token `tok` of the request whose block-table row is `btr`.
@@ -292,8 +311,9 @@ __device__ __forceinline__ void dequant16(uint4 codes, float scale, uint4& lo, u
 
 template <int NP, bool LSU, int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tmap_lat, const __grid_constant__ CUtensorMap tmap_rope,
-                      const DecodeParams p) {
+    mla_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
+    const CUtensorMap& tmap_lat = maps.lat;
+    const CUtensorMap& tmap_rope = maps.rope;
     using C = Cfg<NP>;
     extern __shared__ uint8_t smem_raw[];
     // align by offset from the shared array so every derived pointer stays a
@@ -328,14 +348,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
         ctrl->abort = 0;
         fence_mbar_init();
     }
+    if (warp == 1 && lane == 0) {
+        if (!LSU) {
+            prefetch_tensormap(&tmap_lat);
+            prefetch_tensormap(&tmap_rope);
+        }
+        prefetch_tensormap(&maps.q);
+        prefetch_tensormap(&maps.qpe);
+    }
+    // everything above touches only this CTA; the previous kernel in the
+    // stream may still be writing the inputs or reading the workspace
+    griddep_wait();
+    if (threadIdx.x == 0) {
+        int4* r = reinterpret_cast<int4*>(status_rec(p));
+#pragma unroll
+        for (int k = 0; k < kStatusRecWords / 4; ++k) r[k] = make_int4(0, 0, 0, 0);
+    }
     if (warp == 0) {
         tmem_alloc(&ctrl->tmem_base, C::kTmemCols);
         tmem_relinquish();
         tc_fence_before();
-    }
-    if (!LSU && warp == 1 && lane == 0) {
-        prefetch_tensormap(&tmap_lat);
-        prefetch_tensormap(&tmap_rope);
     }
     if (warp == 2) {
         // tiles per request, their total, and where this cluster's range starts
@@ -352,7 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
         const int te = static_cast<int>(static_cast<long long>(g + 1) * total / G);
         int b0 = 0, j0 = 0;
         long long acc = 0;
-        for (int base = 0; base < p.B && tb < te; base += 32) {
+        for (int base = 0; base < p.B; base += 32) {
             const int b = base + lane;
             const int tl = b < p.B ? (max(__ldg(p.seq_lens + b), 0) + kTile - 1) / kTile : 0;
             int incl = tl;
@@ -388,10 +420,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
     }
     __syncthreads();
     cluster_sync_all();  // the peer's barriers exist before any remote arrive
-    if (threadIdx.x == 0) MLA_KTRACE(1);
+    if (threadIdx.x == 0) {
+        MLA_KTRACE(1);
+#ifdef MLA_TRACE
+        unsigned sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        MLA_KSM(0, sm);
+        MLA_KSM(1, ctrl->t_end - ctrl->t_begin);
+#endif
+        griddep_launch_dependents();  // the merge grid may be scheduled as CTAs retire
+    }
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
     const int ntiles = ctrl->t_end - ctrl->t_begin;
+    if (ntiles == 0 && ctrl->j0 > 0 && rank == 0 && threadIdx.x >= 128 && threadIdx.x < 192) {
+        // An empty range strictly inside request b0 (more clusters than
+        // tiles): the merge of b0 counts this cluster's slot, so mark it empty.
+        const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + ctrl->b0;
+        p.part_lse[pslot * 64 + (threadIdx.x - 128)] = -INFINITY;
+    }
 
     if (ntiles > 0) {
         if (warp == 0 && lane == 0) {
@@ -460,8 +507,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint32_t idPV = idesc_bf16(128, NP, true, true);
             constexpr uint32_t p_sbo = 8 * NP * 2;
+            int seg = -1;
             for (int i = 0; i < ntiles; ++i) {
                 const bool new_seg = (i == 0) || (it.j == 0);
+                if (new_seg) ++seg;
+                const uint32_t tO = tmem + (seg & 1) * 2 * NP;
                 if (!mbar_wait(&ctrl->p_full, i & 1, &ctrl->abort)) {
                     fail(p, ctrl, kErrWaitTimeout, kSitePFull, i);
                     report(p, kRolePV, kSitePFull, i);
@@ -476,7 +526,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                     const uint64_t da = smem_desc(smem_u32(pair_ring + slot * C::kPairBytes), 16384, 1024, kSw128);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16(tmem + mt * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
+                        umma_bf16(tO + mt * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
                                   (new_seg && kk == 0) ? 0u : 1u);
                     umma_commit(&ctrl->pair_empty[slot]);
                 }
@@ -540,7 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 fail(p, ctrl, kErrWaitTimeout, fsite, ftile);
                 report(p, kRoleTma, fsite, ftile);
             }
-            if (bad) atomicOr(p.status, kErrBadBlock);
+            if (bad) atomicOr(status_rec(p), kErrBadBlock);
         } else if (LSU && warp >= 8) {
             // ------------------------------------- load/convert producers
             // Each warp keeps a fixed, in-order share of every tile: warps 8/9 the
@@ -678,7 +728,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 fail(p, ctrl, kErrWaitTimeout, fsite, ftile);
                 report(p, kRoleLsu0 + pw, fsite, ftile);
             }
-            if (bad) atomicOr(p.status, kErrBadBlock);
+            if (bad) atomicOr(status_rec(p), kErrBadBlock);
         } else if (warp >= 4 && warp < 8) {
             // ------------------------------------------ softmax + epilogue
             const int st = threadIdx.x - 128;  // token row of the tile / TMEM lane
@@ -700,89 +750,148 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
             for (int c = 0; c < NP; ++c) l[c] = 0.f;
             int seg_start_j = it.j;
             bool seg_has_pv = false;
-            // the segment whose output is still in TMEM: written once its last PV is done
-            bool epi_pending = false;
-            bool epi_final = false;
-            int epi_b = 0;
+            int seg = 0;               // segment index: its O accumulator is (seg & 1)
+            uint32_t obuf = 0;         // column of the current O accumulator
+            // The segment that ended with the previous tile: its row sums and maxima
+            // are captured, its output is written out once its last PV is done.
+            bool pend = false;
+            bool pend_final = false;
+            int pend_b = 0;
+            // Output rows being drained from an O accumulator a few columns per
+            // tile: plain stores that the memory pipe absorbs in the background
+            // (a whole segment at once would stall the group behind the cache stream).
+            int dr_left = 0, dr_step = 0, dr_b = 0;
+            bool dr_final = false;
+            uint32_t dr_obuf = 0;
+            constexpr int kDC = 8;  // columns per drain step
+            const int dr_per_half = (HQg + kDC - 1) / kDC;
 
-            auto epilogue = [&]() {
+            // This CTA's half of the NP query rows of request bq (row group gy)
+            // by TMA, in the layout S reads as its B operand: latent chunks
+            // 256*rank + 64k (k = 0..3) K-major with 128-B swizzle at k*NP*128,
+            // then the rope half (32 dims) with 64-B swizzle at 4*NP*128. Rows
+            // past the group's real rows belong to other requests (or are zero
+            // past the end); their score columns are masked to -inf.
+            auto issue_q = [&](int bq) {
+                const int y = bq * p.HQ + gy * 64;
+                const uint64_t pol = l2_policy_evict_first();
+                mbar_arrive_expect_tx(&ctrl->q_full, C::kQBytes);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    tma_load_2d(qs + k * NP * 128, &maps.q, &ctrl->q_full, 256 * rank + 64 * k, y, pol);
+                tma_load_2d(qs + 4 * NP * 128, &maps.qpe, &ctrl->q_full, 32 * rank, y, pol);
+            };
+
+            // Row sums and maxima of the segment that just ended into dlt / dm,
+            // then fresh softmax state for the next one.
+            auto capture = [&](int i) {
+                if (st == 0) MLA_TRACE_POINT(i, kTrEpiStart);
 #pragma unroll
                 for (int c = 0; c < NP; ++c) {
                     const float v = warp_sum(l[c]);
                     if (lane == 0) ctrl->red[sw][c] = v;
                 }
                 named_bar_sync(1, 128);
-                const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + epi_b;
-                __syncwarp();
-#pragma unroll 1
-                for (int mt = 0; mt < 2; ++mt) {
-                    const int d = 256 * rank + mt * 128 + st;
-#pragma unroll 1
-                    for (int c0 = 0; c0 < NP && c0 < HQg; c0 += 16) {
-                        uint32_t o[16];
-                        tmem_ld_x16(tmem + lane_base + mt * NP + c0, o);
-#pragma unroll
-                        for (int cc = 0; cc < 16; ++cc) {
-                            const int c = c0 + cc;
-                            if (c >= HQg) break;
-                            const float lt = ctrl->red[0][c] + ctrl->red[1][c] + ctrl->red[2][c] + ctrl->red[3][c];
-                            const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
-                            if (epi_final) {
-                                const int64_t idx = (static_cast<int64_t>(epi_b) * p.HQ + gy * 64 + c) * kD + d;
-                                if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
-                                else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
-                            } else {
-                                p.part_o[(pslot * 64 + c) * kD + d] = v;
-                            }
-                        }
-                    }
+                if (st < NP) {
+                    ctrl->dlt[st] = ctrl->red[0][st] + ctrl->red[1][st] + ctrl->red[2][st] + ctrl->red[3][st];
+                    ctrl->dm[st] = ctrl->m[st];
+                    ctrl->m[st] = -INFINITY;
                 }
-                if (rank == 0 && st < HQg) {
-                    const float lt = ctrl->red[0][st] + ctrl->red[1][st] + ctrl->red[2][st] + ctrl->red[3][st];
-                    const float lv = lt > 0.f ? (ctrl->m[st] + log2f(lt)) * kLn2 : -INFINITY;
-                    if (epi_final) p.lse[static_cast<int64_t>(epi_b) * p.HQ + gy * 64 + st] = lv;
-                    else p.part_lse[pslot * 64 + st] = lv;
-                }
-                tc_fence_before();
-                named_bar_sync(1, 128);
-                if (st < NP) ctrl->m[st] = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < NP; ++c) l[c] = 0.f;
                 named_bar_sync(1, 128);
+                if (st == 0) MLA_TRACE_POINT(i, kTrEpiRed);
             };
 
-            load_q<NP>(p, it.b, gy, rank, qs, st);
-            fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (st == 0) mbar_arrive(&ctrl->q_full);
+            // The captured segment (accumulator src) has finished its last PV:
+            // write its LSE and start draining its rows.
+            auto start_drain = [&](uint32_t src) {
+                const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + pend_b;
+                if (rank == 0 && st < HQg) {
+                    const float lt = ctrl->dlt[st];
+                    const float lv = lt > 0.f ? (ctrl->dm[st] + log2f(lt)) * kLn2 : -INFINITY;
+                    if (pend_final) p.lse[static_cast<int64_t>(pend_b) * p.HQ + gy * 64 + st] = lv;
+                    else p.part_lse[pslot * 64 + st] = lv;
+                }
+                dr_left = 2 * dr_per_half;
+                dr_step = 0;
+                dr_b = pend_b;
+                dr_final = pend_final;
+                dr_obuf = src;
+                pend = false;
+            };
+
+            // One drain step: kDC columns of one 128-dim half, O / l, into the
+            // output rows (a whole request) or the cluster's partial slot.
+            auto drain_step = [&]() {
+                const int mt = dr_step / dr_per_half;
+                const int c0 = (dr_step - mt * dr_per_half) * kDC;
+                uint32_t o[kDC];
+                tmem_ld_x8(tmem + lane_base + dr_obuf + mt * NP + c0, o);
+                const int64_t d = 256 * rank + 128 * mt + st;
+                const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + dr_b;
+#pragma unroll
+                for (int cc = 0; cc < kDC; ++cc) {
+                    const int c = c0 + cc;
+                    if (c < HQg) {
+                        const float lt = ctrl->dlt[c];
+                        const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
+                        if (dr_final) {
+                            const int64_t idx = (static_cast<int64_t>(dr_b) * p.HQ + gy * 64 + c) * kD + d;
+                            if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
+                            else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+                        } else {
+                            p.part_o[(pslot * 64 + c) * kD + d] = v;
+                        }
+                    }
+                }
+                ++dr_step;
+                --dr_left;
+            };
+
+            if (st == 0) issue_q(it.b);
             bool alive = true;
             for (int i = 0; i < ntiles; ++i) {
                 const int b = it.b, j = it.j, T = it.T;
                 const bool last_of_seg = (j == it.tiles - 1) || (i == ntiles - 1);
-                if (epi_pending) {
-                    // the previous segment ended with tile i-1: write it out once its PV is done
-                    group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteOEpi, i);
-                    tc_fence_after();
-                    epilogue();
-                    epi_pending = false;
+                if (i > 0 && j == 0) {
+                    // the previous segment ended with tile i-1. The older one still
+                    // draining (if any) finishes first: its accumulator is the one
+                    // this segment will use, and dlt / dm are about to be replaced.
+                    if (dr_left > 0) {
+                        tc_fence_after();
+                        while (dr_left > 0) drain_step();
+                        tc_fence_before();
+                    }
+                    if (st == 0) MLA_TRACE_POINT(i, kTrEpiHalf);
+                    capture(i);
+                    pend = true;
                     seg_has_pv = false;
+                    ++seg;
+                    obuf = (seg & 1) * 2 * NP;
                 }
                 group_wait(&ctrl->s_full[i & 1], (i >> 1) & 1, p, ctrl, kSiteSFull, i);
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmSFull);
+                if (st == 0) {
+                    MLA_TRACE_POINT(i, kTrSmSFull);
+                    if (last_of_seg && i + 1 < ntiles) {
+                        // S(i) is complete, so Q may be replaced by the next request's
+                        TileIt nx = it;
+                        nx.next(p.seq_lens, p.B);
+                        issue_q(nx.b);
+                    }
+                }
                 tc_fence_after();
                 __syncwarp();
                 uint32_t sr[NP];
                 tmem_ld_np<NP>(tmem + lane_base + C::kColS + (i & 1) * NP, sr);
                 tc_fence_before();
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmTmemLd);
-                if (last_of_seg && i + 1 < ntiles) {
-                    // S(i) is complete, so Q may be replaced by the next request's
+                if (st == 0 && (i == 0 || j == 0) && !last_of_seg) {
+                    // warm L2 with the next request's queries and page list
                     TileIt nx = it;
+                    nx.j = nx.tiles - 1;
                     nx.next(p.seq_lens, p.B);
-                    load_q<NP>(p, nx.b, gy, rank, qs, st);
-                    fence_proxy_async_smem();
-                    named_bar_sync(1, 128);
-                    if (st == 0) mbar_arrive(&ctrl->q_full);
+                    if (nx.b < p.B) prefetch_request(p, nx.b, gy);
                 }
                 // send this CTA's partial scores once the peer has read the last ones
                 if (i > 0) group_wait(&ctrl->xfree, (i - 1) & 1, p, ctrl, kSiteXFree, i, true);
@@ -864,11 +973,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
 #pragma unroll 1
                             for (int c0 = 0; c0 < NP; c0 += 16) {
                                 uint32_t o[16];
-                                tmem_ld_x16(tmem + lane_base + mt * NP + c0, o);
+                                tmem_ld_x16(tmem + lane_base + obuf + mt * NP + c0, o);
 #pragma unroll
                                 for (int cc = 0; cc < 16; ++cc)
                                     o[cc] = __float_as_uint(__uint_as_float(o[cc]) * ctrl->alpha[c0 + cc]);
-                                tmem_st_x16(tmem + lane_base + mt * NP + c0, o);
+                                tmem_st_x16(tmem + lane_base + obuf + mt * NP + c0, o);
                             }
                         tmem_wait_st();
                     }
@@ -909,16 +1018,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                                                pack_bf16x2(x[8 * u + 4], x[8 * u + 5]), pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
                     *reinterpret_cast<uint4*>(prow + ((u ^ sz) << 4)) = v;
                 }
-                if (tok >= T) {
+                if (j * kTile + kTile > T) {
                     // rows past the request hold stale data (maybe NaN); P is 0 there,
-                    // but 0 * NaN would still poison O, so clear them
+                    // but 0 * NaN would still poison O, so clear them. In each 64-dim
+                    // chunk the token rows r0..127 are one contiguous range; the 128
+                    // threads write consecutive 16-byte units of it.
+                    const int r0 = max(T - j * kTile, 0);
                     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                    for (int pp = 0; pp < 2; ++pp) {
-                        uint8_t* ps = pair_ring + ((2 * i + pp) % C::kRL) * C::kPairBytes + st * 128;
+                    const int nunits = (kTile - r0) * 8;  // 16-byte units per chunk
 #pragma unroll
-                        for (int c = 0; c < 2; ++c)
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(ps + c * 16384 + u * 16) = z;
+                    for (int q = 0; q < 4; ++q) {
+                        uint8_t* base = pair_ring + ((2 * i + (q >> 1)) % C::kRL) * C::kPairBytes + (q & 1) * 16384 + r0 * 128;
+                        for (int u = st; u < nunits; u += 128) *reinterpret_cast<uint4*>(base + u * 16) = z;
                     }
                 }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmPStore);
@@ -928,24 +1039,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 if (ctrl->abort) { alive = false; break; }  // same value in every thread after the barrier
                 if (st == 0) {
                     MLA_TRACE_POINT(i, kTrSmPArrive);
+                    MLA_TTRACE(i);
                     mbar_arrive(&ctrl->p_full);
                 }
                 seg_has_pv = true;
+                if (pend) {
+                    // PV(i-1), the captured segment's last, is long done by now
+                    group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteOEpi, i);
+                    tc_fence_after();
+                    start_drain(obuf ^ (2 * NP));
+                    if (st == 0) MLA_TRACE_POINT(i, kTrEpiStored);
+                } else if (dr_left > 0) {
+                    tc_fence_after();
+                    drain_step();
+                    tc_fence_before();
+                }
                 if (last_of_seg) {
-                    epi_pending = true;
-                    epi_final = (seg_start_j == 0) && (j == it.tiles - 1);
-                    epi_b = b;
+                    pend_final = (seg_start_j == 0) && (j == it.tiles - 1);
+                    pend_b = b;
                     seg_start_j = 0;
                 }
                 it.next(p.seq_lens, p.B);
             }
-            if (alive && epi_pending) {
+            if (alive) {
+                // the last segment: finish the older drain, capture, wait for its
+                // last PV, write it out
                 const int il = ntiles - 1;
+                tc_fence_after();
+                while (dr_left > 0) drain_step();
+                capture(il + 1);
                 group_wait(&ctrl->o_done[il & 1], (il >> 1) & 1, p, ctrl, kSiteOFinal, il);
                 named_bar_sync(1, 128);
                 if (!ctrl->abort) {  // same value in every thread after the barrier
                     tc_fence_after();
-                    epilogue();
+                    start_drain(obuf);
+                    while (dr_left > 0) drain_step();
+                    if (st == 0) MLA_TRACE_POINT(il + 1, kTrEpiEnd);
                 }
             }
             if (st == 0) MLA_KTRACE(2);
@@ -963,21 +1092,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
 
 // ---------------------------------------------------------------- merging
 
-// Cluster g of G got tiles [g*tot/G, (g+1)*tot/G); with more clusters than
-// tiles some ranges are empty and wrote no partial. tot == 0: all live.
-__device__ __forceinline__ bool seg_live(long long tot, int G, long long g) {
-    return tot == 0 || (g * tot / G) < ((g + 1) * tot / G);
-}
-
 // Merge `nseg` partials of one row: out = sum_i w_i o_i with
 // w_i = exp(lse_i - L), L = ln sum exp(lse_i); all -inf -> (0, -inf).
 // One warp; lane owns dims 4*lane + 128*k, k = 0..3.
 __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, const float* pl, int64_t l_stride,
-                                          int nseg, void* out, int out_f32, float* lse_out, int lane,
-                                          long long tot = 0, int G = 1, long long g0 = 0) {
+                                          int nseg, void* out, int out_f32, float* lse_out, int lane) {
     float mx = -INFINITY;
-    for (int s = lane; s < nseg; s += 32)
-        if (seg_live(tot, G, g0 + s)) mx = fmaxf(mx, pl[s * l_stride]);
+    for (int s = lane; s < nseg; s += 32) mx = fmaxf(mx, pl[s * l_stride]);
     mx = warp_max(mx);
     float4 acc[4];
 #pragma unroll
@@ -986,14 +1107,12 @@ __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, con
     if (mx != -INFINITY) {
         float ws = 0.f;
         for (int s = lane; s < nseg; s += 32) {
-            if (!seg_live(tot, G, g0 + s)) continue;
             const float v = pl[s * l_stride];
             if (v != -INFINITY) ws += expf(v - mx);
         }
         ws = warp_sum(ws);
         L = mx + logf(ws);
         for (int s = 0; s < nseg; ++s) {
-            if (!seg_live(tot, G, g0 + s)) continue;
             const float v = pl[s * l_stride];
             if (v == -INFINITY) continue;
             const float w = expf(v - L);
@@ -1021,12 +1140,19 @@ __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, con
     if (lane == 0 && lse_out) *lse_out = L;
 }
 
-// Per request b (blockIdx.x) and row group (blockIdx.y): merge the partials
-// of a request cut across clusters, and write (0, -inf) for empty requests.
-__global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParams p, int G) {
-    const int b = blockIdx.x, gy = blockIdx.y;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Decode merge: one row of one request per 128 threads (2 rows per block),
+// each thread 4 of the 512 dims. Rows of requests that one cluster held
+// whole were written by the decode kernel; rows of requests cut across
+// clusters g0..g1 combine their partial slots g + b; rows of empty requests
+// get (0, -inf). Block (0, 0) also folds the per-CTA status records of the
+// decode grid into the workspace header.
+__global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParams p, int G, int nrec) {
     MLA_MTRACE(0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int RB = (min(64, p.HQ) + 1) >> 1;  // blocks per (request, row group)
+    const int b = blockIdx.x / RB, gy = blockIdx.y;
+    const int n = (blockIdx.x - b * RB) * 2 + (tid >> 7);
+    const int t = tid & 127;
     __shared__ long long red_pre[8], red_tot[8];
     long long pre = 0, tot = 0;
     for (int i = tid; i < p.B; i += 256) {
@@ -1043,29 +1169,92 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
     __syncthreads();
     pre = 0;
     tot = 0;
+#pragma unroll
     for (int w = 0; w < 8; ++w) { pre += red_pre[w]; tot += red_tot[w]; }
-    const int tiles_b = (max(__ldg(p.seq_lens + b), 0) + kTile - 1) / kTile;
-    const int HQg = min(64, p.HQ - gy * 64);
-    if (tiles_b == 0) {
-        for (int n = warp; n < HQg; n += 8) {
-            const int64_t row = static_cast<int64_t>(b) * p.HQ + gy * 64 + n;
-            merge_row(nullptr, 0, nullptr, 0, 0, static_cast<uint8_t*>(p.out) + row * kD * (p.out_f32 ? 4 : 2),
-                      p.out_f32, p.lse + row, lane);
+    griddep_wait();  // the decode grid has finished and its writes are visible
+
+    if (blockIdx.x == 0 && blockIdx.y == 0 && warp == 0) {
+        // status summary: OR of all records; the lowest failing CTA's site,
+        // tile, index and role reports
+        int bits = 0, first = INT_MAX;
+        for (int c = lane; c < nrec; c += 32) {
+            const int v = p.rec[static_cast<int64_t>(c) * kStatusRecWords];
+            bits |= v;
+            if (v && c < first) first = c;
         }
-        return;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            bits |= __shfl_xor_sync(0xffffffffu, bits, o);
+            first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+        }
+        if (lane < 16) {
+            int v = 0;
+            if (lane == 0) v = bits;
+            else if (first != INT_MAX) {
+                const int* r = p.rec + static_cast<int64_t>(first) * kStatusRecWords;
+                v = lane == 1 ? r[1] : lane == 2 ? r[2] : lane == 3 ? first : (lane < 12 ? r[lane] : 0);
+            }
+            p.status[lane] = v;
+        }
     }
-    // cluster holding tile t: the largest g with floor(g * tot / G) <= t
-    const long long g0 = ((pre + 1) * G - 1) / tot;
-    const long long g1 = ((pre + tiles_b) * G - 1) / tot;
-    if (g0 == g1) return;  // one cluster held the whole request and wrote the output
-    const int nseg = static_cast<int>(g1 - g0 + 1);
-    const int64_t slot0 = static_cast<int64_t>(gy) * p.SPG + g0 + b;
-    for (int n = warp; n < HQg; n += 8) {
-        const int64_t row = static_cast<int64_t>(b) * p.HQ + gy * 64 + n;
-        merge_row(p.part_o + (slot0 * 64 + n) * kD, 64 * kD, p.part_lse + slot0 * 64 + n, 64, nseg,
-                  static_cast<uint8_t*>(p.out) + row * kD * (p.out_f32 ? 4 : 2), p.out_f32, p.lse + row, lane,
-                  tot, G, g0);
+
+    const int HQg = min(64, p.HQ - gy * 64);
+    if (b >= p.B || n >= HQg) return;
+    const int tiles_b = (max(__ldg(p.seq_lens + b), 0) + kTile - 1) / kTile;
+    const int64_t row = static_cast<int64_t>(b) * p.HQ + gy * 64 + n;
+    const int d = 4 * t;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = -INFINITY;
+    if (tiles_b > 0) {
+        // the clusters holding the first and last tile: the largest g with
+        // floor(g * tot / G) <= tile
+        const long long g0 = ((pre + 1) * G - 1) / tot;
+        const long long g1 = ((pre + tiles_b) * G - 1) / tot;
+        if (g0 == g1) return;  // one cluster held the whole request and wrote the output
+        const int nseg = static_cast<int>(g1 - g0 + 1);
+        const int64_t slot0 = static_cast<int64_t>(gy) * p.SPG + g0 + b;
+        const float* pl = p.part_lse + slot0 * 64 + n;
+        const float* po = p.part_o + (slot0 * 64 + n) * kD + d;
+        // the slot LSEs, 32 at a time, one per lane (each warp of the row
+        // computes the same weights)
+        float mx = -INFINITY;
+        for (int c0 = 0; c0 < nseg; c0 += 32)
+            mx = fmaxf(mx, c0 + lane < nseg ? pl[(c0 + lane) * 64] : -INFINITY);
+        mx = warp_max(mx);
+        if (mx != -INFINITY) {
+            float ws = 0.f;
+            for (int c0 = 0; c0 < nseg; c0 += 32) {
+                const float v = c0 + lane < nseg ? pl[(c0 + lane) * 64] : -INFINITY;
+                ws += v != -INFINITY ? expf(v - mx) : 0.f;
+            }
+            L = mx + logf(warp_sum(ws));
+            for (int c0 = 0; c0 < nseg; c0 += 32) {
+                const float v = c0 + lane < nseg ? pl[(c0 + lane) * 64] : -INFINITY;
+                const float wl = v != -INFINITY ? expf(v - L) : 0.f;
+                const int cn = min(32, nseg - c0);
+                const float* src = po + static_cast<int64_t>(c0) * 64 * kD;
+#pragma unroll 8
+                for (int k = 0; k < cn; ++k) {
+                    const float w = __shfl_sync(0xffffffffu, wl, k);
+                    // an empty slot (w = 0) was never written: read, then drop
+                    const float4 o = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(k) * 64 * kD);
+                    if (w != 0.f) {
+                        acc.x += w * o.x;
+                        acc.y += w * o.y;
+                        acc.z += w * o.z;
+                        acc.w += w * o.w;
+                    }
+                }
+            }
+        }
     }
+    if (p.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * kD + d) = acc;
+    } else {
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * kD + d) =
+            make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
+    if (t == 0) p.lse[row] = L;
     MLA_MTRACE(1);
 }
 
@@ -1081,6 +1270,23 @@ __global__ void __launch_bounds__(256) mla_merge_lse_kernel(const float* __restr
 }
 
 // ------------------------------------------------------------------ launch
+
+// Launch configuration that lets the grid start while the previous kernel
+// in the stream drains (the kernel calls griddep_wait() before touching
+// global memory that kernel may use).
+static cudaLaunchConfig_t pdl_config(dim3 grid, int threads, size_t smem, cudaStream_t stream,
+                                     cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
 
 template <int NP, bool LSU, int KIND>
 struct Variant {
@@ -1109,10 +1315,10 @@ struct Variant {
         return clusters[dev];
     }
 
-    static cudaError_t launch(const CUtensorMap& tl, const CUtensorMap& tr, const DecodeParams& p, int G, int GY,
-                              cudaStream_t stream) {
-        mla_decode_kernel<NP, LSU, KIND><<<dim3(2 * G, GY), kThreads, Cfg<NP>::kSmemBytes, stream>>>(tl, tr, p);
-        return cudaGetLastError();
+    static cudaError_t launch(const DecodeMaps& maps, const DecodeParams& p, int G, int GY, cudaStream_t stream) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pdl_config(dim3(2 * G, GY), kThreads, Cfg<NP>::kSmemBytes, stream, attr);
+        return cudaLaunchKernelEx(&cfg, mla_decode_kernel<NP, LSU, KIND>, maps, p);
     }
 };
 
@@ -1135,14 +1341,16 @@ int decode_clusters(int NP, bool lsu, int kind, int requested_ctas) {
 #undef MLA_PICK
 }
 
-cudaError_t launch_decode(const CUtensorMap& tl, const CUtensorMap& tr, const DecodeParams& p, int NP, bool lsu,
-                          int kind, int G, int GY, cudaStream_t stream) {
-#define MLA_LAUNCH(a, b, c) Variant<a, b, c>::launch(tl, tr, p, G, GY, stream)
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,
+                          cudaStream_t stream) {
+#define MLA_LAUNCH(a, b, c) Variant<a, b, c>::launch(maps, p, G, GY, stream)
     cudaError_t e = MLA_DISPATCH(NP, MLA_LAUNCH);
 #undef MLA_LAUNCH
     if (e != cudaSuccess) return e;
-    mla_decode_merge_kernel<<<dim3(p.B, GY), 256, 0, stream>>>(p, G);
-    return cudaGetLastError();
+    const int RB = (min(64, p.HQ) + 1) / 2;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(p.B) * RB, GY), 256, 0, stream, attr);
+    return cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel, p, G, 2 * G * GY);
 }
 
 cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, int64_t N, void* out, int out_f32,
@@ -1159,6 +1367,11 @@ cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, 
 #ifdef MLA_TRACE
 extern "C" __attribute__((visibility("default"))) int mla_trace_dump(void* host) {
     return static_cast<int>(cudaMemcpyFromSymbol(host, mla::g_trace, sizeof(mla::g_trace)));
+}
+extern "C" __attribute__((visibility("default"))) int mla_ttrace_dump(void* ttrace, void* ksm) {
+    cudaError_t e = cudaMemcpyFromSymbol(ttrace, mla::g_ttrace, sizeof(mla::g_ttrace));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    return static_cast<int>(cudaMemcpyFromSymbol(ksm, mla::g_ksm, sizeof(mla::g_ksm)));
 }
 extern "C" __attribute__((visibility("default"))) int mla_ktrace_dump(void* host) {
     cudaError_t e = cudaMemcpyFromSymbol(host, mla::g_ktrace, sizeof(mla::g_ktrace));

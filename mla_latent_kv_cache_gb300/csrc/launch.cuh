@@ -7,6 +7,10 @@
 
 namespace mla {
 
+// Per-CTA status record (int32 words): 0 status bits, 1 first wait site,
+// 2 its tile, 4 + role: (site << 24) | tile where that role gave up.
+constexpr int kStatusRecWords = 16;
+
 // Everything a decode launch needs; passed by value as a kernel parameter.
 struct DecodeParams {
     const __nv_bfloat16* q_lat;
@@ -18,7 +22,8 @@ struct DecodeParams {
     const int32_t* seq_lens;
     void* out;
     float* lse;
-    int* status;       // device status word (workspace header)
+    int* status;       // workspace header: status summary written by the merge step
+    int* rec;          // [CTAs][kStatusRecWords] per-CTA status records
     float* part_o;     // [GY][SPG][64][512] fp32 partial outputs
     float* part_lse;   // [GY][SPG][64] fp32 partial LSEs
     float scale_log2;  // softmax scale * log2(e)
@@ -35,8 +40,16 @@ cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const 
 // Clusters (of 2 CTAs) the decode kernel variant runs with: the number that
 // fit on the current device at once, or requested_ctas / 2 when given.
 int decode_clusters(int NP, bool lsu, int kind, int requested_ctas);
-cudaError_t launch_decode(const CUtensorMap& tmap_lat, const CUtensorMap& tmap_rope, const DecodeParams& p, int NP,
-                          bool lsu, int kind, int G, int GY, cudaStream_t stream);
+// TMA descriptors of one decode call: the pool as 64-dim latent chunks
+// (128-B swizzle) and 32-dim rope halves (64-B swizzle), unused when the
+// load/convert warps read the pool; the queries as 64-dim chunks of q_lat
+// and 32-dim halves of q_pe, NP rows high.
+struct DecodeMaps {
+    CUtensorMap lat, rope, q, qpe;
+};
+
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,
+                          cudaStream_t stream);
 cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, int64_t N, void* out, int out_f32,
                              float* lse, cudaStream_t stream);
 

@@ -155,6 +155,13 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start before the previous kernel in the stream ends;
+// griddep_wait() blocks until that kernel has finished and its writes are
+// visible. griddep_launch_dependents() lets the next such grid start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
