@@ -124,7 +124,12 @@ struct Cfg {
     static constexpr int kOffQ = kOffRope + kRR * kRopeBytes;
     static constexpr int kOffX = (kOffQ + kQBytes + 1023) / 1024 * 1024;
     static constexpr int kOffP = kOffX + kXBytes;
-    static constexpr int kOffCtrl = kOffP + kPBufs * kPBytes;
+    // Send buffer of the score exchange: the partial S is staged here and
+    // pushed to the peer by one bulk copy (NP <= 32; at NP = 64 it would cost
+    // a pair slot, so the rows go out as st.async stores instead).
+    static constexpr bool kBulkX = NP <= 32;
+    static constexpr int kOffSend = kOffP + kPBufs * kPBytes;
+    static constexpr int kOffCtrl = kOffSend + (kBulkX ? kXBytes : 0);
     static constexpr int kSmemBytes = kOffCtrl + 3072 + 1024;  // + control block, alignment slack
     // TMEM: two O accumulators of 2 x NP columns (one per alternating
     // segment, so a finished segment drains while the next accumulates),
@@ -896,11 +901,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 // send this CTA's partial scores once the peer has read the last ones
                 if (i > 0) group_wait(&ctrl->xfree, (i - 1) & 1, p, ctrl, kSiteXFree, i, true);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFree);
+                if constexpr (C::kBulkX) {
+                    // stage the row in the send buffer (same swizzled layout as the
+                    // peer's exchange buffer); one thread pushes the whole block
+                    uint8_t* sendb = smem + C::kOffSend;
 #pragma unroll
-                for (int u = 0; u < NP / 4; ++u)
-                    st_async_v4(x_peer + st * NP * 4 + ((u ^ xs) << 4), sr[4 * u], sr[4 * u + 1], sr[4 * u + 2],
-                                sr[4 * u + 3], xfull_peer);
-                if (st == 0) mbar_arrive_expect_tx(&ctrl->xfull, kXferBytes);
+                    for (int u = 0; u < NP / 4; ++u)
+                        *reinterpret_cast<uint4*>(sendb + st * NP * 4 + ((u ^ xs) << 4)) =
+                            make_uint4(sr[4 * u], sr[4 * u + 1], sr[4 * u + 2], sr[4 * u + 3]);
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, 128);
+                    if (st == 0) {
+                        mbar_arrive_expect_tx(&ctrl->xfull, kXferBytes);
+                        bulk_s2cluster(x_peer, sendb, kXferBytes, xfull_peer);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < NP / 4; ++u)
+                        st_async_v4(x_peer + st * NP * 4 + ((u ^ xs) << 4), sr[4 * u], sr[4 * u + 1], sr[4 * u + 2],
+                                    sr[4 * u + 3], xfull_peer);
+                    if (st == 0) mbar_arrive_expect_tx(&ctrl->xfull, kXferBytes);
+                }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmSent);
                 group_wait(&ctrl->xfull, i & 1, p, ctrl, kSiteXFull, i, true);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFull);

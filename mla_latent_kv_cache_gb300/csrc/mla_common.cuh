@@ -147,6 +147,17 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
         : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into another CTA's (cluster address), counted
+// as a transaction on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                               uint32_t remote_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
+        "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
+        : "memory");
+}
+
 // Arrive on an mbarrier in another CTA of the cluster without ordering this
 // thread's earlier memory operations (a release at cluster scope would wait
 // for its in-flight remote stores, about a microsecond). Used only to hand a
