@@ -164,7 +164,9 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     // TMA row coordinates of the queries are 32-bit
     if (static_cast<int64_t>(B) * HQ + 64 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
     const int NP = rows_padded(HQ < 64 ? HQ : 64);
-    const bool lsu = cache_kind == MLA_CACHE_FP8_DS_MLA_656 || (page_size % 8) != 0;
+    // pages whose rows cannot be fetched as 8-row TMA boxes go through the
+    // load/convert warps
+    const bool lsu = (page_size % 8) != 0;
     const int G = mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
     if (G <= 0) return MLA_ERR_CUDA;
     if (workspace_bytes < decode_ws_bytes(B, HQ, G)) return MLA_ERR_WORKSPACE;
@@ -198,16 +200,41 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
         if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
     }
     if (!lsu) {
+        // pool rows as 2-D tensors, gcd(page_size, 128) rows per box so a box
+        // never crosses a page
         const int br = gcd_int(page_size, 128);
-        cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(num_slots)};
-        cuuint64_t gstride[1] = {static_cast<cuuint64_t>(mla::kRowBf16)};
+        const bool fp8 = cache_kind == MLA_CACHE_FP8_DS_MLA_656;
+        const cuuint64_t row_bytes = fp8 ? mla::kRowFp8 : mla::kRowBf16;
         cuuint32_t estride[2] = {1u, 1u};
-        cuuint32_t box_lat[2] = {64u, static_cast<cuuint32_t>(br)};
+        CUresult r;
+        if (!fp8) {
+            cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(num_slots)};
+            cuuint64_t gstride[1] = {row_bytes};
+            cuuint32_t box_lat[2] = {64u, static_cast<cuuint32_t>(br)};
+            r = enc(&tmap_lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box_lat,
+                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+        } else {
+            // bytes of the 656-byte row: codes [0, 512), scales [512, 528)
+            cuuint64_t gdim[2] = {row_bytes, static_cast<cuuint64_t>(num_slots)};
+            cuuint64_t gstride[1] = {row_bytes};
+            cuuint32_t box_codes[2] = {256u, static_cast<cuuint32_t>(br)};
+            cuuint32_t box_scales[2] = {16u, static_cast<cuuint32_t>(br)};
+            r = enc(&tmap_lat, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), gdim, gstride, box_codes,
+                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+            r = enc(&maps.aux, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), gdim, gstride, box_scales,
+                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+        }
+        // rope: the row as bf16 elements; the rope half at element 512 (bf16)
+        // or 264 (fp8: byte 528) + 32 * rank
+        cuuint64_t gdim[2] = {row_bytes / 2, static_cast<cuuint64_t>(num_slots)};
+        cuuint64_t gstride[1] = {row_bytes};
         cuuint32_t box_rope[2] = {32u, static_cast<cuuint32_t>(br)};
-        CUresult r = enc(&tmap_lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride,
-                         box_lat, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
         r = enc(&tmap_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box_rope,
                 estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

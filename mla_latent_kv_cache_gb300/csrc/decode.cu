@@ -37,7 +37,9 @@
 //   warp 2      : tile-range scan at start
 //   warp 3      : lane 0 issues the O += C^T.P MMAs
 //   warps 4..7  : softmax, P, output epilogue (thread t <-> token t <-> TMEM lane t)
-//   warps 8..11 : load/convert producers (fp8 pools or odd page sizes)
+//   warps 8..11 : fp8 pools: expand the e4m3 codes that the TMA producer
+//                 landed in a tile's pair slots into bf16 in place; odd page
+//                 sizes: load/convert producers that read the pool directly
 //
 // Online softmax with a lazily raised maximum: m moves only when a score
 // exceeds it by more than 2^8 (log2 units), so P <= 256 and rescaling O is
@@ -108,6 +110,7 @@ __device__ unsigned long long g_mtrace[512][2];
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kPrefetchTiles = 2;          // L2 lookahead of the load/convert producers
+constexpr int kRawSlots = 3;               // fp8 tiles in flight between TMA and the expand warps
 
 template <int NP>
 struct Cfg {
@@ -147,6 +150,7 @@ struct Ctrl {
     uint64_t s_full[2], s_free[2], p_full, o_done[2], q_full;
     uint64_t xfull;          // the peer's partial S landed (st.async transactions + 1 local arrive)
     uint64_t xfree;          // the peer has read this CTA's last partial S (1 remote arrive)
+    uint64_t raw_full[3];    // fp8: a tile's codes and scales landed in its pair slots
     uint32_t tmem_base;
     int abort;
     int t_begin, t_end, b0, j0;
@@ -228,7 +232,7 @@ __device__ __forceinline__ void tmem_ld_np(uint32_t taddr, uint32_t (&r)[NP]) {
 enum WaitSite : int {
     kSiteQFull = 1, kSiteSFree, kSitePairFull, kSiteRopeFull, kSitePFull, kSiteTmaPairEmpty, kSiteTmaRopeEmpty,
     kSiteLsuPairEmpty, kSiteLsuRopeEmpty, kSiteSFull, kSiteXFree, kSiteXFull, kSiteOEpi, kSiteORescale, kSiteOPbuf,
-    kSiteOFinal
+    kSiteOFinal, kSiteRawFull
 };
 
 // This CTA's status record; zeroed by the CTA itself at launch and folded
@@ -314,8 +318,12 @@ __device__ __forceinline__ void dequant16(uint4 codes, float scale, uint4& lo, u
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Threads per CTA: 8 warps, plus 4 load/convert or expand warps.
+template <bool LSU, int KIND>
+constexpr int decode_threads() { return (LSU || KIND == 1) ? 384 : 256; }
+
 template <int NP, bool LSU, int KIND>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, KIND>(), 1)
     mla_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     const CUtensorMap& tmap_lat = maps.lat;
     const CUtensorMap& tmap_rope = maps.rope;
@@ -339,7 +347,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
     if (threadIdx.x == 0) {
         // TMA: one expect_tx arrival per fill; load/convert warps: one arrival per
         // warp that writes part of the fill (2 per pair, 4 per rope slot)
-        for (int i = 0; i < C::kRL; ++i) { mbar_init(&ctrl->pair_full[i], LSU ? 2 : 1); mbar_init(&ctrl->pair_empty[i], 1); }
+        // pair fill arrivals: TMA (1, with bytes), load/convert warps (2 per
+        // pair), expand warps (4 per pair)
+        constexpr int kPairArrivals = LSU ? 2 : (KIND == 1 ? 4 : 1);
+        for (int i = 0; i < C::kRL; ++i) { mbar_init(&ctrl->pair_full[i], kPairArrivals); mbar_init(&ctrl->pair_empty[i], 1); }
+        for (int i = 0; i < kRawSlots; ++i) mbar_init(&ctrl->raw_full[i], 1);
         for (int i = 0; i < C::kRR; ++i) { mbar_init(&ctrl->rope_full[i], LSU ? 4 : 1); mbar_init(&ctrl->rope_empty[i], 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->s_full[i], 1);
@@ -564,14 +576,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                         ftile = i;
                         break;
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->pair_full[slot], 2 * chunk_bytes);
+                    if constexpr (KIND == 0) {
+                        if (lane == 0) mbar_arrive_expect_tx(&ctrl->pair_full[slot], 2 * chunk_bytes);
+                        __syncwarp();
+                        if (lane < nruns) {
+                            uint8_t* dst = pair_ring + slot * C::kPairBytes + lane * BR * 128;
+#pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                tma_load_2d(dst + c * 16384, &tmap_lat, &ctrl->pair_full[slot],
+                                            256 * rank + 128 * pp + 64 * c, y, pol);
+                        }
+                    }
+                }
+                if (!ok) break;
+                if constexpr (KIND == 1) {
+                    // this CTA's 256 codes of each row ([row][256 B]) into the first
+                    // pair slot, the row's four scales ([row][16 B]) into the second
+                    const int s0 = (2 * i) % C::kRL, s1 = (2 * i + 1) % C::kRL;
+                    uint64_t* rb = &ctrl->raw_full[i % kRawSlots];
+                    if (lane == 0) mbar_arrive_expect_tx(rb, static_cast<uint32_t>(nruns * BR * (256 + 16)));
                     __syncwarp();
                     if (lane < nruns) {
-                        uint8_t* dst = pair_ring + slot * C::kPairBytes + lane * BR * 128;
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            tma_load_2d(dst + c * 16384, &tmap_lat, &ctrl->pair_full[slot], 256 * rank + 128 * pp + 64 * c,
-                                        y, pol);
+                        tma_load_2d(pair_ring + s0 * C::kPairBytes + lane * BR * 256, &tmap_lat, rb, 256 * rank, y, pol);
+                        tma_load_2d(pair_ring + s1 * C::kPairBytes + lane * BR * 16, &maps.aux, rb, 512, y, pol);
                     }
                 }
                 if (!ok) break;
@@ -587,7 +614,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 __syncwarp();
                 if (lane < nruns)
                     tma_load_2d(rope_ring + rr * C::kRopeBytes + lane * BR * 64, &tmap_rope, &ctrl->rope_full[rr],
-                                512 + 32 * rank, y, pol);
+                                (KIND == 0 ? 512 : 264) + 32 * rank, y, pol);
                 if (lane == 0) MLA_TRACE_POINT(i, kTrProdIssued);
                 it.next(p.seq_lens, p.B);
             }
@@ -596,6 +623,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(LSU ? 384 : 256, 1)
                 report(p, kRoleTma, fsite, ftile);
             }
             if (bad) atomicOr(status_rec(p), kErrBadBlock);
+        } else if (!LSU && KIND == 1 && warp >= 8) {
+            // ------------------------------------------------- fp8 expand warps
+            // Warp 8 + w expands rows [32w, 32w + 32) of each tile: two rows per
+            // step, a lane per 16 codes. All rows are read into registers and
+            // the four warps meet before any bf16 is written over the codes.
+            const int cw = warp - 8;
+            bool ok = true;
+            int ftile = 0;
+            for (int i = 0; i < ntiles; ++i) {
+                const int s0 = (2 * i) % C::kRL, s1 = (2 * i + 1) % C::kRL;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&ctrl->raw_full[i % kRawSlots], (i / kRawSlots) & 1, &ctrl->abort))) {
+                    ok = false;
+                    ftile = i;
+                }
+                // every expand warp reaches the barriers below, so a timeout in
+                // one warp cannot strand the others
+                if (!named_bar_and(4, 128, ok ? 1 : 0)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* codes = pair_ring + s0 * C::kPairBytes;
+                const uint8_t* scales = pair_ring + s1 * C::kPairBytes;
+                const int unit = lane & 15;
+                uint4 v[16];
+                float sc[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int row = 32 * cw + 2 * k + (lane >> 4);
+                    v[k] = *reinterpret_cast<const uint4*>(codes + row * 256 + unit * 16);
+                    sc[k] = *reinterpret_cast<const float*>(scales + row * 16 + 4 * (2 * rank + (unit >> 3)));
+                }
+                named_bar_sync(4, 128);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int row = 32 * cw + 2 * k + (lane >> 4);
+                    uint4 lo, hi;
+                    dequant16(v[k], sc[k], lo, hi);
+                    // dims 16*unit .. +16 of this CTA's 256: chunk unit/4 (64 dims),
+                    // 16-byte units 2*(unit%4), +1 within the 128-byte row
+                    const int c = unit >> 2, un = (unit & 3) * 2;
+                    uint8_t* rowp = pair_ring + (c < 2 ? s0 : s1) * C::kPairBytes + (c & 1) * 16384 + row * 128;
+                    *reinterpret_cast<uint4*>(rowp + ((un ^ (row & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(rowp + (((un + 1) ^ (row & 7)) << 4)) = hi;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ctrl->pair_full[s0]);
+                    mbar_arrive(&ctrl->pair_full[s1]);
+                }
+            }
+            if (!ok && lane == 0) {
+                fail(p, ctrl, kErrWaitTimeout, kSiteRawFull, ftile);
+                report(p, kRoleLsu0 + cw, kSiteRawFull, ftile);
+            }
         } else if (LSU && warp >= 8) {
             // ------------------------------------- load/convert producers
             // Each warp keeps a fixed, in-order share of every tile: warps 8/9 the
@@ -1311,7 +1394,7 @@ static cudaLaunchConfig_t pdl_config(dim3 grid, int threads, size_t smem, cudaSt
 
 template <int NP, bool LSU, int KIND>
 struct Variant {
-    static constexpr int kThreads = LSU ? 384 : 256;
+    static constexpr int kThreads = decode_threads<LSU, KIND>();
 
     // Set the shared-memory attribute (once per device) and return how many
     // clusters of 2 fit on the device at once.
@@ -1351,10 +1434,11 @@ static int pick_clusters(int requested_ctas) {
     return max(1, requested_ctas / 2);
 }
 
-#define MLA_DISPATCH(NPV, EXPR)                                                                         \
-    (kind == 1 ? (NPV == 16 ? EXPR(16, true, 1) : NPV == 32 ? EXPR(32, true, 1) : EXPR(64, true, 1)) \
-     : lsu     ? (NPV == 16 ? EXPR(16, true, 0) : NPV == 32 ? EXPR(32, true, 0) : EXPR(64, true, 0)) \
-               : (NPV == 16 ? EXPR(16, false, 0) : NPV == 32 ? EXPR(32, false, 0) : EXPR(64, false, 0)))
+#define MLA_DISPATCH_NP(NPV, EXPR, L, K) \
+    (NPV == 16 ? EXPR(16, L, K) : NPV == 32 ? EXPR(32, L, K) : EXPR(64, L, K))
+#define MLA_DISPATCH(NPV, EXPR)                                                                            \
+    (kind == 1 ? (lsu ? MLA_DISPATCH_NP(NPV, EXPR, true, 1) : MLA_DISPATCH_NP(NPV, EXPR, false, 1)) \
+               : (lsu ? MLA_DISPATCH_NP(NPV, EXPR, true, 0) : MLA_DISPATCH_NP(NPV, EXPR, false, 0)))
 
 int decode_clusters(int NP, bool lsu, int kind, int requested_ctas) {
 #define MLA_PICK(a, b, c) pick_clusters<Variant<a, b, c>>(requested_ctas)

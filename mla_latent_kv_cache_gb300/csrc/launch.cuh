@@ -40,12 +40,13 @@ cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const 
 // Clusters (of 2 CTAs) the decode kernel variant runs with: the number that
 // fit on the current device at once, or requested_ctas / 2 when given.
 int decode_clusters(int NP, bool lsu, int kind, int requested_ctas);
-// TMA descriptors of one decode call: the pool as 64-dim latent chunks
-// (128-B swizzle) and 32-dim rope halves (64-B swizzle), unused when the
-// load/convert warps read the pool; the queries as 64-dim chunks of q_lat
-// and 32-dim halves of q_pe, NP rows high.
+// TMA descriptors of one decode call, unused when the load/convert warps
+// read the pool. bf16 pools: lat = 64-dim latent chunks (128-B swizzle),
+// rope = 32-dim rope halves (64-B swizzle). fp8 pools: lat = 256 code bytes
+// of a row, aux = its 16 scale bytes, rope = 32-dim rope halves. q / qpe:
+// 64-dim chunks of q_lat and 32-dim halves of q_pe, NP rows high.
 struct DecodeMaps {
-    CUtensorMap lat, rope, q, qpe;
+    CUtensorMap lat, aux, rope, q, qpe;
 };
 
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,
