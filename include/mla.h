@@ -47,7 +47,9 @@ typedef enum {
     MLA_ERR_INVALID_ARG = -1,  /* bad size, null or misaligned pointer */
     MLA_ERR_UNSUPPORTED = -2,  /* valid request this build does not handle */
     MLA_ERR_WORKSPACE = -3,    /* workspace too small */
-    MLA_ERR_CUDA = -4          /* a CUDA runtime call or launch failed */
+    MLA_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
+    MLA_ERR_SCRATCH_LIMIT = -5 /* mla_decode_static_scratch: the call needs more
+                                  than MLA_STATIC_SCRATCH_BYTES of scratch */
 } mla_status;
 
 enum { MLA_CACHE_BF16_576 = 0, MLA_CACHE_FP8_DS_MLA_656 = 1 };
@@ -159,6 +161,32 @@ MLA_API int mla_merge_lse(const float* part_out, const float* part_lse, int S, i
 
 /* Number of SMs of the current device (what num_ctas = 0 means), or < 0. */
 MLA_API int mla_num_sms(void);
+
+/*
+ * mla_decode_static_scratch - mla_decode with its workspace taken from a
+ * scratch array that the library holds in device memory, for callers that
+ * cannot allocate: a C host with no device allocator, or a serving loop that
+ * must not call cudaMalloc on the decode path (cudaMalloc may synchronise the
+ * device and stall the other streams). The source pages have no counterpart;
+ * the operation is exactly mla_decode's, and every argument has the meaning
+ * mla_decode gives it.
+ *   MLA_STATIC_SCRATCH_BYTES bounds the scratch (one array per device, placed
+ *   when the library's device code is loaded). A call whose
+ *   mla_decode_workspace_bytes(B, q_len, Hq, num_ctas) exceeds it returns
+ *   MLA_ERR_SCRATCH_LIMIT and launches nothing; pass a smaller num_ctas or
+ *   use mla_decode with your own workspace.
+ *   Nothing in the scratch has to start at zero: each CTA clears its own
+ *   status record and the merge step rewrites the status header.
+ *   The first call on a device looks the array up (cudaGetSymbolAddress, which
+ *   may load the device code); make it before any stream capture. Calls share
+ *   one array per device, so calls that can overlap (different streams, or
+ *   several host threads) race on it: order them on one stream.
+ */
+#define MLA_STATIC_SCRATCH_BYTES (32u << 20)
+MLA_API int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const void* cache, int cache_kind,
+                                      int64_t num_slots, int page_size, const int32_t* block_table,
+                                      int64_t block_table_stride, const int32_t* seq_lens, int B, int q_len, int Hq,
+                                      float scale, void* out, int out_dtype, float* lse, int num_ctas, void* stream);
 
 /* Static English text for a status code. */
 MLA_API const char* mla_status_string(int status);

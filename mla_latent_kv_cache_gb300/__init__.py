@@ -62,6 +62,9 @@ def load() -> ctypes.CDLL:
             lib.mla_decode.argtypes = [vp, vp, vp, i32, i64, i32, vp, i64, vp, i32, i32, i32, f32, vp, i32, vp,
                                        vp, sz, i32, vp]
             lib.mla_decode.restype = i32
+            lib.mla_decode_static_scratch.argtypes = [vp, vp, vp, i32, i64, i32, vp, i64, vp, i32, i32, i32, f32, vp,
+                                                      i32, vp, i32, vp]
+            lib.mla_decode_static_scratch.restype = i32
             lib.mla_merge_lse.argtypes = [vp, vp, i32, i64, vp, i32, vp, vp]
             lib.mla_merge_lse.restype = i32
             _lib = lib
@@ -134,6 +137,25 @@ def mla_decode(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens,
                              Hq, float(scale), out.data_ptr(), out_dtype, lse.data_ptr(), workspace.data_ptr(),
                              workspace.numel() * workspace.element_size(), num_ctas, _stream(stream)),
            "mla_decode")
+
+
+def mla_decode_static_scratch(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens, q_len, scale, out,
+                              lse, num_ctas: int = 0, stream=None) -> None:
+    """mla_decode with the library's static device scratch as its workspace
+    (see include/mla.h: at most MLA_STATIC_SCRATCH_BYTES; calls sharing a
+    device must be ordered on one stream)."""
+    B = seq_lens.numel()
+    Hq = q_lat.shape[-2]
+    assert q_lat.is_contiguous() and q_pe.is_contiguous() and block_table.dtype == torch.int32
+    assert seq_lens.dtype == torch.int32 and lse.dtype == torch.float32
+    out_dtype = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
+    nbytes = cache.numel() * cache.element_size()
+    rb = mla_row_bytes(cache_kind)
+    _check(load().mla_decode_static_scratch(q_lat.data_ptr(), q_pe.data_ptr(), cache.data_ptr(), cache_kind,
+                                            nbytes // rb, page_size, block_table.data_ptr(), block_table.stride(0),
+                                            seq_lens.data_ptr(), B, q_len, Hq, float(scale), out.data_ptr(),
+                                            out_dtype, lse.data_ptr(), num_ctas, _stream(stream)),
+           "mla_decode_static_scratch")
 
 
 def mla_merge_lse(part_out: torch.Tensor, part_lse: torch.Tensor, out: torch.Tensor, lse=None, stream=None) -> None:

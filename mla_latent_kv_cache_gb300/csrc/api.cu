@@ -84,6 +84,25 @@ WsLayout decode_ws_layout(int B, int HQ, int G) {
 
 size_t decode_ws_bytes(int B, int HQ, int G) { return decode_ws_layout(B, HQ, G).total; }
 
+// Workspace of mla_decode_static_scratch: one array per device, placed when
+// this library's device code is loaded, for callers that cannot allocate.
+static __device__ __align__(256) unsigned char g_decode_scratch[MLA_STATIC_SCRATCH_BYTES];
+
+// Its address on the current device, looked up once per device.
+void* decode_scratch_ptr() {
+    static std::mutex mu;
+    static void* ptr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+        ptr[dev] = p;
+    }
+    return ptr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -99,6 +118,7 @@ const char* mla_status_string(int status) {
         case MLA_ERR_UNSUPPORTED: return "unsupported configuration or device";
         case MLA_ERR_WORKSPACE: return "workspace too small";
         case MLA_ERR_CUDA: return "CUDA error";
+        case MLA_ERR_SCRATCH_LIMIT: return "call needs more than the static decode scratch holds";
         default: return "unknown status";
     }
 }
@@ -270,6 +290,20 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     p.SPG = G + B;
     cudaError_t e = mla::launch_decode(maps, p, NP, lsu, cache_kind, G, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const void* cache, int cache_kind,
+                              int64_t num_slots, int page_size, const int32_t* block_table,
+                              int64_t block_table_stride, const int32_t* seq_lens, int B, int q_len, int Hq,
+                              float scale, void* out, int out_dtype, float* lse, int num_ctas, void* stream) {
+    const size_t need = mla_decode_workspace_bytes(B, q_len, Hq, num_ctas);
+    if (need == 0) return MLA_ERR_INVALID_ARG;
+    if (need > MLA_STATIC_SCRATCH_BYTES) return MLA_ERR_SCRATCH_LIMIT;
+    void* scratch = decode_scratch_ptr();
+    if (!scratch) return MLA_ERR_CUDA;
+    return mla_decode(q_lat, q_pe, cache, cache_kind, num_slots, page_size, block_table, block_table_stride,
+                      seq_lens, B, q_len, Hq, scale, out, out_dtype, lse, scratch, MLA_STATIC_SCRATCH_BYTES,
+                      num_ctas, stream);
 }
 
 int mla_merge_lse(const float* part_out, const float* part_lse, int S, int64_t N, void* out, int out_dtype,
