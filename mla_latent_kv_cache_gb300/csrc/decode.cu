@@ -120,26 +120,31 @@ struct Cfg {
     static constexpr int kRL = (NP == 16) ? 5 : 4;    // pair slots (2 per tile)
     static constexpr int kRR = (NP == 64) ? 1 : 3;    // rope slots (1 per tile; freed right after S)
     static constexpr int kQBytes = NP * (4 * 128 + 64);
-    static constexpr int kXBytes = 128 * NP * 4;      // the peer's partial S of one tile
+    // 32 and 64 query rows: the two CTAs split the softmax columns, each owning
+    // kNH of them; 16 rows: both run the whole softmax
+    static constexpr bool kSplit = NP >= 32;
+    static constexpr int kNH = kSplit ? NP / 2 : NP;
+    static constexpr int kXBytes = 128 * kNH * 4;     // the peer's partial S of this CTA's columns
     static constexpr int kPBufs = (NP == 64) ? 1 : 2; // P (bf16) buffers
     static constexpr int kPBytes = 128 * NP * 2;
     static constexpr int kOffRope = kRL * kPairBytes;
     static constexpr int kOffQ = kOffRope + kRR * kRopeBytes;
     static constexpr int kOffX = (kOffQ + kQBytes + 1023) / 1024 * 1024;
     static constexpr int kOffP = kOffX + kXBytes;
-    // Send buffer of the score exchange: the partial S is staged here and
-    // pushed to the peer by one bulk copy (NP <= 32; at NP = 64 it would cost
-    // a pair slot, so the rows go out as st.async stores instead).
-    static constexpr bool kBulkX = NP <= 32;
+    // Send buffer of the score exchange: the partial S of the peer's columns
+    // is staged here and pushed to the peer by one bulk copy.
     static constexpr int kOffSend = kOffP + kPBufs * kPBytes;
-    static constexpr int kOffCtrl = kOffSend + (kBulkX ? kXBytes : 0);
-    static constexpr int kSmemBytes = kOffCtrl + 3072 + 1024;  // + control block, alignment slack
+    static constexpr int kOffCtrl = kOffSend + kXBytes;
+    static constexpr int kSmemBytes = kOffCtrl + 3584 + 1024;  // + control block, alignment slack
     // TMEM: two O accumulators of 2 x NP columns (one per alternating
     // segment, so a finished segment drains while the next accumulates),
     // then two S buffers of NP columns
     static constexpr int kTmemCols = NP == 16 ? 128 : NP == 32 ? 256 : 512;
     static constexpr int kColS = 4 * NP;
-    static constexpr uint32_t kPSwizzle = NP == 16 ? kSw32 : NP == 32 ? kSw64 : kSw128;
+    // P: NP / kNH column blocks of [128 tokens][kNH bf16], MN-major, swizzled by
+    // the block width, so each CTA's softmax columns are one contiguous block
+    static constexpr uint32_t kPSwizzle = kNH == 16 ? kSw32 : kSw64;
+    static constexpr int kPBlockBytes = 128 * kNH * 2;
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(kTmemCols >= 32, "tmem");
 };
@@ -158,10 +163,15 @@ struct Ctrl {
     alignas(16) float m[64];         // running max per row (log2 units); read as float4
     alignas(16) float alpha[64];
     alignas(16) float red[4][64];
-    float dlt[64];                   // row sums of the segment being written out
-    float dm[64];                    // and its row maxima
+    alignas(16) float dlt[2][64];    // row sums of a finished segment, by segment parity
+    float dm[64];                    // and the row maxima of this CTA's columns
+    alignas(16) float palpha[2][32]; // the peer's rescale factors for its columns, by P buffer
+    alignas(16) int pflag[2][4];     // and whether it rescaled this tile
+    uint64_t pin[2];                 // the peer's P block and message landed (by P buffer)
+    uint64_t rp_free[2];             // the peer's P buffer may be written (its PV is done)
+    uint64_t dfull[2];               // the peer's row sums of a segment landed (by parity)
 };
-static_assert(sizeof(Ctrl) <= 3072, "control block");
+static_assert(sizeof(Ctrl) <= 3584, "control block");
 static_assert(offsetof(Ctrl, m) % 16 == 0 && offsetof(Ctrl, alpha) % 16 == 0, "vector loads of m / alpha");
 
 __device__ __forceinline__ int swz_p(int row, uint32_t mode) {
@@ -232,7 +242,7 @@ __device__ __forceinline__ void tmem_ld_np(uint32_t taddr, uint32_t (&r)[NP]) {
 enum WaitSite : int {
     kSiteQFull = 1, kSiteSFree, kSitePairFull, kSiteRopeFull, kSitePFull, kSiteTmaPairEmpty, kSiteTmaRopeEmpty,
     kSiteLsuPairEmpty, kSiteLsuRopeEmpty, kSiteSFull, kSiteXFree, kSiteXFull, kSiteOEpi, kSiteORescale, kSiteOPbuf,
-    kSiteOFinal, kSiteRawFull
+    kSiteOFinal, kSiteRawFull, kSiteDFull, kSitePIn, kSiteRpFree
 };
 
 // This CTA's status record; zeroed by the CTA itself at launch and folded
@@ -362,6 +372,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
         mbar_init(&ctrl->q_full, 1);
         mbar_init(&ctrl->xfull, 1);
         mbar_init(&ctrl->xfree, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctrl->pin[i], 1);
+            mbar_init(&ctrl->rp_free[i], 1);
+            mbar_init(&ctrl->dfull[i], 1);
+        }
         ctrl->abort = 0;
         fence_mbar_init();
     }
@@ -523,7 +538,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             TileIt it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint32_t idPV = idesc_bf16(128, NP, true, true);
-            constexpr uint32_t p_sbo = 8 * NP * 2;
+            constexpr uint32_t p_sbo = 8 * C::kNH * 2;
             int seg = -1;
             for (int i = 0; i < ntiles; ++i) {
                 const bool new_seg = (i == 0) || (it.j == 0);
@@ -536,14 +551,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 }
                 tc_fence_after();
                 MLA_TRACE_POINT(i, kTrPvIssue);
-                const uint64_t dp = smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), p_sbo, p_sbo, C::kPSwizzle);
+                const uint64_t dp = smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), C::kPBlockBytes, p_sbo,
+                                              C::kPSwizzle);
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     const int slot = (2 * i + mt) % C::kRL;
                     const uint64_t da = smem_desc(smem_u32(pair_ring + slot * C::kPairBytes), 16384, 1024, kSw128);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16(tO + mt * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
+                        umma_bf16(tO + mt * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * C::kNH * 2) >> 4), idPV,
                                   (new_seg && kk == 0) ? 0u : 1u);
                     umma_commit(&ctrl->pair_empty[slot]);
                 }
@@ -827,15 +843,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             const uint32_t x_local = smem_u32(xbuf);
             const uint32_t x_peer = mapa_shared(x_local, peer);
             const uint32_t xfull_peer = mapa_shared(smem_u32(&ctrl->xfull), peer);
-            constexpr uint32_t kXferBytes = 128 * NP * 4;
             const uint32_t xfree_peer = mapa_shared(smem_u32(&ctrl->xfree), peer);
-            // 16-byte unit swizzle of the exchange rows (NP/4 units per row)
-            const int xs = (NP == 16) ? ((st >> 1) & 3) : (st & 7);
+            // Softmax columns of this CTA: [own0, own0 + NH); the partial scores of
+            // [snd0, snd0 + NH) go to the peer (all columns when not split).
+            constexpr int NH = C::kNH;
+            constexpr uint32_t kXferBytes = 128 * NH * 4;
+            const int own0 = C::kSplit ? rank * NH : 0;
+            const int snd0 = C::kSplit ? peer * NH : 0;
+            // 16-byte unit swizzle of the exchange rows (NH/4 units per row)
+            const int xs = (NH == 16) ? ((st >> 1) & 3) : (st & 7);
             TileIt it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
-            float l[NP];
+            float l[NH];
 #pragma unroll
-            for (int c = 0; c < NP; ++c) l[c] = 0.f;
+            for (int c = 0; c < NH; ++c) l[c] = 0.f;
             int seg_start_j = it.j;
             bool seg_has_pv = false;
             int seg = 0;               // segment index: its O accumulator is (seg & 1)
@@ -854,6 +875,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             constexpr int kDC = 8;  // columns per drain step
             const int dr_per_half = (HQg + kDC - 1) / kDC;
 
+            // O columns [col0, col0 + NH) of accumulator ob, both 128-dim halves,
+            // times alpha[0 .. NH) (the caller has waited for the last PV into it)
+            auto rescale_o = [&](uint32_t ob, int col0, const float* alpha) {
+                tc_fence_after();
+                __syncwarp();
+#pragma unroll 1
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll 1
+                    for (int c0 = 0; c0 < NH; c0 += 16) {
+                        uint32_t o[16];
+                        tmem_ld_x16(tmem + lane_base + ob + mt * NP + col0 + c0, o);
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc) o[cc] = __float_as_uint(__uint_as_float(o[cc]) * alpha[c0 + cc]);
+                        tmem_st_x16(tmem + lane_base + ob + mt * NP + col0 + c0, o);
+                    }
+                tmem_wait_st();
+            };
+
             // This CTA's half of the NP query rows of request bq (row group gy)
             // by TMA, in the layout S reads as its B operand: latent chunks
             // 256*rank + 64k (k = 0..3) K-major with 128-B swizzle at k*NP*128,
@@ -870,42 +909,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 tma_load_2d(qs + 4 * NP * 128, &maps.qpe, &ctrl->q_full, 32 * rank, y, pol);
             };
 
-            // Row sums and maxima of the segment that just ended into dlt / dm,
-            // then fresh softmax state for the next one.
-            auto capture = [&](int i) {
+            // Row sums and maxima of segment sg, which just ended, into
+            // dlt[sg & 1] / dm (this CTA's columns; with split columns the sums
+            // also go to the peer, whose drain needs every column's), then fresh
+            // softmax state for the next segment.
+            auto capture = [&](int i, int sg) {
                 if (st == 0) MLA_TRACE_POINT(i, kTrEpiStart);
 #pragma unroll
-                for (int c = 0; c < NP; ++c) {
+                for (int c = 0; c < NH; ++c) {
                     const float v = warp_sum(l[c]);
                     if (lane == 0) ctrl->red[sw][c] = v;
                 }
                 named_bar_sync(1, 128);
-                if (st < NP) {
-                    ctrl->dlt[st] = ctrl->red[0][st] + ctrl->red[1][st] + ctrl->red[2][st] + ctrl->red[3][st];
-                    ctrl->dm[st] = ctrl->m[st];
-                    ctrl->m[st] = -INFINITY;
+                float* dl = ctrl->dlt[sg & 1];
+                if (st < NH) {
+                    const int c = own0 + st;
+                    dl[c] = ctrl->red[0][st] + ctrl->red[1][st] + ctrl->red[2][st] + ctrl->red[3][st];
+                    ctrl->dm[c] = ctrl->m[c];
+                    ctrl->m[c] = -INFINITY;
                 }
 #pragma unroll
-                for (int c = 0; c < NP; ++c) l[c] = 0.f;
+                for (int c = 0; c < NH; ++c) l[c] = 0.f;
                 named_bar_sync(1, 128);
+                if constexpr (C::kSplit) {
+                    if (st == 0) mbar_arrive_expect_tx(&ctrl->dfull[sg & 1], NH * 4);
+                    if (st < NH / 4) {
+                        const float4 v = reinterpret_cast<const float4*>(dl + own0)[st];
+                        st_async_v4(mapa_shared(smem_u32(dl + own0 + 4 * st), peer), __float_as_uint(v.x),
+                                    __float_as_uint(v.y), __float_as_uint(v.z), __float_as_uint(v.w),
+                                    mapa_shared(smem_u32(&ctrl->dfull[sg & 1]), peer));
+                    }
+                }
                 if (st == 0) MLA_TRACE_POINT(i, kTrEpiRed);
             };
 
-            // The captured segment (accumulator src) has finished its last PV:
-            // write its LSE and start draining its rows.
-            auto start_drain = [&](uint32_t src) {
+            // The captured segment sg (accumulator src) has finished its last
+            // PV: write the LSE of this CTA's columns and start draining its rows
+            // (every column, once the peer's row sums are in).
+            int dr_sg = 0;
+            auto start_drain = [&](uint32_t src, int sg, int i) {
+                if constexpr (C::kSplit) group_wait(&ctrl->dfull[sg & 1], (sg >> 1) & 1, p, ctrl, kSiteDFull, i, true);
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + pend_b;
-                if (rank == 0 && st < HQg) {
-                    const float lt = ctrl->dlt[st];
-                    const float lv = lt > 0.f ? (ctrl->dm[st] + log2f(lt)) * kLn2 : -INFINITY;
-                    if (pend_final) p.lse[static_cast<int64_t>(pend_b) * p.HQ + gy * 64 + st] = lv;
-                    else p.part_lse[pslot * 64 + st] = lv;
+                const int c = own0 + st;
+                if (st < NH && c < HQg && (C::kSplit || rank == 0)) {
+                    const float lt = ctrl->dlt[sg & 1][c];
+                    const float lv = lt > 0.f ? (ctrl->dm[c] + log2f(lt)) * kLn2 : -INFINITY;
+                    if (pend_final) p.lse[static_cast<int64_t>(pend_b) * p.HQ + gy * 64 + c] = lv;
+                    else p.part_lse[pslot * 64 + c] = lv;
                 }
                 dr_left = 2 * dr_per_half;
                 dr_step = 0;
                 dr_b = pend_b;
                 dr_final = pend_final;
                 dr_obuf = src;
+                dr_sg = sg;
                 pend = false;
             };
 
@@ -922,7 +979,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 for (int cc = 0; cc < kDC; ++cc) {
                     const int c = c0 + cc;
                     if (c < HQg) {
-                        const float lt = ctrl->dlt[c];
+                        const float lt = ctrl->dlt[dr_sg & 1][c];
                         const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
                         if (dr_final) {
                             const int64_t idx = (static_cast<int64_t>(dr_b) * p.HQ + gy * 64 + c) * kD + d;
@@ -952,7 +1009,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                         tc_fence_before();
                     }
                     if (st == 0) MLA_TRACE_POINT(i, kTrEpiHalf);
-                    capture(i);
+                    capture(i, seg);
                     pend = true;
                     seg_has_pv = false;
                     ++seg;
@@ -973,6 +1030,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 uint32_t sr[NP];
                 tmem_ld_np<NP>(tmem + lane_base + C::kColS + (i & 1) * NP, sr);
                 tc_fence_before();
+                // partial score of own column k / of the peer's column k (indices
+                // stay compile-time constants so sr[] remains in registers)
+                auto own_s = [&](int k) -> uint32_t {
+                    if constexpr (C::kSplit) return rank ? sr[NH + k] : sr[k];
+                    else return sr[k];
+                };
+                auto snd_s = [&](int k) -> uint32_t {
+                    if constexpr (C::kSplit) return rank ? sr[k] : sr[NH + k];
+                    else return sr[k];
+                };
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmTmemLd);
                 if (st == 0 && (i == 0 || j == 0) && !last_of_seg) {
                     // warm L2 with the next request's queries and page list
@@ -984,57 +1051,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 // send this CTA's partial scores once the peer has read the last ones
                 if (i > 0) group_wait(&ctrl->xfree, (i - 1) & 1, p, ctrl, kSiteXFree, i, true);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFree);
-                if constexpr (C::kBulkX) {
-                    // stage the row in the send buffer (same swizzled layout as the
-                    // peer's exchange buffer); one thread pushes the whole block
+                {
+                    // stage columns [snd0, snd0 + NH) of the row in the send buffer
+                    // (the peer's exchange-buffer layout); one thread pushes the block
                     uint8_t* sendb = smem + C::kOffSend;
 #pragma unroll
-                    for (int u = 0; u < NP / 4; ++u)
-                        *reinterpret_cast<uint4*>(sendb + st * NP * 4 + ((u ^ xs) << 4)) =
-                            make_uint4(sr[4 * u], sr[4 * u + 1], sr[4 * u + 2], sr[4 * u + 3]);
+                    for (int u = 0; u < NH / 4; ++u)
+                        *reinterpret_cast<uint4*>(sendb + st * NH * 4 + ((u ^ xs) << 4)) =
+                            make_uint4(snd_s(4 * u), snd_s(4 * u + 1), snd_s(4 * u + 2), snd_s(4 * u + 3));
                     fence_proxy_async_smem();
                     named_bar_sync(1, 128);
                     if (st == 0) {
                         mbar_arrive_expect_tx(&ctrl->xfull, kXferBytes);
                         bulk_s2cluster(x_peer, sendb, kXferBytes, xfull_peer);
                     }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < NP / 4; ++u)
-                        st_async_v4(x_peer + st * NP * 4 + ((u ^ xs) << 4), sr[4 * u], sr[4 * u + 1], sr[4 * u + 2],
-                                    sr[4 * u + 3], xfull_peer);
-                    if (st == 0) mbar_arrive_expect_tx(&ctrl->xfull, kXferBytes);
                 }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmSent);
                 group_wait(&ctrl->xfull, i & 1, p, ctrl, kSiteXFull, i, true);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFull);
-                float x[NP];
+                // x[k]: full score of column own0 + k
+                float x[NH];
 #pragma unroll
-                for (int u = 0; u < NP / 4; ++u) {
-                    const float4 v = *reinterpret_cast<const float4*>(xbuf + st * NP * 4 + ((u ^ xs) << 4));
-                    x[4 * u] = __uint_as_float(sr[4 * u]) + v.x;
-                    x[4 * u + 1] = __uint_as_float(sr[4 * u + 1]) + v.y;
-                    x[4 * u + 2] = __uint_as_float(sr[4 * u + 2]) + v.z;
-                    x[4 * u + 3] = __uint_as_float(sr[4 * u + 3]) + v.w;
+                for (int u = 0; u < NH / 4; ++u) {
+                    const float4 v = *reinterpret_cast<const float4*>(xbuf + st * NH * 4 + ((u ^ xs) << 4));
+                    x[4 * u] = __uint_as_float(own_s(4 * u)) + v.x;
+                    x[4 * u + 1] = __uint_as_float(own_s(4 * u + 1)) + v.y;
+                    x[4 * u + 2] = __uint_as_float(own_s(4 * u + 2)) + v.z;
+                    x[4 * u + 3] = __uint_as_float(own_s(4 * u + 3)) + v.w;
                 }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXRead);
 
                 const int tok = j * kTile + st;
                 const bool all_vis = (j * kTile + kTile + p.Qt - 1) <= T;
-                const float4* m4 = reinterpret_cast<const float4*>(ctrl->m);
+                const float4* m4 = reinterpret_cast<const float4*>(ctrl->m + own0);
                 if (all_vis) {
                     // every real row sees every token of the tile
 #pragma unroll
-                    for (int c = 0; c < NP; ++c) x[c] = (c < HQg) ? x[c] * p.scale_log2 : -INFINITY;
+                    for (int c = 0; c < NH; ++c) x[c] = (own0 + c < HQg) ? x[c] * p.scale_log2 : -INFINITY;
                 } else {
                     // tail of a request: per-row causal limit and the end of the request
 #pragma unroll
-                    for (int c = 0; c < NP; ++c)
-                        x[c] = (tok + ctrl->colvis[c] < T) ? x[c] * p.scale_log2 : -INFINITY;
+                    for (int c = 0; c < NH; ++c)
+                        x[c] = (tok + ctrl->colvis[own0 + c] < T) ? x[c] * p.scale_log2 : -INFINITY;
                 }
                 int need = 0;
 #pragma unroll
-                for (int u = 0; u < NP / 4; ++u) {
+                for (int u = 0; u < NH / 4; ++u) {
                     const float4 mv = m4[u];
                     need |= (x[4 * u] > mv.x + kRescaleThreshold) | (x[4 * u + 1] > mv.y + kRescaleThreshold) |
                             (x[4 * u + 2] > mv.z + kRescaleThreshold) | (x[4 * u + 3] > mv.w + kRescaleThreshold);
@@ -1051,43 +1113,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 }
                 if (need) {
 #pragma unroll
-                    for (int c = 0; c < NP; ++c) {
+                    for (int c = 0; c < NH; ++c) {
                         const float v = warp_max(x[c]);
                         if (lane == 0) ctrl->red[sw][c] = v;
                     }
                     named_bar_sync(1, 128);
-                    if (st < NP) {
+                    if (st < NH) {
+                        const int c = own0 + st;
                         const float mt = fmaxf(fmaxf(ctrl->red[0][st], ctrl->red[1][st]),
                                                fmaxf(ctrl->red[2][st], ctrl->red[3][st]));
-                        const float mo = ctrl->m[st];
+                        const float mo = ctrl->m[c];
                         const float mn = fmaxf(mo, mt);
-                        ctrl->alpha[st] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
-                        ctrl->m[st] = mn;
+                        ctrl->alpha[c] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
+                        ctrl->m[c] = mn;
                     }
                     named_bar_sync(1, 128);
 #pragma unroll
-                    for (int c = 0; c < NP; ++c) l[c] *= ctrl->alpha[c];
+                    for (int c = 0; c < NH; ++c) l[c] *= ctrl->alpha[own0 + c];
                     if (seg_has_pv) {
                         // O holds earlier tiles of this segment: wait for their PV, rescale
                         group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i);
-                        tc_fence_after();
-                        __syncwarp();
-#pragma unroll 1
-                        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll 1
-                            for (int c0 = 0; c0 < NP; c0 += 16) {
-                                uint32_t o[16];
-                                tmem_ld_x16(tmem + lane_base + obuf + mt * NP + c0, o);
-#pragma unroll
-                                for (int cc = 0; cc < 16; ++cc)
-                                    o[cc] = __float_as_uint(__uint_as_float(o[cc]) * ctrl->alpha[c0 + cc]);
-                                tmem_st_x16(tmem + lane_base + obuf + mt * NP + c0, o);
-                            }
-                        tmem_wait_st();
+                        rescale_o(obuf, own0, ctrl->alpha + own0);
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < NP / 4; ++u) {
+                for (int u = 0; u < NH / 4; ++u) {
                     const float4 mv = m4[u];
                     const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
@@ -1113,11 +1163,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                     if (!okp && lane == 0) fail(p, ctrl, kErrWaitTimeout, kSiteOPbuf, i);
                 }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmExp);
-                // P row `st`: NP bf16, MN-major, swizzled as the MMA reads it
-                uint8_t* prow = pbufs + (i % C::kPBufs) * C::kPBytes + st * NP * 2;
+                const int pb = i % C::kPBufs;
+                if constexpr (C::kSplit) {
+                    // this CTA's PV(i - kPBufs) is done: the peer may write its P
+                    // block of tile i into this CTA's P buffer
+                    if (st == 0 && i >= C::kPBufs)
+                        mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&ctrl->rp_free[pb]), peer));
+                    if (st == 0) mbar_arrive_expect_tx(&ctrl->pin[pb], C::kPBlockBytes + NH * 4 + 16);
+                }
+                // P row `st` of this CTA's column block: NH bf16, MN-major, swizzled
+                // as the MMA reads it
+                uint8_t* pblk = pbufs + pb * C::kPBytes + (own0 / NH) * C::kPBlockBytes;
+                uint8_t* prow = pblk + st * NH * 2;
                 const int sz = swz_p(st, C::kPSwizzle);
 #pragma unroll
-                for (int u = 0; u < NP / 8; ++u) {
+                for (int u = 0; u < NH / 8; ++u) {
                     const uint4 v = make_uint4(pack_bf16x2(x[8 * u + 0], x[8 * u + 1]), pack_bf16x2(x[8 * u + 2], x[8 * u + 3]),
                                                pack_bf16x2(x[8 * u + 4], x[8 * u + 5]), pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
                     *reinterpret_cast<uint4*>(prow + ((u ^ sz) << 4)) = v;
@@ -1140,6 +1200,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 fence_proxy_async_smem();
                 tc_fence_before();
                 named_bar_sync(1, 128);
+                if constexpr (C::kSplit) {
+                    if (st == 0 && !ctrl->abort) {
+                        // push this CTA's P block and rescale message into the peer's
+                        // P buffer once its PV(i - kPBufs) is done
+                        bool okr = true;
+                        if (i >= C::kPBufs)
+                            okr = mbar_wait_cluster(&ctrl->rp_free[pb], ((i / C::kPBufs) - 1) & 1, &ctrl->abort);
+                        if (!okr) {
+                            fail(p, ctrl, kErrWaitTimeout, kSiteRpFree, i);
+                            report(p, kRoleSoftmax, kSiteRpFree, i);
+                        } else {
+                            const uint32_t pin_peer = mapa_shared(smem_u32(&ctrl->pin[pb]), peer);
+                            bulk_s2cluster(mapa_shared(smem_u32(pblk), peer), pblk, C::kPBlockBytes, pin_peer);
+                            const uint32_t* al = reinterpret_cast<const uint32_t*>(ctrl->alpha + own0);
+                            const uint32_t pa = mapa_shared(smem_u32(ctrl->palpha[pb]), peer);
+#pragma unroll
+                            for (int u = 0; u < NH / 4; ++u)
+                                st_async_v4(pa + 16 * u, al[4 * u], al[4 * u + 1], al[4 * u + 2], al[4 * u + 3], pin_peer);
+                            st_async_v4(mapa_shared(smem_u32(ctrl->pflag[pb]), peer), static_cast<uint32_t>(need), 0u,
+                                        0u, 0u, pin_peer);
+                        }
+                    }
+                    // the peer's P block and message: then its rescale of its
+                    // columns applies to this CTA's O before PV(i)
+                    group_wait(&ctrl->pin[pb], (i / C::kPBufs) & 1, p, ctrl, kSitePIn, i, true);
+                    if (ctrl->pflag[pb][0] && seg_has_pv) {
+                        group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i);
+                        rescale_o(obuf, snd0, ctrl->palpha[pb]);
+                        tc_fence_before();
+                    }
+                    named_bar_sync(1, 128);
+                }
                 if (ctrl->abort) { alive = false; break; }  // same value in every thread after the barrier
                 if (st == 0) {
                     MLA_TRACE_POINT(i, kTrSmPArrive);
@@ -1151,7 +1243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                     // PV(i-1), the captured segment's last, is long done by now
                     group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteOEpi, i);
                     tc_fence_after();
-                    start_drain(obuf ^ (2 * NP));
+                    start_drain(obuf ^ (2 * NP), seg - 1, i);
                     if (st == 0) MLA_TRACE_POINT(i, kTrEpiStored);
                 } else if (dr_left > 0) {
                     tc_fence_after();
@@ -1171,12 +1263,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 const int il = ntiles - 1;
                 tc_fence_after();
                 while (dr_left > 0) drain_step();
-                capture(il + 1);
+                capture(il + 1, seg);
                 group_wait(&ctrl->o_done[il & 1], (il >> 1) & 1, p, ctrl, kSiteOFinal, il);
                 named_bar_sync(1, 128);
                 if (!ctrl->abort) {  // same value in every thread after the barrier
                     tc_fence_after();
-                    start_drain(obuf);
+                    start_drain(obuf, seg, il + 1);
                     while (dr_left > 0) drain_step();
                     if (st == 0) MLA_TRACE_POINT(il + 1, kTrEpiEnd);
                 }
