@@ -366,7 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->s_full[i], 1);
             mbar_init(&ctrl->s_free[i], 1);
-            mbar_init(&ctrl->o_done[i], 1);
+            mbar_init(&ctrl->o_done[i], 2);  // one commit per PV issuer
         }
         mbar_init(&ctrl->p_full, 1);
         mbar_init(&ctrl->q_full, 1);
@@ -533,8 +533,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 MLA_TRACE_POINT(i, kTrSIssued);
                 it.next(p.seq_lens, p.B);
             }
-        } else if (warp == 3 && lane == 0) {
-            // ------------------------------------------------- PV issuer
+        } else if ((warp == 3 || warp == 2) && lane == 0) {
+            // ------------------------------------------------- PV issuers
+            // warp 3 issues the first 128 latent dims of this CTA (O half 0), warp
+            // 2 the second: independent accumulators, so two threads halve the
+            // issue time and the pair slots come free sooner
+            const int mt = warp == 3 ? 0 : 1;
             TileIt it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint32_t idPV = idesc_bf16(128, NP, true, true);
@@ -550,21 +554,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                     break;
                 }
                 tc_fence_after();
-                MLA_TRACE_POINT(i, kTrPvIssue);
+                if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssue);
                 const uint64_t dp = smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), C::kPBlockBytes, p_sbo,
                                               C::kPSwizzle);
+                const int slot = (2 * i + mt) % C::kRL;
+                const uint64_t da = smem_desc(smem_u32(pair_ring + slot * C::kPairBytes), 16384, 1024, kSw128);
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    const int slot = (2 * i + mt) % C::kRL;
-                    const uint64_t da = smem_desc(smem_u32(pair_ring + slot * C::kPairBytes), 16384, 1024, kSw128);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16(tO + mt * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * C::kNH * 2) >> 4), idPV,
-                                  (new_seg && kk == 0) ? 0u : 1u);
-                    umma_commit(&ctrl->pair_empty[slot]);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16(tO + mt * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * C::kNH * 2) >> 4), idPV,
+                              (new_seg && kk == 0) ? 0u : 1u);
+                umma_commit(&ctrl->pair_empty[slot]);
                 umma_commit(&ctrl->o_done[i & 1]);
-                MLA_TRACE_POINT(i, kTrPvIssued);
+                if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssued);
                 it.next(p.seq_lens, p.B);
             }
         } else if (!LSU && warp == 1) {
@@ -947,20 +948,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             // PV: write the LSE of this CTA's columns and start draining its rows
             // (every column, once the peer's row sums are in).
             int dr_sg = 0;
-            auto start_drain = [&](uint32_t src, int sg, int i) {
+            auto start_drain = [&](uint32_t src, int sg, int i, int sb, bool sfinal) {
                 if constexpr (C::kSplit) group_wait(&ctrl->dfull[sg & 1], (sg >> 1) & 1, p, ctrl, kSiteDFull, i, true);
-                const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + pend_b;
+                const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + sb;
                 const int c = own0 + st;
                 if (st < NH && c < HQg && (C::kSplit || rank == 0)) {
                     const float lt = ctrl->dlt[sg & 1][c];
                     const float lv = lt > 0.f ? (ctrl->dm[c] + log2f(lt)) * kLn2 : -INFINITY;
-                    if (pend_final) p.lse[static_cast<int64_t>(pend_b) * p.HQ + gy * 64 + c] = lv;
+                    if (sfinal) p.lse[static_cast<int64_t>(sb) * p.HQ + gy * 64 + c] = lv;
                     else p.part_lse[pslot * 64 + c] = lv;
                 }
                 dr_left = 2 * dr_per_half;
                 dr_step = 0;
-                dr_b = pend_b;
-                dr_final = pend_final;
+                dr_b = sb;
+                dr_final = sfinal;
                 dr_obuf = src;
                 dr_sg = sg;
                 pend = false;
@@ -994,27 +995,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 --dr_left;
             };
 
+            // The request and kind of the segment captured last (drained once its
+            // last PV is done).
+            int cap_b = 0;
+            bool cap_final = false;
+
+            // Hand tile t to the PV issuer: with split columns, wait for the peer's
+            // P block and message and apply its rescale to this CTA's O first;
+            // then start or advance the drain. False when the group aborts.
+            auto finish = [&](int t) -> bool {
+                if constexpr (C::kSplit) {
+                    const int fpb = t % C::kPBufs;
+                    group_wait(&ctrl->pin[fpb], (t / C::kPBufs) & 1, p, ctrl, kSitePIn, t, true);
+                    if (ctrl->pflag[fpb][0] && seg_has_pv) {
+                        group_wait(&ctrl->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, p, ctrl, kSiteORescale, t);
+                        rescale_o(obuf, snd0, ctrl->palpha[fpb]);
+                        tc_fence_before();
+                    }
+                    named_bar_sync(1, 128);
+                }
+                if (ctrl->abort) return false;  // same value in every thread after the barrier
+                if (st == 0) {
+                    MLA_TRACE_POINT(t, kTrSmPArrive);
+                    MLA_TTRACE(t);
+                    mbar_arrive(&ctrl->p_full);
+                }
+                seg_has_pv = true;
+                if (pend) {
+                    // PV(t-1), the captured segment's last, is long done by now
+                    group_wait(&ctrl->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, p, ctrl, kSiteOEpi, t);
+                    tc_fence_after();
+                    start_drain(obuf ^ (2 * NP), seg - 1, t, cap_b, cap_final);
+                    if (st == 0) MLA_TRACE_POINT(t, kTrEpiStored);
+                } else if (dr_left > 0) {
+                    tc_fence_after();
+                    drain_step();
+                    tc_fence_before();
+                }
+                return true;
+            };
+
             if (st == 0) issue_q(it.b);
             bool alive = true;
             for (int i = 0; i < ntiles; ++i) {
                 const int b = it.b, j = it.j, T = it.T;
                 const bool last_of_seg = (j == it.tiles - 1) || (i == ntiles - 1);
-                if (i > 0 && j == 0) {
-                    // the previous segment ended with tile i-1. The older one still
-                    // draining (if any) finishes first: its accumulator is the one
-                    // this segment will use, and dlt / dm are about to be replaced.
-                    if (dr_left > 0) {
-                        tc_fence_after();
-                        while (dr_left > 0) drain_step();
-                        tc_fence_before();
-                    }
-                    if (st == 0) MLA_TRACE_POINT(i, kTrEpiHalf);
-                    capture(i, seg);
-                    pend = true;
-                    seg_has_pv = false;
-                    ++seg;
-                    obuf = (seg & 1) * 2 * NP;
-                }
                 group_wait(&ctrl->s_full[i & 1], (i >> 1) & 1, p, ctrl, kSiteSFull, i);
                 if (st == 0) {
                     MLA_TRACE_POINT(i, kTrSmSFull);
@@ -1067,6 +1092,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                     }
                 }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmSent);
+                if (i > 0 && j == 0) {
+                    // the previous segment ended with tile i-1. The older one still
+                    // draining (if any) finishes first: its accumulator is the one
+                    // this segment will use, and dlt / dm are about to be replaced.
+                    if (dr_left > 0) {
+                        tc_fence_after();
+                        while (dr_left > 0) drain_step();
+                        tc_fence_before();
+                    }
+                    if (st == 0) MLA_TRACE_POINT(i, kTrEpiHalf);
+                    capture(i, seg);
+                    pend = true;
+                    cap_b = pend_b;
+                    cap_final = pend_final;
+                    seg_has_pv = false;
+                    ++seg;
+                    obuf = (seg & 1) * 2 * NP;
+                }
                 group_wait(&ctrl->xfull, i & 1, p, ctrl, kSiteXFull, i, true);
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFull);
                 // x[k]: full score of column own0 + k
@@ -1222,33 +1265,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                                         0u, 0u, pin_peer);
                         }
                     }
-                    // the peer's P block and message: then its rescale of its
-                    // columns applies to this CTA's O before PV(i)
-                    group_wait(&ctrl->pin[pb], (i / C::kPBufs) & 1, p, ctrl, kSitePIn, i, true);
-                    if (ctrl->pflag[pb][0] && seg_has_pv) {
-                        group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i);
-                        rescale_o(obuf, snd0, ctrl->palpha[pb]);
-                        tc_fence_before();
-                    }
-                    named_bar_sync(1, 128);
                 }
-                if (ctrl->abort) { alive = false; break; }  // same value in every thread after the barrier
-                if (st == 0) {
-                    MLA_TRACE_POINT(i, kTrSmPArrive);
-                    MLA_TTRACE(i);
-                    mbar_arrive(&ctrl->p_full);
-                }
-                seg_has_pv = true;
-                if (pend) {
-                    // PV(i-1), the captured segment's last, is long done by now
-                    group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteOEpi, i);
-                    tc_fence_after();
-                    start_drain(obuf ^ (2 * NP), seg - 1, i);
-                    if (st == 0) MLA_TRACE_POINT(i, kTrEpiStored);
-                } else if (dr_left > 0) {
-                    tc_fence_after();
-                    drain_step();
-                    tc_fence_before();
+                if (!finish(i)) {
+                    alive = false;
+                    break;
                 }
                 if (last_of_seg) {
                     pend_final = (seg_start_j == 0) && (j == it.tiles - 1);
@@ -1268,7 +1288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 named_bar_sync(1, 128);
                 if (!ctrl->abort) {  // same value in every thread after the barrier
                     tc_fence_after();
-                    start_drain(obuf, seg, il + 1);
+                    start_drain(obuf, seg, il + 1, pend_b, pend_final);
                     while (dr_left > 0) drain_step();
                     if (st == 0) MLA_TRACE_POINT(il + 1, kTrEpiEnd);
                 }
