@@ -288,6 +288,9 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     p.HQ = HQ;
     p.out_f32 = out_dtype == MLA_OUT_F32;
     p.SPG = G + B;
+    // what a request boundary costs a cluster, in tiles (measured: about one
+    // and a half tiles at 16 query rows; the 64-row drain is four times larger)
+    p.wseg = NP == 16 ? 2 : NP == 32 ? 4 : 8;
     cudaError_t e = mla::launch_decode(maps, p, NP, lsu, cache_kind, G, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

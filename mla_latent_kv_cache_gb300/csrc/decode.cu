@@ -219,6 +219,64 @@ __device__ __forceinline__ void prefetch_request(const DecodeParams& p, int b, i
     }
 }
 
+// Work split. Tiles of all requests in order form one sequence; a non-empty
+// request also carries wseg units of cost before its first tile (what a
+// request boundary costs a cluster: the next request's queries, the drain of
+// the previous output). Cluster g of G takes the tiles whose cost coordinate
+// lies in [g*C/G, (g+1)*C/G), C the total cost. Both functions are called by
+// a whole warp and return the same value in every lane.
+
+// Total tiles and total cost over all requests.
+__device__ __forceinline__ void work_totals(const int32_t* sl, int B, int wseg, int lane, long long& tiles,
+                                            long long& cost) {
+    long long t = 0, c = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int b = base + lane;
+        const int tl = b < B ? (max(__ldg(sl + b), 0) + kTile - 1) / kTile : 0;
+        int st = tl, sc = tl > 0 ? tl + wseg : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            st += __shfl_xor_sync(0xffffffffu, st, o);
+            sc += __shfl_xor_sync(0xffffffffu, sc, o);
+        }
+        t += st;
+        c += sc;
+    }
+    tiles = t;
+    cost = c;
+}
+
+// Number of tiles whose cost coordinate is below x.
+__device__ __forceinline__ long long tiles_before_cost(const int32_t* sl, int B, int wseg, long long x, int lane) {
+    long long acc_c = 0, acc_t = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int b = base + lane;
+        const int tl = b < B ? (max(__ldg(sl + b), 0) + kTile - 1) / kTile : 0;
+        const int cb = tl > 0 ? tl + wseg : 0;
+        int ic = cb, it = tl;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vc = __shfl_up_sync(0xffffffffu, ic, o);
+            const int vt = __shfl_up_sync(0xffffffffu, it, o);
+            if (lane >= o) {
+                ic += vc;
+                it += vt;
+            }
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, b < B && acc_c + ic > x);
+        if (hit) {
+            const int L = __ffs(hit) - 1;
+            const long long cs = acc_c + __shfl_sync(0xffffffffu, ic, L) - __shfl_sync(0xffffffffu, cb, L);
+            const long long ts = acc_t + __shfl_sync(0xffffffffu, it, L) - __shfl_sync(0xffffffffu, tl, L);
+            const long long in = x - cs - wseg;  // tiles of request L below x
+            return ts + (in > 0 ? in : 0);
+        }
+        acc_c += __shfl_sync(0xffffffffu, ic, 31);
+        acc_t += __shfl_sync(0xffffffffu, it, 31);
+    }
+    return acc_t;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -402,18 +460,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
         tc_fence_before();
     }
     if (warp == 2) {
-        // tiles per request, their total, and where this cluster's range starts
-        long long total = 0;
-        for (int base = 0; base < p.B; base += 32) {
-            const int b = base + lane;
-            const int tl = b < p.B ? (max(__ldg(p.seq_lens + b), 0) + kTile - 1) / kTile : 0;
-            int s = tl;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            total += s;
-        }
-        const int tb = static_cast<int>(static_cast<long long>(g) * total / G);
-        const int te = static_cast<int>(static_cast<long long>(g + 1) * total / G);
+        // this cluster's tile range (cost-weighted split) and where it starts
+        long long total = 0, cost = 0;
+        work_totals(p.seq_lens, p.B, p.wseg, lane, total, cost);
+        const int tb = static_cast<int>(tiles_before_cost(p.seq_lens, p.B, p.wseg, g * cost / G, lane));
+        const int te = static_cast<int>(tiles_before_cost(p.seq_lens, p.B, p.wseg, (g + 1) * cost / G, lane));
         int b0 = 0, j0 = 0;
         long long acc = 0;
         for (int base = 0; base < p.B; base += 32) {
@@ -1369,12 +1420,15 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
     const int b = blockIdx.x / RB, gy = blockIdx.y;
     const int n = (blockIdx.x - b * RB) * 2 + (tid >> 7);
     const int t = tid & 127;
+    // cost coordinate of request b's first tile, and the total cost (the
+    // decode kernel's work split)
     __shared__ long long red_pre[8], red_tot[8];
     long long pre = 0, tot = 0;
     for (int i = tid; i < p.B; i += 256) {
         const long long tl = (max(__ldg(p.seq_lens + i), 0) + kTile - 1) / kTile;
-        tot += tl;
-        if (i < b) pre += tl;
+        const long long c = tl > 0 ? tl + p.wseg : 0;
+        tot += c;
+        if (i < b) pre += c;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -1383,7 +1437,7 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
     }
     if (lane == 0) { red_pre[warp] = pre; red_tot[warp] = tot; }
     __syncthreads();
-    pre = 0;
+    pre = p.wseg;
     tot = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) { pre += red_pre[w]; tot += red_tot[w]; }
@@ -1423,7 +1477,7 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
     float L = -INFINITY;
     if (tiles_b > 0) {
         // the clusters holding the first and last tile: the largest g with
-        // floor(g * tot / G) <= tile
+        // floor(g * tot / G) <= cost coordinate of the tile
         const long long g0 = ((pre + 1) * G - 1) / tot;
         const long long g1 = ((pre + tiles_b) * G - 1) / tot;
         if (g0 == g1) return;  // one cluster held the whole request and wrote the output

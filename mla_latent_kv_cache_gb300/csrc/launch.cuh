@@ -32,6 +32,7 @@ struct DecodeParams {
     int B, Qt, Hq, HQ; // HQ = Hq * Qt rows per request
     int out_f32;
     int SPG;           // partial slots per row group = clusters + B
+    int wseg;          // work-split cost of a request boundary, in tiles
 };
 
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
