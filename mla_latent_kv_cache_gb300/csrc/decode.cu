@@ -117,8 +117,8 @@ struct Cfg {
     static_assert(NP == 16 || NP == 32 || NP == 64, "NP");
     static constexpr int kPairBytes = 2 * 128 * 128;  // 2 x (64 dims x 128 tokens), 128-B swizzled
     static constexpr int kRopeBytes = 128 * 64;       // 32 rope dims x 128 tokens, 64-B swizzled
-    static constexpr int kRL = (NP == 16) ? 5 : 4;    // pair slots (2 per tile)
-    static constexpr int kRR = (NP == 64) ? 1 : 3;    // rope slots (1 per tile; freed right after S)
+    static constexpr int kRL = (NP == 64) ? 4 : 5;    // pair slots (2 per tile)
+    static constexpr int kRR = (NP == 16) ? 3 : (NP == 32 ? 2 : 1);  // rope slots (1 per tile; freed right after S)
     static constexpr int kQBytes = NP * (4 * 128 + 64);
     // 32 and 64 query rows: the two CTAs split the softmax columns, each owning
     // kNH of them; 16 rows: both run the whole softmax
@@ -132,9 +132,13 @@ struct Cfg {
     static constexpr int kOffX = (kOffQ + kQBytes + 1023) / 1024 * 1024;
     static constexpr int kOffP = kOffX + kXBytes;
     // Send buffer of the score exchange: the partial S of the peer's columns
-    // is staged here and pushed to the peer by one bulk copy.
+    // is staged here and pushed to the peer by one bulk copy. At 32 rows it is
+    // the tile's own P buffer (the same 8 KB, idle until P is written), which
+    // pays for the fifth pair slot.
+    static constexpr bool kSendInP = (NP == 32);
+    static_assert(!kSendInP || kXBytes == kPBytes, "send staging in the P buffer");
     static constexpr int kOffSend = kOffP + kPBufs * kPBytes;
-    static constexpr int kOffCtrl = kOffSend + kXBytes;
+    static constexpr int kOffCtrl = kOffSend + (kSendInP ? 0 : kXBytes);
     static constexpr int kSmemBytes = kOffCtrl + 3584 + 1024;  // + control block, alignment slack
     // TMEM: two O accumulators of 2 x NP columns (one per alternating
     // segment, so a finished segment drains while the next accumulates),
@@ -1126,11 +1130,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 }
                 // send this CTA's partial scores once the peer has read the last ones
                 if (i > 0) group_wait(&ctrl->xfree, (i - 1) & 1, p, ctrl, kSiteXFree, i, true);
+                if constexpr (C::kSendInP) {
+                    // the staging goes into this tile's P buffer: PV(i - kPBufs) has read it
+                    if (i >= C::kPBufs)
+                        group_wait(&ctrl->o_done[(i - C::kPBufs) & 1], ((i - C::kPBufs) >> 1) & 1, p, ctrl, kSiteOPbuf, i);
+                }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFree);
                 {
                     // stage columns [snd0, snd0 + NH) of the row in the send buffer
                     // (the peer's exchange-buffer layout); one thread pushes the block
-                    uint8_t* sendb = smem + C::kOffSend;
+                    uint8_t* sendb = C::kSendInP ? pbufs + (i % C::kPBufs) * C::kPBytes : smem + C::kOffSend;
 #pragma unroll
                     for (int u = 0; u < NH / 4; ++u)
                         *reinterpret_cast<uint4*>(sendb + st * NH * 4 + ((u ^ xs) << 4)) =
@@ -1255,6 +1264,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                     if (lane == 0) okp = !ctrl->abort && mbar_wait(&ctrl->o_done[jp & 1], (jp >> 1) & 1, &ctrl->abort);
                     okp = __shfl_sync(0xffffffffu, okp ? 1 : 0, 0) != 0;
                     if (!okp && lane == 0) fail(p, ctrl, kErrWaitTimeout, kSiteOPbuf, i);
+                }
+                if constexpr (C::kSendInP) {
+                    // the peer has consumed this tile's scores, so the bulk copy has
+                    // read the staging that P is about to replace
+                    group_wait(&ctrl->xfree, i & 1, p, ctrl, kSiteXFree, i, true);
                 }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmExp);
                 const int pb = i % C::kPBufs;
