@@ -2,8 +2,8 @@
 
 Bars: cache writes and indexing bit-exact; decode outputs within
 |d| <= 1e-2 + 2e-2 |ref| per element and LSE within 1e-3 (bf16 cache);
-|d| <= 5e-2 for fp8_ds_mla caches against the oracle run on the same
-(dequantised) cache. Inputs are seeded (mla_latent_kv_cache_gb300.workloads);
+|d| <= 5e-2 (outputs and LSE) for fp8_ds_mla caches against the oracle run on
+the same (dequantised) cache. Inputs are seeded (mla_latent_kv_cache_gb300.workloads);
 pools start as NaN sentinels so a read of a wrong slot shows up.
 """
 import numpy as np
@@ -41,7 +41,11 @@ def check_decode(out, lse, ref_o, ref_l, rows, kind=0, what=""):
     ninf = np.isneginf(ref_l)
     assert np.array_equal(np.isneginf(l), ninf), f"{what}: -inf pattern of lse"
     if (~ninf).any():
-        assert np.abs(l[~ninf] - ref_l[~ninf]).max() <= 1e-3, f"{what}: lse off by {np.abs(l[~ninf] - ref_l[~ninf]).max():.3e}"
+        # fp8 pools: the dequantised rows reach the MMA rounded to bf16, which
+        # moves every score (and so the LSE) by up to ~1e-2 on short requests
+        lse_tol = 1e-3 if kind == 0 else 5e-2
+        assert np.abs(l[~ninf] - ref_l[~ninf]).max() <= lse_tol, \
+            f"{what}: lse off by {np.abs(l[~ninf] - ref_l[~ninf]).max():.3e}"
     assert np.all(o[ninf] == 0), f"{what}: rows with no visible token must be 0"
 
 
@@ -175,6 +179,34 @@ def test_decode_row_shapes_and_causal(Hq, Qt):
     o, l, rows = oracle_step(wl, range(wl.B))
     out, lse = run_step(wl)
     check_decode(out, lse, o, l, rows, what=f"Hq={Hq} Qt={Qt}")
+
+
+@pytest.mark.parametrize("rows", [16, 32, 64])
+@pytest.mark.parametrize("num_ctas", [2, 6, 40, 400])
+def test_many_request_boundaries(rows, num_ctas):
+    """Short, empty and long requests against few and many clusters: request
+    boundaries inside a cluster's range, drains overtaken by one-tile
+    segments, clusters with empty ranges, and at 32 and 64 rows the split
+    softmax columns (exchanged P blocks, rescale factors and row sums)."""
+    rng = np.random.default_rng(100 + rows + num_ctas)
+    sl = [int(x) for x in rng.choice([0, 1, 2, 127, 128, 129, 300, 1000, 2500], size=24)]
+    Hq, Qt = {16: (16, 1), 32: (8, 4), 64: (16, 4)}[rows]
+    wl = W.make("bounds", B=len(sl), Hq=Hq, Qt=Qt, page_size=16, seq_lens=sl, seed=50 + rows + num_ctas,
+                device=DEV)
+    o, l, rr = oracle_step(wl, range(wl.B))
+    out, lse = run_step(wl, num_ctas=num_ctas)
+    check_decode(out, lse, o, l, rr, what=f"rows={rows} ctas={num_ctas}")
+
+
+@pytest.mark.parametrize("num_ctas", [4, 0])
+def test_fp8_split_columns_boundaries(num_ctas):
+    """fp8 pool (TMA + in-place expansion) with 64 rows and ragged requests."""
+    sl = [0, 1, 64, 65, 127, 300, 900, 2049, 5]
+    wl = W.make("fp8b", B=len(sl), Hq=64, Qt=1, page_size=64, seq_lens=sl, kind=W.KIND_FP8, write_all=True,
+                seed=77 + num_ctas, device=DEV)
+    o, l, rr = oracle_step(wl, range(wl.B))
+    out, lse = run_step(wl, num_ctas=num_ctas)
+    check_decode(out, lse, o, l, rr, kind=1, what=f"fp8 ctas={num_ctas}")
 
 
 def test_single_token_is_bit_exact():
