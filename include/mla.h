@@ -188,6 +188,16 @@ MLA_API int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const
                                       int64_t block_table_stride, const int32_t* seq_lens, int B, int q_len, int Hq,
                                       float scale, void* out, int out_dtype, float* lse, int num_ctas, void* stream);
 
+/*
+ * mla_test_hold_next_decode - test support for the device-side failure path.
+ * The next mla_decode call in this process withholds its first hand-off from
+ * the softmax warps to the PV issuers, so their bounded wait gives up after
+ * about one second: the call's status word then has bit 1 set (words 1..11
+ * name the wait site and role), its outputs are invalid, and the device
+ * context stays usable. Nothing else sets it; it has no other effect.
+ */
+MLA_API void mla_test_hold_next_decode(void);
+
 /* Static English text for a status code. */
 MLA_API const char* mla_status_string(int status);
 

@@ -65,6 +65,8 @@ def load() -> ctypes.CDLL:
             lib.mla_decode_static_scratch.argtypes = [vp, vp, vp, i32, i64, i32, vp, i64, vp, i32, i32, i32, f32, vp,
                                                       i32, vp, i32, vp]
             lib.mla_decode_static_scratch.restype = i32
+            lib.mla_test_hold_next_decode.argtypes = []
+            lib.mla_test_hold_next_decode.restype = None
             lib.mla_merge_lse.argtypes = [vp, vp, i32, i64, vp, i32, vp, vp]
             lib.mla_merge_lse.restype = i32
             _lib = lib
@@ -182,6 +184,19 @@ def decode(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens, q_l
     mla_decode(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens, q_len, scale, out, lse, workspace,
                num_ctas, stream)
     return out, lse, workspace
+
+
+def device_status_words(workspace: torch.Tensor, n: int = 12) -> list:
+    """The workspace status header of the last mla_decode that used it:
+    word 0 status bits, words 1..3 the first failing CTA's wait site, tile and
+    index, words 4..11 where each of its roles gave up ((site << 24) | tile)."""
+    return [int(v) for v in workspace[:4 * n].view(torch.int32).tolist()]
+
+
+def test_hold_next_decode() -> None:
+    """Test support: make the next mla_decode's PV issuers time out (see
+    include/mla.h)."""
+    load().mla_test_hold_next_decode()
 
 
 def device_status(workspace: torch.Tensor) -> int:

@@ -3,6 +3,7 @@
 // or synchronises.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -83,6 +84,9 @@ WsLayout decode_ws_layout(int B, int HQ, int G) {
 }
 
 size_t decode_ws_bytes(int B, int HQ, int G) { return decode_ws_layout(B, HQ, G).total; }
+
+// Set by mla_test_hold_next_decode, consumed by the next mla_decode.
+std::atomic<int> g_test_hold{0};
 
 // Workspace of mla_decode_static_scratch: one array per device, placed when
 // this library's device code is loaded, for callers that cannot allocate.
@@ -291,6 +295,7 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     // what a request boundary costs a cluster, in tiles (measured: about one
     // and a half tiles at 16 query rows; the 64-row drain is four times larger)
     p.wseg = NP == 16 ? 2 : NP == 32 ? 4 : 8;
+    p.test_hold = g_test_hold.exchange(0);
     cudaError_t e = mla::launch_decode(maps, p, NP, lsu, cache_kind, G, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -308,6 +313,8 @@ int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const void* c
                       seq_lens, B, q_len, Hq, scale, out, out_dtype, lse, scratch, MLA_STATIC_SCRATCH_BYTES,
                       num_ctas, stream);
 }
+
+void mla_test_hold_next_decode(void) { g_test_hold.store(1); }
 
 int mla_merge_lse(const float* part_out, const float* part_lse, int S, int64_t N, void* out, int out_dtype,
                   float* lse, void* stream) {

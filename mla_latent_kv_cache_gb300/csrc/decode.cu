@@ -1073,7 +1073,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 if (st == 0) {
                     MLA_TRACE_POINT(t, kTrSmPArrive);
                     MLA_TTRACE(t);
-                    mbar_arrive(&ctrl->p_full);
+                    // the test hook withholds tile 0, so the PV issuers' bounded wait
+                    // gives up and every role leaves through the abort path
+                    if (!(p.test_hold && t == 0)) mbar_arrive(&ctrl->p_full);
                 }
                 seg_has_pv = true;
                 if (pend) {

@@ -33,6 +33,7 @@ struct DecodeParams {
     int out_f32;
     int SPG;           // partial slots per row group = clusters + B
     int wseg;          // work-split cost of a request boundary, in tiles
+    int test_hold;     // test hook: 1 = withhold the first hand-off to the PV issuers
 };
 
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
