@@ -1463,7 +1463,8 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
         // status summary: OR of all records; the lowest failing CTA's site,
         // tile, index and role reports
         int bits = 0, first = INT_MAX;
-        for (int c = lane; c < nrec; c += 32) {
+#pragma unroll 8
+        for (int c = lane; c < nrec; c += 32) {  // independent loads, in flight together
             const int v = p.rec[static_cast<int64_t>(c) * kStatusRecWords];
             bits |= v;
             if (v && c < first) first = c;
@@ -1501,6 +1502,16 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
         const int64_t slot0 = static_cast<int64_t>(gy) * p.SPG + g0 + b;
         const float* pl = p.part_lse + slot0 * 64 + n;
         const float* po = p.part_o + (slot0 * 64 + n) * kD + d;
+        // up to 8 slots: their partial outputs are requested before the weights
+        // are known, so the loads overlap the LSE round trip (empty slots hold
+        // stale values and get weight 0)
+        constexpr int kSpec = 8;
+        float4 ov[kSpec];
+        if (nseg <= kSpec) {
+#pragma unroll
+            for (int k = 0; k < kSpec; ++k)
+                if (k < nseg) ov[k] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * 64 * kD);
+        }
         // the slot LSEs, 32 at a time, one per lane (each warp of the row
         // computes the same weights)
         float mx = -INFINITY;
@@ -1514,7 +1525,21 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
                 ws += v != -INFINITY ? expf(v - mx) : 0.f;
             }
             L = mx + logf(warp_sum(ws));
-            for (int c0 = 0; c0 < nseg; c0 += 32) {
+            if (nseg <= kSpec) {
+                const float v = lane < nseg ? pl[lane * 64] : -INFINITY;
+                const float wl = v != -INFINITY ? expf(v - L) : 0.f;
+#pragma unroll
+                for (int k = 0; k < kSpec; ++k) {
+                    const float w = __shfl_sync(0xffffffffu, wl, k);
+                    if (k < nseg && w != 0.f) {
+                        acc.x += w * ov[k].x;
+                        acc.y += w * ov[k].y;
+                        acc.z += w * ov[k].z;
+                        acc.w += w * ov[k].w;
+                    }
+                }
+            }
+            for (int c0 = 0; nseg > kSpec && c0 < nseg; c0 += 32) {
                 const float v = c0 + lane < nseg ? pl[(c0 + lane) * 64] : -INFINITY;
                 const float wl = v != -INFINITY ? expf(v - L) : 0.f;
                 const int cn = min(32, nseg - c0);
