@@ -3,6 +3,7 @@
 // or synchronises.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -63,17 +64,18 @@ int gcd_int(int a, int b) {
 
 int rows_padded(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
 
-// G = clusters of the decode grid (2 CTAs each).
-// Workspace: [header 256 B][per-CTA status records][partial LSEs][partial outputs],
-// each part 256-byte aligned.
+// Workspace for a grid of `ctas` CTAs: [header 256 B][per-CTA status
+// records][partial LSEs][partial outputs], each part 256-byte aligned, with
+// ctas + B partial slots per row group (a worker, a CTA or a cluster of two,
+// cuts at most one request that another worker continues).
 struct WsLayout {
     size_t rec_off, lse_off, o_off, total;
 };
 
-WsLayout decode_ws_layout(int B, int HQ, int G) {
+WsLayout decode_ws_layout(int B, int HQ, int ctas) {
     const size_t GY = (static_cast<size_t>(HQ) + 63) / 64;
-    const size_t slots = GY * static_cast<size_t>(G + B) * 64;
-    const size_t rec_bytes = (2 * static_cast<size_t>(G) * GY * mla::kStatusRecWords * sizeof(int) + 255) / 256 * 256;
+    const size_t slots = GY * static_cast<size_t>(ctas + B) * 64;
+    const size_t rec_bytes = (static_cast<size_t>(ctas) * GY * mla::kStatusRecWords * sizeof(int) + 255) / 256 * 256;
     const size_t lse_bytes = (slots * sizeof(float) + 255) / 256 * 256;
     WsLayout l;
     l.rec_off = kWsHeader;
@@ -83,7 +85,11 @@ WsLayout decode_ws_layout(int B, int HQ, int G) {
     return l;
 }
 
-size_t decode_ws_bytes(int B, int HQ, int G) { return decode_ws_layout(B, HQ, G).total; }
+// CTAs the workspace is sized for: num_ctas, or one per SM when 0; at least
+// one cluster of two.
+int ws_ctas(int num_ctas, int sms) { return num_ctas > 0 ? (num_ctas < 2 ? 2 : num_ctas) : (sms < 2 ? 2 : sms); }
+
+size_t decode_ws_bytes(int B, int HQ, int ctas) { return decode_ws_layout(B, HQ, ctas).total; }
 
 // Set by mla_test_hold_next_decode, consumed by the next mla_decode.
 std::atomic<int> g_test_hold{0};
@@ -150,13 +156,12 @@ int mla_cache_write(const void* latent, int64_t latent_stride, const void* k_pe,
 
 size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas) {
     if (B <= 0 || q_len <= 0 || Hq <= 0 || num_ctas < 0) return 0;
-    int G = num_ctas / 2;  // clusters of 2 CTAs
+    int sms = 0;
     if (num_ctas == 0) {
-        const int sms = mla_num_sms();
+        sms = mla_num_sms();
         if (sms <= 0) return 0;
-        G = sms / 2;
     }
-    return decode_ws_bytes(B, Hq * q_len, G < 1 ? 1 : G);
+    return decode_ws_bytes(B, Hq * q_len, ws_ctas(num_ctas, sms));
 }
 
 int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache_kind, int64_t num_slots,
@@ -191,13 +196,20 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     // pages whose rows cannot be fetched as 8-row TMA boxes go through the
     // load/convert warps
     const bool lsu = (page_size % 8) != 0;
-    const int G = mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
-    if (G <= 0) return MLA_ERR_CUDA;
-    if (workspace_bytes < decode_ws_bytes(B, HQ, G)) return MLA_ERR_WORKSPACE;
+    // bf16 pools with up to 32 query rows: folded 64-token tiles, one CTA per
+    // worker; otherwise 128-token tiles split over clusters of two CTAs
+    const bool fold = !lsu && cache_kind == MLA_CACHE_BF16_576 && NP <= 32;
+    const int nctas = ws_ctas(num_ctas, di.sms);  // what the workspace holds records and slots for
+    int W = fold ? mla::decode_fold_ctas(NP, num_ctas) : mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
+    if (W <= 0) return MLA_ERR_CUDA;
+    W = std::min(W, fold ? nctas : nctas / 2);
+    const int tile = fold ? 64 : 128;
+    const WsLayout wl = decode_ws_layout(B, HQ, nctas);
+    if (workspace_bytes < wl.total) return MLA_ERR_WORKSPACE;
 
     // Two TMA descriptors over the pool [num_slots, 576] bf16: 64-dim latent
     // chunks (128-byte swizzle) and 32-dim rope halves (64-byte swizzle), both
-    // gcd(page_size, 128) rows high so a box never crosses a page.
+    // gcd(page_size, tile) rows high so a box never crosses a page.
     mla::DecodeMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     CUtensorMap& tmap_lat = maps.lat;
@@ -224,9 +236,9 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
         if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
     }
     if (!lsu) {
-        // pool rows as 2-D tensors, gcd(page_size, 128) rows per box so a box
+        // pool rows as 2-D tensors, gcd(page_size, tile) rows per box so a box
         // never crosses a page
-        const int br = gcd_int(page_size, 128);
+        const int br = gcd_int(page_size, tile);
         const bool fp8 = cache_kind == MLA_CACHE_FP8_DS_MLA_656;
         const cuuint64_t row_bytes = fp8 ? mla::kRowFp8 : mla::kRowBf16;
         cuuint32_t estride[2] = {1u, 1u};
@@ -254,8 +266,8 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
         }
-        // rope: the row as bf16 elements; the rope half at element 512 (bf16)
-        // or 264 (fp8: byte 528) + 32 * rank
+        // rope: the row as bf16 elements; the rope halves at element 512 (bf16)
+        // or 264 (fp8: byte 528), 32 values each
         cuuint64_t gdim[2] = {row_bytes / 2, static_cast<cuuint64_t>(num_slots)};
         cuuint64_t gstride[1] = {row_bytes};
         cuuint32_t box_rope[2] = {32u, static_cast<cuuint32_t>(br)};
@@ -267,7 +279,6 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const WsLayout wl = decode_ws_layout(B, HQ, G);
 
     mla::DecodeParams p;
     p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
@@ -285,18 +296,21 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     p.part_o = reinterpret_cast<float*>(ws + wl.o_off);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.page_size = page_size;
-    p.run_rows = gcd_int(page_size, 128);
+    p.run_rows = gcd_int(page_size, tile);
+    p.tile_shift = fold ? 6 : 7;
     p.B = B;
     p.Qt = q_len;
     p.Hq = Hq;
     p.HQ = HQ;
     p.out_f32 = out_dtype == MLA_OUT_F32;
-    p.SPG = G + B;
-    // what a request boundary costs a cluster, in tiles (measured: about one
-    // and a half tiles at 16 query rows; the 64-row drain is four times larger)
-    p.wseg = NP == 16 ? 2 : NP == 32 ? 4 : 8;
+    p.SPG = W + B;
+    // what a request boundary costs a worker, in tiles (measured on the
+    // cluster kernel: about one and a half 128-token tiles at 16 query rows;
+    // the 64-row drain is four times larger; folded tiles are half as long)
+    p.wseg = (NP == 16 ? 2 : NP == 32 ? 4 : 8) * (fold ? 2 : 1);
     p.test_hold = g_test_hold.exchange(0);
-    cudaError_t e = mla::launch_decode(maps, p, NP, lsu, cache_kind, G, GY, s);
+    cudaError_t e = fold ? mla::launch_decode_fold(maps, p, NP, W, GY, s)
+                         : mla::launch_decode(maps, p, NP, lsu, cache_kind, W, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

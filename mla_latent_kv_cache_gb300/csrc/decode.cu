@@ -182,13 +182,15 @@ __device__ __forceinline__ int swz_p(int row, uint32_t mode) {
     return mode == kSw128 ? (row & 7) : mode == kSw64 ? ((row >> 1) & 3) : ((row >> 2) & 1);
 }
 
-struct TileIt {
+// Walks the tiles (1 << SH tokens each) of consecutive requests.
+template <int SH>
+struct TileItT {
     int b, j, tiles, T;
     __device__ __forceinline__ void init(const int32_t* sl, int b0, int j0) {
         b = b0;
         j = j0;
         T = max(__ldg(sl + b), 0);
-        tiles = (T + kTile - 1) / kTile;
+        tiles = (T + (1 << SH) - 1) >> SH;
     }
     __device__ __forceinline__ void next(const int32_t* sl, int B) {
         if (++j >= tiles) {
@@ -197,11 +199,12 @@ struct TileIt {
                 ++b;
                 if (b >= B) { T = 0; tiles = 1; break; }
                 T = max(__ldg(sl + b), 0);
-                tiles = (T + kTile - 1) / kTile;
+                tiles = (T + (1 << SH) - 1) >> SH;
             } while (tiles == 0);
         }
     }
 };
+using TileIt = TileItT<7>;
 
 // L2 prefetch of what the first tiles of request b read besides the cache:
 // its query rows of row group gy and its block-table row (whole 16-byte
@@ -231,12 +234,13 @@ __device__ __forceinline__ void prefetch_request(const DecodeParams& p, int b, i
 // a whole warp and return the same value in every lane.
 
 // Total tiles and total cost over all requests.
+template <int SH>
 __device__ __forceinline__ void work_totals(const int32_t* sl, int B, int wseg, int lane, long long& tiles,
                                             long long& cost) {
     long long t = 0, c = 0;
     for (int base = 0; base < B; base += 32) {
         const int b = base + lane;
-        const int tl = b < B ? (max(__ldg(sl + b), 0) + kTile - 1) / kTile : 0;
+        const int tl = b < B ? (max(__ldg(sl + b), 0) + (1 << SH) - 1) >> SH : 0;
         int st = tl, sc = tl > 0 ? tl + wseg : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -251,11 +255,12 @@ __device__ __forceinline__ void work_totals(const int32_t* sl, int B, int wseg, 
 }
 
 // Number of tiles whose cost coordinate is below x.
+template <int SH>
 __device__ __forceinline__ long long tiles_before_cost(const int32_t* sl, int B, int wseg, long long x, int lane) {
     long long acc_c = 0, acc_t = 0;
     for (int base = 0; base < B; base += 32) {
         const int b = base + lane;
-        const int tl = b < B ? (max(__ldg(sl + b), 0) + kTile - 1) / kTile : 0;
+        const int tl = b < B ? (max(__ldg(sl + b), 0) + (1 << SH) - 1) >> SH : 0;
         const int cb = tl > 0 ? tl + wseg : 0;
         int ic = cb, it = tl;
 #pragma unroll
@@ -279,6 +284,48 @@ __device__ __forceinline__ long long tiles_before_cost(const int32_t* sl, int B,
         acc_t += __shfl_sync(0xffffffffu, it, 31);
     }
     return acc_t;
+}
+
+// Tile range [tb, te) of worker g of G and the request / tile it starts at.
+// Called by a whole warp; every lane returns the same values.
+struct TileRange {
+    int tb, te, b0, j0;
+};
+template <int SH>
+__device__ __forceinline__ TileRange scan_range(const DecodeParams& p, int g, int G, int lane) {
+    long long total = 0, cost = 0;
+    work_totals<SH>(p.seq_lens, p.B, p.wseg, lane, total, cost);
+    const int tb = static_cast<int>(tiles_before_cost<SH>(p.seq_lens, p.B, p.wseg, g * cost / G, lane));
+    const int te = static_cast<int>(tiles_before_cost<SH>(p.seq_lens, p.B, p.wseg, (g + 1) * cost / G, lane));
+    int b0 = 0, j0 = 0;
+    long long acc = 0;
+    for (int base = 0; base < p.B; base += 32) {
+        const int b = base + lane;
+        const int tl = b < p.B ? (max(__ldg(p.seq_lens + b), 0) + (1 << SH) - 1) >> SH : 0;
+        int incl = tl;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const long long gi = acc + incl;
+        const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && tl > 0 && gi > tb);
+        if (hit) {
+            const int L = __ffs(hit) - 1;
+            const long long gl = __shfl_sync(0xffffffffu, gi, L);
+            const int tll = __shfl_sync(0xffffffffu, tl, L);
+            b0 = base + L;
+            j0 = static_cast<int>(tb - (gl - tll));
+            break;
+        }
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    TileRange r;
+    r.tb = tb;
+    r.te = te;
+    r.b0 = b0;
+    r.j0 = j0;
+    return r;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -313,7 +360,8 @@ __device__ __forceinline__ int* status_rec(const DecodeParams& p) {
     return p.rec + static_cast<int64_t>(blockIdx.y * gridDim.x + blockIdx.x) * kStatusRecWords;
 }
 
-__device__ __forceinline__ void fail(const DecodeParams& p, Ctrl* ctrl, int code, int site = 0, int tile = 0) {
+template <class CT>
+__device__ __forceinline__ void fail(const DecodeParams& p, CT* ctrl, int code, int site = 0, int tile = 0) {
     int* r = status_rec(p);
     atomicOr(r, code);
     if (site && atomicCAS(r + 1, 0, site) == 0) r[2] = tile;
@@ -333,7 +381,8 @@ __device__ __forceinline__ void report(const DecodeParams& p, int role, int site
 // Softmax-group wait. A thread whose wait fails raises the abort flag and
 // carries on (its results no longer matter); the group leaves its tile loop
 // together after the tile's last barrier, where every thread reads the flag.
-__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, const DecodeParams& p, Ctrl* ctrl,
+template <class CT>
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, const DecodeParams& p, CT* ctrl,
                                            int site, int tile, bool cluster_scope = false) {
     const bool ok = cluster_scope ? mbar_wait_cluster(bar, parity, &ctrl->abort) : mbar_wait(bar, parity, &ctrl->abort);
     if (!ok) {
@@ -465,38 +514,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
     }
     if (warp == 2) {
         // this cluster's tile range (cost-weighted split) and where it starts
-        long long total = 0, cost = 0;
-        work_totals(p.seq_lens, p.B, p.wseg, lane, total, cost);
-        const int tb = static_cast<int>(tiles_before_cost(p.seq_lens, p.B, p.wseg, g * cost / G, lane));
-        const int te = static_cast<int>(tiles_before_cost(p.seq_lens, p.B, p.wseg, (g + 1) * cost / G, lane));
-        int b0 = 0, j0 = 0;
-        long long acc = 0;
-        for (int base = 0; base < p.B; base += 32) {
-            const int b = base + lane;
-            const int tl = b < p.B ? (max(__ldg(p.seq_lens + b), 0) + kTile - 1) / kTile : 0;
-            int incl = tl;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            const long long gi = acc + incl;
-            const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && tl > 0 && gi > tb);
-            if (hit) {
-                const int L = __ffs(hit) - 1;
-                const long long gl = __shfl_sync(0xffffffffu, gi, L);
-                const int tll = __shfl_sync(0xffffffffu, tl, L);
-                b0 = base + L;
-                j0 = static_cast<int>(tb - (gl - tll));
-                break;
-            }
-            acc += __shfl_sync(0xffffffffu, incl, 31);
-        }
+        const TileRange r = scan_range<7>(p, g, G, lane);
         if (lane == 0) {
-            ctrl->t_begin = tb;
-            ctrl->t_end = te;
-            ctrl->b0 = b0;
-            ctrl->j0 = j0;
+            ctrl->t_begin = r.tb;
+            ctrl->t_end = r.te;
+            ctrl->b0 = r.b0;
+            ctrl->j0 = r.j0;
         }
     }
     if (threadIdx.x >= 128 && threadIdx.x < 128 + 64) {
@@ -1373,6 +1396,700 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
     }
 }
 
+// ---------------------------------------------------------------- folded tiles
+//
+// bf16 pools, page sizes that are a multiple of 8, up to 32 query rows: one CTA
+// per worker and no cluster. A tile is 64 tokens of whole 576-value rows,
+// held as the 128-row A operand of one UMMA: row t (t < 64) carries token t's
+// first half (latent [0, 256) and rope [512, 544)), row 64 + t its second half
+// (latent [256, 512) and rope [544, 576)). With the query rows stacked the same
+// way, B = [Q_a; Q_b] (N = 2 NP):
+//   D[t, c]           = c_a(t) . q_a(c)   TMEM lanes 0..63,   columns [0, NP)
+//   D[64 + t, NP + c] = c_b(t) . q_b(c)   TMEM lanes 64..127, columns [NP, 2 NP)
+// so s(t, c) = D[t, c] + D[64 + t, NP + c]: the two halves of a token meet in
+// shared memory between softmax warps 4/6 and 5/7, and each keeps half of the
+// columns. (One 3-D TMA box per run carrying both halves halves the number of
+// boxes, but measured slower: its loads land 2-4 us after issue, not ~1 us.) The value product reads the same tile as the MN-major A operand of
+// four M = 128 UMMAs (latent dims 128 m + [0, 128)), K = 64 tokens:
+//   O^T[512, NP] += C^T[512, 64] . P[64, NP]
+// Nothing crosses between CTAs: a tile's shared memory is held from its load
+// to its value product only, with no exchange latency in between.
+
+template <int NP>
+struct FoldCfg {
+    static_assert(NP == 16 || NP == 32, "NP");
+    static constexpr int kTok = 64;                    // tokens per tile
+    static constexpr int kPairBytes = 2 * 128 * 128;   // K-blocks 2pp, 2pp+1: 64 dims x (64 + 64) rows, 128-B swizzled
+    static constexpr int kRopeBytes = 128 * 64;        // 32 rope dims x 128 rows, 64-B swizzled
+    static constexpr int kRL = (NP == 16) ? 5 : 4;     // pair slots (2 per tile)
+    static constexpr int kRR = 3;                      // rope slots (1 per tile; freed right after S)
+    static constexpr int kQBytes = 2 * NP * (4 * 128 + 64);
+    static constexpr int kNH = NP / 2;                 // softmax columns per thread
+    static constexpr int kXBytes = 128 * kNH * 4;      // the partner lane's half scores
+    static constexpr int kPBufs = 2;
+    static constexpr int kPBytes = kTok * NP * 2;      // P [64 tokens][NP] bf16, MN-major
+    static constexpr int kOffRope = kRL * kPairBytes;
+    static constexpr int kOffQ = kOffRope + kRR * kRopeBytes;
+    static constexpr int kOffX = (kOffQ + kQBytes + 1023) / 1024 * 1024;
+    static constexpr int kOffP = kOffX + kXBytes;
+    static constexpr int kOffCtrl = kOffP + kPBufs * kPBytes;
+    static constexpr int kSmemBytes = kOffCtrl + 3072 + 1024;  // + control block, alignment slack
+    // TMEM: two O accumulators of 4 x NP columns (M-tile m at m * NP), then
+    // two S buffers of 2 x NP columns
+    static constexpr int kColS = 8 * NP;
+    static constexpr int kTmemCols = NP == 16 ? 256 : 512;
+    static constexpr uint32_t kPSwizzle = NP == 16 ? kSw32 : kSw64;  // one row of P = one swizzle atom
+    static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kColS + 4 * NP <= kTmemCols, "tmem");
+};
+
+struct FoldCtrl {
+    uint64_t pair_full[5], pair_empty[5];
+    uint64_t rope_full[3], rope_empty[3];
+    uint64_t s_full[2], s_free[2], p_full, o_done[2], q_full;
+    uint32_t tmem_base;
+    int abort;
+    int t_begin, t_end, b0, j0;
+    int colvis[64];                  // query row -> trailing tokens it may not see
+    alignas(16) float m[64];         // running max per row (log2 units)
+    alignas(16) float alpha[64];
+    alignas(16) float red[4][64];
+    alignas(16) float dlt[2][64];    // row sums of a finished segment, by segment parity
+    float dm[2][64];                 // and its row maxima
+};
+static_assert(sizeof(FoldCtrl) <= 3072, "control block");
+
+template <int NP>
+__global__ void __launch_bounds__(288, 1)
+    mla_decode_fold_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
+    using C = FoldCfg<NP>;
+    constexpr int kT = C::kTok;
+    using It = TileItT<6>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* pair_ring = smem;
+    uint8_t* rope_ring = smem + C::kOffRope;
+    uint8_t* qs = smem + C::kOffQ;
+    uint8_t* xbuf = smem + C::kOffX;
+    uint8_t* pbufs = smem + C::kOffP;
+    FoldCtrl* ctrl = reinterpret_cast<FoldCtrl*>(smem + C::kOffCtrl);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blockIdx.x, G = gridDim.x, gy = blockIdx.y;
+    if (threadIdx.x == 0) MLA_KTRACE(0);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kRL; ++i) { mbar_init(&ctrl->pair_full[i], 1); mbar_init(&ctrl->pair_empty[i], 1); }
+        for (int i = 0; i < C::kRR; ++i) { mbar_init(&ctrl->rope_full[i], 1); mbar_init(&ctrl->rope_empty[i], 1); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctrl->s_full[i], 1);
+            mbar_init(&ctrl->s_free[i], 1);
+            mbar_init(&ctrl->o_done[i], 2);  // one commit per PV issuer
+        }
+        mbar_init(&ctrl->p_full, 1);
+        mbar_init(&ctrl->q_full, 1);
+        ctrl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1 && lane == 0) {
+        prefetch_tensormap(&maps.lat);
+        prefetch_tensormap(&maps.rope);
+        prefetch_tensormap(&maps.q);
+        prefetch_tensormap(&maps.qpe);
+    }
+    // the previous kernel in the stream may still be writing the inputs or
+    // reading the workspace
+    griddep_wait();
+    if (threadIdx.x == 0) {
+        int4* r = reinterpret_cast<int4*>(status_rec(p));
+#pragma unroll
+        for (int k = 0; k < kStatusRecWords / 4; ++k) r[k] = make_int4(0, 0, 0, 0);
+    }
+    if (warp == 0) {
+        tmem_alloc(&ctrl->tmem_base, C::kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    if (warp == 2) {
+        const TileRange r = scan_range<6>(p, g, G, lane);
+        if (lane == 0) {
+            ctrl->t_begin = r.tb;
+            ctrl->t_end = r.te;
+            ctrl->b0 = r.b0;
+            ctrl->j0 = r.j0;
+        }
+    }
+    if (threadIdx.x >= 128 && threadIdx.x < 128 + 64) {
+        const int c = threadIdx.x - 128;
+        const int r = gy * 64 + c;
+        ctrl->colvis[c] = (r < p.HQ) ? (p.Qt - 1 - r / p.Hq) : (INT_MAX / 2);
+        ctrl->m[c] = -INFINITY;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        MLA_KTRACE(1);
+        griddep_launch_dependents();  // the merge grid may be scheduled as CTAs retire
+    }
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    const int ntiles = ctrl->t_end - ctrl->t_begin;
+    if (ntiles == 0 && ctrl->j0 > 0 && threadIdx.x >= 128 && threadIdx.x < 192) {
+        // an empty range strictly inside request b0 (more workers than tiles):
+        // the merge of b0 counts this worker's slot, so mark it empty
+        const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + ctrl->b0;
+        p.part_lse[pslot * 64 + (threadIdx.x - 128)] = -INFINITY;
+    }
+
+    if (ntiles > 0) {
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------- S issuer
+            It it;
+            it.init(p.seq_lens, ctrl->b0, ctrl->j0);
+            const uint32_t idS = idesc_bf16(128, 2 * NP, false, false);
+            const uint64_t dq = smem_desc(smem_u32(qs), 16, 1024, kSw128);
+            const uint64_t dqr = smem_desc(smem_u32(qs) + 8 * NP * 128, 16, 512, kSw64);
+            int seg = 0;
+            for (int i = 0; i < ntiles; ++i) {
+                if (i == 0 || it.j == 0) {
+                    if (!mbar_wait(&ctrl->q_full, seg & 1, &ctrl->abort)) {
+                        fail(p, ctrl, kErrWaitTimeout, kSiteQFull, i);
+                        report(p, kRoleS, kSiteQFull, i);
+                        break;
+                    }
+                    ++seg;
+                }
+                if (i >= 2 && !mbar_wait(&ctrl->s_free[i & 1], ((i - 2) >> 1) & 1, &ctrl->abort)) {
+                    fail(p, ctrl, kErrWaitTimeout, kSiteSFree, i);
+                    report(p, kRoleS, kSiteSFree, i);
+                    break;
+                }
+                const uint32_t tS = tmem + C::kColS + (i & 1) * 2 * NP;
+                bool ok = true;
+                int site = kSitePairFull;
+                for (int pp = 0; pp < 2 && ok; ++pp) {
+                    const int u = 2 * i + pp, slot = u % C::kRL;
+                    if (!mbar_wait(&ctrl->pair_full[slot], (u / C::kRL) & 1, &ctrl->abort)) { ok = false; break; }
+                    tc_fence_after();
+                    if (pp == 0) MLA_TRACE_POINT(i, kTrSPair0);
+                    const uint64_t da = smem_desc(smem_u32(pair_ring + slot * C::kPairBytes), 16, 1024, kSw128);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_bf16(tS, da + ((c * 16384 + kk * 32) >> 4),
+                                      dq + (((2 * pp + c) * 2 * NP * 128 + kk * 32) >> 4), idS, (pp | c | kk) != 0);
+                }
+                const int rr = i % C::kRR;
+                if (ok && !mbar_wait(&ctrl->rope_full[rr], (i / C::kRR) & 1, &ctrl->abort)) {
+                    ok = false;
+                    site = kSiteRopeFull;
+                }
+                if (!ok) {
+                    fail(p, ctrl, kErrWaitTimeout, site, i);
+                    report(p, kRoleS, site, i);
+                    break;
+                }
+                tc_fence_after();
+                MLA_TRACE_POINT(i, kTrSAllIn);
+                const uint64_t dr = smem_desc(smem_u32(rope_ring + rr * C::kRopeBytes), 16, 512, kSw64);
+                umma_bf16(tS, dr, dqr, idS, 1u);
+                umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
+                umma_commit(&ctrl->s_full[i & 1]);
+                umma_commit(&ctrl->rope_empty[rr]);
+                MLA_TRACE_POINT(i, kTrSIssued);
+                it.next(p.seq_lens, p.B);
+            }
+        } else if ((warp == 3 || warp == 2) && lane == 0) {
+            // ------------------------------------------------- PV issuers
+            // issuer mt reads pair slot 2i + mt: latent dims 128 mt + [0, 128)
+            // of the first half (M-tile mt) and of the second (M-tile 2 + mt)
+            const int mt = warp == 3 ? 0 : 1;
+            It it;
+            it.init(p.seq_lens, ctrl->b0, ctrl->j0);
+            const uint32_t idPV = idesc_bf16(128, NP, true, true);
+            constexpr uint32_t p_sbo = 8 * NP * 2;
+
+            int seg = -1;
+            for (int i = 0; i < ntiles; ++i) {
+                const bool new_seg = (i == 0) || (it.j == 0);
+                if (new_seg) ++seg;
+                const uint32_t tO = tmem + (seg & 1) * 4 * NP;
+                if (!mbar_wait(&ctrl->p_full, i & 1, &ctrl->abort)) {
+                    fail(p, ctrl, kErrWaitTimeout, kSitePFull, i);
+                    report(p, kRolePV, kSitePFull, i);
+                    break;
+                }
+                tc_fence_after();
+                if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssue);
+                const uint64_t dp = smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), C::kPBytes, p_sbo,
+                                              C::kPSwizzle);
+                const int slot = (2 * i + mt) % C::kRL;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    // tokens 16 kk .. 16 kk + 15 of half hh: rows 64 hh + 16 kk ..
+                    const uint64_t da =
+                        smem_desc(smem_u32(pair_ring + slot * C::kPairBytes + hh * 8192), 16384, 1024, kSw128);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tO + (2 * hh + mt) * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
+                                  (new_seg && kk == 0) ? 0u : 1u);
+                }
+                umma_commit(&ctrl->pair_empty[slot]);
+                umma_commit(&ctrl->o_done[i & 1]);
+                if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssued);
+                it.next(p.seq_lens, p.B);
+            }
+        } else if (warp == 1 || warp == 8) {
+            // ------------------------------------------------- TMA producers
+            // Warp 1 loads pair 0 and the rope of every tile, warp 8 pair 1 (with
+            // 16-token pages a tile is 40 boxes of 2 KB, and one warp issuing them
+            // all takes about as long as the tile's compute). Lane r owns run r of
+            // the tile (a page-contiguous run of BR rows); each run lands twice per
+            // K-block: its first halves in rows [r BR, (r+1) BR), its second halves
+            // 64 rows further. Page numbers are read one tile ahead.
+            const int pp = warp == 1 ? 0 : 1;
+            It it;
+            it.init(p.seq_lens, ctrl->b0, ctrl->j0);
+            const uint64_t pol = l2_policy_evict_first();
+            const int BR = p.run_rows;
+            bool bad = false, ok = true;
+            int fsite = 0, ftile = 0;
+            auto run_slot = [&](const It& t) -> int {
+                const int valid = min(kT, t.T - t.j * kT);
+                const int nr = (valid + BR - 1) / BR;
+                const int32_t* btr = p.block_table + static_cast<int64_t>(t.b) * p.bt_stride;
+                return lane < nr ? static_cast<int>(token_slot(p, btr, t.j * kT + lane * BR, bad)) : 0;
+            };
+            int y_next = run_slot(it);
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int valid = min(kT, it.T - it.j * kT);
+                const int nruns = (valid + BR - 1) / BR;
+                const int y = y_next;
+                const uint32_t run_bytes = static_cast<uint32_t>(nruns * BR * 128);
+                It nx = it;
+                nx.next(p.seq_lens, p.B);
+                if (i + 1 < ntiles) y_next = run_slot(nx);
+                if (lane == 0) MLA_TRACE_POINT(i, kTrProdStart + 0 * pp);
+                {
+                    const int u = 2 * i + pp, slot = u % C::kRL;
+                    if (u >= C::kRL &&
+                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->pair_empty[slot], ((u / C::kRL) - 1) & 1, &ctrl->abort))) {
+                        ok = false;
+                        fsite = kSiteTmaPairEmpty;
+                        ftile = i;
+                        break;
+                    }
+                    if (lane == 0) MLA_TRACE_POINT(i, kTrEpiStart + pp);  // slot free
+                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->pair_full[slot], 4 * run_bytes);
+                    __syncwarp();
+                    if (lane < nruns) {
+                        uint8_t* dst = pair_ring + slot * C::kPairBytes + lane * BR * 128;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh)
+                                tma_load_2d(dst + c * 16384 + hh * 8192, &maps.lat, &ctrl->pair_full[slot],
+                                            256 * hh + 128 * pp + 64 * c, y, pol);
+                    }
+                }
+                if (pp == 0) {
+                    const int rr = i % C::kRR;
+                    if (i >= C::kRR &&
+                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->rope_empty[rr], ((i / C::kRR) - 1) & 1, &ctrl->abort))) {
+                        ok = false;
+                        fsite = kSiteTmaRopeEmpty;
+                        ftile = i;
+                        break;
+                    }
+                    if (lane == 0) MLA_TRACE_POINT(i, kTrEpiStored);  // pair issued, rope slot free
+                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], run_bytes);
+                    __syncwarp();
+                    if (lane < nruns) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+                            tma_load_2d(rope_ring + rr * C::kRopeBytes + hh * 4096 + lane * BR * 64, &maps.rope,
+                                        &ctrl->rope_full[rr], 512 + 32 * hh, y, pol);
+                    }
+                    if (lane == 0) MLA_TRACE_POINT(i, kTrProdIssued);
+                }
+                it = nx;
+            }
+            if (!ok && lane == 0) {
+                fail(p, ctrl, kErrWaitTimeout, fsite, ftile);
+                report(p, pp ? kRoleLsu0 : kRoleTma, fsite, ftile);  // no load/convert warps here: their slot
+            }
+            if (bad) atomicOr(status_rec(p), kErrBadBlock);
+        } else if (warp >= 4 && warp < 8) {
+            // ------------------------------------------ softmax + epilogue
+            // Thread st reads TMEM lane st = A row st: half hf of token tt (warps
+            // 4, 5 the first halves, 6, 7 the second). It keeps columns [own0,
+            // own0 + NH) and hands the other NH partial scores to its partner
+            // st ^ 64, the other half of the same token.
+            const int st = threadIdx.x - 128;
+            const int sw = warp - 4;
+            const int hf = sw >> 1;
+            const int tt = st & 63;
+            const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
+            const int HQg = min(64, p.HQ - gy * 64);
+            constexpr int NH = C::kNH;
+            const int own0 = hf * NH;
+            // exchange rows of NH floats, 16-byte units swizzled by row; thread st
+            // writes row st ^ 64 and reads row st (same swizzle: bit 6 is not in it)
+            const int xs = (NH == 16) ? ((st >> 1) & 3) : ((st >> 2) & 1);
+            It it;
+            it.init(p.seq_lens, ctrl->b0, ctrl->j0);
+            float l[NH];
+#pragma unroll
+            for (int c = 0; c < NH; ++c) l[c] = 0.f;
+            int seg_start_j = it.j;
+            bool seg_has_pv = false;
+            int seg = 0;
+            uint32_t obuf = 0;
+            bool pend = false, pend_final = false;
+            int pend_b = 0;
+            int dr_left = 0, dr_step = 0, dr_b = 0, dr_sg = 0;
+            bool dr_final = false;
+            uint32_t dr_obuf = 0;
+            constexpr int kDC = 8;  // columns per drain step
+            const int dr_per_mt = (HQg + kDC - 1) / kDC;
+
+            // Column reductions over the tile's tokens: a warp reduces its 32
+            // lanes (one half), red[warp][column] meets the other warps' (the
+            // identity in the columns of the half the warp does not hold).
+            auto red_store = [&](int c, float v, float ident) {
+                if (lane == 0) {
+                    ctrl->red[sw][own0 + c] = v;
+                    ctrl->red[sw][(NH - own0) + c] = ident;
+                }
+            };
+
+            // O columns [0, NP) of accumulator ob, all four M-tiles, times alpha
+            // (the caller has waited for the last PV into it)
+            auto rescale_o = [&](uint32_t ob) {
+                tc_fence_after();
+                __syncwarp();
+#pragma unroll 1
+                for (int m4 = 0; m4 < 4; ++m4)
+#pragma unroll 1
+                    for (int c0 = 0; c0 < NP; c0 += 16) {
+                        uint32_t o[16];
+                        tmem_ld_x16(tmem + lane_base + ob + m4 * NP + c0, o);
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc)
+                            o[cc] = __float_as_uint(__uint_as_float(o[cc]) * ctrl->alpha[c0 + cc]);
+                        tmem_st_x16(tmem + lane_base + ob + m4 * NP + c0, o);
+                    }
+                tmem_wait_st();
+            };
+
+            // The NP query rows of request bq (row group gy) by TMA, stacked as
+            // S reads them: K-block k holds rows [0, NP) = latent dims 64k.. and
+            // rows [NP, 2NP) = dims 256 + 64k.. (128-B swizzle, at k * 2NP * 128),
+            // then the rope halves (64-B swizzle, at 8 NP * 128).
+            auto issue_q = [&](int bq) {
+                const int y = bq * p.HQ + gy * 64;
+                const uint64_t pol = l2_policy_evict_first();
+                mbar_arrive_expect_tx(&ctrl->q_full, C::kQBytes);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+                        tma_load_2d(qs + (k * 2 + hh) * NP * 128, &maps.q, &ctrl->q_full, 256 * hh + 64 * k, y, pol);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    tma_load_2d(qs + 8 * NP * 128 + hh * NP * 64, &maps.qpe, &ctrl->q_full, 32 * hh, y, pol);
+            };
+
+            // Row sums and maxima of segment sg, which just ended, into
+            // dlt / dm [sg & 1]; fresh softmax state for the next segment.
+            auto capture = [&](int sg) {
+#pragma unroll
+                for (int c = 0; c < NH; ++c) red_store(c, warp_sum(l[c]), 0.f);
+                named_bar_sync(1, 128);
+                if (st < NP) {
+                    ctrl->dlt[sg & 1][st] = ctrl->red[0][st] + ctrl->red[1][st] + ctrl->red[2][st] + ctrl->red[3][st];
+                    ctrl->dm[sg & 1][st] = ctrl->m[st];
+                    ctrl->m[st] = -INFINITY;
+                }
+#pragma unroll
+                for (int c = 0; c < NH; ++c) l[c] = 0.f;
+                named_bar_sync(1, 128);
+            };
+
+            // The captured segment sg (accumulator src) has had its last PV:
+            // write its LSEs and start draining its rows.
+            auto start_drain = [&](uint32_t src, int sg, int sb, bool sfinal) {
+                const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + sb;
+                if (st < NP && st < HQg) {
+                    const float lt = ctrl->dlt[sg & 1][st];
+                    const float lv = lt > 0.f ? (ctrl->dm[sg & 1][st] + log2f(lt)) * kLn2 : -INFINITY;
+                    if (sfinal) p.lse[static_cast<int64_t>(sb) * p.HQ + gy * 64 + st] = lv;
+                    else p.part_lse[pslot * 64 + st] = lv;
+                }
+                dr_left = 4 * dr_per_mt;
+                dr_step = 0;
+                dr_b = sb;
+                dr_final = sfinal;
+                dr_obuf = src;
+                dr_sg = sg;
+                pend = false;
+            };
+
+            // One drain step: kDC columns of one M-tile, O / l, into the output
+            // rows (a whole request) or this worker's partial slot.
+            auto drain_step = [&]() {
+                const int m4 = dr_step / dr_per_mt;
+                const int c0 = (dr_step - m4 * dr_per_mt) * kDC;
+                uint32_t o[kDC];
+                tmem_ld_x8(tmem + lane_base + dr_obuf + m4 * NP + c0, o);
+                const int64_t d = 128 * m4 + st;
+                const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + dr_b;
+#pragma unroll
+                for (int cc = 0; cc < kDC; ++cc) {
+                    const int c = c0 + cc;
+                    if (c < HQg) {
+                        const float lt = ctrl->dlt[dr_sg & 1][c];
+                        const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
+                        if (dr_final) {
+                            const int64_t idx = (static_cast<int64_t>(dr_b) * p.HQ + gy * 64 + c) * kD + d;
+                            if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
+                            else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+                        } else {
+                            p.part_o[(pslot * 64 + c) * kD + d] = v;
+                        }
+                    }
+                }
+                ++dr_step;
+                --dr_left;
+            };
+
+            int cap_b = 0;
+            bool cap_final = false;
+
+            // Hand tile t to the PV issuers, then start or advance the drain.
+            // False when the group aborts.
+            auto finish = [&](int t) -> bool {
+                if (ctrl->abort) return false;  // same value in every thread after the last barrier
+                if (st == 0) {
+                    // the test hook withholds tile 0, so the PV issuers' bounded wait
+                    // gives up and every role leaves through the abort path
+                    MLA_TRACE_POINT(t, kTrSmPArrive);
+                    MLA_TTRACE(t);
+                    if (!(p.test_hold && t == 0)) mbar_arrive(&ctrl->p_full);
+                }
+                seg_has_pv = true;
+                if (pend) {
+                    // PV(t-1), the captured segment's last, is long done by now
+                    group_wait(&ctrl->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, p, ctrl, kSiteOEpi, t);
+                    tc_fence_after();
+                    start_drain(obuf ^ (4 * NP), seg - 1, cap_b, cap_final);
+                } else if (dr_left > 0) {
+                    tc_fence_after();
+                    drain_step();
+                    tc_fence_before();
+                }
+                return true;
+            };
+
+            if (st == 0) issue_q(it.b);
+            bool alive = true;
+            for (int i = 0; i < ntiles; ++i) {
+                const int b = it.b, j = it.j, T = it.T;
+                const bool last_of_seg = (j == it.tiles - 1) || (i == ntiles - 1);
+                group_wait(&ctrl->s_full[i & 1], (i >> 1) & 1, p, ctrl, kSiteSFull, i);
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmSFull);
+                if (st == 0 && last_of_seg && i + 1 < ntiles) {
+                    // S(i) is complete, so Q may be replaced by the next request's
+                    It nx = it;
+                    nx.next(p.seq_lens, p.B);
+                    issue_q(nx.b);
+                }
+                tc_fence_after();
+                __syncwarp();
+                // this lane's half of the scores: columns [hf NP, hf NP + NP) (a TMEM
+                // load takes one column address per warp: hf is the same in the warp)
+                uint32_t sr[NP];
+                tmem_ld_np<NP>(tmem + lane_base + C::kColS + (i & 1) * 2 * NP + hf * NP, sr);
+                tc_fence_before();
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmTmemLd);
+                // own / partner columns, compile-time indices so sr[] stays in registers
+                auto own_s = [&](int k) -> uint32_t { return hf ? sr[NH + k] : sr[k]; };
+                auto snd_s = [&](int k) -> uint32_t { return hf ? sr[k] : sr[NH + k]; };
+                if (st == 0 && (i == 0 || j == 0) && !last_of_seg) {
+                    // warm L2 with the next request's queries and page list
+                    It nx = it;
+                    nx.j = nx.tiles - 1;
+                    nx.next(p.seq_lens, p.B);
+                    if (nx.b < p.B) prefetch_request(p, nx.b, gy);
+                }
+#pragma unroll
+                for (int u = 0; u < NH / 4; ++u)
+                    *reinterpret_cast<uint4*>(xbuf + (st ^ 64) * NH * 4 + ((u ^ xs) << 4)) =
+                        make_uint4(snd_s(4 * u), snd_s(4 * u + 1), snd_s(4 * u + 2), snd_s(4 * u + 3));
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmSent);
+                if (i > 0 && j == 0) {
+                    // the previous segment ended with tile i-1: finish the older
+                    // drain (its accumulator is the one this segment will use)
+                    if (dr_left > 0) {
+                        tc_fence_after();
+                        while (dr_left > 0) drain_step();
+                        tc_fence_before();
+                    }
+                    capture(seg);  // its barriers also order the exchange rows
+                    pend = true;
+                    cap_b = pend_b;
+                    cap_final = pend_final;
+                    seg_has_pv = false;
+                    ++seg;
+                    obuf = (seg & 1) * 4 * NP;
+                } else {
+                    named_bar_sync(1, 128);
+                }
+                if (st == 0) mbar_arrive(&ctrl->s_free[i & 1]);  // every thread has read S(i)
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmXFull);
+                float x[NH];
+#pragma unroll
+                for (int u = 0; u < NH / 4; ++u) {
+                    const float4 v = *reinterpret_cast<const float4*>(xbuf + st * NH * 4 + ((u ^ xs) << 4));
+                    x[4 * u] = __uint_as_float(own_s(4 * u)) + v.x;
+                    x[4 * u + 1] = __uint_as_float(own_s(4 * u + 1)) + v.y;
+                    x[4 * u + 2] = __uint_as_float(own_s(4 * u + 2)) + v.z;
+                    x[4 * u + 3] = __uint_as_float(own_s(4 * u + 3)) + v.w;
+                }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmXRead);
+                const int tok = j * kT + tt;
+                const bool all_vis = (j * kT + kT + p.Qt - 1) <= T;
+                const float4* m4p = reinterpret_cast<const float4*>(ctrl->m + own0);
+                if (all_vis) {
+#pragma unroll
+                    for (int c = 0; c < NH; ++c) x[c] = (own0 + c < HQg) ? x[c] * p.scale_log2 : -INFINITY;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NH; ++c)
+                        x[c] = (tok + ctrl->colvis[own0 + c] < T) ? x[c] * p.scale_log2 : -INFINITY;
+                }
+                int need = 0;
+#pragma unroll
+                for (int u = 0; u < NH / 4; ++u) {
+                    const float4 mv = m4p[u];
+                    need |= (x[4 * u] > mv.x + kRescaleThreshold) | (x[4 * u + 1] > mv.y + kRescaleThreshold) |
+                            (x[4 * u + 2] > mv.z + kRescaleThreshold) | (x[4 * u + 3] > mv.w + kRescaleThreshold);
+                }
+                // (also: every thread has read its exchange row)
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmMath);
+                need = named_bar_or(2, 128, need);
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmBarOr);
+                if (need) {
+                    // column maxima over the tile's 64 tokens
+#pragma unroll
+                    for (int c = 0; c < NH; ++c) red_store(c, warp_max(x[c]), -INFINITY);
+                    named_bar_sync(1, 128);
+                    if (st < NP) {
+                        const int c = st;
+                        const float mt = fmaxf(fmaxf(ctrl->red[0][c], ctrl->red[1][c]), fmaxf(ctrl->red[2][c], ctrl->red[3][c]));
+                        const float mo = ctrl->m[c];
+                        const float mn = fmaxf(mo, mt);
+                        ctrl->alpha[c] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
+                        ctrl->m[c] = mn;
+                    }
+                    named_bar_sync(1, 128);
+#pragma unroll
+                    for (int c = 0; c < NH; ++c) l[c] *= ctrl->alpha[own0 + c];
+                    if (seg_has_pv) {
+                        // O holds earlier tiles of this segment: wait for their PV, rescale
+                        // every column (each thread its TMEM lane of the four M-tiles)
+                        group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i);
+                        rescale_o(obuf);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < NH / 4; ++u) {
+                    const float4 mv = m4p[u];
+                    const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = 4 * u + k;
+                        const float mk = (mm[k] == -INFINITY) ? 0.f : mm[k];
+                        const float pc = ex2(x[c] - mk);
+                        l[c] += pc;
+                        x[c] = pc;
+                    }
+                }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmExpLoop);
+                // the P buffer of this tile was last read by PV(i - kPBufs)
+                if (i >= C::kPBufs) {
+                    const int jp = i - C::kPBufs;
+                    bool okp = true;
+                    if (lane == 0) okp = !ctrl->abort && mbar_wait(&ctrl->o_done[jp & 1], (jp >> 1) & 1, &ctrl->abort);
+                    okp = __shfl_sync(0xffffffffu, okp ? 1 : 0, 0) != 0;
+                    if (!okp && lane == 0) fail(p, ctrl, kErrWaitTimeout, kSiteOPbuf, i);
+                }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmExp);
+                // P row tt, columns [own0, own0 + NH): NH / 8 16-byte units
+                const int pb = i % C::kPBufs;
+                uint8_t* prow = pbufs + pb * C::kPBytes + tt * NP * 2;
+                const int sz = swz_p(tt, C::kPSwizzle);
+#pragma unroll
+                for (int u = 0; u < NH / 8; ++u) {
+                    const int un = own0 / 8 + u;
+                    const uint4 v = make_uint4(pack_bf16x2(x[8 * u + 0], x[8 * u + 1]), pack_bf16x2(x[8 * u + 2], x[8 * u + 3]),
+                                               pack_bf16x2(x[8 * u + 4], x[8 * u + 5]), pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
+                    *reinterpret_cast<uint4*>(prow + ((un ^ sz) << 4)) = v;
+                }
+                if (j * kT + tt >= T) {
+                    // this row's token is past the request: its bytes are stale (maybe
+                    // NaN); P is 0 there, but 0 * NaN would still poison O, so clear
+                    // the row in the four K-blocks (rotated units: no bank conflicts)
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint8_t* row = pair_ring + ((2 * i + (q >> 1)) % C::kRL) * C::kPairBytes + (q & 1) * 16384 + st * 128;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(row + (((u + st) & 7) << 4)) = z;
+                    }
+                }
+                if (st == 0) MLA_TRACE_POINT(i, kTrSmPStore);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(1, 128);
+                if (!finish(i)) {
+                    alive = false;
+                    break;
+                }
+                if (last_of_seg) {
+                    pend_final = (seg_start_j == 0) && (j == it.tiles - 1);
+                    pend_b = b;
+                    seg_start_j = 0;
+                }
+                it.next(p.seq_lens, p.B);
+            }
+            if (alive) {
+                // the last segment: finish the older drain, capture, wait for its
+                // last PV, write it out
+                const int il = ntiles - 1;
+                tc_fence_after();
+                while (dr_left > 0) drain_step();
+                capture(seg);
+                group_wait(&ctrl->o_done[il & 1], (il >> 1) & 1, p, ctrl, kSiteOFinal, il);
+                named_bar_sync(1, 128);
+                if (!ctrl->abort) {
+                    tc_fence_after();
+                    start_drain(obuf, seg, pend_b, pend_final);
+                    while (dr_left > 0) drain_step();
+                }
+            }
+            if (st == 0) MLA_KTRACE(2);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) MLA_KTRACE(3);
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
 // ---------------------------------------------------------------- merging
 
 // Merge `nseg` partials of one row: out = sum_i w_i o_i with
@@ -1441,7 +2158,7 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
     __shared__ long long red_pre[8], red_tot[8];
     long long pre = 0, tot = 0;
     for (int i = tid; i < p.B; i += 256) {
-        const long long tl = (max(__ldg(p.seq_lens + i), 0) + kTile - 1) / kTile;
+        const long long tl = (max(__ldg(p.seq_lens + i), 0) + (1 << p.tile_shift) - 1) >> p.tile_shift;
         const long long c = tl > 0 ? tl + p.wseg : 0;
         tot += c;
         if (i < b) pre += c;
@@ -1487,7 +2204,7 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
 
     const int HQg = min(64, p.HQ - gy * 64);
     if (b >= p.B || n >= HQg) return;
-    const int tiles_b = (max(__ldg(p.seq_lens + b), 0) + kTile - 1) / kTile;
+    const int tiles_b = (max(__ldg(p.seq_lens + b), 0) + (1 << p.tile_shift) - 1) >> p.tile_shift;
     const int64_t row = static_cast<int64_t>(b) * p.HQ + gy * 64 + n;
     const int d = 4 * t;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1663,6 +2380,53 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP,
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(p.B) * RB, GY), 256, 0, stream, attr);
     return cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel, p, G, 2 * G * GY);
+}
+
+template <int NP>
+struct FoldVariant {
+    // Set the shared-memory attribute (once per device) and return how many
+    // CTAs fit on the device at once.
+    static int max_ctas() {
+        static int done[64] = {0};
+        static int ctas[64] = {0};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return -1;
+        if (!done[dev]) {
+            auto k = mla_decode_fold_kernel<NP>;
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, FoldCfg<NP>::kSmemBytes) != cudaSuccess)
+                return -1;
+            int per_sm = 0, sms = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 288, FoldCfg<NP>::kSmemBytes) != cudaSuccess ||
+                per_sm <= 0)
+                return -1;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return -1;
+            ctas[dev] = per_sm * sms;
+            done[dev] = 1;
+        }
+        return ctas[dev];
+    }
+
+    static cudaError_t launch(const DecodeMaps& maps, const DecodeParams& p, int W, int GY, cudaStream_t stream) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pdl_config(dim3(W, GY), 288, FoldCfg<NP>::kSmemBytes, stream, attr);
+        return cudaLaunchKernelEx(&cfg, mla_decode_fold_kernel<NP>, maps, p);
+    }
+};
+
+int decode_fold_ctas(int NP, int requested_ctas) {
+    const int mx = NP == 16 ? FoldVariant<16>::max_ctas() : FoldVariant<32>::max_ctas();
+    if (mx <= 0) return -1;
+    return requested_ctas > 0 ? requested_ctas : mx;
+}
+
+cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int W, int GY,
+                               cudaStream_t stream) {
+    cudaError_t e = NP == 16 ? FoldVariant<16>::launch(maps, p, W, GY, stream) : FoldVariant<32>::launch(maps, p, W, GY, stream);
+    if (e != cudaSuccess) return e;
+    const int RB = (min(64, p.HQ) + 1) / 2;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(p.B) * RB, GY), 256, 0, stream, attr);
+    return cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel, p, W, W * GY);
 }
 
 cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, int64_t N, void* out, int out_f32,

@@ -28,10 +28,11 @@ struct DecodeParams {
     float* part_lse;   // [GY][SPG][64] fp32 partial LSEs
     float scale_log2;  // softmax scale * log2(e)
     int page_size;
-    int run_rows;      // TMA box height: gcd(page_size, 128)
+    int run_rows;      // TMA box height: gcd(page_size, tile)
+    int tile_shift;    // log2 of the tokens per tile: 7 (cluster kernel) or 6 (folded tiles)
     int B, Qt, Hq, HQ; // HQ = Hq * Qt rows per request
     int out_f32;
-    int SPG;           // partial slots per row group = clusters + B
+    int SPG;           // partial slots per row group = workers + B
     int wseg;          // work-split cost of a request boundary, in tiles
     int test_hold;     // test hook: 1 = withhold the first hand-off to the PV issuers
 };
@@ -51,6 +52,11 @@ struct DecodeMaps {
     CUtensorMap lat, aux, rope, q, qpe;
 };
 
+// CTAs of the folded-tile decode kernel (bf16 pools, page_size % 8 == 0, at
+// most 32 query rows): the number that fit at once, or requested_ctas.
+int decode_fold_ctas(int NP, int requested_ctas);
+cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int W, int GY,
+                               cudaStream_t stream);
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,
                           cudaStream_t stream);
 cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, int64_t N, void* out, int out_f32,

@@ -66,15 +66,15 @@ def test_host_validation_rejects_bad_arguments(lib):
 
 
 def test_workspace_size_formula(lib):
-    # header + [CTAs][16] int32 status records + [groups][clusters + B][64] lse
-    # + [groups][clusters + B][64][512] partial outputs, clusters = ctas / 2,
+    # header + [CTAs][16] int32 status records + [groups][CTAs + B][64] lse
+    # + [groups][CTAs + B][64][512] partial outputs, CTAs = max(2, num_ctas),
     # each part rounded up to 256 bytes
     def up(x):
         return -(-x // 256) * 256
-    for B, q, H, G in [(2, 1, 8, 152), (64, 1, 16, 152), (128, 4, 16, 152), (3, 1, 80, 7)]:
+    for B, q, H, G in [(2, 1, 8, 152), (64, 1, 16, 152), (128, 4, 16, 152), (3, 1, 80, 7), (5, 1, 16, 1)]:
         gy = -(-(H * q) // 64)
-        clusters = max(1, G // 2)
-        slots = gy * (clusters + B) * 64
-        rec_b = up(2 * clusters * gy * 16 * 4)
+        ctas = max(2, G)
+        slots = gy * (ctas + B) * 64
+        rec_b = up(ctas * gy * 16 * 4)
         assert m.mla_decode_workspace_bytes(B, q, H, G) == 256 + rec_b + up(slots * 4) + slots * 512 * 4
     assert lib.mla_decode_workspace_bytes(0, 1, 8, 4) == 0

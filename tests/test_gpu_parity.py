@@ -162,7 +162,7 @@ def test_decode_cta_counts(num_ctas):
     check_decode(out, lse, o, l, rows, what=f"ctas={num_ctas}")
 
 
-@pytest.mark.parametrize("page_size", [1, 8, 16, 64, 784])
+@pytest.mark.parametrize("page_size", [1, 8, 16, 32, 64, 96, 784])
 def test_decode_page_sizes_ragged(page_size):
     sl = [1, 17, 300, 1000, 129, 784, 785]
     wl = W.make("ps", B=len(sl), Hq=8, Qt=1, page_size=page_size, seq_lens=sl, seed=30 + page_size,
