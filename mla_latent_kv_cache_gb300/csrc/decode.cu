@@ -2140,24 +2140,30 @@ __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, con
     if (lane == 0 && lse_out) *lse_out = L;
 }
 
-// Decode merge: one row of one request per 128 threads (2 rows per block),
-// each thread 4 of the 512 dims. Rows of requests that one cluster held
-// whole were written by the decode kernel; rows of requests cut across
-// clusters g0..g1 combine their partial slots g + b; rows of empty requests
-// get (0, -inf). Block (0, 0) also folds the per-CTA status records of the
-// decode grid into the workspace header.
-__global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParams p, int G, int nrec) {
+// Decode merge: RPB rows of one request per block, GRP groups of 128 threads
+// per row; thread t of group grp holds dims 4t .. 4t+3 of the row's partial
+// slots k = grp (mod GRP), and the groups' sums meet in shared memory (GRP = 4
+// when rows have dozens of slots, 1 otherwise). Rows of requests that one
+// worker held whole were written by the decode kernel; rows of requests cut
+// across workers g0..g1 combine their partial slots g + b; rows of empty
+// requests get (0, -inf). Block (0, 0) also folds the per-CTA status records
+// of the decode grid into the workspace header.
+template <int RPB, int GRP>
+__global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const DecodeParams p, int G, int nrec) {
+    constexpr int kThreads = 128 * RPB * GRP;
     MLA_MTRACE(0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int RB = (min(64, p.HQ) + 1) >> 1;  // blocks per (request, row group)
+    const int RB = (min(64, p.HQ) + RPB - 1) / RPB;  // blocks per (request, row group)
     const int b = blockIdx.x / RB, gy = blockIdx.y;
-    const int n = (blockIdx.x - b * RB) * 2 + (tid >> 7);
-    const int t = tid & 127;
+    const int rb = tid / (128 * GRP);
+    const int n = (blockIdx.x - b * RB) * RPB + rb;
+    const int t = tid & 127, grp = (tid >> 7) % GRP;
     // cost coordinate of request b's first tile, and the total cost (the
     // decode kernel's work split)
-    __shared__ long long red_pre[8], red_tot[8];
+    __shared__ long long red_pre[kThreads / 32], red_tot[kThreads / 32];
+    __shared__ float4 part[GRP > 1 ? GRP - 1 : 1][128];
     long long pre = 0, tot = 0;
-    for (int i = tid; i < p.B; i += 256) {
+    for (int i = tid; i < p.B; i += kThreads) {
         const long long tl = (max(__ldg(p.seq_lens + i), 0) + (1 << p.tile_shift) - 1) >> p.tile_shift;
         const long long c = tl > 0 ? tl + p.wseg : 0;
         tot += c;
@@ -2173,7 +2179,7 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
     pre = p.wseg;
     tot = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) { pre += red_pre[w]; tot += red_tot[w]; }
+    for (int w = 0; w < kThreads / 32; ++w) { pre += red_pre[w]; tot += red_tot[w]; }
     griddep_wait();  // the decode grid has finished and its writes are visible
 
     if (blockIdx.x == 0 && blockIdx.y == 0 && warp == 0) {
@@ -2210,27 +2216,26 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = -INFINITY;
     if (tiles_b > 0) {
-        // the clusters holding the first and last tile: the largest g with
+        // the workers holding the first and last tile: the largest g with
         // floor(g * tot / G) <= cost coordinate of the tile
         const long long g0 = ((pre + 1) * G - 1) / tot;
         const long long g1 = ((pre + tiles_b) * G - 1) / tot;
-        if (g0 == g1) return;  // one cluster held the whole request and wrote the output
+        if (g0 == g1) return;  // one worker held the whole request and wrote the output
         const int nseg = static_cast<int>(g1 - g0 + 1);
         const int64_t slot0 = static_cast<int64_t>(gy) * p.SPG + g0 + b;
         const float* pl = p.part_lse + slot0 * 64 + n;
         const float* po = p.part_o + (slot0 * 64 + n) * kD + d;
-        // up to 8 slots: their partial outputs are requested before the weights
-        // are known, so the loads overlap the LSE round trip (empty slots hold
-        // stale values and get weight 0)
-        constexpr int kSpec = 8;
+        // this group's slots k = grp, grp + GRP, ...: the first kSpec of them are
+        // requested before the weights are known, so the loads overlap the LSE
+        // round trip (empty slots hold stale values and get weight 0)
+        constexpr int kSpec = GRP > 1 ? 4 : 8;
+        const int nmine = nseg > grp ? (nseg - grp + GRP - 1) / GRP : 0;
         float4 ov[kSpec];
-        if (nseg <= kSpec) {
 #pragma unroll
-            for (int k = 0; k < kSpec; ++k)
-                if (k < nseg) ov[k] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * 64 * kD);
-        }
-        // the slot LSEs, 32 at a time, one per lane (each warp of the row
-        // computes the same weights)
+        for (int k = 0; k < kSpec; ++k)
+            if (k < nmine) ov[k] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(grp + GRP * k) * 64 * kD);
+        // the slot LSEs, 32 at a time, one per lane (every warp computes the
+        // same weights)
         float mx = -INFINITY;
         for (int c0 = 0; c0 < nseg; c0 += 32)
             mx = fmaxf(mx, c0 + lane < nseg ? pl[(c0 + lane) * 64] : -INFINITY);
@@ -2242,38 +2247,45 @@ __global__ void __launch_bounds__(256) mla_decode_merge_kernel(const DecodeParam
                 ws += v != -INFINITY ? expf(v - mx) : 0.f;
             }
             L = mx + logf(warp_sum(ws));
-            if (nseg <= kSpec) {
-                const float v = lane < nseg ? pl[lane * 64] : -INFINITY;
-                const float wl = v != -INFINITY ? expf(v - L) : 0.f;
+            auto add = [&](int k, const float4& o) {
+                const float v = pl[k * 64];
+                const float w = v != -INFINITY ? expf(v - L) : 0.f;
+                if (w != 0.f) {
+                    acc.x += w * o.x;
+                    acc.y += w * o.y;
+                    acc.z += w * o.z;
+                    acc.w += w * o.w;
+                }
+            };
 #pragma unroll
-                for (int k = 0; k < kSpec; ++k) {
-                    const float w = __shfl_sync(0xffffffffu, wl, k);
-                    if (k < nseg && w != 0.f) {
-                        acc.x += w * ov[k].x;
-                        acc.y += w * ov[k].y;
-                        acc.z += w * ov[k].z;
-                        acc.w += w * ov[k].w;
-                    }
-                }
+            for (int k = 0; k < kSpec; ++k)
+                if (k < nmine) add(grp + GRP * k, ov[k]);
+            // the rest, 8 loads in flight at a time
+            for (int k0 = kSpec; k0 < nmine; k0 += 8) {
+                float4 o8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (k0 + k < nmine)
+                        o8[k] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(grp + GRP * (k0 + k)) * 64 * kD);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (k0 + k < nmine) add(grp + GRP * (k0 + k), o8[k]);
             }
-            for (int c0 = 0; nseg > kSpec && c0 < nseg; c0 += 32) {
-                const float v = c0 + lane < nseg ? pl[(c0 + lane) * 64] : -INFINITY;
-                const float wl = v != -INFINITY ? expf(v - L) : 0.f;
-                const int cn = min(32, nseg - c0);
-                const float* src = po + static_cast<int64_t>(c0) * 64 * kD;
-#pragma unroll 8
-                for (int k = 0; k < cn; ++k) {
-                    const float w = __shfl_sync(0xffffffffu, wl, k);
-                    // an empty slot (w = 0) was never written: read, then drop
-                    const float4 o = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(k) * 64 * kD);
-                    if (w != 0.f) {
-                        acc.x += w * o.x;
-                        acc.y += w * o.y;
-                        acc.z += w * o.z;
-                        acc.w += w * o.w;
-                    }
-                }
-            }
+        }
+    }
+    if constexpr (GRP > 1) {
+        // the groups' sums (every group has L; the empty-request path too). The
+        // block has one row, so every return above was taken by all of it.
+        if (grp > 0) part[grp - 1][t] = acc;
+        __syncthreads();
+        if (grp > 0) return;
+#pragma unroll
+        for (int q = 0; q < GRP - 1; ++q) {
+            const float4 o = part[q][t];
+            acc.x += o.x;
+            acc.y += o.y;
+            acc.z += o.z;
+            acc.w += o.w;
         }
     }
     if (p.out_f32) {
@@ -2314,6 +2326,20 @@ static cudaLaunchConfig_t pdl_config(dim3 grid, int threads, size_t smem, cudaSt
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cfg;
+}
+
+// The merge grid for G workers: rows whose requests are cut into dozens of
+// slots (workers >= 8 per request) get four thread groups each; otherwise two
+// rows share a block of one group each.
+static cudaError_t launch_decode_merge(const DecodeParams& p, int G, int nrec, int GY, cudaStream_t stream) {
+    const bool wide = G >= 8 * p.B;
+    const int rows = min(64, p.HQ);
+    const int RB = wide ? rows : (rows + 1) / 2;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg =
+        pdl_config(dim3(static_cast<unsigned>(p.B) * RB, GY), wide ? 512 : 256, 0, stream, attr);
+    return wide ? cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<1, 4>, p, G, nrec)
+                : cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<2, 1>, p, G, nrec);
 }
 
 template <int NP, bool LSU, int KIND>
@@ -2376,10 +2402,7 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP,
     cudaError_t e = MLA_DISPATCH(NP, MLA_LAUNCH);
 #undef MLA_LAUNCH
     if (e != cudaSuccess) return e;
-    const int RB = (min(64, p.HQ) + 1) / 2;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(p.B) * RB, GY), 256, 0, stream, attr);
-    return cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel, p, G, 2 * G * GY);
+    return launch_decode_merge(p, G, 2 * G * GY, GY, stream);
 }
 
 template <int NP>
@@ -2423,10 +2446,7 @@ cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, in
                                cudaStream_t stream) {
     cudaError_t e = NP == 16 ? FoldVariant<16>::launch(maps, p, W, GY, stream) : FoldVariant<32>::launch(maps, p, W, GY, stream);
     if (e != cudaSuccess) return e;
-    const int RB = (min(64, p.HQ) + 1) / 2;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(p.B) * RB, GY), 256, 0, stream, attr);
-    return cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel, p, W, W * GY);
+    return launch_decode_merge(p, W, W * GY, GY, stream);
 }
 
 cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, int64_t N, void* out, int out_f32,
