@@ -129,12 +129,14 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *                failing CTA; words 4..11 where each of its roles gave up.
  *                Calls sharing a workspace must be ordered on one stream.
  *   num_ctas     CTAs sharing the token stream (0 = as many as fit on the
- *                device, one per SM). CTAs work in clusters of two that split
- *                each token's 576 dims between them, so num_ctas / 2 clusters
- *                run. The tokens of all requests are cut into 128-token tiles
- *                dealt out as equal contiguous ranges, one per cluster;
- *                requests cut across clusters are merged from fp32 partials by
- *                a second kernel.
+ *                device, one per SM). bf16 pools whose page_size is a multiple
+ *                of 8 with at most 32 rows (Hq * q_len) per group: each CTA is
+ *                a worker on 64-token tiles of whole rows. Otherwise CTAs work
+ *                in clusters of two that split each token's 576 dims between
+ *                them, num_ctas / 2 workers on 128-token tiles. The tiles of
+ *                all requests are dealt out as equal contiguous ranges, one per
+ *                worker; requests cut across workers are merged from fp32
+ *                partials by a second kernel.
  * Limits: Hq * q_len rows are processed in groups of at most 64. Returns
  * MLA_ERR_UNSUPPORTED on a device other than sm_103 / sm_100 family.
  */
@@ -182,7 +184,7 @@ MLA_API int mla_num_sms(void);
  *   one array per device, so calls that can overlap (different streams, or
  *   several host threads) race on it: order them on one stream.
  */
-#define MLA_STATIC_SCRATCH_BYTES (32u << 20)
+#define MLA_STATIC_SCRATCH_BYTES (64u << 20)
 MLA_API int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const void* cache, int cache_kind,
                                       int64_t num_slots, int page_size, const int32_t* block_table,
                                       int64_t block_table_stride, const int32_t* seq_lens, int B, int q_len, int Hq,

@@ -13,7 +13,7 @@ from mla_latent_kv_cache_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 MLA_ERR_SCRATCH_LIMIT = -5
-MLA_STATIC_SCRATCH_BYTES = 32 << 20
+MLA_STATIC_SCRATCH_BYTES = 64 << 20
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -72,6 +72,12 @@ def test_repeated_call_is_identical():
     torch.cuda.synchronize()
     assert torch.equal(first[0], second[0]) and torch.equal(first[1], second[1])
     assert torch.isfinite(first[0]).all()
+
+
+def test_every_bench_workload_fits_the_scratch():
+    # batched, long, MTP verify and fp8 shapes at one CTA per SM
+    for B, q, Hq in [(64, 1, 16), (4, 1, 32), (128, 4, 16), (64, 1, 64)]:
+        assert 0 < m.mla_decode_workspace_bytes(B, q, Hq) <= MLA_STATIC_SCRATCH_BYTES
 
 
 def test_oversized_call_is_rejected_before_any_launch():
