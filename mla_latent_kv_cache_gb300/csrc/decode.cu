@@ -1409,9 +1409,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // so s(t, c) = D[t, c] + D[64 + t, NP + c]: the two halves of a token meet in
 // shared memory between softmax warps 4/6 and 5/7, and each keeps half of the
 // columns. (One 3-D TMA box per run carrying both halves halves the number of
-// boxes, but measured slower: its loads land 2-4 us after issue, not ~1 us.) The value product reads the same tile as the MN-major A operand of
-// four M = 128 UMMAs (latent dims 128 m + [0, 128)), K = 64 tokens:
+// boxes, but measured slower: its loads land 2-4 us after issue, not ~1 us.)
+// The value product reads the same tile as the MN-major A operand of four
+// M = 128 UMMAs, K = 64 tokens; M-tile kb covers the latent dims of K-block kb
+// in both halves, [64 kb, 64 kb + 64) and [256 + 64 kb, 256 + 64 kb + 64):
 //   O^T[512, NP] += C^T[512, 64] . P[64, NP]
+// so each 16-KB K-block is read by four S and four PV MMAs and nothing else,
+// and the ring is in K-block slots that free one by one.
 // Nothing crosses between CTAs: a tile's shared memory is held from its load
 // to its value product only, with no exchange latency in between.
 
@@ -1419,16 +1423,16 @@ template <int NP>
 struct FoldCfg {
     static_assert(NP == 16 || NP == 32, "NP");
     static constexpr int kTok = 64;                    // tokens per tile
-    static constexpr int kPairBytes = 2 * 128 * 128;   // K-blocks 2pp, 2pp+1: 64 dims x (64 + 64) rows, 128-B swizzled
+    static constexpr int kBlkBytes = 128 * 128;        // a K-block: 64 dims x (64 + 64) rows, 128-B swizzled
     static constexpr int kRopeBytes = 128 * 64;        // 32 rope dims x 128 rows, 64-B swizzled
-    static constexpr int kRL = (NP == 16) ? 5 : 4;     // pair slots (2 per tile)
-    static constexpr int kRR = 3;                      // rope slots (1 per tile; freed right after S)
+    static constexpr int kRL = (NP == 16) ? 11 : 9;    // K-block slots (4 per tile)
+    static constexpr int kRR = 2;                      // rope slots (1 per tile; freed right after S)
     static constexpr int kQBytes = 2 * NP * (4 * 128 + 64);
     static constexpr int kNH = NP / 2;                 // softmax columns per thread
     static constexpr int kXBytes = 128 * kNH * 4;      // the partner lane's half scores
     static constexpr int kPBufs = 2;
     static constexpr int kPBytes = kTok * NP * 2;      // P [64 tokens][NP] bf16, MN-major
-    static constexpr int kOffRope = kRL * kPairBytes;
+    static constexpr int kOffRope = kRL * kBlkBytes;
     static constexpr int kOffQ = kOffRope + kRR * kRopeBytes;
     static constexpr int kOffX = (kOffQ + kQBytes + 1023) / 1024 * 1024;
     static constexpr int kOffP = kOffX + kXBytes;
@@ -1444,8 +1448,8 @@ struct FoldCfg {
 };
 
 struct FoldCtrl {
-    uint64_t pair_full[5], pair_empty[5];
-    uint64_t rope_full[3], rope_empty[3];
+    uint64_t blk_full[11], blk_empty[11];
+    uint64_t rope_full[2], rope_empty[2];
     uint64_t s_full[2], s_free[2], p_full, o_done[2], q_full;
     uint32_t tmem_base;
     int abort;
@@ -1453,9 +1457,9 @@ struct FoldCtrl {
     int colvis[64];                  // query row -> trailing tokens it may not see
     alignas(16) float m[64];         // running max per row (log2 units)
     alignas(16) float alpha[64];
-    alignas(16) float red[4][64];
-    alignas(16) float dlt[2][64];    // row sums of a finished segment, by segment parity
-    float dm[2][64];                 // and its row maxima
+    alignas(16) float red[4][32];    // per-warp column reductions (at most 32 columns here)
+    alignas(16) float dlt[2][32];    // row sums of a finished segment, by segment parity
+    float dm[2][32];                 // and its row maxima
 };
 static_assert(sizeof(FoldCtrl) <= 3072, "control block");
 
@@ -1467,7 +1471,7 @@ __global__ void __launch_bounds__(288, 1)
     using It = TileItT<6>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* pair_ring = smem;
+    uint8_t* ring = smem;
     uint8_t* rope_ring = smem + C::kOffRope;
     uint8_t* qs = smem + C::kOffQ;
     uint8_t* xbuf = smem + C::kOffX;
@@ -1479,8 +1483,9 @@ __global__ void __launch_bounds__(288, 1)
     if (threadIdx.x == 0) MLA_KTRACE(0);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kRL; ++i) { mbar_init(&ctrl->pair_full[i], 1); mbar_init(&ctrl->pair_empty[i], 1); }
-        for (int i = 0; i < C::kRR; ++i) { mbar_init(&ctrl->rope_full[i], 1); mbar_init(&ctrl->rope_empty[i], 1); }
+        for (int i = 0; i < C::kRL; ++i) { mbar_init(&ctrl->blk_full[i], 1); mbar_init(&ctrl->blk_empty[i], 1); }
+        // a rope slot is filled by both producer warps (one half each)
+        for (int i = 0; i < C::kRR; ++i) { mbar_init(&ctrl->rope_full[i], 2); mbar_init(&ctrl->rope_empty[i], 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->s_full[i], 1);
             mbar_init(&ctrl->s_free[i], 1);
@@ -1566,18 +1571,15 @@ __global__ void __launch_bounds__(288, 1)
                 const uint32_t tS = tmem + C::kColS + (i & 1) * 2 * NP;
                 bool ok = true;
                 int site = kSitePairFull;
-                for (int pp = 0; pp < 2 && ok; ++pp) {
-                    const int u = 2 * i + pp, slot = u % C::kRL;
-                    if (!mbar_wait(&ctrl->pair_full[slot], (u / C::kRL) & 1, &ctrl->abort)) { ok = false; break; }
+                for (int kb = 0; kb < 4 && ok; ++kb) {
+                    const int u = 4 * i + kb, slot = u % C::kRL;
+                    if (!mbar_wait(&ctrl->blk_full[slot], (u / C::kRL) & 1, &ctrl->abort)) { ok = false; break; }
                     tc_fence_after();
-                    if (pp == 0) MLA_TRACE_POINT(i, kTrSPair0);
-                    const uint64_t da = smem_desc(smem_u32(pair_ring + slot * C::kPairBytes), 16, 1024, kSw128);
+                    if (kb == 0) MLA_TRACE_POINT(i, kTrSPair0);
+                    const uint64_t da = smem_desc(smem_u32(ring + slot * C::kBlkBytes), 16, 1024, kSw128);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            umma_bf16(tS, da + ((c * 16384 + kk * 32) >> 4),
-                                      dq + (((2 * pp + c) * 2 * NP * 128 + kk * 32) >> 4), idS, (pp | c | kk) != 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4), idS, (kb | kk) != 0);
                 }
                 const int rr = i % C::kRR;
                 if (ok && !mbar_wait(&ctrl->rope_full[rr], (i / C::kRR) & 1, &ctrl->abort)) {
@@ -1601,8 +1603,9 @@ __global__ void __launch_bounds__(288, 1)
             }
         } else if ((warp == 3 || warp == 2) && lane == 0) {
             // ------------------------------------------------- PV issuers
-            // issuer mt reads pair slot 2i + mt: latent dims 128 mt + [0, 128)
-            // of the first half (M-tile mt) and of the second (M-tile 2 + mt)
+            // issuer mt takes K-blocks 2 mt and 2 mt + 1: M-tile kb reads K-block
+            // kb's slot as C^T (its two 64-dim atoms are the halves, 8 KB apart)
+            // and frees the slot when its four MMAs are done
             const int mt = warp == 3 ? 0 : 1;
             It it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
@@ -1623,30 +1626,31 @@ __global__ void __launch_bounds__(288, 1)
                 if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssue);
                 const uint64_t dp = smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), C::kPBytes, p_sbo,
                                               C::kPSwizzle);
-                const int slot = (2 * i + mt) % C::kRL;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    // tokens 16 kk .. 16 kk + 15 of half hh: rows 64 hh + 16 kk ..
-                    const uint64_t da =
-                        smem_desc(smem_u32(pair_ring + slot * C::kPairBytes + hh * 8192), 16384, 1024, kSw128);
+                for (int q = 0; q < 2; ++q) {
+                    const int kb = 2 * mt + q;
+                    const int slot = (4 * i + kb) % C::kRL;
+                    // tokens 16 kk .. 16 kk + 15: rows 16 kk .. of both halves
+                    const uint64_t da = smem_desc(smem_u32(ring + slot * C::kBlkBytes), 8192, 1024, kSw128);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tO + (2 * hh + mt) * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
+                        umma_bf16(tO + kb * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
                                   (new_seg && kk == 0) ? 0u : 1u);
+                    umma_commit(&ctrl->blk_empty[slot]);
                 }
-                umma_commit(&ctrl->pair_empty[slot]);
                 umma_commit(&ctrl->o_done[i & 1]);
                 if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssued);
                 it.next(p.seq_lens, p.B);
             }
         } else if (warp == 1 || warp == 8) {
             // ------------------------------------------------- TMA producers
-            // Warp 1 loads pair 0 and the rope of every tile, warp 8 pair 1 (with
-            // 16-token pages a tile is 40 boxes of 2 KB, and one warp issuing them
-            // all takes about as long as the tile's compute). Lane r owns run r of
-            // the tile (a page-contiguous run of BR rows); each run lands twice per
-            // K-block: its first halves in rows [r BR, (r+1) BR), its second halves
-            // 64 rows further. Page numbers are read one tile ahead.
+            // Warp 1 loads K-blocks 0, 1 and the first rope half of every tile,
+            // warp 8 K-blocks 2, 3 and the second rope half (with 16-token pages a
+            // tile is 40 boxes of 2 KB, and one warp issuing them all takes about
+            // as long as the tile's compute). Lane r owns run r of the tile (a
+            // page-contiguous run of BR rows); each run lands twice per K-block:
+            // its first halves in rows [r BR, (r+1) BR), its second halves 64
+            // rows further. Page numbers are read one tile ahead.
             const int pp = warp == 1 ? 0 : 1;
             It it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
@@ -1670,29 +1674,28 @@ __global__ void __launch_bounds__(288, 1)
                 nx.next(p.seq_lens, p.B);
                 if (i + 1 < ntiles) y_next = run_slot(nx);
                 if (lane == 0) MLA_TRACE_POINT(i, kTrProdStart + 0 * pp);
-                {
-                    const int u = 2 * i + pp, slot = u % C::kRL;
+                for (int q = 0; q < 2; ++q) {
+                    const int kb = 2 * pp + q;
+                    const int u = 4 * i + kb, slot = u % C::kRL;
                     if (u >= C::kRL &&
-                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->pair_empty[slot], ((u / C::kRL) - 1) & 1, &ctrl->abort))) {
+                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->blk_empty[slot], ((u / C::kRL) - 1) & 1, &ctrl->abort))) {
                         ok = false;
                         fsite = kSiteTmaPairEmpty;
                         ftile = i;
                         break;
                     }
-                    if (lane == 0) MLA_TRACE_POINT(i, kTrEpiStart + pp);  // slot free
-                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->pair_full[slot], 4 * run_bytes);
+                    if (lane == 0 && q == 0) MLA_TRACE_POINT(i, kTrEpiStart + pp);  // slot free
+                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->blk_full[slot], 2 * run_bytes);
                     __syncwarp();
                     if (lane < nruns) {
-                        uint8_t* dst = pair_ring + slot * C::kPairBytes + lane * BR * 128;
+                        uint8_t* dst = ring + slot * C::kBlkBytes + lane * BR * 128;
 #pragma unroll
-                        for (int c = 0; c < 2; ++c)
-#pragma unroll
-                            for (int hh = 0; hh < 2; ++hh)
-                                tma_load_2d(dst + c * 16384 + hh * 8192, &maps.lat, &ctrl->pair_full[slot],
-                                            256 * hh + 128 * pp + 64 * c, y, pol);
+                        for (int hh = 0; hh < 2; ++hh)
+                            tma_load_2d(dst + hh * 8192, &maps.lat, &ctrl->blk_full[slot], 256 * hh + 64 * kb, y, pol);
                     }
                 }
-                if (pp == 0) {
+                if (!ok) break;
+                {
                     const int rr = i % C::kRR;
                     if (i >= C::kRR &&
                         !__all_sync(0xffffffffu, mbar_wait(&ctrl->rope_empty[rr], ((i / C::kRR) - 1) & 1, &ctrl->abort))) {
@@ -1701,16 +1704,13 @@ __global__ void __launch_bounds__(288, 1)
                         ftile = i;
                         break;
                     }
-                    if (lane == 0) MLA_TRACE_POINT(i, kTrEpiStored);  // pair issued, rope slot free
-                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], run_bytes);
+                    if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrEpiStored);  // K-blocks issued, rope slot free
+                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], run_bytes / 2);
                     __syncwarp();
-                    if (lane < nruns) {
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh)
-                            tma_load_2d(rope_ring + rr * C::kRopeBytes + hh * 4096 + lane * BR * 64, &maps.rope,
-                                        &ctrl->rope_full[rr], 512 + 32 * hh, y, pol);
-                    }
-                    if (lane == 0) MLA_TRACE_POINT(i, kTrProdIssued);
+                    if (lane < nruns)
+                        tma_load_2d(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
+                                    &ctrl->rope_full[rr], 512 + 32 * pp, y, pol);
+                    if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrProdIssued);
                 }
                 it = nx;
             }
@@ -1842,7 +1842,8 @@ __global__ void __launch_bounds__(288, 1)
                 const int c0 = (dr_step - m4 * dr_per_mt) * kDC;
                 uint32_t o[kDC];
                 tmem_ld_x8(tmem + lane_base + dr_obuf + m4 * NP + c0, o);
-                const int64_t d = 128 * m4 + st;
+                // M-tile m4, lane st: latent dim 64 m4 + st (first half) or 256 + 64 m4 + st - 64
+                const int64_t d = (st < 64 ? 0 : 192) + 64 * m4 + st;
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + dr_b;
 #pragma unroll
                 for (int cc = 0; cc < kDC; ++cc) {
@@ -2043,7 +2044,7 @@ __global__ void __launch_bounds__(288, 1)
                     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        uint8_t* row = pair_ring + ((2 * i + (q >> 1)) % C::kRL) * C::kPairBytes + (q & 1) * 16384 + st * 128;
+                        uint8_t* row = ring + ((4 * i + q) % C::kRL) * C::kBlkBytes + st * 128;
 #pragma unroll
                         for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(row + (((u + st) & 7) << 4)) = z;
                     }
