@@ -12,7 +12,10 @@ Functions whose result is pinned by tests (see ``tests/test_oracle_pins.py``):
 ``cache_write`` (byte geometry, bf16 bit copy, e4m3 round trip), ``decode``
 (absorbed == naive identity, closed forms, causal truncation, rope-free
 invariance), ``merge`` (partition invariance) and the e4m3 codec (agreement
-with torch's float8_e4m3fn cast and with a brute-force table search).
+with torch's float8_e4m3fn cast and with a brute-force table search); and
+``gather_upconvert`` / ``f32_to_bf16`` in ``tests/test_oracle_gather.py``
+(torch's bf16 and e4m3 conversions, numpy float32 products, exact power-of-two
+scales, the cache write's round-trip bound, brute-force row bookkeeping).
 """
 from __future__ import annotations
 
@@ -69,6 +72,10 @@ def _load():
             lib.oracle_decode.restype = i32
             lib.oracle_merge.argtypes = [p, p, i32, i64, p, p]
             lib.oracle_merge.restype = None
+            lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_gather_upconvert.argtypes = [p, i64, i32, p, i64, p, i32, i64, p, i64]
+            lib.oracle_gather_upconvert.restype = i32
             lib.oracle_row_values.restype = i32
             lib.oracle_num_threads.restype = i32
             lib.oracle_row_bytes.argtypes = [i32]
@@ -189,3 +196,28 @@ def merge(part_o, part_lse):
     lse = np.empty((N,), dtype=np.float64)
     lib.oracle_merge(_ptr(po), _ptr(pl), S, N, _ptr(out), _ptr(lse))
     return out, lse
+
+
+def f32_to_bf16(x: float) -> int:
+    """bf16 bits of an fp32 value, round to nearest even."""
+    return int(_load().oracle_f32_to_bf16(float(x)))
+
+
+def gather_upconvert(cache: np.ndarray, page_size: int, block_table, cu_seq_lens, num_rows: int,
+                     dst: np.ndarray = None, dst_stride: int = W) -> np.ndarray:
+    """Context gather of an fp8_ds_mla pool (uint8 [num_slots, 656]) into bf16
+    rows: returns `dst` (uint16 bits [num_rows, dst_stride], a fresh array of
+    0xFFFF sentinels when not given) with rows cu[b] + j filled."""
+    lib = _load()
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and cache.shape[1] == ROW_BYTES[1]
+    bt = _as_np(block_table, np.int32)
+    cu = _as_np(cu_seq_lens, np.int32)
+    B = cu.shape[0] - 1
+    if dst is None:
+        dst = np.full((num_rows, dst_stride), 0xFFFF, dtype=np.uint16)
+    assert dst.dtype == np.uint16 and dst.flags.c_contiguous and dst.shape[1] == dst_stride
+    rc = lib.oracle_gather_upconvert(_ptr(cache), cache.shape[0], page_size, _ptr(bt),
+                                     bt.shape[1] if bt.ndim == 2 else 1, _ptr(cu), B, num_rows, _ptr(dst), dst_stride)
+    if rc != 0:
+        raise ValueError("oracle_gather_upconvert: block id or slot out of range")
+    return dst

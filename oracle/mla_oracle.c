@@ -166,6 +166,64 @@ static void read_row(const uint8_t *cache, int kind, int64_t slot, double *v) {
     }
 }
 
+/* ---------------------------------------------------- context gather */
+
+/* bf16 bits of an fp32 value, round to nearest with ties to even (the 16
+ * dropped bits decide; a NaN stays a quiet NaN). */
+uint16_t oracle_f32_to_bf16(float x) {
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x0040u);
+    const uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* The prefill-context gather of an fp8_ds_mla pool [P3: the commit "derive
+ * mla_dims from the runtime layers" and the PR description, where the
+ * fp8_ds_mla context-gather path (cp_gather_and_upconvert_fp8_kv_cache)
+ * fills a workspace whose rows must be 576 wide]. For request b < B and
+ * context token j < cu[b+1] - cu[b]:
+ *   slot = block_table[b][j / ps] * ps + j % ps                  (64-bit)
+ *   dst[cu[b] + j][d]       = bf16(fp32(e4m3(code_d)) * scale_{d / 128})   d < 512
+ *   dst[cu[b] + j][512 + e] = k_pe_e, the stored bf16 bits                 e < 64
+ * The dequantised value is one fp32 multiply (the e4m3 value is exact in
+ * fp32) rounded once more to bf16, round to nearest even: the two roundings
+ * of the plainest reading (dequantise in fp32, store the 576-wide bf16 row).
+ * Rows with cu[b] + j >= num_rows are skipped; other dst rows are untouched.
+ * A page id outside the pool writes that row as zeros and the call returns
+ * -1 (0 otherwise). */
+int oracle_gather_upconvert(const uint8_t *cache, int64_t num_slots, int page_size,
+                            const int32_t *block_table, int64_t bt_stride,
+                            const int32_t *cu_seq_lens, int B, int64_t num_rows,
+                            uint16_t *dst, int64_t dst_stride) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t r0 = cu_seq_lens[b], len = (int64_t)cu_seq_lens[b + 1] - r0;
+        for (int64_t j = 0; j < len; ++j) {
+            const int64_t r = r0 + j;
+            if (r < 0 || r >= num_rows) continue;
+            uint16_t *out = dst + r * dst_stride;
+            const int64_t page = block_table[(int64_t)b * bt_stride + j / page_size];
+            const int64_t slot = page * page_size + j % page_size;
+            if (page < 0 || slot >= num_slots) {
+                memset(out, 0, MLA_W * sizeof(uint16_t));
+                bad = 1;
+                continue;
+            }
+            const uint8_t *row = cache + slot * (int64_t)ROW_FP8;
+            for (int d = 0; d < MLA_D; ++d) {
+                float sc;
+                memcpy(&sc, row + 512 + 4 * (d / 128), 4);
+                const float v = (float)oracle_e4m3_to_f64(row[d]) * sc;  /* exact widening, one fp32 multiply */
+                out[d] = oracle_f32_to_bf16(v);
+            }
+            for (int e = 0; e < MLA_P; ++e) memcpy(out + MLA_D + e, row + 528 + 2 * e, 2);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
 /* ---------------------------------------------------------------- decode */
 
 /* Absorbed MLA decode, definition form.
