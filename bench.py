@@ -8,6 +8,7 @@ once; also decode steps/s and context tokens/s.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config batched|long|mtp|fp8|tiny]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
+  python bench.py --config gather        # the fp8_ds_mla prefill-context gather (mla_gather_upconvert)
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
 on the launching stream, with L2 flushed (a 256 MiB write) before every step
@@ -41,7 +42,11 @@ CONFIG_TEXT = {
     "long": "B=4 Hq=32 seq 262144 page 64 bf16",
     "mtp": "B=128 Hq=16 Qt=4 causal, 9.8M-slot pool above slot 3,728,270, seq 0/1/U{2048..100000}, page 16 bf16",
     "fp8": "B=64 Hq=64 seq 32768 page 64 fp8_ds_mla (656 B rows)",
+    "gather": "fp8_ds_mla pool of the fp8 workload (B=64 x 32768 tokens, page 64) gathered into "
+              "[2097152, 576] bf16 rows",
 }
+GATHER_METRIC = "fp8_ds_mla context gather + upconvert HBM GB/s (656 B read + 1152 B written per token)"
+GATHER_BYTES_PER_TOKEN = 656 + 1152
 
 
 def dist_env():
@@ -329,6 +334,190 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def _gather_inputs(dev, rank=0):
+    """The fp8 workload's pool, written by the cache-write kernel, and its
+    prefix sums of context lengths (the gather's cu_seq_lens)."""
+    import numpy as np
+    import torch
+    import mla_latent_kv_cache_gb300 as m
+    from mla_latent_kv_cache_gb300 import workloads as W
+    wl = W.fp8(device=dev, seed=6 + 1000 * rank)
+    m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+    sl = wl.seq_lens.cpu().numpy().astype(np.int64)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(sl)]).astype(np.int32)).to(dev)
+    return wl, cu, int(sl.sum())
+
+
+def gather_cpu_sample(wl, budget_s=10.0):
+    """Time the oracle's gather on whole requests (in turn) for about
+    `budget_s`; returns (bytes, seconds, requests, threads)."""
+    import numpy as np
+    import oracle
+    from mla_latent_kv_cache_gb300 import workloads as W
+    sl = wl.seq_lens.cpu().numpy()
+    prep, done, secs, n = {}, 0, 0.0, 0
+    while secs < budget_s:
+        b = n % wl.B
+        if b not in prep:
+            c = W.compact(wl, [b])
+            prep[b] = (c["pool"], c["block_table"], np.array([0, int(sl[b])], dtype=np.int32))
+        pool, bt, cu = prep[b]
+        t0 = time.perf_counter()
+        oracle.gather_upconvert(pool, wl.page_size, bt, cu, int(sl[b]))
+        secs += time.perf_counter() - t0
+        done += int(sl[b]) * GATHER_BYTES_PER_TOKEN
+        n += 1
+    return done, secs, n, 1  # the oracle's gather is a plain loop on one thread
+
+
+def run_gather(args):
+    import torch
+    import torch.distributed as dist
+
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    from mla_latent_kv_cache_gb300 import build as mbuild
+    mbuild.build()
+    import mla_latent_kv_cache_gb300 as m
+
+    wl, cu, rows = _gather_inputs(dev, rank)
+    step_bytes = rows * GATHER_BYTES_PER_TOKEN
+    dst = torch.empty((rows, 576), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(bt=wl.block_table, c=cu, out=dst):
+        m.mla_gather_upconvert(wl.pool, wl.page_size, bt, c, out)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    K = min(args.steps, 400)  # ~0.6 ms a step: about a quarter of a second
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks_bench_gather.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    if ws_ > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if ws_ > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+
+    # end to end: the block table and prefix sums from pinned host memory, the
+    # gathered rows back to pinned host memory, every step
+    h_bt = wl.block_table.cpu().pin_memory()
+    h_cu = cu.cpu().pin_memory()
+    h_dst = torch.empty((rows, 576), dtype=torch.bfloat16).pin_memory()
+    d_bt = torch.empty_like(wl.block_table)
+    d_cu = torch.empty_like(cu)
+    h2d = h_bt.numel() * 4 + h_cu.numel() * 4
+    d2h = rows * 576 * 2
+    Ke = 10
+    eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+    for i in range(Ke + 2):
+        flush.fill_(1)
+        if i >= 2:
+            eve[i - 2][0].record(stream)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_cu.copy_(h_cu, non_blocking=True)
+        step(d_bt, d_cu, dst)
+        h_dst.copy_(dst, non_blocking=True)
+        if i >= 2:
+            eve[i - 2][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eve) / Ke
+    assert torch.equal(h_dst[::4096].to(dev), dst[::4096]), "end-to-end rows differ"
+
+    tot_bytes, step_ms_max = aggregate(step_bytes, step_ms)
+    _, e2e_ms_max = aggregate(step_bytes, e2e_ms)
+    if rank != 0:
+        if ws_ > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = measured_peaks()
+    value = tot_bytes / (step_ms_max * 1e-3) / 1e9
+    achieved = step_bytes / (step_ms * 1e-3) / 1e9
+    line = {
+        "metric": GATHER_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws_, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+fp32->bf16",
+        "data": "synthetic (seeded N(0,1) bf16 sources quantised by the cache-write kernel, shuffled block tables)",
+        "config": {"workload": "gather", "shape": CONFIG_TEXT["gather"], "tokens": rows,
+                   "bytes_per_step": step_bytes,
+                   "l2": "flushed before every step (256 MiB write, outside the timed events)",
+                   "step": "mla_gather_upconvert of every context token of the pool's 64 requests",
+                   "parallelism": f"replicas x{ws_} (requests are independent)"},
+        "tokens_per_s": round(rows * ws_ / (step_ms_max * 1e-3), 1),
+        "pct_of_measured_hbm": round(100 * value / ws_ / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "gather_upconvert_fp8_kernel, CUDA events",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: copy, read+write)",
+                     "algorithmic_bytes_per_launch": step_bytes},
+        "e2e": {"value": round(tot_bytes / (e2e_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms_max, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if ws_ == 1 and not args.no_cpu:
+        b, sec, n, th = gather_cpu_sample(wl)
+        line["cpu_baseline"] = {"value": round(b / sec / 1e9, 4), "unit": "GB/s", "cores": th, "kind": "oracle",
+                                "sample": f"{n} whole-request gathers of the gather workload "
+                                          f"({b // GATHER_BYTES_PER_TOKEN} tokens, {sec:.1f} s), C oracle, one thread"}
+    print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        dist.destroy_process_group()
+
+
+def run_gather_reference(args):
+    """The oracle's gather as the reference arm (rank 0 only): each step whole
+    requests of the gather workload, about a minute in total."""
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cuda":
+        from mla_latent_kv_cache_gb300 import build as mbuild
+        mbuild.build()
+        wl, _, _ = _gather_inputs(dev)
+    else:
+        raise SystemExit("the gather workload's pool is written by the GPU cache-write kernel")
+    per_step = max(0.05, 60.0 / (args.steps + args.warmup))
+    tb, ts, tn = 0, 0.0, 0
+    for i in range(args.warmup + args.steps):
+        b, sec, n, th = gather_cpu_sample(wl, budget_s=per_step)
+        if i >= args.warmup:
+            tb, ts, tn = tb + b, ts + sec, tn + n
+    v = tb / ts / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": GATHER_METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * ts / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+fp32->bf16",
+        "data": "synthetic", "config": {"workload": "gather", "shape": CONFIG_TEXT["gather"]},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": th, "kind": "oracle",
+                         "sample": f"each step: whole requests of the gather workload for {per_step:.2f} s "
+                                   f"({tn} requests over the timed steps)"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 # ------------------------------------------------------------ CPU oracle leg
 
 def _oracle_prepare(wl, b):
@@ -451,7 +640,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.config == "gather":
+        run_gather_reference(args) if args.impl == "reference" else run_gather(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

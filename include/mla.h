@@ -82,6 +82,38 @@ MLA_API int mla_cache_write(const void* latent, int64_t latent_stride, const voi
                     int cache_kind, void* stream);
 
 /*
+ * mla_gather_upconvert - the prefill-context gather of an fp8_ds_mla pool into
+ * 576-wide bf16 rows (vLLM PR #55543, the commit that derives mla_dims from
+ * the runtime layers and the PR description: the fp8_ds_mla context-gather
+ * path, cp_gather_and_upconvert_fp8_kv_cache, fills a workspace whose rows
+ * must be 576 wide). For request b < B and context token
+ * j < cu_seq_lens[b+1] - cu_seq_lens[b]:
+ *   slot = block_table[b][j / page_size] * page_size + j % page_size  (64-bit)
+ *   dst[cu_seq_lens[b] + j][d]       = bf16(e4m3(code_d) * scale_{d/128}), d < 512
+ *   dst[cu_seq_lens[b] + j][512 + e] = the row's rope value e as stored, e < 64
+ * The product is one fp32 multiply (the e4m3 value widens exactly), rounded
+ * to bf16 to nearest even.
+ *   cache        device, the fp8_ds_mla pool written by mla_cache_write:
+ *                num_slots rows of 656 bytes, 16-byte aligned.
+ *   page_size    tokens per page, >= 1.
+ *   block_table  device, int32 [B, block_table_stride]; entries past
+ *                ceil(len_b / page_size) are never read.
+ *   cu_seq_lens  device, int32 [B + 1], non-decreasing, cu_seq_lens[0] = 0
+ *                (read on the device only).
+ *   num_rows     rows of dst the call may write (normally cu_seq_lens[B]);
+ *                rows cu_seq_lens[b] + j >= num_rows are skipped.
+ *   dst          device, bf16 [num_rows, dst_stride], 16-byte aligned,
+ *                caller-owned; rows no request names are not touched.
+ *   dst_stride   elements between rows, >= 576 and a multiple of 8.
+ * A block-table entry outside the pool writes its row as zeros. Returns
+ * MLA_ERR_INVALID_ARG for bad sizes or pointers (B = 0 or num_rows = 0 is a
+ * no-op), MLA_ERR_CUDA if the launch fails. Does not synchronise.
+ */
+MLA_API int mla_gather_upconvert(const void* cache, int64_t num_slots, int page_size, const int32_t* block_table,
+                                 int64_t block_table_stride, const int32_t* cu_seq_lens, int B, int64_t num_rows,
+                                 void* dst, int64_t dst_stride, void* stream);
+
+/*
  * mla_decode_workspace_bytes - bytes of device workspace mla_decode needs.
  *   B, q_len, Hq   as for mla_decode.
  *   num_ctas       the value that will be passed to mla_decode (0 = as many

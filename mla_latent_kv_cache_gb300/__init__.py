@@ -68,6 +68,8 @@ def load() -> ctypes.CDLL:
             lib.mla_test_hold_next_decode.argtypes = []
             lib.mla_test_hold_next_decode.restype = None
             lib.mla_merge_lse.argtypes = [vp, vp, i32, i64, vp, i32, vp, vp]
+            lib.mla_gather_upconvert.argtypes = [vp, i64, i32, vp, i64, vp, i32, i64, vp, i64, vp]
+            lib.mla_gather_upconvert.restype = i32
             lib.mla_merge_lse.restype = i32
             _lib = lib
     return _lib
@@ -115,6 +117,21 @@ def mla_cache_write(latent: torch.Tensor, k_pe: torch.Tensor, slot_mapping: torc
                                   k_pe.data_ptr(), k_pe.stride(0) if k_pe.dim() == 2 else 64,
                                   slot_mapping.data_ptr(), T, cache.data_ptr(), nbytes // rb, cache_kind,
                                   _stream(stream)), "mla_cache_write")
+
+
+def mla_gather_upconvert(cache: torch.Tensor, page_size: int, block_table: torch.Tensor, cu_seq_lens: torch.Tensor,
+                         dst: torch.Tensor, num_rows: int = None, stream=None) -> None:
+    """Context gather of an fp8_ds_mla pool into bf16 rows (include/mla.h)."""
+    assert cache.dtype == torch.uint8 and cache.dim() == 2 and cache.shape[1] == 656 and cache.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.stride(1) == 1
+    assert cu_seq_lens.dtype == torch.int32 and cu_seq_lens.is_contiguous()
+    assert dst.dtype == torch.bfloat16 and dst.dim() == 2 and dst.stride(1) == 1
+    rows = dst.shape[0] if num_rows is None else int(num_rows)
+    assert rows <= dst.shape[0]
+    st = load().mla_gather_upconvert(cache.data_ptr(), cache.shape[0], int(page_size), block_table.data_ptr(),
+                                     block_table.stride(0), cu_seq_lens.data_ptr(), cu_seq_lens.shape[0] - 1, rows,
+                                     dst.data_ptr(), dst.stride(0), _stream(stream))
+    _check(st, "mla_gather_upconvert")
 
 
 def mla_decode_workspace_bytes(B: int, q_len: int, Hq: int, num_ctas: int = 0) -> int:

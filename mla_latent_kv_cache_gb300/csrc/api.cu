@@ -4,6 +4,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
+#include <cstdint>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -151,6 +153,21 @@ int mla_cache_write(const void* latent, int64_t latent_stride, const void* k_pe,
         return MLA_ERR_INVALID_ARG;
     cudaError_t e = mla::launch_cache_write(latent, latent_stride, k_pe, k_pe_stride, slot_mapping, num_tokens, cache,
                                             cache_kind, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_gather_upconvert(const void* cache, int64_t num_slots, int page_size, const int32_t* block_table,
+                         int64_t block_table_stride, const int32_t* cu_seq_lens, int B, int64_t num_rows, void* dst,
+                         int64_t dst_stride, void* stream) {
+    if (B < 0 || num_rows < 0 || page_size <= 0 || num_slots <= 0) return MLA_ERR_INVALID_ARG;
+    if (B == 0 || num_rows == 0) return MLA_OK;
+    if (!cache || !block_table || !cu_seq_lens || !dst) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(cache) || !aligned16(dst)) return MLA_ERR_INVALID_ARG;
+    if (block_table_stride < 1 || dst_stride < mla::kW || dst_stride % 8) return MLA_ERR_INVALID_ARG;
+    if (num_rows > (static_cast<int64_t>(UINT32_MAX) / 4) * 32) return MLA_ERR_UNSUPPORTED;  // grid size
+    cudaError_t e = mla::launch_gather_upconvert(cache, num_slots, page_size, block_table, block_table_stride,
+                                                 cu_seq_lens, B, num_rows, dst, dst_stride,
+                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

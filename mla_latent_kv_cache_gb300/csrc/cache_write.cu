@@ -81,6 +81,86 @@ __global__ void __launch_bounds__(256) cache_write_fp8_kernel(const __nv_bfloat1
     }
 }
 
+// Prefill-context gather of an fp8_ds_mla pool into 576-wide bf16 rows (vLLM
+// PR #55543: the fp8_ds_mla context-gather path, cp_gather_and_upconvert_fp8_
+// kv_cache, fills a workspace whose rows must be 576 wide). Row r = cu[b] + j
+// of dst gets request b's context token j: its 512 codes times their block
+// scale (one fp32 multiply, then bf16 round to nearest even) and its 64 rope
+// values as stored. One warp per row, kGatherRows consecutive rows per warp:
+// their slots and loads go out before any row is converted.
+constexpr int kGatherRows = 4;
+
+__global__ void __launch_bounds__(256) gather_upconvert_fp8_kernel(const uint8_t* __restrict__ cache, int64_t num_slots,
+                                                                   int page_size, const int32_t* __restrict__ block_table,
+                                                                   int64_t bt_stride, const int32_t* __restrict__ cu,
+                                                                   int B, int64_t num_rows,
+                                                                   __nv_bfloat16* __restrict__ dst, int64_t dst_stride) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r0 = (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kGatherRows;
+    if (r0 >= num_rows) return;
+    // the request holding row r0: the last b with cu[b] <= r0 (cu is non-decreasing)
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(cu + mid) <= r0) lo = mid;
+        else hi = mid;
+    }
+    int b = lo;
+    int64_t slot[kGatherRows];
+    bool have[kGatherRows], ok[kGatherRows];
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k) {
+        const int64_t r = r0 + k;
+        while (b < B && __ldg(cu + b + 1) <= r) ++b;
+        const int64_t c0 = b < B ? __ldg(cu + b) : 0;
+        have[k] = r < num_rows && b < B && r >= c0;
+        ok[k] = false;
+        slot[k] = 0;
+        if (have[k]) {
+            const int64_t j = r - c0;
+            const int64_t page = __ldg(block_table + static_cast<int64_t>(b) * bt_stride + j / page_size);
+            const int64_t s = page * page_size + j % page_size;
+            ok[k] = page >= 0 && s < num_slots;
+            slot[k] = ok[k] ? s : 0;
+        }
+    }
+    uint4 codes[kGatherRows], rope[kGatherRows];
+    float sc[kGatherRows];
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k) {
+        const uint8_t* row = cache + slot[k] * static_cast<int64_t>(kRowFp8);
+        if (ok[k]) {
+            codes[k] = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+            sc[k] = __ldg(reinterpret_cast<const float*>(row + 512) + (lane >> 3));
+            if (lane < 8) rope[k] = __ldg(reinterpret_cast<const uint4*>(row + 528) + lane);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kGatherRows; ++k) {
+        if (!have[k]) continue;
+        uint4* out = reinterpret_cast<uint4*>(dst + (r0 + k) * dst_stride);
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), c = a, e = a;
+        if (ok[k]) {
+            dequant16(codes[k], sc[k], a, c);
+            if (lane < 8) e = rope[k];
+        }
+        out[2 * lane] = a;  // values 16 lane .. 16 lane + 15
+        out[2 * lane + 1] = c;
+        if (lane < 8) out[64 + lane] = e;
+    }
+}
+
+cudaError_t launch_gather_upconvert(const void* cache, int64_t num_slots, int page_size, const int32_t* block_table,
+                                    int64_t bt_stride, const int32_t* cu_seq_lens, int B, int64_t num_rows, void* dst,
+                                    int64_t dst_stride, cudaStream_t stream) {
+    if (num_rows == 0 || B == 0) return cudaSuccess;
+    const int64_t blocks = (num_rows + 8 * kGatherRows - 1) / (8 * kGatherRows);
+    gather_upconvert_fp8_kernel<<<dim3(static_cast<unsigned>(blocks)), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(cache), num_slots, page_size, block_table, bt_stride, cu_seq_lens, B, num_rows,
+        static_cast<__nv_bfloat16*>(dst), dst_stride);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
                                const int64_t* slot_mapping, int64_t num_tokens, void* cache, int kind,
                                cudaStream_t stream) {

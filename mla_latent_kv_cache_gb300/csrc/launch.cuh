@@ -40,6 +40,10 @@ struct DecodeParams {
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
                                const int64_t* slot_mapping, int64_t num_tokens, void* cache, int kind,
                                cudaStream_t stream);
+// Context gather of an fp8_ds_mla pool into bf16 rows (mla_gather_upconvert).
+cudaError_t launch_gather_upconvert(const void* cache, int64_t num_slots, int page_size, const int32_t* block_table,
+                                    int64_t bt_stride, const int32_t* cu_seq_lens, int B, int64_t num_rows, void* dst,
+                                    int64_t dst_stride, cudaStream_t stream);
 // Clusters (of 2 CTAs) the decode kernel variant runs with: the number that
 // fit on the current device at once, or requested_ctas / 2 when given.
 int decode_clusters(int NP, bool lsu, int kind, int requested_ctas);

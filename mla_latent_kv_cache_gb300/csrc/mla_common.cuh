@@ -320,4 +320,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// e4m3 x16 (one uint4) times scale -> 16 bf16 (two uint4): each code widens
+// exactly (e4m3 -> half -> float), one fp32 multiply, round to nearest even.
+__device__ __forceinline__ void dequant16(uint4 codes, float scale, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
+        const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+        o[2 * i] = pack_bf16x2(f01.x * scale, f01.y * scale);
+        o[2 * i + 1] = pack_bf16x2(f23.x * scale, f23.y * scale);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 }  // namespace mla

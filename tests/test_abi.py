@@ -63,6 +63,16 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mla_decode(*bad) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_lse(16, 16, -1, 4, 16, 0, 16, None) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_lse(16, 16, 2, 0, 16, 0, 16, None) == m.MLA_OK
+    # mla_gather_upconvert(cache, num_slots, page_size, block_table, bt_stride, cu, B, num_rows, dst, dst_stride, stream)
+    g = [16, 100, 16, 16, 4, 16, 2, 10, 16, 576, None]
+    assert lib.mla_gather_upconvert(*(g[:6] + [0] + g[7:])) == m.MLA_OK             # B = 0: nothing to do
+    assert lib.mla_gather_upconvert(*(g[:7] + [0] + g[8:])) == m.MLA_OK             # no rows: nothing to do
+    assert lib.mla_gather_upconvert(*(g[:2] + [0] + g[3:])) == m.MLA_ERR_INVALID_ARG  # page_size
+    assert lib.mla_gather_upconvert(*(g[:9] + [512] + g[10:])) == m.MLA_ERR_INVALID_ARG  # rows narrower than 576
+    assert lib.mla_gather_upconvert(*(g[:9] + [580] + g[10:])) == m.MLA_ERR_INVALID_ARG  # stride not a multiple of 8
+    assert lib.mla_gather_upconvert(*(g[:8] + [24] + g[9:])) == m.MLA_ERR_INVALID_ARG   # dst not 16-byte aligned
+    assert lib.mla_gather_upconvert(*([None] + g[1:])) == m.MLA_ERR_INVALID_ARG       # no cache
+    assert lib.mla_gather_upconvert(*(g[:6] + [-1] + g[7:])) == m.MLA_ERR_INVALID_ARG  # B < 0
 
 
 def test_workspace_size_formula(lib):
