@@ -35,6 +35,7 @@ METRIC = "MLA paged decode latent-cache HBM GB/s (% of GB300 peak) and decode st
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SRC = os.path.join(ROOT, "mla_latent_kv_cache_gb300", "csrc", "decode.cu")
+GATHER_SRC = os.path.join(ROOT, "mla_latent_kv_cache_gb300", "csrc", "cache_write.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 CONFIG_TEXT = {
     "tiny": "B=2 Hq=8 seq {37,200} page 16 bf16",
@@ -83,18 +84,18 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha():
-    return hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()[:16]
+def kernel_sha(src=DECODE_SRC):
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
 
 
 def traffic_for(config):
-    """DRAM bytes per decode launch from a committed ncu capture, if it was
-    taken on the current decode kernel source; else None."""
+    """DRAM bytes per launch of the workload's dominant kernel from a committed
+    ncu capture, if it was taken on the current kernel source; else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     d = json.load(open(TRAFFIC_FILE))
     e = d.get(config)
-    if not e or e.get("kernel_src_sha") != kernel_sha():
+    if not e or e.get("kernel_src_sha") != kernel_sha(GATHER_SRC if config == "gather" else DECODE_SRC):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -465,7 +466,7 @@ def run_gather(args):
         "tokens_per_s": round(rows * ws_ / (step_ms_max * 1e-3), 1),
         "pct_of_measured_hbm": round(100 * value / ws_ / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": traffic_for("gather"),
                      "kernel": "gather_upconvert_fp8_kernel, CUDA events",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: copy, read+write)",
                      "algorithmic_bytes_per_launch": step_bytes},
