@@ -13,6 +13,8 @@ Functions whose result is pinned by tests (see ``tests/test_oracle_pins.py``):
 (absorbed == naive identity, closed forms, causal truncation, rope-free
 invariance), ``merge`` (partition invariance) and the e4m3 codec (agreement
 with torch's float8_e4m3fn cast and with a brute-force table search); and
+``decode_varlen`` in ``tests/test_oracle_varlen.py`` (fp64 brute force of the
+definition, per-request verify lengths, empty leading queries); and
 ``gather_upconvert`` / ``f32_to_bf16`` in ``tests/test_oracle_gather.py``
 (torch's bf16 and e4m3 conversions, numpy float32 products, exact power-of-two
 scales, the cache write's round-trip bound, brute-force row bookkeeping).
@@ -70,6 +72,8 @@ def _load():
             lib.oracle_decode.argtypes = [p, p, p, i32, i64, i32, p, i64, p, i32, i32,
                                           i32, dbl, p, i32, p, p]
             lib.oracle_decode.restype = i32
+            lib.oracle_decode_varlen.argtypes = [p, p, p, i32, i64, i32, p, i64, p, p, i32, i32, dbl, p, p]
+            lib.oracle_decode_varlen.restype = i32
             lib.oracle_merge.argtypes = [p, p, i32, i64, p, p]
             lib.oracle_merge.restype = None
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -182,6 +186,29 @@ def decode(q_lat, q_pe, cache: np.ndarray, kind: int, page_size: int, block_tabl
                            _ptr(rq) if rq is not None else None, nr, _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_decode: block id or slot out of range")
+    return out, lse
+
+
+def decode_varlen(q_lat, q_pe, cache: np.ndarray, kind: int, page_size: int, block_table, seq_lens, cu_q_lens,
+                  Hq: int, scale: float):
+    """Decode with a verify length of its own per request: cu_q_lens [B+1]
+    prefix sums of query tokens; returns (out [cu_q[B], Hq, 512] fp64,
+    lse [cu_q[B], Hq] fp64)."""
+    lib = _load()
+    cu = _as_np(cu_q_lens, np.int32)
+    B = cu.shape[0] - 1
+    R = int(cu[-1])
+    ql = _as_bits16(q_lat).reshape(R, Hq, D)
+    qp = _as_bits16(q_pe).reshape(R, Hq, P)
+    bt = _as_np(block_table, np.int32)
+    sl = _as_np(seq_lens, np.int32)
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    out = np.empty((R, Hq, D), dtype=np.float64)
+    lse = np.empty((R, Hq), dtype=np.float64)
+    rc = lib.oracle_decode_varlen(_ptr(ql), _ptr(qp), _ptr(cache), kind, cache.shape[0], page_size, _ptr(bt),
+                                  bt.shape[1], _ptr(sl), _ptr(cu), B, Hq, float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_decode_varlen: block id or slot out of range")
     return out, lse
 
 

@@ -239,6 +239,48 @@ int oracle_gather_upconvert(const uint8_t *cache, int64_t num_slots, int page_si
  * `reqs` (n_reqs entries) restricts the work to those requests; NULL = all.
  * Rows of other requests in `out` / `lse` are left untouched.
  * Returns 0, or -1 if a slot or block id is out of range. */
+/* One output row of the definition above: query token qt of a verify step
+ * of Qt tokens over a request of T tokens whose block-table row is btr. */
+static int decode_row(const uint16_t *ql, const uint16_t *qp, const uint8_t *cache, int kind,
+                      int64_t num_slots, int page_size, const int32_t *btr, int64_t T,
+                      int Qt, int qt, double scale, double *o, double *lse_out) {
+    int64_t nvis = T - Qt + qt + 1;
+    if (nvis < 0) nvis = 0;
+    for (int d = 0; d < MLA_D; ++d) o[d] = 0.0;
+    if (nvis == 0) { *lse_out = -INFINITY; return 0; }
+    double q[MLA_W], c[MLA_W];
+    for (int d = 0; d < MLA_D; ++d) q[d] = oracle_bf16_to_f64(ql[d]);
+    for (int e = 0; e < MLA_P; ++e) q[MLA_D + e] = oracle_bf16_to_f64(qp[e]);
+    double *s = (double *)malloc(sizeof(double) * (size_t)nvis);
+    int64_t *slots = (int64_t *)malloc(sizeof(int64_t) * (size_t)nvis);
+    for (int64_t j = 0; j < nvis; ++j) {
+        int64_t blk = btr[j / page_size];
+        int64_t slot = blk * (int64_t)page_size + j % page_size;
+        if (blk < 0 || slot >= num_slots) { free(s); free(slots); *lse_out = NAN; return -1; }
+        slots[j] = slot;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nvis; ++j) {
+        read_row(cache, kind, slots[j], c);
+        double dot = 0.0;
+        for (int d = 0; d < MLA_W; ++d) dot += q[d] * c[d];
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        double p = exp(s[j] - m);
+        l += p;
+        read_row(cache, kind, slots[j], c);
+        for (int d = 0; d < MLA_D; ++d) o[d] += p * c[d];
+    }
+    for (int d = 0; d < MLA_D; ++d) o[d] /= l;
+    *lse_out = m + log(l);
+    free(s);
+    free(slots);
+    return 0;
+}
+
 int oracle_decode(const uint16_t *q_lat, const uint16_t *q_pe,
                   const uint8_t *cache, int kind, int64_t num_slots,
                   int page_size, const int32_t *block_table,
@@ -255,46 +297,39 @@ int oracle_decode(const uint16_t *q_lat, const uint16_t *q_pe,
         int h = (int)(task % Hq);
         int b = reqs ? reqs[bi] : bi;
         int64_t row = ((int64_t)b * Qt + qt) * Hq + h;
-        const uint16_t *ql = q_lat + row * MLA_D;
-        const uint16_t *qp = q_pe + row * MLA_P;
-        double *o = out + row * MLA_D;
-        int64_t T = seq_lens[b];
-        int64_t nvis = T - Qt + qt + 1;
-        if (nvis < 0) nvis = 0;
-        for (int d = 0; d < MLA_D; ++d) o[d] = 0.0;
-        if (nvis == 0) { lse[row] = -INFINITY; continue; }
-        double q[MLA_W], c[MLA_W];
-        for (int d = 0; d < MLA_D; ++d) q[d] = oracle_bf16_to_f64(ql[d]);
-        for (int e = 0; e < MLA_P; ++e) q[MLA_D + e] = oracle_bf16_to_f64(qp[e]);
-        double *s = (double *)malloc(sizeof(double) * (size_t)nvis);
-        int64_t *slots = (int64_t *)malloc(sizeof(int64_t) * (size_t)nvis);
-        int ok = 1;
-        for (int64_t j = 0; j < nvis && ok; ++j) {
-            int64_t blk = block_table[(int64_t)b * bt_stride + j / page_size];
-            int64_t slot = blk * (int64_t)page_size + j % page_size;
-            if (blk < 0 || slot >= num_slots) { ok = 0; break; }
-            slots[j] = slot;
-        }
-        if (!ok) { bad = 1; free(s); free(slots); lse[row] = NAN; continue; }
-        double m = -INFINITY;
-        for (int64_t j = 0; j < nvis; ++j) {
-            read_row(cache, kind, slots[j], c);
-            double dot = 0.0;
-            for (int d = 0; d < MLA_W; ++d) dot += q[d] * c[d];
-            s[j] = scale * dot;
-            if (s[j] > m) m = s[j];
-        }
-        double l = 0.0;
-        for (int64_t j = 0; j < nvis; ++j) {
-            double p = exp(s[j] - m);
-            l += p;
-            read_row(cache, kind, slots[j], c);
-            for (int d = 0; d < MLA_D; ++d) o[d] += p * c[d];
-        }
-        for (int d = 0; d < MLA_D; ++d) o[d] /= l;
-        lse[row] = m + log(l);
-        free(s);
-        free(slots);
+        if (decode_row(q_lat + row * MLA_D, q_pe + row * MLA_P, cache, kind, num_slots, page_size,
+                       block_table + (int64_t)b * bt_stride, seq_lens[b], Qt, qt, scale,
+                       out + row * MLA_D, lse + row))
+            bad = 1;
+    }
+    return bad ? -1 : 0;
+}
+
+/* The same definition with a verify step of its own length per request (a
+ * chunked verify batch; [P2 "Speculative decoding (MTP)"]: a verify step of
+ * 1 + k query tokens reads the latent once per request, k per request):
+ * request b's query tokens are cu_q[b] .. cu_q[b+1] - 1 (Qt_b of them, the
+ * last Qt_b of its T_b tokens), its rows (cu_q[b] + qt) * Hq + h, and query
+ * qt sees tokens 0 .. T_b - Qt_b + qt. All cu_q[B] * Hq rows are computed. */
+int oracle_decode_varlen(const uint16_t *q_lat, const uint16_t *q_pe,
+                         const uint8_t *cache, int kind, int64_t num_slots,
+                         int page_size, const int32_t *block_table,
+                         int64_t bt_stride, const int32_t *seq_lens,
+                         const int32_t *cu_q, int B, int Hq, double scale,
+                         double *out, double *lse) {
+    int64_t ntask = (int64_t)cu_q[B] * Hq;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t row = 0; row < ntask; ++row) {
+        int64_t tq = row / Hq;
+        int b = 0;
+        while (b + 1 < B && cu_q[b + 1] <= tq) ++b;
+        int Qt = cu_q[b + 1] - cu_q[b];
+        int qt = (int)(tq - cu_q[b]);
+        if (decode_row(q_lat + row * MLA_D, q_pe + row * MLA_P, cache, kind, num_slots, page_size,
+                       block_table + (int64_t)b * bt_stride, seq_lens[b], Qt, qt, scale,
+                       out + row * MLA_D, lse + row))
+            bad = 1;
     }
     return bad ? -1 : 0;
 }
