@@ -178,6 +178,30 @@ MLA_API int mla_decode(const void* q_lat, const void* q_pe, const void* cache, i
                size_t workspace_bytes, int num_ctas, void* stream);
 
 /*
+ * mla_decode_varlen - mla_decode for a batch whose requests verify different
+ * numbers of tokens (a chunked verify step: "qwen-mla-vllm" README,
+ * "Speculative decoding (MTP)", a verify step of 1 + k tokens reads the latent
+ * once per request; here k is per request). Request b verifies
+ * q_len_b = cu_q_lens[b+1] - cu_q_lens[b] tokens, the last q_len_b of its
+ * seq_lens[b]; its rows are r = (cu_q_lens[b] + t) * Hq + h (t < q_len_b) and
+ * query t sees tokens 0 .. seq_lens[b] - q_len_b + t. Every other argument,
+ * the outputs' layout (rows r above) and the status words are as mla_decode.
+ *   total_q_tokens  cu_q_lens[B] (host copy): the query tokens in q_lat, q_pe,
+ *                   out and lse.
+ *   cu_q_lens       device, int32 [B + 1], non-decreasing, cu_q_lens[0] = 0,
+ *                   every q_len_b <= max_q_len.
+ *   max_q_len       the largest q_len_b, >= 1. Rows are processed in groups of
+ *                   64 as in mla_decode with q_len = max_q_len; the workspace
+ *                   is mla_decode_workspace_bytes(B, max_q_len, Hq, num_ctas).
+ * While max_q_len * Hq <= 64 every request's cache is read once.
+ */
+MLA_API int mla_decode_varlen(const void* q_lat, const void* q_pe, int64_t total_q_tokens, const void* cache,
+                              int cache_kind, int64_t num_slots, int page_size, const int32_t* block_table,
+                              int64_t block_table_stride, const int32_t* seq_lens, const int32_t* cu_q_lens, int B,
+                              int max_q_len, int Hq, float scale, void* out, int out_dtype, float* lse,
+                              void* workspace, size_t workspace_bytes, int num_ctas, void* stream);
+
+/*
  * mla_merge_lse - combine S partial results of the same N rows computed over
  * disjoint token sets (flash-decoding split-KV / decode context parallel
  * combine; vLLM PR #55543 commit 5.1-5.4 "(0, -inf) per the DCP merge

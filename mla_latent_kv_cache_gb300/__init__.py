@@ -68,6 +68,9 @@ def load() -> ctypes.CDLL:
             lib.mla_test_hold_next_decode.argtypes = []
             lib.mla_test_hold_next_decode.restype = None
             lib.mla_merge_lse.argtypes = [vp, vp, i32, i64, vp, i32, vp, vp]
+            lib.mla_decode_varlen.argtypes = [vp, vp, i64, vp, i32, i64, i32, vp, i64, vp, vp, i32, i32, i32, f32,
+                                              vp, i32, vp, vp, ctypes.c_size_t, i32, vp]
+            lib.mla_decode_varlen.restype = i32
             lib.mla_gather_upconvert.argtypes = [vp, i64, i32, vp, i64, vp, i32, i64, vp, i64, vp]
             lib.mla_gather_upconvert.restype = i32
             lib.mla_merge_lse.restype = i32
@@ -117,6 +120,26 @@ def mla_cache_write(latent: torch.Tensor, k_pe: torch.Tensor, slot_mapping: torc
                                   k_pe.data_ptr(), k_pe.stride(0) if k_pe.dim() == 2 else 64,
                                   slot_mapping.data_ptr(), T, cache.data_ptr(), nbytes // rb, cache_kind,
                                   _stream(stream)), "mla_cache_write")
+
+
+def mla_decode_varlen(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens, cu_q_lens, max_q_len,
+                      scale, out, lse, workspace, num_ctas: int = 0, stream=None) -> None:
+    """Decode with per-request verify lengths (include/mla.h): q_lat [total_q, Hq, 512],
+    cu_q_lens int32 [B+1] on the device."""
+    total_q, Hq = q_lat.shape[0], q_lat.shape[1]
+    assert q_lat.shape == (total_q, Hq, 512) and q_pe.shape == (total_q, Hq, 64)
+    assert q_lat.is_contiguous() and q_pe.is_contiguous() and out.is_contiguous() and lse.is_contiguous()
+    assert cu_q_lens.dtype == torch.int32 and cu_q_lens.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.stride(1) == 1 and seq_lens.dtype == torch.int32
+    B = seq_lens.shape[0]
+    assert cu_q_lens.shape[0] == B + 1
+    odt = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
+    st = load().mla_decode_varlen(q_lat.data_ptr(), q_pe.data_ptr(), total_q, cache.data_ptr(), int(cache_kind),
+                                  cache.shape[0], int(page_size), block_table.data_ptr(), block_table.stride(0),
+                                  seq_lens.data_ptr(), cu_q_lens.data_ptr(), B, int(max_q_len), Hq, float(scale),
+                                  out.data_ptr(), odt, lse.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                  int(num_ctas), _stream(stream))
+    _check(st, "mla_decode_varlen")
 
 
 def mla_gather_upconvert(cache: torch.Tensor, page_size: int, block_table: torch.Tensor, cu_seq_lens: torch.Tensor,

@@ -181,11 +181,18 @@ size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas) {
     return decode_ws_bytes(B, Hq * q_len, ws_ctas(num_ctas, sms));
 }
 
-int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache_kind, int64_t num_slots,
-               int page_size, const int32_t* block_table, int64_t block_table_stride, const int32_t* seq_lens, int B,
-               int q_len, int Hq, float scale, void* out, int out_dtype, float* lse, void* workspace,
-               size_t workspace_bytes, int num_ctas, void* stream) {
-    if (B <= 0 || q_len <= 0 || Hq <= 0 || page_size <= 0 || num_slots <= 0 || num_ctas < 0)
+}  // extern "C"
+
+namespace {
+
+// mla_decode and mla_decode_varlen: q_len is the (largest) verify length,
+// cu_q null or the device prefix sums of per-request lengths, total_q the
+// query tokens in q_lat / out (B * q_len for the uniform call).
+int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void* cache, int cache_kind,
+                int64_t num_slots, int page_size, const int32_t* block_table, int64_t block_table_stride,
+                const int32_t* seq_lens, const int32_t* cu_q, int B, int q_len, int Hq, float scale, void* out,
+                int out_dtype, float* lse, void* workspace, size_t workspace_bytes, int num_ctas, void* stream) {
+    if (B <= 0 || q_len <= 0 || Hq <= 0 || page_size <= 0 || num_slots <= 0 || num_ctas < 0 || total_q <= 0)
         return MLA_ERR_INVALID_ARG;
     if (num_slots > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
     if (cache_kind != MLA_CACHE_BF16_576 && cache_kind != MLA_CACHE_FP8_DS_MLA_656) return MLA_ERR_INVALID_ARG;
@@ -208,7 +215,7 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     const int GY = (HQ + 63) / 64;
     if (GY > 65535) return MLA_ERR_UNSUPPORTED;
     // TMA row coordinates of the queries are 32-bit
-    if (static_cast<int64_t>(B) * HQ + 64 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+    if (total_q * Hq + 64 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
     const int NP = rows_padded(HQ < 64 ? HQ : 64);
     // pages whose rows cannot be fetched as 8-row TMA boxes go through the
     // load/convert warps
@@ -234,8 +241,8 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     auto enc = encode_fn();
     if (!enc) return MLA_ERR_CUDA;
     {
-        // queries: q_lat [B*HQ, 512] and q_pe [B*HQ, 64] bf16, NP-row boxes
-        const cuuint64_t rows = static_cast<cuuint64_t>(B) * HQ;
+        // queries: q_lat [total_q * Hq, 512] and q_pe [total_q * Hq, 64] bf16, NP-row boxes
+        const cuuint64_t rows = static_cast<cuuint64_t>(total_q) * Hq;
         cuuint64_t gq[2] = {static_cast<cuuint64_t>(mla::kD), rows};
         cuuint64_t sq[1] = {static_cast<cuuint64_t>(mla::kD * 2)};
         cuuint64_t gp[2] = {64u, rows};
@@ -326,9 +333,35 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     // the 64-row drain is four times larger; folded tiles are half as long)
     p.wseg = (NP == 16 ? 2 : NP == 32 ? 4 : 8) * (fold ? 2 : 1);
     p.test_hold = g_test_hold.exchange(0);
+    p.cu_q = cu_q;
     cudaError_t e = fold ? mla::launch_decode_fold(maps, p, NP, W, GY, s)
                          : mla::launch_decode(maps, p, NP, lsu, cache_kind, W, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache_kind, int64_t num_slots,
+               int page_size, const int32_t* block_table, int64_t block_table_stride, const int32_t* seq_lens, int B,
+               int q_len, int Hq, float scale, void* out, int out_dtype, float* lse, void* workspace,
+               size_t workspace_bytes, int num_ctas, void* stream) {
+    if (B <= 0 || q_len <= 0) return MLA_ERR_INVALID_ARG;
+    return decode_impl(q_lat, q_pe, static_cast<int64_t>(B) * q_len, cache, cache_kind, num_slots, page_size,
+                       block_table, block_table_stride, seq_lens, nullptr, B, q_len, Hq, scale, out, out_dtype, lse,
+                       workspace, workspace_bytes, num_ctas, stream);
+}
+
+int mla_decode_varlen(const void* q_lat, const void* q_pe, int64_t total_q_tokens, const void* cache,
+                      int cache_kind, int64_t num_slots, int page_size, const int32_t* block_table,
+                      int64_t block_table_stride, const int32_t* seq_lens, const int32_t* cu_q_lens, int B,
+                      int max_q_len, int Hq, float scale, void* out, int out_dtype, float* lse, void* workspace,
+                      size_t workspace_bytes, int num_ctas, void* stream) {
+    if (!cu_q_lens) return MLA_ERR_INVALID_ARG;
+    return decode_impl(q_lat, q_pe, total_q_tokens, cache, cache_kind, num_slots, page_size, block_table,
+                       block_table_stride, seq_lens, cu_q_lens, B, max_q_len, Hq, scale, out, out_dtype, lse,
+                       workspace, workspace_bytes, num_ctas, stream);
 }
 
 int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const void* cache, int cache_kind,

@@ -163,7 +163,7 @@ struct Ctrl {
     uint32_t tmem_base;
     int abort;
     int t_begin, t_end, b0, j0;
-    int colvis[64];                  // query row -> trailing tokens it may not see
+    int colvis[64];                  // uniform verify length: query row -> trailing tokens it may not see
     alignas(16) float m[64];         // running max per row (log2 units); read as float4
     alignas(16) float alpha[64];
     alignas(16) float red[4][64];
@@ -206,14 +206,29 @@ struct TileItT {
 };
 using TileIt = TileItT<7>;
 
+// Query rows of request b: the first row of its verify step and the step's
+// length in tokens (Qt for every request unless per-request lengths are given),
+// and how many of its rows fall in row group gy (0 .. 64).
+__device__ __forceinline__ int64_t req_row0(const DecodeParams& p, int b) {
+    return p.cu_q ? static_cast<int64_t>(__ldg(p.cu_q + b)) * p.Hq : static_cast<int64_t>(b) * p.HQ;
+}
+__device__ __forceinline__ int req_qt(const DecodeParams& p, int b) {
+    return p.cu_q ? __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b) : p.Qt;
+}
+__device__ __forceinline__ int req_rows_in_group(const DecodeParams& p, int b, int gy) {
+    return min(64, max(0, req_qt(p, b) * p.Hq - gy * 64));
+}
+
 // L2 prefetch of what the first tiles of request b read besides the cache:
 // its query rows of row group gy and its block-table row (whole 16-byte
 // units inside the row only).
 __device__ __forceinline__ void prefetch_request(const DecodeParams& p, int b, int gy) {
-    const int HQg = min(64, p.HQ - gy * 64);
-    const int64_t row0 = static_cast<int64_t>(b) * p.HQ + gy * 64;
-    prefetch_l2_bulk(p.q_lat + row0 * kD, static_cast<uint32_t>(HQg * kD * 2));
-    prefetch_l2_bulk(p.q_pe + row0 * kP, static_cast<uint32_t>(HQg * kP * 2));
+    const int HQg = req_rows_in_group(p, b, gy);
+    const int64_t row0 = req_row0(p, b) + gy * 64;
+    if (HQg > 0) {
+        prefetch_l2_bulk(p.q_lat + row0 * kD, static_cast<uint32_t>(HQg * kD * 2));
+        prefetch_l2_bulk(p.q_pe + row0 * kP, static_cast<uint32_t>(HQg * kP * 2));
+    }
     const int T = max(__ldg(p.seq_lens + b), 0);
     const int64_t pages = (static_cast<int64_t>(T) + p.page_size - 1) / p.page_size;
     uintptr_t a0 = reinterpret_cast<uintptr_t>(p.block_table + static_cast<int64_t>(b) * p.bt_stride);
@@ -900,7 +915,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             const int st = threadIdx.x - 128;  // token row of the tile / TMEM lane
             const int sw = warp - 4;
             const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-            const int HQg = min(64, p.HQ - gy * 64);
             const int peer = rank ^ 1;
             const uint32_t x_local = smem_u32(xbuf);
             const uint32_t x_peer = mapa_shared(x_local, peer);
@@ -935,7 +949,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             bool dr_final = false;
             uint32_t dr_obuf = 0;
             constexpr int kDC = 8;  // columns per drain step
-            const int dr_per_half = (HQg + kDC - 1) / kDC;
+            // rows (in this row group) of the segment being drained, and the drain
+            // steps per 128-dim half: recomputed from dr_b where needed, so
+            // nothing more stays live across the tile loop
+            auto dr_rows = [&]() { return req_rows_in_group(p, dr_b, gy); };
 
             // O columns [col0, col0 + NH) of accumulator ob, both 128-dim halves,
             // times alpha[0 .. NH) (the caller has waited for the last PV into it)
@@ -962,7 +979,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             // past the group's real rows belong to other requests (or are zero
             // past the end); their score columns are masked to -inf.
             auto issue_q = [&](int bq) {
-                const int y = bq * p.HQ + gy * 64;
+                const int y = static_cast<int>(req_row0(p, bq) + gy * 64);
                 const uint64_t pol = l2_policy_evict_first();
                 mbar_arrive_expect_tx(&ctrl->q_full, C::kQBytes);
 #pragma unroll
@@ -1012,14 +1029,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             auto start_drain = [&](uint32_t src, int sg, int i, int sb, bool sfinal) {
                 if constexpr (C::kSplit) group_wait(&ctrl->dfull[sg & 1], (sg >> 1) & 1, p, ctrl, kSiteDFull, i, true);
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + sb;
+                const int shq = req_rows_in_group(p, sb, gy);
                 const int c = own0 + st;
-                if (st < NH && c < HQg && (C::kSplit || rank == 0)) {
+                if (st < NH && c < shq && (C::kSplit || rank == 0)) {
                     const float lt = ctrl->dlt[sg & 1][c];
                     const float lv = lt > 0.f ? (ctrl->dm[c] + log2f(lt)) * kLn2 : -INFINITY;
-                    if (sfinal) p.lse[static_cast<int64_t>(sb) * p.HQ + gy * 64 + c] = lv;
+                    if (sfinal) p.lse[req_row0(p, sb) + gy * 64 + c] = lv;
                     else p.part_lse[pslot * 64 + c] = lv;
                 }
-                dr_left = 2 * dr_per_half;
+                dr_left = 2 * ((shq + kDC - 1) / kDC);
                 dr_step = 0;
                 dr_b = sb;
                 dr_final = sfinal;
@@ -1031,6 +1049,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             // One drain step: kDC columns of one 128-dim half, O / l, into the
             // output rows (a whole request) or the cluster's partial slot.
             auto drain_step = [&]() {
+                const int dr_hq = dr_rows();
+                const int dr_per_half = (dr_hq + kDC - 1) / kDC;
                 const int mt = dr_step / dr_per_half;
                 const int c0 = (dr_step - mt * dr_per_half) * kDC;
                 uint32_t o[kDC];
@@ -1040,11 +1060,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 #pragma unroll
                 for (int cc = 0; cc < kDC; ++cc) {
                     const int c = c0 + cc;
-                    if (c < HQg) {
+                    if (c < dr_hq) {
                         const float lt = ctrl->dlt[dr_sg & 1][c];
                         const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
                         if (dr_final) {
-                            const int64_t idx = (static_cast<int64_t>(dr_b) * p.HQ + gy * 64 + c) * kD + d;
+                            const int64_t idx = (req_row0(p, dr_b) + gy * 64 + c) * kD + d;
                             if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
                             else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
                         } else {
@@ -1193,17 +1213,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXRead);
 
                 const int tok = j * kTile + st;
-                const bool all_vis = (j * kTile + kTile + p.Qt - 1) <= T;
+                // this tile's request: its verify length and its rows in this row group
+                const int seg_qt = req_qt(p, b), seg_hq = req_rows_in_group(p, b, gy);
+                const bool all_vis = (j * kTile + kTile + seg_qt - 1) <= T;
                 const float4* m4 = reinterpret_cast<const float4*>(ctrl->m + own0);
                 if (all_vis) {
                     // every real row sees every token of the tile
 #pragma unroll
-                    for (int c = 0; c < NH; ++c) x[c] = (own0 + c < HQg) ? x[c] * p.scale_log2 : -INFINITY;
+                    for (int c = 0; c < NH; ++c) x[c] = (own0 + c < seg_hq) ? x[c] * p.scale_log2 : -INFINITY;
                 } else {
-                    // tail of a request: per-row causal limit and the end of the request
+                    // tail of a request: query token r / Hq of the step sees tokens up to
+                    // T - Qt + r / Hq, and rows past the request's are padding
+                    if (p.cu_q) {
 #pragma unroll
-                    for (int c = 0; c < NH; ++c)
-                        x[c] = (tok + ctrl->colvis[own0 + c] < T) ? x[c] * p.scale_log2 : -INFINITY;
+                        for (int c = 0; c < NH; ++c) {
+                            const int r = gy * 64 + own0 + c;
+                            const bool v = own0 + c < seg_hq && tok + seg_qt - 1 - r / p.Hq < T;
+                            x[c] = v ? x[c] * p.scale_log2 : -INFINITY;
+                        }
+                    } else {
+                        // the same limits, tabulated once (every request has p.Qt tokens)
+#pragma unroll
+                        for (int c = 0; c < NH; ++c)
+                            x[c] = (tok + ctrl->colvis[own0 + c] < T) ? x[c] * p.scale_log2 : -INFINITY;
+                    }
                 }
                 int need = 0;
 #pragma unroll
@@ -1437,7 +1470,7 @@ struct FoldCtrl {
     uint32_t tmem_base;
     int abort;
     int t_begin, t_end, b0, j0;
-    int colvis[64];                  // query row -> trailing tokens it may not see
+    int colvis[64];                  // uniform verify length: query row -> trailing tokens it may not see
     alignas(16) float m[64];         // running max per row (log2 units)
     alignas(16) float alpha[64];
     alignas(16) float red[4][32];    // per-warp column reductions (at most 32 columns here)
@@ -1713,7 +1746,6 @@ __global__ void __launch_bounds__(288, 1)
             const int hf = sw >> 1;
             const int tt = st & 63;
             const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-            const int HQg = min(64, p.HQ - gy * 64);
             constexpr int NH = C::kNH;
             const int own0 = hf * NH;
             // exchange rows of NH floats, 16-byte units swizzled by row; thread st
@@ -1721,6 +1753,8 @@ __global__ void __launch_bounds__(288, 1)
             const int xs = (NH == 16) ? ((st >> 1) & 3) : ((st >> 2) & 1);
             It it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
+            // the current segment's verify length and its rows in this row group
+            int seg_qt = req_qt(p, it.b), seg_hq = req_rows_in_group(p, it.b, gy);
             float l[NH];
 #pragma unroll
             for (int c = 0; c < NH; ++c) l[c] = 0.f;
@@ -1734,7 +1768,8 @@ __global__ void __launch_bounds__(288, 1)
             bool dr_final = false;
             uint32_t dr_obuf = 0;
             constexpr int kDC = 8;  // columns per drain step
-            const int dr_per_mt = (HQg + kDC - 1) / kDC;
+            int dr_hq = 0, dr_per_mt = 1;  // rows of the segment being drained (in this row group)
+            int64_t dr_row0 = 0;           // and its first output row
 
             // Column reductions over the tile's tokens: a warp reduces its 32
             // lanes (one half), red[warp][column] meets the other warps' (the
@@ -1770,7 +1805,7 @@ __global__ void __launch_bounds__(288, 1)
             // rows [NP, 2NP) = dims 256 + 64k.. (128-B swizzle, at k * 2NP * 128),
             // then the rope halves (64-B swizzle, at 8 NP * 128).
             auto issue_q = [&](int bq) {
-                const int y = bq * p.HQ + gy * 64;
+                const int y = static_cast<int>(req_row0(p, bq) + gy * 64);
                 const uint64_t pol = l2_policy_evict_first();
                 mbar_arrive_expect_tx(&ctrl->q_full, C::kQBytes);
 #pragma unroll
@@ -1801,15 +1836,18 @@ __global__ void __launch_bounds__(288, 1)
 
             // The captured segment sg (accumulator src) has had its last PV:
             // write its LSEs and start draining its rows.
-            auto start_drain = [&](uint32_t src, int sg, int sb, bool sfinal) {
+            auto start_drain = [&](uint32_t src, int sg, int sb, bool sfinal, int shq) {
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + sb;
-                if (st < NP && st < HQg) {
+                dr_row0 = req_row0(p, sb) + gy * 64;
+                if (st < NP && st < shq) {
                     const float lt = ctrl->dlt[sg & 1][st];
                     const float lv = lt > 0.f ? (ctrl->dm[sg & 1][st] + log2f(lt)) * kLn2 : -INFINITY;
-                    if (sfinal) p.lse[static_cast<int64_t>(sb) * p.HQ + gy * 64 + st] = lv;
+                    if (sfinal) p.lse[dr_row0 + st] = lv;
                     else p.part_lse[pslot * 64 + st] = lv;
                 }
-                dr_left = 4 * dr_per_mt;
+                dr_hq = shq;
+                dr_per_mt = max(1, (shq + kDC - 1) / kDC);
+                dr_left = shq > 0 ? 4 * dr_per_mt : 0;
                 dr_step = 0;
                 dr_b = sb;
                 dr_final = sfinal;
@@ -1831,11 +1869,11 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
                 for (int cc = 0; cc < kDC; ++cc) {
                     const int c = c0 + cc;
-                    if (c < HQg) {
+                    if (c < dr_hq) {
                         const float lt = ctrl->dlt[dr_sg & 1][c];
                         const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
                         if (dr_final) {
-                            const int64_t idx = (static_cast<int64_t>(dr_b) * p.HQ + gy * 64 + c) * kD + d;
+                            const int64_t idx = (dr_row0 + c) * kD + d;
                             if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
                             else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
                         } else {
@@ -1847,7 +1885,7 @@ __global__ void __launch_bounds__(288, 1)
                 --dr_left;
             };
 
-            int cap_b = 0;
+            int cap_b = 0, cap_hq = 0;
             bool cap_final = false;
 
             // Hand tile t to the PV issuers, then start or advance the drain.
@@ -1866,7 +1904,7 @@ __global__ void __launch_bounds__(288, 1)
                     // PV(t-1), the captured segment's last, is long done by now
                     group_wait(&ctrl->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, p, ctrl, kSiteOEpi, t);
                     tc_fence_after();
-                    start_drain(obuf ^ (4 * NP), seg - 1, cap_b, cap_final);
+                    start_drain(obuf ^ (4 * NP), seg - 1, cap_b, cap_final, cap_hq);
                 } else if (dr_left > 0) {
                     tc_fence_after();
                     drain_step();
@@ -1923,6 +1961,9 @@ __global__ void __launch_bounds__(288, 1)
                     pend = true;
                     cap_b = pend_b;
                     cap_final = pend_final;
+                    cap_hq = seg_hq;
+                    seg_qt = req_qt(p, b);
+                    seg_hq = req_rows_in_group(p, b, gy);
                     seg_has_pv = false;
                     ++seg;
                     obuf = (seg & 1) * 4 * NP;
@@ -1942,15 +1983,27 @@ __global__ void __launch_bounds__(288, 1)
                 }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXRead);
                 const int tok = j * kT + tt;
-                const bool all_vis = (j * kT + kT + p.Qt - 1) <= T;
+                const bool all_vis = (j * kT + kT + seg_qt - 1) <= T;
                 const float4* m4p = reinterpret_cast<const float4*>(ctrl->m + own0);
                 if (all_vis) {
 #pragma unroll
-                    for (int c = 0; c < NH; ++c) x[c] = (own0 + c < HQg) ? x[c] * p.scale_log2 : -INFINITY;
+                    for (int c = 0; c < NH; ++c) x[c] = (own0 + c < seg_hq) ? x[c] * p.scale_log2 : -INFINITY;
                 } else {
+                    // tail of a request: query token r / Hq of the step sees tokens up to
+                    // T - Qt + r / Hq, and rows past the request's are padding
+                    if (p.cu_q) {
 #pragma unroll
-                    for (int c = 0; c < NH; ++c)
-                        x[c] = (tok + ctrl->colvis[own0 + c] < T) ? x[c] * p.scale_log2 : -INFINITY;
+                        for (int c = 0; c < NH; ++c) {
+                            const int r = gy * 64 + own0 + c;
+                            const bool v = own0 + c < seg_hq && tok + seg_qt - 1 - r / p.Hq < T;
+                            x[c] = v ? x[c] * p.scale_log2 : -INFINITY;
+                        }
+                    } else {
+                        // the same limits, tabulated once (every request has p.Qt tokens)
+#pragma unroll
+                        for (int c = 0; c < NH; ++c)
+                            x[c] = (tok + ctrl->colvis[own0 + c] < T) ? x[c] * p.scale_log2 : -INFINITY;
+                    }
                 }
                 int need = 0;
 #pragma unroll
@@ -2058,7 +2111,7 @@ __global__ void __launch_bounds__(288, 1)
                 named_bar_sync(1, 128);
                 if (!ctrl->abort) {
                     tc_fence_after();
-                    start_drain(obuf, seg, pend_b, pend_final);
+                    start_drain(obuf, seg, pend_b, pend_final, seg_hq);
                     while (dr_left > 0) drain_step();
                 }
             }
@@ -2192,10 +2245,10 @@ __global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const
         }
     }
 
-    const int HQg = min(64, p.HQ - gy * 64);
-    if (b >= p.B || n >= HQg) return;
+    if (b >= p.B) return;
+    if (n >= req_rows_in_group(p, b, gy)) return;  // the same for the whole block when it holds one row
     const int tiles_b = (max(__ldg(p.seq_lens + b), 0) + (1 << p.tile_shift) - 1) >> p.tile_shift;
-    const int64_t row = static_cast<int64_t>(b) * p.HQ + gy * 64 + n;
+    const int64_t row = req_row0(p, b) + gy * 64 + n;
     const int d = 4 * t;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = -INFINITY;

@@ -30,11 +30,12 @@ struct DecodeParams {
     int page_size;
     int run_rows;      // TMA box height: gcd(page_size, tile)
     int tile_shift;    // log2 of the tokens per tile: 7 (cluster kernel) or 6 (folded tiles)
-    int B, Qt, Hq, HQ; // HQ = Hq * Qt rows per request
+    int B, Qt, Hq, HQ; // HQ = Hq * Qt rows per request (the largest Qt when cu_q is given)
     int out_f32;
     int SPG;           // partial slots per row group = workers + B
     int wseg;          // work-split cost of a request boundary, in tiles
     int test_hold;     // test hook: 1 = withhold the first hand-off to the PV issuers
+    const int32_t* cu_q;  // [B + 1] prefix sums of query tokens per request, or null: Qt each
 };
 
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,

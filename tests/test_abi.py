@@ -63,6 +63,12 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mla_decode(*bad) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_lse(16, 16, -1, 4, 16, 0, 16, None) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_lse(16, 16, 2, 0, 16, 0, 16, None) == m.MLA_OK
+    # mla_decode_varlen(q_lat, q_pe, total_q, cache, kind, num_slots, page_size, bt, bt_stride, seq_lens, cu_q, B,
+    #                   max_q_len, Hq, scale, out, out_dtype, lse, ws, ws_bytes, num_ctas, stream)
+    v = [16, 16, 6, 16, 0, 100, 16, 16, 4, 16, 16, 2, 3, 8, 0.1, 16, 0, 16, 256, 1 << 20, 0, None]
+    assert lib.mla_decode_varlen(*(v[:10] + [None] + v[11:])) == m.MLA_ERR_INVALID_ARG  # no prefix sums
+    assert lib.mla_decode_varlen(*(v[:2] + [0] + v[3:])) == m.MLA_ERR_INVALID_ARG       # no query tokens
+    assert lib.mla_decode_varlen(*(v[:12] + [0] + v[13:])) == m.MLA_ERR_INVALID_ARG     # max_q_len = 0
     # mla_gather_upconvert(cache, num_slots, page_size, block_table, bt_stride, cu, B, num_rows, dst, dst_stride, stream)
     g = [16, 100, 16, 16, 4, 16, 2, 10, 16, 576, None]
     assert lib.mla_gather_upconvert(*(g[:6] + [0] + g[7:])) == m.MLA_OK             # B = 0: nothing to do
