@@ -43,6 +43,8 @@ CONFIG_TEXT = {
     "long": "B=4 Hq=32 seq 262144 page 64 bf16",
     "mtp": "B=128 Hq=16 Qt=4 causal, 9.8M-slot pool above slot 3,728,270, seq 0/1/U{2048..100000}, page 16 bf16",
     "fp8": "B=64 Hq=64 seq 32768 page 64 fp8_ds_mla (656 B rows)",
+    "verify": "the mtp workload with a verify length of its own per request, U{1..4} (seeded): "
+              "mla_decode_varlen",
     "gather": "fp8_ds_mla pool of the fp8 workload (B=64 x 32768 tokens, page 64) gathered into "
               "[2097152, 576] bf16 rows",
 }
@@ -162,6 +164,12 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
+def verify_qlens(B, rank=0):
+    """The verify workload's per-request verify lengths, U{1..4} (seeded)."""
+    import numpy as np
+    return np.random.default_rng(7 + 1000 * rank).integers(1, 5, size=B)
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -178,7 +186,21 @@ def run_gpu(args):
     import mla_latent_kv_cache_gb300 as m
     from mla_latent_kv_cache_gb300 import workloads as W
 
-    wl = W.CONFIGS[args.config](device=dev, seed={"tiny": 1, "batched": 2, "long": 3, "mtp": 4, "fp8": 5}[args.config] + 1000 * rank)
+    varlen = args.config == "verify"
+    base_cfg = "mtp" if varlen else args.config
+    wl = W.CONFIGS[base_cfg](device=dev, seed={"tiny": 1, "batched": 2, "long": 3, "mtp": 4, "fp8": 5}[base_cfg] + 1000 * rank)
+    cu_q = None
+    q_lat_s, q_pe_s = wl.q_lat, wl.q_pe  # the step's query rows
+    if varlen:
+        # per-request verify lengths U{1..4}: request b's queries are the first
+        # q_len_b of its four query rows
+        import numpy as np
+        qlens = verify_qlens(wl.B, rank)
+        pick = torch.tensor([b * wl.Qt + t for b in range(wl.B) for t in range(int(qlens[b]))], dtype=torch.int64,
+                            device=dev)
+        q_lat_s = wl.q_lat[pick].contiguous()
+        q_pe_s = wl.q_pe[pick].contiguous()
+        cu_q = torch.from_numpy(np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)).to(dev)
     # the fp8 pool is written once (the step then writes only the last token per request)
     if wl.kind == 1:
         m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
@@ -196,17 +218,23 @@ def run_gpu(args):
     cache_bytes = wl.cache_bytes()
     ctx_tokens = wl.context_tokens()
     B, Qt, Hq = wl.B, wl.Qt, wl.Hq
-    out = torch.empty((B * Qt, Hq, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((B * Qt, Hq), dtype=torch.float32, device=dev)
+    R = q_lat_s.shape[0]  # query tokens of the step
+    out = torch.empty((R, Hq, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, Hq), dtype=torch.float32, device=dev)
     wsb = m.mla_decode_workspace_bytes(B, Qt, Hq, 0)
     workspace = torch.empty((wsb,), dtype=torch.uint8, device=dev)
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    def decode(q_lat, q_pe, bt, sl, cq, o, l):
+        if varlen:
+            m.mla_decode_varlen(q_lat, q_pe, wl.pool, wl.kind, wl.page_size, bt, sl, cq, Qt, wl.scale, o, l, workspace)
+        else:
+            m.mla_decode(q_lat, q_pe, wl.pool, wl.kind, wl.page_size, bt, sl, Qt, wl.scale, o, l, workspace)
+
     def step():
         m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
-        m.mla_decode(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens, Qt,
-                     wl.scale, out, lse, workspace)
+        decode(q_lat_s, q_pe_s, wl.block_table, wl.seq_lens, cu_q, out, lse)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -230,8 +258,7 @@ def run_gpu(args):
         ev[i][0].record(stream)
         m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
         evd[i][0].record(stream)
-        m.mla_decode(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens, Qt,
-                     wl.scale, out, lse, workspace)
+        decode(q_lat_s, q_pe_s, wl.block_table, wl.seq_lens, cu_q, out, lse)
         evd[i][1].record(stream)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
@@ -259,8 +286,10 @@ def run_gpu(args):
         return {k: buf[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
                 for k, v in like.items()}
 
-    src = dict(q_lat=wl.q_lat, q_pe=wl.q_pe, w_latent=wl.w_latent, w_k_pe=wl.w_k_pe, w_slots=wl.w_slots,
+    src = dict(q_lat=q_lat_s, q_pe=q_pe_s, w_latent=wl.w_latent, w_k_pe=wl.w_k_pe, w_slots=wl.w_slots,
                block_table=wl.block_table, seq_lens=wl.seq_lens)
+    if varlen:
+        src["cu_q"] = cu_q
     in_offs, in_bytes = packed(src)
     host_in_buf = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
     for k, v in views(host_in_buf, in_offs, src).items():
@@ -281,8 +310,8 @@ def run_gpu(args):
             eve[i - 3][0].record(stream)
         dev_in_buf.copy_(host_in_buf, non_blocking=True)
         m.mla_cache_write(dev_in["w_latent"], dev_in["w_k_pe"], dev_in["w_slots"], wl.pool, wl.kind)
-        m.mla_decode(dev_in["q_lat"], dev_in["q_pe"], wl.pool, wl.kind, wl.page_size, dev_in["block_table"],
-                     dev_in["seq_lens"], Qt, wl.scale, dev_out["out"], dev_out["lse"], workspace)
+        decode(dev_in["q_lat"], dev_in["q_pe"], dev_in["block_table"], dev_in["seq_lens"], dev_in.get("cu_q"),
+               dev_out["out"], dev_out["lse"])
         host_out_buf.copy_(dev_out_buf, non_blocking=True)
         if i >= 3:
             eve[i - 3][1].record(stream)
@@ -311,7 +340,8 @@ def run_gpu(args):
         "config": {"workload": args.config, "shape": CONFIG_TEXT[args.config], "context_tokens": ctx_tokens,
                    "cache_bytes_per_step": cache_bytes, "row_bytes": wl.row_bytes,
                    "l2": "flushed before every step (256 MiB write, outside the timed events)",
-                   "step": "mla_cache_write of the step's new rows + mla_decode (decode + split merge)",
+                   "step": "mla_cache_write of the step's new rows + " + ("mla_decode_varlen" if varlen else "mla_decode")
+                           + " (decode + split merge)",
                    "parallelism": f"replicas x{ws_} (requests are independent)"},
         "decode_steps_per_s": round(1e3 / step_ms_max, 1),
         "ctx_tokens_per_s": round(ctx_tokens * ws_ / (step_ms_max * 1e-3), 1),
@@ -532,18 +562,25 @@ def _oracle_prepare(wl, b):
     return c, pool
 
 
-def _oracle_run(wl, prep, cap=None):
+def _oracle_run(wl, prep, cap=None, qt=None):
     """Time the oracle's decode of a prepared request (its first `cap`
-    tokens when given); returns (bytes, seconds)."""
+    tokens when given; a verify step of `qt` tokens, its first qt query rows,
+    when given); returns (bytes, seconds)."""
     import oracle
     c, pool = prep
     sl = c["seq_lens"].copy()
     if cap is not None:
         sl[0] = min(int(sl[0]), int(cap))
+    qt = wl.Qt if qt is None else int(qt)
     t0 = time.perf_counter()
-    oracle.decode(c["q_lat"], c["q_pe"], pool, wl.kind, wl.page_size, c["block_table"], sl, 1, wl.Qt, wl.Hq,
+    oracle.decode(c["q_lat"][:qt], c["q_pe"][:qt], pool, wl.kind, wl.page_size, c["block_table"], sl, 1, qt, wl.Hq,
                   wl.scale)
     return int(sl[0]) * wl.row_bytes, time.perf_counter() - t0
+
+
+def _qt_for(config, wl):
+    """Per-request verify lengths of the workload (None: wl.Qt for all)."""
+    return verify_qlens(wl.B) if config == "verify" else None
 
 
 def oracle_sample(config, wl, budget_s=15.0):
@@ -555,12 +592,13 @@ def oracle_sample(config, wl, budget_s=15.0):
     order = [int(b) for b in sorted(range(wl.B), key=lambda b: sl[b]) if sl[b] > 0]
     order = order[len(order) // 2:] + order[:len(order) // 2]
     prep = {}
+    qts = _qt_for(config, wl)
     done_bytes, secs, n = 0, 0.0, 0
     while secs < budget_s:
         b = order[n % len(order)]
         if b not in prep:
             prep[b] = _oracle_prepare(wl, b)
-        nb, dt = _oracle_run(wl, prep[b])
+        nb, dt = _oracle_run(wl, prep[b], qt=None if qts is None else qts[b])
         done_bytes += nb
         secs += dt
         n += 1
@@ -586,15 +624,17 @@ def run_reference(args):
     import oracle
     import torch
     from mla_latent_kv_cache_gb300 import workloads as W
-    wl = W.CONFIGS[args.config](device="cuda" if torch.cuda.is_available() else "cpu")
+    wl = W.CONFIGS["mtp" if args.config == "verify" else args.config](
+        device="cuda" if torch.cuda.is_available() else "cpu")
     sl = wl.seq_lens.cpu().numpy()
     live = [int(b) for b in range(wl.B) if sl[b] > 0]
     prep = {}
+    qts = _qt_for(args.config, wl)
 
     def run_req(b, cap=None):
         if b not in prep:
             prep[b] = _oracle_prepare(wl, b)
-        return _oracle_run(wl, prep[b], cap)
+        return _oracle_run(wl, prep[b], cap, None if qts is None else qts[b])
 
     # calibrate context tokens per second on one whole request
     nb, dt = run_req(live[0])
