@@ -102,23 +102,52 @@ def traffic_for(config):
     return e.get("dram_bytes_per_launch")
 
 
+def timing_events(n, stream):
+    """n pairs of timing events, each recorded once so that the CUDA events
+    exist before the timed loop (torch creates an event on its first record):
+    the loop then makes no event-creating driver calls."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        b.record(stream)
+    return evs
+
+
+def step_time_summary(times_ms):
+    """Median step time and the steps that took over ten times it (and over a
+    millisecond): a stall of the device or the host inside a step's events
+    shows up here rather than only as a lower mean."""
+    t = sorted(times_ms)
+    med = t[len(t) // 2]
+    slow = [x for x in times_ms if x > 10 * med and x > 1.0]
+    return {"median_ms": round(med, 5), "stalled_steps": len(slow), "stalled_ms": round(sum(slow) - med * len(slow), 1)}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # Three fields per sample: the throttle reasons come from the one bitmask
+    # (NVML's clocks-event-reason bits), not five separate queries, and there
+    # is no power reading. With nine fields (power and each reason on its
+    # own) polled every 50 or 200 ms, a timed region of about a second now and
+    # then took whole seconds longer, the time landing inside the steps' events
+    # (and the JSON line's stalled_steps saying so).
+    Q = "index,clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
     def __init__(self, gpu_index: int, out_path: str | None):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
         self.out_path = out_path
+        self.first_timed = 0  # index of the first sample taken inside the timed region
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -128,6 +157,19 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def mark(self):
+        """The timed region starts: clock statistics use the samples from here on."""
+        self.first_timed = len(self.lines)
+
+    def wait_first(self, settle_s: float = 1.0, samples: int = 3, timeout_s: float = 10.0):
+        """Block until nvidia-smi has run for `settle_s` and produced `samples`
+        samples, so its start-up is over before the warm-up and timing."""
+        t0 = time.perf_counter()
+        while self.proc is not None and time.perf_counter() - t0 < timeout_s:
+            if len(self.lines) >= samples and time.perf_counter() - t0 >= settle_s:
+                break
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -141,20 +183,24 @@ class ClockSampler:
         if self.out_path:
             with open(self.out_path, "w") as f:
                 f.write(self.Q + "\n" + "\n".join(self.lines) + "\n")
+        return self.summarize(self.lines[self.first_timed:] or self.lines)
+
+    @classmethod
+    def summarize(cls, lines):
+        """Median SM clock, the maximum clock and the throttle reasons seen in
+        nvidia-smi csv lines of the fields in Q."""
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 4:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                clk, clk_max, bits = float(parts[1]), float(parts[2]), int(parts[3], 16)
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
+            sm.append(clk)
+            mx.append(clk_max)
+            reasons.update(n for n, bit in cls.REASON_BITS.items() if bits & bit)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         sm.sort()
@@ -225,6 +271,10 @@ def run_gpu(args):
     workspace = torch.empty((wsb,), dtype=torch.uint8, device=dev)
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    # each call's status word, OR-ed over the timed steps outside their events
+    # (the workspace holds only the last call's)
+    status_word = workspace[:4].view(torch.int32)
+    status_or = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def decode(q_lat, q_pe, bt, sl, cq, o, l):
         if varlen:
@@ -236,6 +286,11 @@ def run_gpu(args):
         m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
         decode(q_lat_s, q_pe_s, wl.block_table, wl.seq_lens, cu_q, out, lse)
 
+    # clock sampling starts before the warm-up so its start-up is over before timing
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_bench_{args.config}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks.start()
+    clocks.wait_first()
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
@@ -243,15 +298,12 @@ def run_gpu(args):
     assert m.device_status(workspace) == 0, "device-side status after warm-up"
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_bench_{args.config}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    ev = timing_events(K, stream)
+    evd = timing_events(K, stream)
     if ws_ > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
+    clocks.mark()
     t_wall = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xFF)
@@ -261,12 +313,14 @@ def run_gpu(args):
         decode(q_lat_s, q_pe_s, wl.block_table, wl.seq_lens, cu_q, out, lse)
         evd[i][1].record(stream)
         ev[i][1].record(stream)
+        torch.bitwise_or(status_or, status_word, out=status_or)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
     if ws_ > 1:
         dist.barrier()
     clk = clocks.stop()
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    step_times = [a.elapsed_time(b) for a, b in ev]
+    step_ms = sum(step_times) / K
     dec_ms = sum(a.elapsed_time(b) for a, b in evd) / K
     assert m.device_status(workspace) == 0, "device-side status after the timed steps"
 
@@ -303,7 +357,7 @@ def run_gpu(args):
     host_out_buf = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
     h2d, d2h = in_bytes, out_bytes
     Ke = max(3, min(K, 200))
-    eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+    eve = timing_events(Ke, stream)
     for i in range(Ke + 3):
         flush.fill_(1)
         if i >= 3:
@@ -315,10 +369,14 @@ def run_gpu(args):
         host_out_buf.copy_(dev_out_buf, non_blocking=True)
         if i >= 3:
             eve[i - 3][1].record(stream)
+        torch.bitwise_or(status_or, status_word, out=status_or)
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in eve) / Ke
     # the end-to-end steps computed what the device-resident steps did
     assert torch.equal(dev_out["out"], out) and torch.equal(dev_out["lse"], lse), "end-to-end outputs differ"
+    status_all = int(status_or.item())
+    if status_all:
+        print(f"bench: a timed decode call reported device status {status_all:#x}", file=sys.stderr)
 
     tot_bytes, step_ms_max = aggregate(cache_bytes, step_ms)
     _, dec_ms_max = aggregate(cache_bytes, dec_ms)
@@ -357,6 +415,8 @@ def run_gpu(args):
         "gpu_launches": 3 * K,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),
+        "step_times": step_time_summary(step_times),
+        "device_status_all_steps": status_all,
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
@@ -423,19 +483,20 @@ def run_gather(args):
     def step(bt=wl.block_table, c=cu, out=dst):
         m.mla_gather_upconvert(wl.pool, wl.page_size, bt, c, out)
 
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks_bench_gather.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks.start()
+    clocks.wait_first()
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
-    K = min(args.steps, 400)  # ~0.6 ms a step: about a quarter of a second
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks_bench_gather.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    K = min(args.steps, 1600)  # ~0.6 ms a step: about a second
+    ev = timing_events(K, stream)
     if ws_ > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
+    clocks.mark()
     t_wall = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xFF)
@@ -447,7 +508,8 @@ def run_gather(args):
     if ws_ > 1:
         dist.barrier()
     clk = clocks.stop()
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    step_times = [a.elapsed_time(b) for a, b in ev]
+    step_ms = sum(step_times) / K
 
     # end to end: the block table and prefix sums from pinned host memory, the
     # gathered rows back to pinned host memory, every step
@@ -459,7 +521,7 @@ def run_gather(args):
     h2d = h_bt.numel() * 4 + h_cu.numel() * 4
     d2h = rows * 576 * 2
     Ke = 10
-    eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+    eve = timing_events(Ke, stream)
     for i in range(Ke + 2):
         flush.fill_(1)
         if i >= 2:
@@ -505,6 +567,7 @@ def run_gather(args):
         "gpu_launches": K,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),
+        "step_times": step_time_summary(step_times),
     }
     if ws_ == 1 and not args.no_cpu:
         b, sec, n, th = gather_cpu_sample(wl)
@@ -673,7 +736,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=6000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="batched", choices=sorted(CONFIG_TEXT))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])

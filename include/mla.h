@@ -256,6 +256,16 @@ MLA_API int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const
  */
 MLA_API void mla_test_hold_next_decode(void);
 
+/*
+ * mla_test_slow_pv_next_decode - test support for the softmax -> PV hand-off.
+ * In the next mla_decode call in this process, one of the two warps that
+ * issue the value products (PV) busy-waits about 20 microseconds after each
+ * of its first 32 tiles, so the softmax warps run up to two tiles ahead of it.
+ * The call's results and status are those of an undelayed call; only its
+ * duration grows. Nothing else sets it.
+ */
+MLA_API void mla_test_slow_pv_next_decode(void);
+
 /* Static English text for a status code. */
 MLA_API const char* mla_status_string(int status);
 

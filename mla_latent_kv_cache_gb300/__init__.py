@@ -67,6 +67,8 @@ def load() -> ctypes.CDLL:
             lib.mla_decode_static_scratch.restype = i32
             lib.mla_test_hold_next_decode.argtypes = []
             lib.mla_test_hold_next_decode.restype = None
+            lib.mla_test_slow_pv_next_decode.argtypes = []
+            lib.mla_test_slow_pv_next_decode.restype = None
             lib.mla_merge_lse.argtypes = [vp, vp, i32, i64, vp, i32, vp, vp]
             lib.mla_decode_varlen.argtypes = [vp, vp, i64, vp, i32, i64, i32, vp, i64, vp, vp, i32, i32, i32, f32,
                                               vp, i32, vp, vp, ctypes.c_size_t, i32, vp]
@@ -237,6 +239,13 @@ def test_hold_next_decode() -> None:
     """Test support: make the next mla_decode's PV issuers time out (see
     include/mla.h)."""
     load().mla_test_hold_next_decode()
+
+
+def test_slow_pv_next_decode() -> None:
+    """Test support: make one PV issuer of the next mla_decode lag the
+    softmax warps by up to two tiles; its results are unchanged (see
+    include/mla.h)."""
+    load().mla_test_slow_pv_next_decode()
 
 
 def device_status(workspace: torch.Tensor) -> int:

@@ -93,7 +93,8 @@ int ws_ctas(int num_ctas, int sms) { return num_ctas > 0 ? (num_ctas < 2 ? 2 : n
 
 size_t decode_ws_bytes(int B, int HQ, int ctas) { return decode_ws_layout(B, HQ, ctas).total; }
 
-// Set by mla_test_hold_next_decode, consumed by the next mla_decode.
+// Set by mla_test_hold_next_decode (1) or mla_test_slow_pv_next_decode (2),
+// consumed by the next mla_decode.
 std::atomic<int> g_test_hold{0};
 
 // Workspace of mla_decode_static_scratch: one array per device, placed when
@@ -379,6 +380,8 @@ int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const void* c
 }
 
 void mla_test_hold_next_decode(void) { g_test_hold.store(1); }
+
+void mla_test_slow_pv_next_decode(void) { g_test_hold.store(2); }
 
 int mla_merge_lse(const float* part_out, const float* part_lse, int S, int64_t N, void* out, int out_dtype,
                   float* lse, void* stream) {

@@ -156,7 +156,13 @@ struct Cfg {
 struct Ctrl {
     uint64_t pair_full[5], pair_empty[5];
     uint64_t rope_full[3], rope_empty[3];
-    uint64_t s_full[2], s_free[2], p_full, o_done[2], q_full;
+    uint64_t s_full[2], s_free[2], o_done[2], q_full;
+    // tile t's P hand-off to the two PV issuers is p_full[t & 1]: the softmax
+    // may hand over tile t + 1 as soon as PV(t - 1) is done, which can be
+    // before a slow issuer has begun to wait for tile t, and one barrier would
+    // then complete a phase past that issuer, whose parity wait could never
+    // end; tile t + 2's hand-off follows PV(t) of both issuers
+    uint64_t p_full[2];
     uint64_t xfull;          // the peer's partial S landed (st.async transactions + 1 local arrive)
     uint64_t xfree;          // the peer has read this CTA's last partial S (1 remote arrive)
     uint64_t raw_full[3];    // fp8: a tile's codes and scales landed in its pair slots
@@ -477,7 +483,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
             mbar_init(&ctrl->s_free[i], 1);
             mbar_init(&ctrl->o_done[i], 2);  // one commit per PV issuer
         }
-        mbar_init(&ctrl->p_full, 1);
+        mbar_init(&ctrl->p_full[0], 1);
+        mbar_init(&ctrl->p_full[1], 1);
         mbar_init(&ctrl->q_full, 1);
         mbar_init(&ctrl->xfull, 1);
         mbar_init(&ctrl->xfree, 1);
@@ -624,7 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 const bool new_seg = (i == 0) || (it.j == 0);
                 if (new_seg) ++seg;
                 const uint32_t tO = tmem + (seg & 1) * 2 * NP;
-                if (!mbar_wait(&ctrl->p_full, i & 1, &ctrl->abort)) {
+                if (!mbar_wait(&ctrl->p_full[i & 1], (i >> 1) & 1, &ctrl->abort)) {
                     fail(p, ctrl, kErrWaitTimeout, kSitePFull, i);
                     report(p, kRolePV, kSitePFull, i);
                     break;
@@ -641,6 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                               (new_seg && kk == 0) ? 0u : 1u);
                 umma_commit(&ctrl->pair_empty[slot]);
                 umma_commit(&ctrl->o_done[i & 1]);
+                if (p.test_hold == 2 && mt == 1 && i < 32) spin_for_ns(20000);  // test hook: a lagging issuer
                 if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssued);
                 it.next(p.seq_lens, p.B);
             }
@@ -1101,7 +1109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                     MLA_TTRACE(t);
                     // the test hook withholds tile 0, so the PV issuers' bounded wait
                     // gives up and every role leaves through the abort path
-                    if (!(p.test_hold && t == 0)) mbar_arrive(&ctrl->p_full);
+                    if (!(p.test_hold == 1 && t == 0)) mbar_arrive(&ctrl->p_full[t & 1]);
                 }
                 seg_has_pv = true;
                 if (pend) {
@@ -1469,7 +1477,13 @@ struct FoldCfg {
 struct FoldCtrl {
     uint64_t blk_full[11], blk_empty[11];
     uint64_t rope_full[2], rope_empty[2];
-    uint64_t s_full[2], s_free[2], p_full, o_done[2], q_full;
+    uint64_t s_full[2], s_free[2], o_done[2], q_full;
+    // tile t's P hand-off to the two PV issuers is p_full[t & 1]: the softmax
+    // may hand over tile t + 1 as soon as PV(t - 1) is done, which can be
+    // before a slow issuer has begun to wait for tile t, and one barrier would
+    // then complete a phase past that issuer, whose parity wait could never
+    // end; tile t + 2's hand-off follows PV(t) of both issuers
+    uint64_t p_full[2];
     uint32_t tmem_base;
     int abort;
     int t_begin, t_end, b0, j0;
@@ -1510,7 +1524,8 @@ __global__ void __launch_bounds__(288, 1)
             mbar_init(&ctrl->s_free[i], 1);
             mbar_init(&ctrl->o_done[i], 2);  // one commit per PV issuer
         }
-        mbar_init(&ctrl->p_full, 1);
+        mbar_init(&ctrl->p_full[0], 1);
+        mbar_init(&ctrl->p_full[1], 1);
         mbar_init(&ctrl->q_full, 1);
         ctrl->abort = 0;
         fence_mbar_init();
@@ -1636,7 +1651,7 @@ __global__ void __launch_bounds__(288, 1)
                 const bool new_seg = (i == 0) || (it.j == 0);
                 if (new_seg) ++seg;
                 const uint32_t tO = tmem + (seg & 1) * 4 * NP;
-                if (!mbar_wait(&ctrl->p_full, i & 1, &ctrl->abort)) {
+                if (!mbar_wait(&ctrl->p_full[i & 1], (i >> 1) & 1, &ctrl->abort)) {
                     fail(p, ctrl, kErrWaitTimeout, kSitePFull, i);
                     report(p, kRolePV, kSitePFull, i);
                     break;
@@ -1658,6 +1673,7 @@ __global__ void __launch_bounds__(288, 1)
                     umma_commit(&ctrl->blk_empty[slot]);
                 }
                 umma_commit(&ctrl->o_done[i & 1]);
+                if (p.test_hold == 2 && mt == 1 && i < 32) spin_for_ns(20000);  // test hook: a lagging issuer
                 if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssued);
                 it.next(p.seq_lens, p.B);
             }
@@ -1900,7 +1916,7 @@ __global__ void __launch_bounds__(288, 1)
                     // gives up and every role leaves through the abort path
                     MLA_TRACE_POINT(t, kTrSmPArrive);
                     MLA_TTRACE(t);
-                    if (!(p.test_hold && t == 0)) mbar_arrive(&ctrl->p_full);
+                    if (!(p.test_hold == 1 && t == 0)) mbar_arrive(&ctrl->p_full[t & 1]);
                 }
                 seg_has_pv = true;
                 if (pend) {

@@ -34,7 +34,8 @@ struct DecodeParams {
     int out_f32;
     int SPG;           // partial slots per row group = workers + B
     int wseg;          // work-split cost of a request boundary, in tiles
-    int test_hold;     // test hook: 1 = withhold the first hand-off to the PV issuers
+    int test_hold;     // test hooks: 1 = withhold the first hand-off to the PV issuers,
+                       // 2 = hold one PV issuer ~20 us after each of its first 32 tiles
     const int32_t* cu_q;  // [B + 1] prefix sums of query tokens per request, or null: Qt each
 };
 

@@ -33,6 +33,13 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
+// Busy-waits about `ns` nanoseconds of %globaltimer (test hooks only).
+static __device__ __noinline__ void spin_for_ns(unsigned long long ns) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) {
+    }
+}
+
 // ------------------------------------------------------------- mbarriers
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
