@@ -112,12 +112,19 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kPrefetchTiles = 2;          // L2 lookahead of the load/convert producers
 constexpr int kRawSlots = 3;               // fp8 tiles in flight between TMA and the expand warps
 
-template <int NP>
+template <int NP, bool LSU>
 struct Cfg {
     static_assert(NP == 16 || NP == 32 || NP == 64, "NP");
     static constexpr int kPairBytes = 2 * 128 * 128;  // 2 x (64 dims x 128 tokens), 128-B swizzled
     static constexpr int kRopeBytes = 128 * 64;       // 32 rope dims x 128 tokens, 64-B swizzled
-    static constexpr int kRL = (NP == 64) ? 4 : 5;    // pair slots (2 per tile)
+    // Pair slots (2 per tile). Pair pk of every tile is freed by PV issuer pk;
+    // the load/convert warps of pair pk order their refills only by their own
+    // earlier waits, which with an odd ring would see the other issuer's
+    // progress only and could not prove that the slot's fill before last was
+    // freed (a parity wait cannot tell the two apart) while issuer pk runs
+    // behind. With an even ring a slot always holds the same pair. The single
+    // TMA producer waits on both pairs, so 5 slots are sound there.
+    static constexpr int kRL = (NP == 64 || LSU) ? 4 : 5;
     static constexpr int kRR = (NP == 16) ? 3 : (NP == 32 ? 2 : 1);  // rope slots (1 per tile; freed right after S)
     static constexpr int kQBytes = NP * (4 * 128 + 64);
     // 32 and 64 query rows: the two CTAs split the softmax columns, each owning
@@ -452,7 +459,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
     mla_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     const CUtensorMap& tmap_lat = maps.lat;
     const CUtensorMap& tmap_rope = maps.rope;
-    using C = Cfg<NP>;
+    using C = Cfg<NP, LSU>;
     extern __shared__ uint8_t smem_raw[];
     // align by offset from the shared array so every derived pointer stays a
     // shared-space pointer (ld/st.shared rather than generic accesses)
@@ -1454,6 +1461,15 @@ struct FoldCfg {
     // (the rope reload waits for one S, well inside a tile's time; 3% faster)
     static constexpr int kRL = (NP == 16) ? 11 : 10;
     static constexpr int kRR = (NP == 16) ? 2 : 1;
+    // Producer warp 1 fills, and PV issuer 0 frees, K-blocks 0 and 1 of each
+    // tile; warp 8 and issuer 1 K-blocks 2 and 3, all in one ring. A producer
+    // orders a refill only by its own earlier waits (and the rope slots it
+    // shares with the other producer), and a parity wait cannot tell the
+    // slot's last phase from the one before it; with 11 slots, or 10 and one
+    // rope slot, those waits do prove the fill before last freed whichever
+    // issuer runs behind (checked on a random-schedule model of the protocol).
+    static __device__ __forceinline__ int slot_of(int i, int kb) { return (4 * i + kb) % kRL; }
+    static __device__ __forceinline__ int fill_of(int i, int kb) { return (4 * i + kb) / kRL; }
     static constexpr int kQBytes = 2 * NP * (4 * 128 + 64);
     static constexpr int kNH = NP / 2;                 // softmax columns per thread
     static constexpr int kXBytes = 128 * kNH * 4;      // the partner lane's half scores
@@ -1606,8 +1622,8 @@ __global__ void __launch_bounds__(288, 1)
                 bool ok = true;
                 int site = kSitePairFull;
                 for (int kb = 0; kb < 4 && ok; ++kb) {
-                    const int u = 4 * i + kb, slot = u % C::kRL;
-                    if (!mbar_wait(&ctrl->blk_full[slot], (u / C::kRL) & 1, &ctrl->abort)) { ok = false; break; }
+                    const int slot = C::slot_of(i, kb);
+                    if (!mbar_wait(&ctrl->blk_full[slot], C::fill_of(i, kb) & 1, &ctrl->abort)) { ok = false; break; }
                     tc_fence_after();
                     if (kb == 0) MLA_TRACE_POINT(i, kTrSPair0);
                     const uint64_t da = smem_desc(smem_u32(ring + slot * C::kBlkBytes), 16, 1024, kSw128);
@@ -1663,7 +1679,7 @@ __global__ void __launch_bounds__(288, 1)
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int kb = 2 * mt + q;
-                    const int slot = (4 * i + kb) % C::kRL;
+                    const int slot = C::slot_of(i, kb);
                     // tokens 16 kk .. 16 kk + 15: rows 16 kk .. of both halves
                     const uint64_t da = smem_desc(smem_u32(ring + slot * C::kBlkBytes), 8192, 1024, kSw128);
 #pragma unroll
@@ -1711,9 +1727,9 @@ __global__ void __launch_bounds__(288, 1)
                 if (lane == 0) MLA_TRACE_POINT(i, kTrProdStart + 0 * pp);
                 for (int q = 0; q < 2; ++q) {
                     const int kb = 2 * pp + q;
-                    const int u = 4 * i + kb, slot = u % C::kRL;
-                    if (u >= C::kRL &&
-                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->blk_empty[slot], ((u / C::kRL) - 1) & 1, &ctrl->abort))) {
+                    const int slot = C::slot_of(i, kb), fill = C::fill_of(i, kb);
+                    if (fill > 0 &&
+                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->blk_empty[slot], (fill - 1) & 1, &ctrl->abort))) {
                         ok = false;
                         fsite = kSiteTmaPairEmpty;
                         ftile = i;
@@ -2099,7 +2115,7 @@ __global__ void __launch_bounds__(288, 1)
                     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        uint8_t* row = ring + ((4 * i + q) % C::kRL) * C::kBlkBytes + st * 128;
+                        uint8_t* row = ring + C::slot_of(i, q) * C::kBlkBytes + st * 128;
 #pragma unroll
                         for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(row + (((u + st) & 7) << 4)) = z;
                     }
@@ -2411,12 +2427,12 @@ struct Variant {
         if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return -1;
         if (!done[dev]) {
             auto k = mla_decode_kernel<NP, LSU, KIND>;
-            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NP>::kSmemBytes) != cudaSuccess)
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NP, LSU>::kSmemBytes) != cudaSuccess)
                 return -1;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2, 1, 1);
             cfg.blockDim = dim3(kThreads, 1, 1);
-            cfg.dynamicSmemBytes = Cfg<NP>::kSmemBytes;
+            cfg.dynamicSmemBytes = Cfg<NP, LSU>::kSmemBytes;
             int n = 0;
             if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) return -1;
             clusters[dev] = n;
@@ -2427,7 +2443,7 @@ struct Variant {
 
     static cudaError_t launch(const DecodeMaps& maps, const DecodeParams& p, int G, int GY, cudaStream_t stream) {
         cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = pdl_config(dim3(2 * G, GY), kThreads, Cfg<NP>::kSmemBytes, stream, attr);
+        cudaLaunchConfig_t cfg = pdl_config(dim3(2 * G, GY), kThreads, Cfg<NP, LSU>::kSmemBytes, stream, attr);
         return cudaLaunchKernelEx(&cfg, mla_decode_kernel<NP, LSU, KIND>, maps, p);
     }
 };
