@@ -17,7 +17,10 @@ with torch's float8_e4m3fn cast and with a brute-force table search); and
 definition, per-request verify lengths, empty leading queries); and
 ``gather_upconvert`` / ``f32_to_bf16`` in ``tests/test_oracle_gather.py``
 (torch's bf16 and e4m3 conversions, numpy float32 products, exact power-of-two
-scales, the cache write's round-trip bound, brute-force row bookkeeping).
+scales, the cache write's round-trip bound, brute-force row bookkeeping); and
+``decode_latent`` (other latent widths) in ``tests/test_oracle_latent.py``
+(numpy brute force at widths 256 / 768 / 1792, equality with ``decode`` at
+512, closed forms).
 """
 from __future__ import annotations
 
@@ -74,6 +77,8 @@ def _load():
             lib.oracle_decode.restype = i32
             lib.oracle_decode_varlen.argtypes = [p, p, p, i32, i64, i32, p, i64, p, p, i32, i32, dbl, p, p]
             lib.oracle_decode_varlen.restype = i32
+            lib.oracle_decode_latent.argtypes = [p, p, p, i32, i32, i64, i32, p, i64, p, i32, i32, i32, dbl, p, p]
+            lib.oracle_decode_latent.restype = i32
             lib.oracle_merge.argtypes = [p, p, i32, i64, p, p]
             lib.oracle_merge.restype = None
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -209,6 +214,27 @@ def decode_varlen(q_lat, q_pe, cache: np.ndarray, kind: int, page_size: int, blo
                                   bt.shape[1], _ptr(sl), _ptr(cu), B, Hq, float(scale), _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_decode_varlen: block id or slot out of range")
+    return out, lse
+
+
+def decode_latent(q_lat, q_pe, cache, D: int, P: int, page_size: int, block_table, seq_lens, B: int, Qt: int,
+                  Hq: int, scale: float):
+    """Decode over a bf16 cache of rows [latent D | rope P] (uint16 bits
+    [num_slots, D + P]); q_lat [B*Qt, Hq, D], q_pe [B*Qt, Hq, P]. Returns
+    (out [B*Qt, Hq, D] fp64, lse [B*Qt, Hq] fp64)."""
+    lib = _load()
+    ql = _as_bits16(q_lat).reshape(B * Qt, Hq, D)
+    qp = _as_bits16(q_pe).reshape(B * Qt, Hq, P) if P else np.zeros((B * Qt, Hq, 1), dtype=np.uint16)
+    c = _as_bits16(cache)
+    assert c.ndim == 2 and c.shape[1] == D + P, c.shape
+    bt = _as_np(block_table, np.int32)
+    sl = _as_np(seq_lens, np.int32)
+    out = np.empty((B * Qt, Hq, D), dtype=np.float64)
+    lse = np.empty((B * Qt, Hq), dtype=np.float64)
+    rc = lib.oracle_decode_latent(_ptr(ql), _ptr(qp), _ptr(c), D, P, c.shape[0], page_size, _ptr(bt),
+                                  bt.shape[1], _ptr(sl), B, Qt, Hq, float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_decode_latent: block id or slot out of range")
     return out, lse
 
 

@@ -334,6 +334,84 @@ int oracle_decode_varlen(const uint16_t *q_lat, const uint16_t *q_pe,
     return bad ? -1 : 0;
 }
 
+/* ------------------------------------------------- other latent widths */
+
+/* The same absorbed decode for a bf16 cache whose rows hold a latent of D
+ * values followed by a rotary key of P values (2 (D + P) bytes a row)
+ * [P2 "How it works": the full-attention layers cache a per-layer latent of
+ * rank 256, 768 or 1792 plus a small rotary and normalisation tail]. The
+ * pages give neither the tail's rotary width nor what its normalisation
+ * stores, so the reading is: the normalisation is applied before a row is
+ * cached, and the decode sees [latent D | rope P] exactly as the 512-wide
+ * definition above sees [latent 512 | rope 64]:
+ *   s_j = scale * (q_lat . c_j[0:D] + q_pe . c_j[D:D+P])
+ *   out = sum_j softmax(s)_j * c_j[0:D]   (D values),  lse = ln sum_j exp(s_j)
+ * with the same visibility rule, (0, -inf) rows, 64-bit slot arithmetic and
+ * fp64 two-pass softmax. q_lat rows are D values, q_pe rows P, out rows D.
+ * Returns 0, or -1 if a block id or slot is out of range. */
+static int decode_row_latent(const uint16_t *ql, const uint16_t *qp, const uint16_t *cache, int D, int P,
+                             int64_t num_slots, int page_size, const int32_t *btr, int64_t T, int Qt,
+                             int qt, double scale, double *o, double *lse_out) {
+    const int Wd = D + P;
+    int64_t nvis = T - Qt + qt + 1;
+    if (nvis < 0) nvis = 0;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (nvis == 0) { *lse_out = -INFINITY; return 0; }
+    double *q = (double *)malloc(sizeof(double) * (size_t)Wd);
+    double *s = (double *)malloc(sizeof(double) * (size_t)nvis);
+    int64_t *slots = (int64_t *)malloc(sizeof(int64_t) * (size_t)nvis);
+    for (int d = 0; d < D; ++d) q[d] = oracle_bf16_to_f64(ql[d]);
+    for (int e = 0; e < P; ++e) q[D + e] = oracle_bf16_to_f64(qp[e]);
+    int bad = 0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        int64_t blk = btr[j / page_size];
+        int64_t slot = blk * (int64_t)page_size + j % page_size;
+        if (blk < 0 || slot >= num_slots) { bad = 1; break; }
+        slots[j] = slot;
+    }
+    if (bad) { free(q); free(s); free(slots); *lse_out = NAN; return -1; }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const uint16_t *c = cache + slots[j] * (int64_t)Wd;
+        double dot = 0.0;
+        for (int d = 0; d < Wd; ++d) dot += q[d] * oracle_bf16_to_f64(c[d]);
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const uint16_t *c = cache + slots[j] * (int64_t)Wd;
+        double pj = exp(s[j] - m);
+        l += pj;
+        for (int d = 0; d < D; ++d) o[d] += pj * oracle_bf16_to_f64(c[d]);
+    }
+    for (int d = 0; d < D; ++d) o[d] /= l;
+    *lse_out = m + log(l);
+    free(q);
+    free(s);
+    free(slots);
+    return 0;
+}
+
+int oracle_decode_latent(const uint16_t *q_lat, const uint16_t *q_pe, const uint16_t *cache, int D, int P,
+                         int64_t num_slots, int page_size, const int32_t *block_table, int64_t bt_stride,
+                         const int32_t *seq_lens, int B, int Qt, int Hq, double scale, double *out,
+                         double *lse) {
+    if (D <= 0 || P < 0 || page_size <= 0) return -1;
+    int64_t ntask = (int64_t)B * Qt * Hq;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t row = 0; row < ntask; ++row) {
+        int b = (int)(row / ((int64_t)Qt * Hq));
+        int qt = (int)((row / Hq) % Qt);
+        if (decode_row_latent(q_lat + row * D, q_pe + row * P, cache, D, P, num_slots, page_size,
+                              block_table + (int64_t)b * bt_stride, seq_lens[b], Qt, qt, scale,
+                              out + row * D, lse + row))
+            bad = 1;
+    }
+    return bad ? -1 : 0;
+}
+
 /* ----------------------------------------------------------------- merge */
 
 /* Combine S partial results of the same rows computed over disjoint token
