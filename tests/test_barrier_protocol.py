@@ -1,17 +1,20 @@
-"""The decode kernels' mbarrier hand-offs on a random-schedule model
-(tests/barrier_model.py), with the ring shapes the kernels use.
+"""The decode kernels' mbarrier hand-offs on random-schedule models
+(tests/barrier_model.py for one CTA, tests/barrier_model_pair.py for the
+cluster kernel's CTA pair), with the shapes the kernels use.
 
 Every shape must finish every schedule with no problem. The schedules include
-ones where a PV issuer or a producer runs far behind the other roles. Two
-shapes the kernels used to have serve as controls, so the model is shown able
-to catch each kind of fault:
-- one hand-off barrier for two P buffers: a PV issuer two phases behind waits
-  forever;
-- an odd pair ring fed by per-pair producers: a slot is reloaded before its
-  PV has freed it."""
+ones where a PV issuer, a producer or one CTA's softmax runs far behind the
+other roles. Controls show that the models catch each kind of fault:
+- one hand-off barrier for two P buffers, which the kernels used to have: a
+  PV issuer two phases behind waits forever;
+- an odd pair ring fed by per-pair producers, which the kernels also used to
+  have: a slot is reloaded before its PV has freed it;
+- the cluster kernel without the wait that protects its score staging: P
+  overwrites the staged scores before the bulk copy has read them."""
 import pytest
 
 from barrier_model import run
+from barrier_model_pair import run_pair
 
 SKEWS = [None, {"PV0": 0.02}, {"PV1": 0.02}, {"PV0": 0.01, "LD1": 0.2}, {"PV1": 0.01, "LD0": 0.2},
          {"PV0": 0.005, "S": 3.0, "LD0": 3.0}]
@@ -56,3 +59,40 @@ def test_one_handoff_barrier_deadlocks():
 def test_odd_ring_with_per_pair_producers_reloads_early():
     bad = failures(40, KB=2, R=5, RR=3, producers=2, PB=2, H=2)
     assert any("unfreed" in e for _, _, e in bad)
+
+
+PAIR_SKEWS = [None, {"PV0_0": 0.02}, {"PV1_1": 0.02}, {"SM0": 0.05}, {"SM1": 0.05, "PV0_0": 0.1}, {"LD0": 0.05},
+              {"S1": 0.05}]
+
+# (name, pair slots, rope slots, P buffers, split softmax columns, score staging in the P buffer)
+PAIR_SHAPES = [
+    ("16 rows", 5, 3, 2, False, False),
+    ("32 rows", 5, 2, 2, True, True),
+    ("64 rows", 4, 1, 1, True, False),
+    ("16 rows, load/convert warps", 4, 3, 2, False, False),
+    ("32 rows, load/convert warps", 4, 2, 2, True, True),
+]
+
+
+def pair_failures(seeds, **shape):
+    out = []
+    for w in PAIR_SKEWS:
+        for seed in range(seeds):
+            e = run_pair(seed, weights=w, **shape)
+            if e:
+                out.append((w, seed, e[0]))
+    return out
+
+
+@pytest.mark.parametrize("name,R,RR,PB,split,send_in_p", PAIR_SHAPES, ids=[s[0] for s in PAIR_SHAPES])
+def test_cluster_exchanges_survive_skew(name, R, RR, PB, split, send_in_p):
+    bad = pair_failures(20, R=R, RR=RR, PB=PB, split=split, send_in_p=send_in_p)
+    assert not bad, bad[:3]
+
+
+def test_score_staging_needs_the_peer_to_have_read_it():
+    """At 32 rows the partial scores are staged in the tile's P buffer; writing
+    P before the peer has consumed them (its xfree arrive) lets P overwrite the
+    staging before the bulk copy has read it."""
+    bad = pair_failures(20, R=5, RR=2, PB=2, split=True, send_in_p=True, skip_xfree_before_p=True)
+    assert any("source changed" in e for _, _, e in bad)
