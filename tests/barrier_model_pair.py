@@ -13,7 +13,8 @@ remote arrive on `xfree`. With split softmax columns, each CTA also pushes
 its P block into the peer's P buffer. That copy lands on the peer's `pin`,
 and it is sent only after the peer's `rp_free` has said that its PV of the
 buffer's previous tile is done. With 32 query rows the score staging is
-the tile's own P buffer.
+the tile's own P buffer. With an fp8 pool, the TMA lands codes and scales
+and the expand warps widen them in place before S may read the slots.
 
 A bulk copy reads its source and writes its destination at one random later
 moment. The model reports:
@@ -30,7 +31,12 @@ from barrier_model import Bar
 
 
 def run_pair(seed: int, *, R: int, RR: int, PB: int, split: bool, send_in_p: bool, N: int = 30,
-             weights: dict | None = None, skip_xfree_before_p: bool = False) -> list[str]:
+             weights: dict | None = None, skip_xfree_before_p: bool = False, fp8: bool = False,
+             raw_slots: int = 3) -> list[str]:
+    """fp8: the TMA lands a tile's codes and scales in its two pair slots and
+    completes raw_full[i % raw_slots]; the expand warps (one actor: four warps
+    that meet at a named barrier every tile) wait for it, widen the codes in
+    place and then arrive on both slots' pair_full."""
     rnd = random.Random(seed)
     errors: list[str] = []
     asyncs = []                                 # (name, fn): fire at a random later moment
@@ -40,6 +46,8 @@ def run_pair(seed: int, *, R: int, RR: int, PB: int, split: bool, send_in_p: boo
         def __init__(self, c):
             self.c = c
             self.pair_full = [Bar(1) for _ in range(R)]
+            self.raw_full = [Bar(1) for _ in range(raw_slots)]
+            self.raw_data = [None] * raw_slots
             self.pair_empty = [Bar(1) for _ in range(R)]
             self.rope_full = [Bar(1) for _ in range(RR)]
             self.rope_empty = [Bar(1) for _ in range(RR)]
@@ -79,12 +87,25 @@ def run_pair(seed: int, *, R: int, RR: int, PB: int, split: bool, send_in_p: boo
                 if me.slot_held[s] is not None:
                     errors.append(f"CTA{me.c}: load of tile {i} pair {pp} over unfreed {me.slot_held[s]}")
                 me.slot_held[s] = (i, pp)
-                me.pair_full[s].arrive_expect(1, 1)
+                if not fp8:
+                    me.pair_full[s].arrive_expect(1, 1)
 
-                def land(s=s, i=i, pp=pp):
-                    me.slot_data[s] = (i, pp)
-                    me.pair_full[s].complete_tx(1)
-                asyncs.append(("tma", land))
+                    def land(s=s, i=i, pp=pp):
+                        me.slot_data[s] = (i, pp)
+                        me.pair_full[s].complete_tx(1)
+                    asyncs.append(("tma", land))
+                yield None
+            if fp8:
+                # codes into the first slot, scales into the second, one barrier
+                rs = i % raw_slots
+                me.raw_full[rs].arrive_expect(1, 1)
+
+                def land_raw(rs=rs, i=i):
+                    me.slot_data[(2 * i) % R] = ("raw", i)
+                    me.slot_data[(2 * i + 1) % R] = ("raw", i)
+                    me.raw_data[rs] = i
+                    me.raw_full[rs].complete_tx(1)
+                asyncs.append(("tma", land_raw))
                 yield None
             rr = i % RR
             if i >= RR:
@@ -95,6 +116,19 @@ def run_pair(seed: int, *, R: int, RR: int, PB: int, split: bool, send_in_p: boo
                 me.rope_data[rr] = i
                 me.rope_full[rr].complete_tx(1)
             asyncs.append(("tma", land_r))
+            yield None
+
+    def expand(me):
+        for i in range(N):
+            rs = i % raw_slots
+            yield lambda rs=rs, i=i: me.raw_full[rs].passes((i // raw_slots) & 1)
+            s0, s1 = (2 * i) % R, (2 * i + 1) % R
+            if me.raw_data[rs] != i or me.slot_data[s0] != ("raw", i) or me.slot_data[s1] != ("raw", i):
+                errors.append(f"CTA{me.c} expand({i}) found {me.raw_data[rs]} / {me.slot_data[s0]} / {me.slot_data[s1]}")
+            yield None
+            me.slot_data[s0], me.slot_data[s1] = (i, 0), (i, 1)
+            me.pair_full[s0].arrive_expect()
+            me.pair_full[s1].arrive_expect()
             yield None
 
     def s_issuer(me):
@@ -221,6 +255,8 @@ def run_pair(seed: int, *, R: int, RR: int, PB: int, split: bool, send_in_p: boo
     for c in (0, 1):
         me, peer = ctas[c], ctas[1 - c]
         actors[f"LD{c}"] = producer(me)
+        if fp8:
+            actors[f"EX{c}"] = expand(me)
         actors[f"S{c}"] = s_issuer(me)
         actors[f"SM{c}"] = softmax(me, peer)
         actors[f"PV0_{c}"] = pv(me, 0)

@@ -62,15 +62,19 @@ def test_odd_ring_with_per_pair_producers_reloads_early():
 
 
 PAIR_SKEWS = [None, {"PV0_0": 0.02}, {"PV1_1": 0.02}, {"SM0": 0.05}, {"SM1": 0.05, "PV0_0": 0.1}, {"LD0": 0.05},
-              {"S1": 0.05}]
+              {"S1": 0.05}, {"EX0": 0.05}]
 
-# (name, pair slots, rope slots, P buffers, split softmax columns, score staging in the P buffer)
+# (name, pair slots, rope slots, P buffers, split softmax columns, score staging in the P buffer,
+#  fp8 pool: TMA-landed codes widened in place by the expand warps)
 PAIR_SHAPES = [
-    ("16 rows", 5, 3, 2, False, False),
-    ("32 rows", 5, 2, 2, True, True),
-    ("64 rows", 4, 1, 1, True, False),
-    ("16 rows, load/convert warps", 4, 3, 2, False, False),
-    ("32 rows, load/convert warps", 4, 2, 2, True, True),
+    ("16 rows", 5, 3, 2, False, False, False),
+    ("32 rows", 5, 2, 2, True, True, False),
+    ("64 rows", 4, 1, 1, True, False, False),
+    ("16 rows, load/convert warps", 4, 3, 2, False, False, False),
+    ("32 rows, load/convert warps", 4, 2, 2, True, True, False),
+    ("16 rows, fp8", 5, 3, 2, False, False, True),
+    ("32 rows, fp8", 5, 2, 2, True, True, True),
+    ("64 rows, fp8", 4, 1, 1, True, False, True),
 ]
 
 
@@ -84,9 +88,9 @@ def pair_failures(seeds, **shape):
     return out
 
 
-@pytest.mark.parametrize("name,R,RR,PB,split,send_in_p", PAIR_SHAPES, ids=[s[0] for s in PAIR_SHAPES])
-def test_cluster_exchanges_survive_skew(name, R, RR, PB, split, send_in_p):
-    bad = pair_failures(20, R=R, RR=RR, PB=PB, split=split, send_in_p=send_in_p)
+@pytest.mark.parametrize("name,R,RR,PB,split,send_in_p,fp8", PAIR_SHAPES, ids=[s[0] for s in PAIR_SHAPES])
+def test_cluster_exchanges_survive_skew(name, R, RR, PB, split, send_in_p, fp8):
+    bad = pair_failures(20, R=R, RR=RR, PB=PB, split=split, send_in_p=send_in_p, fp8=fp8)
     assert not bad, bad[:3]
 
 
