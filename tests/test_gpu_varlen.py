@@ -84,3 +84,43 @@ def test_uniform_lengths_match_mla_decode_bitwise():
                         wl.scale, out2, lse2, ws)
     torch.cuda.synchronize()
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_verify_workload_sampled():
+    """The bench's verify workload at full size: the MTP pool above the int32
+    wrap, 128 requests with verify lengths U{1..4}, one mla_decode_varlen call
+    as the bench times it; sampled requests (empty and one-token ones, the
+    longest, the one holding the pool's last page) against the oracle."""
+    import bench
+
+    wl = W.CONFIGS["mtp"](device=DEV)
+    qlens = bench.verify_qlens(wl.B)
+    sl = wl.seq_lens.cpu().numpy()
+    zero_one = [int(i) for i in np.nonzero(sl <= 1)[0]][:3]
+    last = int(np.nonzero((wl.block_table == wl.num_slots // wl.page_size - 1).any(dim=1).cpu().numpy())[0][0])
+    reqs = sorted(set(zero_one + [int(np.argmax(sl)), last, 7, 60]))
+    c = W.compact(wl, reqs)
+    pool = c["pool"].copy()
+    oracle.cache_write(c["w_latent"], c["w_k_pe"], c["w_slots"], pool, wl.kind)
+    sel = [k * wl.Qt + t for k, b in enumerate(reqs) for t in range(int(qlens[b]))]
+    cu_c = np.concatenate([[0], np.cumsum([int(qlens[b]) for b in reqs])]).astype(np.int32)
+    ref_o, ref_l = oracle.decode_varlen(c["q_lat"][sel], c["q_pe"][sel], pool, wl.kind, wl.page_size,
+                                        c["block_table"], c["seq_lens"], cu_c, wl.Hq, wl.scale)
+
+    # the device step: each request's first q_len_b query rows, packed
+    pick = torch.tensor([b * wl.Qt + t for b in range(wl.B) for t in range(int(qlens[b]))], dtype=torch.int64,
+                        device=DEV)
+    q_lat = wl.q_lat[pick].contiguous()
+    q_pe = wl.q_pe[pick].contiguous()
+    cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    total = int(cu[-1])
+    m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+    out = torch.empty((total, wl.Hq, 512), dtype=torch.float32, device=DEV)
+    lse = torch.empty((total, wl.Hq), dtype=torch.float32, device=DEV)
+    ws = torch.empty(m.mla_decode_workspace_bytes(wl.B, wl.Qt, wl.Hq, 0), dtype=torch.uint8, device=DEV)
+    m.mla_decode_varlen(q_lat, q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens,
+                        torch.from_numpy(cu).to(DEV), wl.Qt, wl.scale, out, lse, ws)
+    torch.cuda.synchronize()
+    assert m.device_status(ws) == 0
+    rows = [int(cu[b]) + t for b in reqs for t in range(int(qlens[b]))]
+    _check(out[rows], lse[rows], ref_o, ref_l, wl.kind, "verify workload")
