@@ -289,3 +289,18 @@ def test_named_workload_sampled(name):
     check_decode(out, lse, o, l, rows, kind=wl.kind, what=name)
     if name == "mtp":
         assert (wl.block_table[wl.block_table >= 0] >= W.INT32_WRAP_SLOT // 16).all()
+
+
+@pytest.mark.parametrize("page_size,Hq,Qt,kind,num_ctas", [
+    (3, 16, 1, 0, 0), (5, 8, 4, 0, 6), (3, 16, 4, 0, 5), (7, 16, 1, 1, 0), (1, 8, 4, 1, 6), (3, 16, 4, 1, 0)])
+def test_load_convert_warps_ragged(page_size, Hq, Qt, kind, num_ctas):
+    """Page sizes that are not a multiple of 8 rows go through the load/convert
+    warps (a four-slot pair ring): 16, 32 and 64 rows, bf16 and fp8 pools,
+    request boundaries inside and across workers."""
+    sl = [0, 1, 2, 130, 129, 700, 1500, 257, 5]
+    extra = dict(write_all=True) if kind == 1 else {}
+    wl = W.make("lsu", B=len(sl), Hq=Hq, Qt=Qt, page_size=page_size, seq_lens=sl, kind=kind,
+                seed=70 + page_size + Hq + Qt + kind, device=DEV, **extra)
+    o, l, rr = oracle_step(wl, range(wl.B))
+    out, lse = run_step(wl, num_ctas=num_ctas)
+    check_decode(out, lse, o, l, rr, kind=kind, what=f"page={page_size} rows={Hq * Qt} kind={kind}")
