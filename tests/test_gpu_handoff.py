@@ -31,10 +31,13 @@ def _lib():
 
 CASES = [
     # name, kind, Hq, page size: the folded-tile kernel at 16 and 32 query
-    # rows, and the cluster kernel (fp8 pool) at 16
+    # rows, the cluster kernel (fp8 pool) at 16, and its load/convert-warp
+    # variants (pages that are not a multiple of 8 rows) at 16 and 32
     ("fold16", W.KIND_BF16, 16, 16),
     ("fold32", W.KIND_BF16, 32, 64),
     ("cluster16_fp8", W.KIND_FP8, 16, 64),
+    ("lsu16", W.KIND_BF16, 16, 3),
+    ("lsu32", W.KIND_BF16, 32, 5),
 ]
 
 
