@@ -6,9 +6,16 @@ One step = the hot path over one batch: write the step's new cache rows
 (sum of context tokens x row bytes) / step time, each request's rows counted
 once; also decode steps/s and context tokens/s.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config batched|long|mtp|fp8|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mtp|batched|long|fp8|tiny|verify]
+                  [--side long,fp8,...|none] [--clock-csv PATH]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
   python bench.py --config gather        # the fp8_ds_mla prefill-context gather (mla_gather_upconvert)
+
+The headline workload (default mtp: the 9.8M-slot pool, 128 requests of up
+to 100k tokens, 4-token causal verify steps, the largest configuration that
+fits one GPU) gives the line's value, roofline, e2e and cpu_baseline; the
+other workloads (--side) are measured the same way afterwards and reported
+under "workloads" in the same line.
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
 on the launching stream, with L2 flushed (a 256 MiB write) before every step
@@ -216,31 +223,47 @@ def verify_qlens(B, rank=0):
     return np.random.default_rng(7 + 1000 * rank).integers(1, 5, size=B)
 
 
-def run_gpu(args):
+WORKLOAD_SEED = {"tiny": 1, "batched": 2, "long": 3, "mtp": 4, "fp8": 5}
+# workloads measured beside the headline one and reported in its line
+SIDE_WORKLOADS = ("long", "fp8", "batched", "tiny", "verify")
+
+
+def config_dict(name, ctx_tokens, cache_bytes, row_bytes, ws_):
+    """The `config` object of a decode line; both arms use it, so the
+    reference arm's line names the same workload in the same words."""
+    varlen = name == "verify"
+    return {"workload": name, "shape": CONFIG_TEXT[name], "context_tokens": ctx_tokens,
+            "cache_bytes_per_step": cache_bytes, "row_bytes": row_bytes,
+            "l2": "flushed before every step (256 MiB write, outside the timed events)",
+            "step": "mla_cache_write of the step's new rows + " + ("mla_decode_varlen" if varlen else "mla_decode")
+                    + " (decode + split merge)",
+            "parallelism": f"replicas x{ws_} (requests are independent)"}
+
+
+def build_workload(name, dev, rank=0):
+    """The named workload on `dev` (verify: the mtp workload's pool and
+    requests), seeded per rank."""
+    from mla_latent_kv_cache_gb300 import workloads as W
+    base = "mtp" if name == "verify" else name
+    return W.CONFIGS[base](device=dev, seed=WORKLOAD_SEED[base] + 1000 * rank)
+
+
+def measure_gpu(name, args, dev, rank, ws_, clock_csv=None):
+    """Time K steps of workload `name` (device-resident inputs), then the
+    same step end to end from pinned host memory. Returns the numbers of one
+    JSON line (before the max over ranks)."""
     import numpy as np
     import torch
     import torch.distributed as dist
-
-    ws_, rank, local = dist_env()
-    if ws_ > 1:
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
-    torch.cuda.set_device(local)
-    dev = torch.device(f"cuda:{local}")
-
-    from mla_latent_kv_cache_gb300 import build as mbuild
-    mbuild.build()
     import mla_latent_kv_cache_gb300 as m
-    from mla_latent_kv_cache_gb300 import workloads as W
 
-    varlen = args.config == "verify"
-    base_cfg = "mtp" if varlen else args.config
-    wl = W.CONFIGS[base_cfg](device=dev, seed={"tiny": 1, "batched": 2, "long": 3, "mtp": 4, "fp8": 5}[base_cfg] + 1000 * rank)
+    varlen = name == "verify"
+    wl = build_workload(name, dev, rank)
     cu_q = None
     q_lat_s, q_pe_s = wl.q_lat, wl.q_pe  # the step's query rows
     if varlen:
         # per-request verify lengths U{1..4}: request b's queries are the first
         # q_len_b of its four query rows
-        import numpy as np
         qlens = verify_qlens(wl.B, rank)
         pick = torch.tensor([b * wl.Qt + t for b in range(wl.B) for t in range(int(qlens[b]))], dtype=torch.int64,
                             device=dev)
@@ -271,10 +294,11 @@ def run_gpu(args):
     workspace = torch.empty((wsb,), dtype=torch.uint8, device=dev)
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    # each call's status word, OR-ed over the timed steps outside their events
-    # (the workspace holds only the last call's)
+    # each call's status word (and the cache write's), OR-ed over the timed
+    # steps outside their events (the workspace holds only the last call's)
     status_word = workspace[:4].view(torch.int32)
     status_or = torch.zeros(1, dtype=torch.int32, device=dev)
+    write_status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def decode(q_lat, q_pe, bt, sl, cq, o, l):
         if varlen:
@@ -282,18 +306,20 @@ def run_gpu(args):
         else:
             m.mla_decode(q_lat, q_pe, wl.pool, wl.kind, wl.page_size, bt, sl, Qt, wl.scale, o, l, workspace)
 
-    def step():
-        m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
-        decode(q_lat_s, q_pe_s, wl.block_table, wl.seq_lens, cu_q, out, lse)
+    def write(lat, kpe, slots):
+        m.mla_cache_write(lat, kpe, slots, wl.pool, wl.kind, status=write_status)
 
     # clock sampling starts before the warm-up so its start-up is over before timing
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_bench_{args.config}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks = ClockSampler(torch.cuda.current_device(), clock_csv)
     clocks.start()
     clocks.wait_first()
     for _ in range(args.warmup):
         flush.fill_(1)
-        step()
+        write(wl.w_latent, wl.w_k_pe, wl.w_slots)
+        decode(q_lat_s, q_pe_s, wl.block_table, wl.seq_lens, cu_q, out, lse)
+        # the status fold runs in the warm-up too, so its first launch (and
+        # module load) is not inside the timed region
+        torch.bitwise_or(status_or, status_word, out=status_or)
     torch.cuda.synchronize()
     assert m.device_status(workspace) == 0, "device-side status after warm-up"
 
@@ -308,7 +334,7 @@ def run_gpu(args):
     for i in range(K):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
-        m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+        write(wl.w_latent, wl.w_k_pe, wl.w_slots)
         evd[i][0].record(stream)
         decode(q_lat_s, q_pe_s, wl.block_table, wl.seq_lens, cu_q, out, lse)
         evd[i][1].record(stream)
@@ -363,7 +389,7 @@ def run_gpu(args):
         if i >= 3:
             eve[i - 3][0].record(stream)
         dev_in_buf.copy_(host_in_buf, non_blocking=True)
-        m.mla_cache_write(dev_in["w_latent"], dev_in["w_k_pe"], dev_in["w_slots"], wl.pool, wl.kind)
+        write(dev_in["w_latent"], dev_in["w_k_pe"], dev_in["w_slots"])
         decode(dev_in["q_lat"], dev_in["q_pe"], dev_in["block_table"], dev_in["seq_lens"], dev_in.get("cu_q"),
                dev_out["out"], dev_out["lse"])
         host_out_buf.copy_(dev_out_buf, non_blocking=True)
@@ -374,55 +400,103 @@ def run_gpu(args):
     e2e_ms = sum(a.elapsed_time(b) for a, b in eve) / Ke
     # the end-to-end steps computed what the device-resident steps did
     assert torch.equal(dev_out["out"], out) and torch.equal(dev_out["lse"], lse), "end-to-end outputs differ"
-    status_all = int(status_or.item())
+    status_all = int(status_or.item()) | int(write_status.item())
     if status_all:
-        print(f"bench: a timed decode call reported device status {status_all:#x}", file=sys.stderr)
+        print(f"bench: a timed call on '{name}' reported device status {status_all:#x}", file=sys.stderr)
+    res = {"name": name, "wl": wl, "cache_bytes": cache_bytes, "ctx_tokens": ctx_tokens, "step_ms": step_ms,
+           "dec_ms": dec_ms, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "status_all": status_all,
+           "step_times": step_times, "wall": wall, "clk": clk, "K": K}
+    del out, lse, workspace, flush, dev_in_buf, dev_out_buf
+    return res
 
-    tot_bytes, step_ms_max = aggregate(cache_bytes, step_ms)
-    _, dec_ms_max = aggregate(cache_bytes, dec_ms)
-    _, e2e_ms_max = aggregate(cache_bytes, e2e_ms)
+
+def line_numbers(r, ws_, peak):
+    """value, roofline and e2e of one measured workload (max over ranks)."""
+    tot_bytes, step_ms_max = aggregate(r["cache_bytes"], r["step_ms"])
+    _, e2e_ms_max = aggregate(r["cache_bytes"], r["e2e_ms"])
+    achieved = r["cache_bytes"] / (r["dec_ms"] * 1e-3) / 1e9
+    return {
+        "value": round(tot_bytes / (step_ms_max * 1e-3) / 1e9, 1), "ms_per_step": round(step_ms_max, 5),
+        "decode_steps_per_s": round(1e3 / step_ms_max, 1),
+        "ctx_tokens_per_s": round(r["ctx_tokens"] * ws_ / (step_ms_max * 1e-3), 1),
+        "achieved": achieved, "frac": achieved / peak,
+        "e2e": {"value": round(tot_bytes / (e2e_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms_max, 5), "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+    }
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    ws_, rank, local = dist_env()
+    if ws_ > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+
+    from mla_latent_kv_cache_gb300 import build as mbuild
+    mbuild.build()
+
+    peak, peak_kind = measured_peaks()
+    side = [] if args.side == "none" else [w for w in args.side.split(",") if w and w != args.config]
+    r = measure_gpu(args.config, args, dev, rank, ws_, args.clock_csv if rank == 0 else None)
+    head = line_numbers(r, ws_, peak)
+    cpu = cpu_baseline(args.config, r["wl"], one_thread=True) if ws_ == 1 and not args.no_cpu and rank == 0 else None
+    row_bytes = r.pop("wl").row_bytes
+    side_lines = {}
+    for name in side:
+        torch.cuda.empty_cache()
+        rs = measure_gpu(name, args, dev, rank, ws_)
+        n = line_numbers(rs, ws_, peak)
+        entry = {"value": n["value"], "unit": "GB/s", "ms_per_step": n["ms_per_step"],
+                 "decode_steps_per_s": n["decode_steps_per_s"], "ctx_tokens_per_s": n["ctx_tokens_per_s"],
+                 "roofline": {"bound": "hbm", "achieved": round(n["achieved"], 1), "peak": peak,
+                              "frac": round(n["frac"], 4), "traffic": traffic_for(name)},
+                 "e2e": n["e2e"], "config": config_dict(name, rs["ctx_tokens"], rs["cache_bytes"],
+                                                        rs["wl"].row_bytes, ws_),
+                 "clocks": rs["clk"], "step_times": step_time_summary(rs["step_times"]),
+                 "device_status_all_steps": rs["status_all"]}
+        if ws_ == 1 and not args.no_cpu and rank == 0:
+            entry["cpu_baseline"] = cpu_baseline(name, rs["wl"], budget_s=4.0)
+        side_lines[name] = entry
+        del rs, entry
     if rank != 0:
         if ws_ > 1:
             dist.destroy_process_group()
         return
-    peak, peak_kind = measured_peaks()
-    value = tot_bytes / (step_ms_max * 1e-3) / 1e9
-    achieved = cache_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = traffic_for(args.config)
-    cpu = cpu_baseline(args.config, wl) if ws_ == 1 and not args.no_cpu else None
+    cfg = config_dict(args.config, r["ctx_tokens"], r["cache_bytes"], row_bytes, ws_)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws_, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.kind == 0 else "e4m3+bf16",
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": ws_, "steps": r["K"],
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if args.config != "fp8" else "e4m3+bf16",
         "data": "synthetic (seeded N(0,1) bf16 rows, shuffled block tables, NaN-filled free slots)",
-        "config": {"workload": args.config, "shape": CONFIG_TEXT[args.config], "context_tokens": ctx_tokens,
-                   "cache_bytes_per_step": cache_bytes, "row_bytes": wl.row_bytes,
-                   "l2": "flushed before every step (256 MiB write, outside the timed events)",
-                   "step": "mla_cache_write of the step's new rows + " + ("mla_decode_varlen" if varlen else "mla_decode")
-                           + " (decode + split merge)",
-                   "parallelism": f"replicas x{ws_} (requests are independent)"},
-        "decode_steps_per_s": round(1e3 / step_ms_max, 1),
-        "ctx_tokens_per_s": round(ctx_tokens * ws_ / (step_ms_max * 1e-3), 1),
-        "pct_of_8TBps": round(100 * value / ws_ / NOMINAL_HBM_GBS, 2),
-        "pct_of_measured_hbm": round(100 * value / ws_ / peak, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
+        "config": cfg,
+        "decode_steps_per_s": head["decode_steps_per_s"],
+        "ctx_tokens_per_s": head["ctx_tokens_per_s"],
+        "pct_of_8TBps": round(100 * head["value"] / ws_ / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * head["value"] / ws_ / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(head["achieved"], 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(head["frac"], 4), "traffic": traffic_for(args.config),
                      "kernel": "mla_decode call (decode kernel + split-merge kernel), CUDA events",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: copy, read+write)",
-                     "algorithmic_bytes_per_launch": cache_bytes},
-        "e2e": {"value": round(tot_bytes / (e2e_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms_max, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
-        "clocks": clk,
-        "wall_s_timed_region": round(wall, 3),
-        "step_times": step_time_summary(step_times),
-        "device_status_all_steps": status_all,
+                     "algorithmic_bytes_per_launch": r["cache_bytes"]},
+        "e2e": head["e2e"],
+        "gpu_launches": 3 * r["K"],
+        "clocks": r["clk"],
+        "wall_s_timed_region": round(r["wall"], 3),
+        "step_times": step_time_summary(r["step_times"]),
+        "device_status_all_steps": r["status_all"],
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if side_lines:
+        line["workloads"] = side_lines
     print(json.dumps(line), flush=True)
     if ws_ > 1:
         dist.destroy_process_group()
+
 
 
 def _gather_inputs(dev, rank=0):
@@ -483,8 +557,7 @@ def run_gather(args):
     def step(bt=wl.block_table, c=cu, out=dst):
         m.mla_gather_upconvert(wl.pool, wl.page_size, bt, c, out)
 
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks_bench_gather.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    clocks = ClockSampler(local, args.clock_csv)
     clocks.start()
     clocks.wait_first()
     for _ in range(args.warmup):
@@ -668,12 +741,25 @@ def oracle_sample(config, wl, budget_s=15.0):
     return done_bytes, secs, n, n / len(order), oracle.num_threads()
 
 
-def cpu_baseline(config, wl):
-    b, s, n, passes, th = oracle_sample(config, wl)
-    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": th, "kind": "oracle",
-            "sample": f"{n} whole-request decodes of the '{config}' workload ({passes:.2f} passes over its "
-                      f"{int((wl.seq_lens > 0).sum())} non-empty requests, {b // wl.row_bytes} context tokens, "
-                      f"{s:.1f} s), fp64 C oracle with OpenMP over (query, head)"}
+def cpu_baseline(config, wl, budget_s=15.0, one_thread=False):
+    """The oracle, as it stands, on whole requests of the workload for about
+    `budget_s` on all host cores; with `one_thread`, also a shorter run on
+    one thread (value_1_thread)."""
+    import oracle
+    b, s, n, passes, th = oracle_sample(config, wl, budget_s)
+    d = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": th, "kind": "oracle",
+         "sample": f"{n} whole-request decodes of the '{config}' workload ({passes:.2f} passes over its "
+                   f"{int((wl.seq_lens > 0).sum())} non-empty requests, {b // wl.row_bytes} context tokens, "
+                   f"{s:.1f} s), fp64 C oracle with OpenMP over (query, head)"}
+    if one_thread:
+        oracle.set_num_threads(1)
+        try:
+            b1, s1, n1, _, _ = oracle_sample(config, wl, budget_s / 5)
+        finally:
+            oracle.set_num_threads(th)
+        d["value_1_thread"] = round(b1 / s1 / 1e9, 4)
+        d["sample_1_thread"] = f"{n1} whole-request decodes, {b1 // wl.row_bytes} context tokens, {s1:.1f} s"
+    return d
 
 
 def run_reference(args):
@@ -687,8 +773,7 @@ def run_reference(args):
     import oracle
     import torch
     from mla_latent_kv_cache_gb300 import workloads as W
-    wl = W.CONFIGS["mtp" if args.config == "verify" else args.config](
-        device="cuda" if torch.cuda.is_available() else "cpu")
+    wl = build_workload(args.config, "cuda" if torch.cuda.is_available() else "cpu")
     sl = wl.seq_lens.cpu().numpy()
     live = [int(b) for b in range(wl.B) if sl[b] > 0]
     prep = {}
@@ -724,7 +809,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * ts / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.config, "shape": CONFIG_TEXT[args.config]},
+        "data": "synthetic (seeded N(0,1) bf16 rows, shuffled block tables, NaN-filled free slots)",
+        "config": config_dict(args.config, wl.context_tokens(), wl.cache_bytes(), wl.row_bytes, ws_),
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"each step: {budget} context tokens of the '{args.config}' workload, whole "
                                    f"requests taken in turn (the last cut to the budget), all "
@@ -738,7 +824,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=6000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="batched", choices=sorted(CONFIG_TEXT))
+    ap.add_argument("--config", default="mtp", choices=sorted(CONFIG_TEXT),
+                    help="the headline workload (default: mtp, the largest one-GPU configuration)")
+    ap.add_argument("--side", default=",".join(SIDE_WORKLOADS),
+                    help="comma-separated workloads measured after the headline one and reported under "
+                         "'workloads' in its line ('none' to skip)")
+    ap.add_argument("--clock-csv", default=None, help="write the headline run's nvidia-smi clock samples here")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()

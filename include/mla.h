@@ -71,15 +71,22 @@ MLA_API int mla_row_bytes(int cache_kind);
  *   slot_mapping  device, int64 [num_tokens]; a negative entry skips the token.
  *   cache         device, [num_slots, mla_row_bytes(cache_kind)] bytes, 16-byte
  *                 aligned. Rows not named by slot_mapping are left unchanged.
+ *   num_slots     rows in the pool. A slot_mapping entry >= num_slots is
+ *                 skipped on the device: nothing is written for that token,
+ *                 so a bad slot cannot write past the pool (the out-of-range
+ *                 access of "sabi-mla-vllm" README, "B300 fix (0.2.0)").
+ *   status        device, one int32 (4-byte aligned), or NULL. When given,
+ *                 the call ORs bit 2 (value 2, as in the decode status word)
+ *                 into it if it skipped a slot >= num_slots; it never clears
+ *                 it, so zero it before the calls it should cover.
  * fp8 rows: scale_j = absmax_j / 448 by IEEE fp32 division, each code is the
  * round-to-nearest-even, saturating e4m3 encoding of the fp32 quotient x /
  * scale_j. Two tokens mapped to the same slot race (the last write is
- * unspecified). Slots >= num_slots are undefined behaviour (not checked on
- * the device). Returns MLA_ERR_INVALID_ARG on bad sizes, pointers or strides.
+ * unspecified). Returns MLA_ERR_INVALID_ARG on bad sizes, pointers or strides.
  */
 MLA_API int mla_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
                     const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots,
-                    int cache_kind, void* stream);
+                    int cache_kind, int32_t* status, void* stream);
 
 /*
  * mla_gather_upconvert - the prefill-context gather of an fp8_ds_mla pool into
@@ -236,15 +243,34 @@ MLA_API int mla_num_sms(void);
  *   Nothing in the scratch has to start at zero: each CTA clears its own
  *   status record and the merge step rewrites the status header.
  *   The first call on a device looks the array up (cudaGetSymbolAddress, which
- *   may load the device code); make it before any stream capture. Calls share
- *   one array per device, so calls that can overlap (different streams, or
- *   several host threads) race on it: order them on one stream.
+ *   may load the device code); make it before any stream capture. The address
+ *   is kept per device ordinal for the life of the process, so the library
+ *   must not be used across a cudaDeviceReset (or any other teardown of the
+ *   device's primary context). Calls share one array per device, so calls
+ *   that can overlap (different streams, or several host threads) race on
+ *   it: order them on one stream.
+ *   The device-side status words that mla_decode leaves in its workspace
+ *   header land in the scratch here; mla_static_scratch_status copies them
+ *   out.
  */
 #define MLA_STATIC_SCRATCH_BYTES (64u << 20)
 MLA_API int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const void* cache, int cache_kind,
                                       int64_t num_slots, int page_size, const int32_t* block_table,
                                       int64_t block_table_stride, const int32_t* seq_lens, int B, int q_len, int Hq,
                                       float scale, void* out, int out_dtype, float* lse, int num_ctas, void* stream);
+
+/*
+ * mla_static_scratch_status - copy the first n (1..12) int32 status words of
+ * the static scratch into dst, in stream order: after the last
+ * mla_decode_static_scratch call on this device they are the words
+ * mla_decode documents for its workspace header (word 0: bit 1 = a bounded
+ * wait gave up and the outputs are invalid, bit 2 = a block-table entry
+ * outside the pool; words 1..11 where). dst is device memory or pinned host
+ * memory (one cudaMemcpyAsync, direction inferred); it allocates nothing.
+ * Before any static-scratch call on the device the words are undefined.
+ * Returns MLA_ERR_INVALID_ARG for a null dst or n outside 1..12.
+ */
+MLA_API int mla_static_scratch_status(int32_t* dst, int n, void* stream);
 
 /*
  * mla_test_hold_next_decode - test support for the device-side failure path.

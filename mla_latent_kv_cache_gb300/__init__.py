@@ -55,7 +55,7 @@ def load() -> ctypes.CDLL:
             lib.mla_status_string.restype = ctypes.c_char_p
             lib.mla_num_sms.argtypes = []
             lib.mla_num_sms.restype = i32
-            lib.mla_cache_write.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp]
+            lib.mla_cache_write.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, vp]
             lib.mla_cache_write.restype = i32
             lib.mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
             lib.mla_decode_workspace_bytes.restype = sz
@@ -65,6 +65,8 @@ def load() -> ctypes.CDLL:
             lib.mla_decode_static_scratch.argtypes = [vp, vp, vp, i32, i64, i32, vp, i64, vp, i32, i32, i32, f32, vp,
                                                       i32, vp, i32, vp]
             lib.mla_decode_static_scratch.restype = i32
+            lib.mla_static_scratch_status.argtypes = [vp, i32, vp]
+            lib.mla_static_scratch_status.restype = i32
             lib.mla_test_hold_next_decode.argtypes = []
             lib.mla_test_hold_next_decode.restype = None
             lib.mla_test_slow_pv_next_decode.argtypes = []
@@ -109,18 +111,22 @@ def mla_num_sms() -> int:
 
 
 def mla_cache_write(latent: torch.Tensor, k_pe: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor,
-                    cache_kind: int = MLA_CACHE_BF16_576, stream=None) -> None:
+                    cache_kind: int = MLA_CACHE_BF16_576, stream=None, status: torch.Tensor = None) -> None:
     """latent [T,512] bf16, k_pe [T,64] bf16 (row-strided views allowed),
     slot_mapping [T] int64 (-1 = skip), cache [num_slots, row_bytes] (any dtype
-    viewable as bytes). Scatters rows in place."""
+    viewable as bytes). Scatters rows in place; slots >= num_slots are skipped
+    and, when `status` (a device int32 tensor) is given, OR bit 2 into its
+    first element."""
     assert latent.dtype == torch.bfloat16 and k_pe.dtype == torch.bfloat16
     assert latent.stride(-1) == 1 and k_pe.stride(-1) == 1 and slot_mapping.dtype == torch.int64
+    assert status is None or status.dtype == torch.int32
     T = slot_mapping.numel()
     nbytes = cache.numel() * cache.element_size()
     rb = mla_row_bytes(cache_kind)
     _check(load().mla_cache_write(latent.data_ptr(), latent.stride(0) if latent.dim() == 2 else 512,
                                   k_pe.data_ptr(), k_pe.stride(0) if k_pe.dim() == 2 else 64,
                                   slot_mapping.data_ptr(), T, cache.data_ptr(), nbytes // rb, cache_kind,
+                                  status.data_ptr() if status is not None else None,
                                   _stream(stream)), "mla_cache_write")
 
 
@@ -200,6 +206,16 @@ def mla_decode_static_scratch(q_lat, q_pe, cache, cache_kind, page_size, block_t
                                             seq_lens.data_ptr(), B, q_len, Hq, float(scale), out.data_ptr(),
                                             out_dtype, lse.data_ptr(), num_ctas, _stream(stream)),
            "mla_decode_static_scratch")
+
+
+def static_scratch_status_words(n: int = 12, stream=None) -> list:
+    """The status words the last mla_decode_static_scratch call on the
+    current device left in the static scratch (mla_static_scratch_status):
+    word 0 status bits, words 1..11 where a wait gave up (as
+    device_status_words for a caller workspace)."""
+    dst = torch.zeros(n, dtype=torch.int32, device=torch.cuda.current_device())
+    _check(load().mla_static_scratch_status(dst.data_ptr(), n, _stream(stream)), "mla_static_scratch_status")
+    return [int(v) for v in dst.tolist()]
 
 
 def mla_merge_lse(part_out: torch.Tensor, part_lse: torch.Tensor, out: torch.Tensor, lse=None, stream=None) -> None:

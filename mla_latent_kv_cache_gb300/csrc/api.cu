@@ -144,7 +144,7 @@ int mla_num_sms(void) {
 
 int mla_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
                     const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots, int cache_kind,
-                    void* stream) {
+                    int32_t* status, void* stream) {
     if (num_tokens < 0 || num_slots < 0) return MLA_ERR_INVALID_ARG;
     if (cache_kind != MLA_CACHE_BF16_576 && cache_kind != MLA_CACHE_FP8_DS_MLA_656) return MLA_ERR_INVALID_ARG;
     if (num_tokens == 0) return MLA_OK;
@@ -152,8 +152,9 @@ int mla_cache_write(const void* latent, int64_t latent_stride, const void* k_pe,
     if (!aligned16(latent) || !aligned16(k_pe) || !aligned16(cache)) return MLA_ERR_INVALID_ARG;
     if (latent_stride < mla::kD || latent_stride % 8 || k_pe_stride < mla::kP || k_pe_stride % 8)
         return MLA_ERR_INVALID_ARG;
+    if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MLA_ERR_INVALID_ARG;
     cudaError_t e = mla::launch_cache_write(latent, latent_stride, k_pe, k_pe_stride, slot_mapping, num_tokens, cache,
-                                            cache_kind, static_cast<cudaStream_t>(stream));
+                                            num_slots, cache_kind, status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -377,6 +378,15 @@ int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const void* c
     return mla_decode(q_lat, q_pe, cache, cache_kind, num_slots, page_size, block_table, block_table_stride,
                       seq_lens, B, q_len, Hq, scale, out, out_dtype, lse, scratch, MLA_STATIC_SCRATCH_BYTES,
                       num_ctas, stream);
+}
+
+int mla_static_scratch_status(int32_t* dst, int n, void* stream) {
+    if (!dst || n < 1 || n > 12) return MLA_ERR_INVALID_ARG;
+    void* scratch = decode_scratch_ptr();
+    if (!scratch) return MLA_ERR_CUDA;
+    cudaError_t e = cudaMemcpyAsync(dst, scratch, static_cast<size_t>(n) * sizeof(int32_t), cudaMemcpyDefault,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 void mla_test_hold_next_decode(void) { g_test_hold.store(1); }

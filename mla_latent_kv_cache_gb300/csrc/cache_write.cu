@@ -6,7 +6,11 @@
 // latent divided by a per-128-block scale absmax/448, the four fp32 scales and
 // the bf16 k_pe (vLLM PR #55543 commit 5.1-5.4 and PR description "Approach").
 //
-// One warp per token; every row offset is slot * row_bytes in 64-bit.
+// One warp per token; every row offset is slot * row_bytes in 64-bit. A slot
+// at or past num_slots is skipped on the device (nothing is written for that
+// token) and, when the caller passes a status word, sets its bit 2: an
+// out-of-range slot is the illegal memory access of the "sabi-mla-vllm"
+// README, "B300 fix (0.2.0)", and the write must not reach past the pool.
 #include "launch.cuh"
 #include "mla_common.cuh"
 
@@ -17,12 +21,17 @@ __global__ void __launch_bounds__(256) cache_write_bf16_kernel(const __nv_bfloat
                                                                const __nv_bfloat16* __restrict__ k_pe,
                                                                int64_t k_pe_stride,
                                                                const int64_t* __restrict__ slot_mapping,
-                                                               int64_t num_tokens, uint8_t* __restrict__ cache) {
+                                                               int64_t num_tokens, uint8_t* __restrict__ cache,
+                                                               int64_t num_slots, int* __restrict__ status) {
     const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= num_tokens) return;
     const int64_t slot = slot_mapping[t];
     if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (lane == 0 && status) atomicOr(status, kErrBadBlock);
+        return;
+    }
     uint8_t* row = cache + slot * static_cast<int64_t>(kRowBf16);
     const uint4* src_l = reinterpret_cast<const uint4*>(latent + t * latent_stride);
     const uint4* src_r = reinterpret_cast<const uint4*>(k_pe + t * k_pe_stride);
@@ -40,12 +49,17 @@ __global__ void __launch_bounds__(256) cache_write_fp8_kernel(const __nv_bfloat1
                                                               const __nv_bfloat16* __restrict__ k_pe,
                                                               int64_t k_pe_stride,
                                                               const int64_t* __restrict__ slot_mapping,
-                                                              int64_t num_tokens, uint8_t* __restrict__ cache) {
+                                                              int64_t num_tokens, uint8_t* __restrict__ cache,
+                                                              int64_t num_slots, int* __restrict__ status) {
     const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= num_tokens) return;
     const int64_t slot = slot_mapping[t];
     if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (lane == 0 && status) atomicOr(status, kErrBadBlock);
+        return;
+    }
     uint8_t* row = cache + slot * static_cast<int64_t>(kRowFp8);
     // lane owns latent values [16*lane, 16*lane+16); lanes 8j..8j+7 form block j
     const uint4* src = reinterpret_cast<const uint4*>(latent + t * latent_stride) + 2 * lane;
@@ -162,19 +176,21 @@ cudaError_t launch_gather_upconvert(const void* cache, int64_t num_slots, int pa
 }
 
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
-                               const int64_t* slot_mapping, int64_t num_tokens, void* cache, int kind,
-                               cudaStream_t stream) {
+                               const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots,
+                               int kind, int* status, cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;
     const int64_t blocks = (num_tokens + 7) / 8;
     const dim3 grid(static_cast<unsigned>(blocks));
     if (kind == 0)
         cache_write_bf16_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(latent), latent_stride,
                                                           static_cast<const __nv_bfloat16*>(k_pe), k_pe_stride,
-                                                          slot_mapping, num_tokens, static_cast<uint8_t*>(cache));
+                                                          slot_mapping, num_tokens, static_cast<uint8_t*>(cache),
+                                                          num_slots, status);
     else
         cache_write_fp8_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(latent), latent_stride,
                                                          static_cast<const __nv_bfloat16*>(k_pe), k_pe_stride,
-                                                         slot_mapping, num_tokens, static_cast<uint8_t*>(cache));
+                                                         slot_mapping, num_tokens, static_cast<uint8_t*>(cache),
+                                                         num_slots, status);
     return cudaGetLastError();
 }
 

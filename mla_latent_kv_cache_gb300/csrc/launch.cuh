@@ -40,8 +40,8 @@ struct DecodeParams {
 };
 
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
-                               const int64_t* slot_mapping, int64_t num_tokens, void* cache, int kind,
-                               cudaStream_t stream);
+                               const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots,
+                               int kind, int* status, cudaStream_t stream);
 // Context gather of an fp8_ds_mla pool into bf16 rows (mla_gather_upconvert).
 cudaError_t launch_gather_upconvert(const void* cache, int64_t num_slots, int page_size, const int32_t* block_table,
                                     int64_t bt_stride, const int32_t* cu_seq_lens, int B, int64_t num_rows, void* dst,

@@ -87,6 +87,8 @@ def _load():
             lib.oracle_gather_upconvert.restype = i32
             lib.oracle_row_values.restype = i32
             lib.oracle_num_threads.restype = i32
+            lib.oracle_set_num_threads.argtypes = [i32]
+            lib.oracle_set_num_threads.restype = None
             lib.oracle_row_bytes.argtypes = [i32]
             lib.oracle_row_bytes.restype = i32
             _lib = lib
@@ -123,6 +125,12 @@ def _as_np(a, dtype) -> np.ndarray:
 def num_threads() -> int:
     """OpenMP threads the decode loop runs on (OMP_NUM_THREADS)."""
     return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the decode loops use from now on (the CPU-baseline leg times
+    one thread as well as all of them)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def row_values() -> int:

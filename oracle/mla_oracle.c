@@ -450,6 +450,16 @@ void oracle_merge(const float *part_o, const float *part_lse, int S, int64_t N,
     }
 }
 
+/* Sets the threads the decode loops use from now on (no effect without
+ * OpenMP); n < 1 is ignored. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Threads the decode loop uses (1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

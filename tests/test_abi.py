@@ -43,11 +43,12 @@ def test_status_strings(lib):
 
 def test_host_validation_rejects_bad_arguments(lib):
     # every one of these is rejected on the host before any CUDA call
-    assert lib.mla_cache_write(None, 512, None, 64, None, -1, None, 10, 0, None) == m.MLA_ERR_INVALID_ARG
-    assert lib.mla_cache_write(None, 512, None, 64, None, 0, None, 10, 0, None) == m.MLA_OK  # nothing to do
-    assert lib.mla_cache_write(16, 512, 16, 64, 16, 4, 16, 10, 5, None) == m.MLA_ERR_INVALID_ARG  # kind
-    assert lib.mla_cache_write(16, 500, 16, 64, 16, 4, 16, 10, 0, None) == m.MLA_ERR_INVALID_ARG  # stride
-    assert lib.mla_cache_write(8, 512, 16, 64, 16, 4, 16, 10, 0, None) == m.MLA_ERR_INVALID_ARG   # alignment
+    assert lib.mla_cache_write(None, 512, None, 64, None, -1, None, 10, 0, None, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_cache_write(None, 512, None, 64, None, 0, None, 10, 0, None, None) == m.MLA_OK  # nothing to do
+    assert lib.mla_cache_write(16, 512, 16, 64, 16, 4, 16, 10, 5, None, None) == m.MLA_ERR_INVALID_ARG  # kind
+    assert lib.mla_cache_write(16, 500, 16, 64, 16, 4, 16, 10, 0, None, None) == m.MLA_ERR_INVALID_ARG  # stride
+    assert lib.mla_cache_write(8, 512, 16, 64, 16, 4, 16, 10, 0, None, None) == m.MLA_ERR_INVALID_ARG   # alignment
+    assert lib.mla_cache_write(16, 512, 16, 64, 16, 4, 16, 10, 0, 18, None) == m.MLA_ERR_INVALID_ARG    # status word
     args = [16, 16, 16, 0, 100, 16, 16, 4, 16, 2, 1, 8, 0.1, 16, 0, 16, 256, 1 << 20, 0, None]
     bad = list(args)
     bad[9] = 0                                                     # B = 0
@@ -63,6 +64,9 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mla_decode(*bad) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_lse(16, 16, -1, 4, 16, 0, 16, None) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_lse(16, 16, 2, 0, 16, 0, 16, None) == m.MLA_OK
+    assert lib.mla_static_scratch_status(None, 12, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_static_scratch_status(16, 0, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_static_scratch_status(16, 13, None) == m.MLA_ERR_INVALID_ARG
     # mla_decode_varlen(q_lat, q_pe, total_q, cache, kind, num_slots, page_size, bt, bt_stride, seq_lens, cu_q, B,
     #                   max_q_len, Hq, scale, out, out_dtype, lse, ws, ws_bytes, num_ctas, stream)
     v = [16, 16, 6, 16, 0, 100, 16, 16, 4, 16, 16, 2, 3, 8, 0.1, 16, 0, 16, 256, 1 << 20, 0, None]

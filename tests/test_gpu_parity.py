@@ -118,6 +118,33 @@ def test_cache_write_bit_exact_incl_high_slots(kind):
     assert bool((pool[mask] == 0xA5).all())
 
 
+@pytest.mark.parametrize("kind", [0, 1])
+def test_cache_write_skips_slots_past_the_pool(kind):
+    """Slots at or past num_slots are skipped on the device and reported in
+    the status word. The pool is a view of the front of a larger allocation,
+    so even an unguarded write would land in mapped memory: the test checks
+    that the bytes past the pool are unchanged."""
+    rb = W.ROW_BYTES[kind]
+    n = 64
+    big = torch.full((n + 8, rb), 0x5A, dtype=torch.uint8, device=DEV)
+    pool = big[:n]
+    lat, kpe = _write_inputs(5, 40 + kind)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sm = torch.tensor([3, n, n + 5, -1, n - 1], dtype=torch.int64, device=DEV)
+    m.mla_cache_write(lat, kpe, sm, pool, kind, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
+    assert bool((big[n:] == 0x5A).all())
+    ref = np.full((n, rb), 0x5A, dtype=np.uint8)
+    oracle.cache_write(lat[[0, 4]].cpu(), kpe[[0, 4]].cpu(), np.array([3, n - 1]), ref, kind)
+    assert np.array_equal(pool.cpu().numpy(), ref)
+    # in-range slots only: the status word stays clear
+    status.zero_()
+    m.mla_cache_write(lat[:1], kpe[:1], sm[:1], pool, kind, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
 def test_fp8_encoder_on_every_bf16_value():
     """Blocks whose absmax is 448 have scale 1, so codes are the e4m3
     encoding of the bf16 inputs themselves: compare every finite bf16 value
@@ -276,14 +303,14 @@ def test_named_workload_sampled(name):
     if name == "batched":
         reqs = _sample(wl, [5, 40])
     elif name == "long":
-        reqs = [2]
+        reqs = [0, 1, 2, 3]
     elif name == "mtp":
         # the empty and one-token requests, and the request holding the last pool slot
         zero_one = [int(i) for i in np.nonzero(sl <= 1)[0]][:6]
         last = int(np.nonzero((wl.block_table == wl.num_slots // wl.page_size - 1).any(dim=1).cpu().numpy())[0][0])
         reqs = sorted(set(zero_one + [last, 3]))
     else:
-        reqs = [9]
+        reqs = [0, 9, 17, 26, 33, 41, 50, 63]
     o, l, rows = oracle_step(wl, reqs)
     out, lse = run_step(wl)
     check_decode(out, lse, o, l, rows, kind=wl.kind, what=name)

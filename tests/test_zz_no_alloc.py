@@ -40,10 +40,19 @@ def _reference(wl, out_dtype):
     return out, lse
 
 
-def _static(wl, out_dtype):
+def _reference_ctas(wl, out_dtype, num_ctas):
+    out, lse = _outputs(wl, out_dtype)
+    ws = torch.empty(m.mla_decode_workspace_bytes(wl.seq_lens.numel(), wl.Qt, wl.q_lat.shape[-2], num_ctas),
+                     dtype=torch.uint8, device=DEV)
+    m.mla_decode(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens, wl.Qt, wl.scale,
+                 out, lse, ws, num_ctas)
+    return out, lse
+
+
+def _static(wl, out_dtype, num_ctas=0):
     out, lse = _outputs(wl, out_dtype)
     m.mla_decode_static_scratch(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens,
-                                wl.Qt, wl.scale, out, lse)
+                                wl.Qt, wl.scale, out, lse, num_ctas)
     return out, lse
 
 
@@ -96,3 +105,39 @@ def test_oversized_call_is_rejected_before_any_launch():
     assert "static decode scratch" in m.mla_status_string(MLA_ERR_SCRATCH_LIMIT)
     torch.cuda.synchronize()
     assert torch.count_nonzero(out) == 0  # nothing ran
+
+
+def test_other_kernels_reuse_the_scratch():
+    # an fp8 pool at 64 query rows (the cluster kernel with its expand warps),
+    # split over a CTA count of its own, after a bf16 call that left a larger
+    # partial-slot layout behind; then odd page sizes (load/convert warps)
+    wb = W.batched(device=DEV)
+    w8 = W.make("fp8_small", B=3, Hq=64, Qt=1, page_size=64, seq_lens=[3000, 1, 4500], kind=W.KIND_FP8,
+                write_all=True, seed=31, device=DEV)
+    wo = W.make("odd_pages", B=4, Hq=16, Qt=4, page_size=3, seq_lens=[0, 2, 900, 2100], seed=32, device=DEV)
+    for wl in (wb, w8, wo):
+        m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+    ref = [_reference(wb, torch.bfloat16), _reference_ctas(w8, torch.float32, 12),
+           _reference_ctas(wo, torch.float32, 10)]
+    got = [_static(wb, torch.bfloat16), _static(w8, torch.float32, 12), _static(wo, torch.float32, 10)]
+    torch.cuda.synchronize()
+    for (go, gl), (ro, rl) in zip(got, ref):
+        assert torch.equal(go, ro) and torch.equal(gl, rl)
+    assert m.static_scratch_status_words()[0] == 0
+
+
+def test_status_words_of_a_static_call():
+    # a bounded wait that gives up inside a static-scratch call is reported
+    # through mla_static_scratch_status; the next call clears it
+    wl = W.make("hold_static", B=3, Hq=16, Qt=1, page_size=16, seq_lens=[700, 1500, 300], seed=93, device=DEV)
+    m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+    ref = _reference(wl, torch.float32)
+    m.test_hold_next_decode()
+    _static(wl, torch.float32)
+    torch.cuda.synchronize()
+    words = m.static_scratch_status_words()
+    assert words[0] & 1 and words[1] != 0, words
+    got = _static(wl, torch.float32)
+    torch.cuda.synchronize()
+    assert m.static_scratch_status_words()[0] == 0
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
