@@ -240,12 +240,18 @@ def config_dict(name, ctx_tokens, cache_bytes, row_bytes, ws_):
             "parallelism": f"replicas x{ws_} (requests are independent)"}
 
 
-def build_workload(name, dev, rank=0):
+def build_workload(name, dev, rank=0, requests=None):
     """The named workload on `dev` (verify: the mtp workload's pool and
-    requests), seeded per rank."""
+    requests), seeded per rank. `requests` (long and fp8 only) keeps that
+    many of their equal-length requests: a cut-down copy for profiling."""
     from mla_latent_kv_cache_gb300 import workloads as W
     base = "mtp" if name == "verify" else name
-    return W.CONFIGS[base](device=dev, seed=WORKLOAD_SEED[base] + 1000 * rank)
+    kw = {}
+    if requests is not None:
+        if base not in ("long", "fp8"):
+            raise SystemExit("--requests applies to the long and fp8 workloads only")
+        kw["B"] = int(requests)
+    return W.CONFIGS[base](device=dev, seed=WORKLOAD_SEED[base] + 1000 * rank, **kw)
 
 
 def measure_gpu(name, args, dev, rank, ws_, clock_csv=None):
@@ -258,7 +264,7 @@ def measure_gpu(name, args, dev, rank, ws_, clock_csv=None):
     import mla_latent_kv_cache_gb300 as m
 
     varlen = name == "verify"
-    wl = build_workload(name, dev, rank)
+    wl = build_workload(name, dev, rank, args.requests if name == args.config else None)
     cu_q = None
     q_lat_s, q_pe_s = wl.q_lat, wl.q_pe  # the step's query rows
     if varlen:
@@ -467,6 +473,8 @@ def run_gpu(args):
             dist.destroy_process_group()
         return
     cfg = config_dict(args.config, r["ctx_tokens"], r["cache_bytes"], row_bytes, ws_)
+    if args.requests is not None:
+        cfg["cut_down"] = f"first {args.requests} requests only (profiling case)"
     line = {
         "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": ws_, "steps": r["K"],
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
@@ -830,6 +838,9 @@ def main():
                     help="comma-separated workloads measured after the headline one and reported under "
                          "'workloads' in its line ('none' to skip)")
     ap.add_argument("--clock-csv", default=None, help="write the headline run's nvidia-smi clock samples here")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="long / fp8 headline only: keep this many requests (a cut-down case for profiling; "
+                         "the line then describes that case, not the named workload)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()

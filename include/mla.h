@@ -185,6 +185,44 @@ MLA_API int mla_decode(const void* q_lat, const void* q_pe, const void* cache, i
                size_t workspace_bytes, int num_ctas, void* stream);
 
 /*
+ * Other latent widths ("qwen-mla-vllm" README, "How it works": the
+ * full-attention layers cache a per-layer latent of rank 256, 768 or 1792
+ * plus a small rotary and normalisation tail). A row is bf16
+ * [latent D | rope 64], 2 (D + 64) bytes; the normalisation is applied before
+ * a row is cached, so the decode is mla_decode's definition with D latent
+ * values in place of 512. D = 512 is the 576-wide row of mla_cache_write /
+ * mla_decode.
+ *
+ * mla_cache_write_latent - mla_cache_write for bf16 rows of latent width
+ * lat_dim (256, 512, 768 or 1792): latent [num_tokens, lat_dim] (row stride
+ * latent_stride >= lat_dim, a multiple of 8), k_pe, slot_mapping, num_slots
+ * and status as for mla_cache_write, cache [num_slots, 2 (lat_dim + 64)]
+ * bytes, 16-byte aligned. Rows are bit copies.
+ *
+ * mla_decode_latent_workspace_bytes - the workspace of mla_decode_latent
+ * (0 for invalid sizes): the mla_decode layout with lat_dim-wide partials.
+ *
+ * mla_decode_latent - mla_decode over such rows: q_lat [B*q_len, Hq, lat_dim],
+ * q_pe [B*q_len, Hq, 64], out [B*q_len, Hq, lat_dim] (bf16 or fp32), lse
+ * [B*q_len, Hq]; the visibility rule, the (0, -inf) rows, the status words
+ * and every other argument as mla_decode with a bf16 pool. Each CTA works on
+ * 64-token tiles whose rows are folded into two halves (as mla_decode's bf16
+ * path at up to 32 query rows); at lat_dim 1792 the two CTAs of a cluster
+ * each hold one 896-value half of every row and exchange partial scores.
+ * Supported: lat_dim 256 or 512 with Hq * q_len <= 32, lat_dim 768 or 1792
+ * with Hq * q_len <= 16, page_size a multiple of 8; otherwise
+ * MLA_ERR_UNSUPPORTED before any launch.
+ */
+MLA_API int mla_cache_write_latent(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
+                                   const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots,
+                                   int lat_dim, int32_t* status, void* stream);
+MLA_API size_t mla_decode_latent_workspace_bytes(int B, int q_len, int Hq, int lat_dim, int num_ctas);
+MLA_API int mla_decode_latent(const void* q_lat, const void* q_pe, const void* cache, int lat_dim, int64_t num_slots,
+                              int page_size, const int32_t* block_table, int64_t block_table_stride,
+                              const int32_t* seq_lens, int B, int q_len, int Hq, float scale, void* out, int out_dtype,
+                              float* lse, void* workspace, size_t workspace_bytes, int num_ctas, void* stream);
+
+/*
  * mla_decode_varlen - mla_decode for a batch whose requests verify different
  * numbers of tokens (a chunked verify step: "qwen-mla-vllm" README,
  * "Speculative decoding (MTP)", a verify step of 1 + k tokens reads the latent

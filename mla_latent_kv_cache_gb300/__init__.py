@@ -7,8 +7,11 @@ exceptions. There is no fallback: if the library is missing, every call
 raises.
 
 Entry points mirror ``include/mla.h``:
-  mla_cache_write, mla_decode_workspace_bytes, mla_decode, mla_merge_lse,
-  mla_num_sms, mla_row_bytes, mla_status_string.
+  mla_cache_write, mla_decode_workspace_bytes, mla_decode, mla_decode_varlen,
+  mla_merge_lse, mla_gather_upconvert, mla_cache_write_latent,
+  mla_decode_latent_workspace_bytes, mla_decode_latent,
+  mla_decode_static_scratch (+ mla_static_scratch_status), mla_num_sms,
+  mla_row_bytes, mla_status_string.
 ``decode(...)`` is a convenience wrapper that allocates the outputs and the
 workspace with torch and calls ``mla_decode``.
 """
@@ -77,6 +80,13 @@ def load() -> ctypes.CDLL:
             lib.mla_decode_varlen.restype = i32
             lib.mla_gather_upconvert.argtypes = [vp, i64, i32, vp, i64, vp, i32, i64, vp, i64, vp]
             lib.mla_gather_upconvert.restype = i32
+            lib.mla_cache_write_latent.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, vp]
+            lib.mla_cache_write_latent.restype = i32
+            lib.mla_decode_latent_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            lib.mla_decode_latent_workspace_bytes.restype = sz
+            lib.mla_decode_latent.argtypes = [vp, vp, vp, i32, i64, i32, vp, i64, vp, i32, i32, i32, f32, vp, i32,
+                                              vp, vp, sz, i32, vp]
+            lib.mla_decode_latent.restype = i32
             lib.mla_merge_lse.restype = i32
             _lib = lib
     return _lib
@@ -163,6 +173,49 @@ def mla_gather_upconvert(cache: torch.Tensor, page_size: int, block_table: torch
                                      block_table.stride(0), cu_seq_lens.data_ptr(), cu_seq_lens.shape[0] - 1, rows,
                                      dst.data_ptr(), dst.stride(0), _stream(stream))
     _check(st, "mla_gather_upconvert")
+
+
+def mla_cache_write_latent(latent, k_pe, slot_mapping, cache, lat_dim, stream=None, status=None) -> None:
+    """bf16 rows [latent lat_dim | rope 64] (include/mla.h): latent
+    [T, lat_dim] bf16, k_pe [T, 64] bf16, slot_mapping [T] int64, cache
+    [num_slots, 2 (lat_dim + 64)] bytes."""
+    T = slot_mapping.numel()
+    assert latent.dtype == torch.bfloat16 and k_pe.dtype == torch.bfloat16 and slot_mapping.dtype == torch.int64
+    assert latent.stride(-1) == 1 and k_pe.stride(-1) == 1
+    assert status is None or status.dtype == torch.int32
+    row_bytes = 2 * (lat_dim + 64)
+    nbytes = cache.numel() * cache.element_size()
+    _check(load().mla_cache_write_latent(latent.data_ptr(), latent.stride(0), k_pe.data_ptr(), k_pe.stride(0),
+                                         slot_mapping.data_ptr(), T, cache.data_ptr(), nbytes // row_bytes,
+                                         int(lat_dim), status.data_ptr() if status is not None else None,
+                                         _stream(stream)), "mla_cache_write_latent")
+
+
+def mla_decode_latent_workspace_bytes(B: int, q_len: int, Hq: int, lat_dim: int, num_ctas: int = 0) -> int:
+    n = load().mla_decode_latent_workspace_bytes(B, q_len, Hq, lat_dim, num_ctas)
+    if n == 0:
+        raise MlaError(MLA_ERR_INVALID_ARG, "mla_decode_latent_workspace_bytes")
+    return n
+
+
+def mla_decode_latent(q_lat, q_pe, cache, lat_dim, page_size, block_table, seq_lens, q_len, scale, out, lse,
+                      workspace, num_ctas: int = 0, stream=None) -> None:
+    """Decode over bf16 rows of latent width lat_dim (include/mla.h):
+    q_lat [B*q_len, Hq, lat_dim], out [B*q_len, Hq, lat_dim]."""
+    B = seq_lens.numel()
+    Hq = q_lat.shape[-2]
+    assert q_lat.shape[-1] == lat_dim and q_pe.shape[-1] == 64 and out.shape[-1] == lat_dim
+    assert q_lat.is_contiguous() and q_pe.is_contiguous() and out.is_contiguous() and lse.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1 and seq_lens.dtype == torch.int32
+    out_dtype = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
+    row_bytes = 2 * (lat_dim + 64)
+    nbytes = cache.numel() * cache.element_size()
+    _check(load().mla_decode_latent(q_lat.data_ptr(), q_pe.data_ptr(), cache.data_ptr(), int(lat_dim),
+                                    nbytes // row_bytes, int(page_size), block_table.data_ptr(),
+                                    block_table.stride(0), seq_lens.data_ptr(), B, int(q_len), Hq, float(scale),
+                                    out.data_ptr(), out_dtype, lse.data_ptr(), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(), int(num_ctas), _stream(stream)),
+           "mla_decode_latent")
 
 
 def mla_decode_workspace_bytes(B: int, q_len: int, Hq: int, num_ctas: int = 0) -> int:

@@ -74,7 +74,7 @@ struct WsLayout {
     size_t rec_off, lse_off, o_off, total;
 };
 
-WsLayout decode_ws_layout(int B, int HQ, int ctas) {
+WsLayout decode_ws_layout(int B, int HQ, int ctas, int D = 512) {
     const size_t GY = (static_cast<size_t>(HQ) + 63) / 64;
     const size_t slots = GY * static_cast<size_t>(ctas + B) * 64;
     const size_t rec_bytes = (static_cast<size_t>(ctas) * GY * mla::kStatusRecWords * sizeof(int) + 255) / 256 * 256;
@@ -83,7 +83,7 @@ WsLayout decode_ws_layout(int B, int HQ, int ctas) {
     l.rec_off = kWsHeader;
     l.lse_off = l.rec_off + rec_bytes;
     l.o_off = l.lse_off + lse_bytes;
-    l.total = l.o_off + slots * 512 * sizeof(float);
+    l.total = l.o_off + slots * static_cast<size_t>(D) * sizeof(float);
     return l;
 }
 
@@ -91,7 +91,7 @@ WsLayout decode_ws_layout(int B, int HQ, int ctas) {
 // one cluster of two.
 int ws_ctas(int num_ctas, int sms) { return num_ctas > 0 ? (num_ctas < 2 ? 2 : num_ctas) : (sms < 2 ? 2 : sms); }
 
-size_t decode_ws_bytes(int B, int HQ, int ctas) { return decode_ws_layout(B, HQ, ctas).total; }
+size_t decode_ws_bytes(int B, int HQ, int ctas, int D = 512) { return decode_ws_layout(B, HQ, ctas, D).total; }
 
 // Set by mla_test_hold_next_decode (1) or mla_test_slow_pv_next_decode (2),
 // consumed by the next mla_decode.
@@ -193,7 +193,8 @@ namespace {
 int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void* cache, int cache_kind,
                 int64_t num_slots, int page_size, const int32_t* block_table, int64_t block_table_stride,
                 const int32_t* seq_lens, const int32_t* cu_q, int B, int q_len, int Hq, float scale, void* out,
-                int out_dtype, float* lse, void* workspace, size_t workspace_bytes, int num_ctas, void* stream) {
+                int out_dtype, float* lse, void* workspace, size_t workspace_bytes, int num_ctas, void* stream,
+                int D = 512) {
     if (B <= 0 || q_len <= 0 || Hq <= 0 || page_size <= 0 || num_slots <= 0 || num_ctas < 0 || total_q <= 0)
         return MLA_ERR_INVALID_ARG;
     if (num_slots > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
@@ -225,12 +226,14 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     // bf16 pools with up to 32 query rows: folded 64-token tiles, one CTA per
     // worker; otherwise 128-token tiles split over clusters of two CTAs
     const bool fold = !lsu && cache_kind == MLA_CACHE_BF16_576 && NP <= 32;
+    // other latent widths: bf16 rows of D + 64 values, folded tiles only
+    if (D != 512 && (!fold || !mla::fold_supported(NP, D))) return MLA_ERR_UNSUPPORTED;
     const int nctas = ws_ctas(num_ctas, di.sms);  // what the workspace holds records and slots for
-    int W = fold ? mla::decode_fold_ctas(NP, num_ctas) : mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
+    int W = fold ? mla::decode_fold_ctas(NP, D, num_ctas) : mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
     if (W <= 0) return MLA_ERR_CUDA;
-    W = std::min(W, fold ? nctas : nctas / 2);
+    W = std::min(W, (fold && !mla::fold_is_pair(D)) ? nctas : nctas / 2);
     const int tile = fold ? 64 : 128;
-    const WsLayout wl = decode_ws_layout(B, HQ, nctas);
+    const WsLayout wl = decode_ws_layout(B, HQ, nctas, D);
     if (workspace_bytes < wl.total) return MLA_ERR_WORKSPACE;
 
     // Two TMA descriptors over the pool [num_slots, 576] bf16: 64-dim latent
@@ -245,8 +248,8 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     {
         // queries: q_lat [total_q * Hq, 512] and q_pe [total_q * Hq, 64] bf16, NP-row boxes
         const cuuint64_t rows = static_cast<cuuint64_t>(total_q) * Hq;
-        cuuint64_t gq[2] = {static_cast<cuuint64_t>(mla::kD), rows};
-        cuuint64_t sq[1] = {static_cast<cuuint64_t>(mla::kD * 2)};
+        cuuint64_t gq[2] = {static_cast<cuuint64_t>(D), rows};
+        cuuint64_t sq[1] = {static_cast<cuuint64_t>(D) * 2};
         cuuint64_t gp[2] = {64u, rows};
         cuuint64_t sp[1] = {128u};
         cuuint32_t estride[2] = {1u, 1u};
@@ -266,11 +269,11 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
         // never crosses a page
         const int br = gcd_int(page_size, tile);
         const bool fp8 = cache_kind == MLA_CACHE_FP8_DS_MLA_656;
-        const cuuint64_t row_bytes = fp8 ? mla::kRowFp8 : mla::kRowBf16;
+        const cuuint64_t row_bytes = fp8 ? mla::kRowFp8 : static_cast<cuuint64_t>(D + mla::kP) * 2;
         cuuint32_t estride[2] = {1u, 1u};
         CUresult r;
         if (!fp8) {
-            cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kW), static_cast<cuuint64_t>(num_slots)};
+            cuuint64_t gdim[2] = {static_cast<cuuint64_t>(D + mla::kP), static_cast<cuuint64_t>(num_slots)};
             cuuint64_t gstride[1] = {row_bytes};
             cuuint32_t box_lat[2] = {64u, static_cast<cuuint32_t>(br)};
             r = enc(&tmap_lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim, gstride, box_lat,
@@ -336,6 +339,8 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     p.wseg = (NP == 16 ? 2 : NP == 32 ? 4 : 8) * (fold ? 2 : 1);
     p.test_hold = g_test_hold.exchange(0);
     p.cu_q = cu_q;
+    p.lat_dim = D;
+    p.rope_dim = mla::kP;
     cudaError_t e = fold ? mla::launch_decode_fold(maps, p, NP, W, GY, s)
                          : mla::launch_decode(maps, p, NP, lsu, cache_kind, W, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -353,6 +358,44 @@ int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache
     return decode_impl(q_lat, q_pe, static_cast<int64_t>(B) * q_len, cache, cache_kind, num_slots, page_size,
                        block_table, block_table_stride, seq_lens, nullptr, B, q_len, Hq, scale, out, out_dtype, lse,
                        workspace, workspace_bytes, num_ctas, stream);
+}
+
+size_t mla_decode_latent_workspace_bytes(int B, int q_len, int Hq, int lat_dim, int num_ctas) {
+    if (B <= 0 || q_len <= 0 || Hq <= 0 || num_ctas < 0 || lat_dim <= 0 || lat_dim % 128) return 0;
+    int sms = 0;
+    if (num_ctas == 0) {
+        sms = mla_num_sms();
+        if (sms <= 0) return 0;
+    }
+    return decode_ws_bytes(B, Hq * q_len, ws_ctas(num_ctas, sms), lat_dim);
+}
+
+int mla_cache_write_latent(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
+                           const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots,
+                           int lat_dim, int32_t* status, void* stream) {
+    if (num_tokens < 0 || num_slots < 0) return MLA_ERR_INVALID_ARG;
+    if (lat_dim != 256 && lat_dim != 512 && lat_dim != 768 && lat_dim != 1792) return MLA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return MLA_OK;
+    if (!latent || !k_pe || !slot_mapping || !cache) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(latent) || !aligned16(k_pe) || !aligned16(cache)) return MLA_ERR_INVALID_ARG;
+    if (latent_stride < lat_dim || latent_stride % 8 || k_pe_stride < mla::kP || k_pe_stride % 8)
+        return MLA_ERR_INVALID_ARG;
+    if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return MLA_ERR_INVALID_ARG;
+    cudaError_t e = mla::launch_cache_write_latent(latent, latent_stride, k_pe, k_pe_stride, slot_mapping, num_tokens,
+                                                   cache, num_slots, lat_dim, status,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode_latent(const void* q_lat, const void* q_pe, const void* cache, int lat_dim, int64_t num_slots,
+                      int page_size, const int32_t* block_table, int64_t block_table_stride, const int32_t* seq_lens,
+                      int B, int q_len, int Hq, float scale, void* out, int out_dtype, float* lse, void* workspace,
+                      size_t workspace_bytes, int num_ctas, void* stream) {
+    if (B <= 0 || q_len <= 0) return MLA_ERR_INVALID_ARG;
+    if (lat_dim != 256 && lat_dim != 512 && lat_dim != 768 && lat_dim != 1792) return MLA_ERR_UNSUPPORTED;
+    return decode_impl(q_lat, q_pe, static_cast<int64_t>(B) * q_len, cache, MLA_CACHE_BF16_576, num_slots, page_size,
+                       block_table, block_table_stride, seq_lens, nullptr, B, q_len, Hq, scale, out, out_dtype, lse,
+                       workspace, workspace_bytes, num_ctas, stream, lat_dim);
 }
 
 int mla_decode_varlen(const void* q_lat, const void* q_pe, int64_t total_q_tokens, const void* cache,

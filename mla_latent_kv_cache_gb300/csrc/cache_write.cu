@@ -44,6 +44,33 @@ __global__ void __launch_bounds__(256) cache_write_bf16_kernel(const __nv_bfloat
     if (lane < 8) dst[64 + lane] = __ldg(src_r + lane);
 }
 
+// bf16 rows of another latent width: concat(latent[0:D], k_pe[0:64]), D a
+// multiple of 128 (2 (D + 64) bytes a row). One warp per token, 16-byte units.
+__global__ void __launch_bounds__(256) cache_write_bf16_latent_kernel(const __nv_bfloat16* __restrict__ latent,
+                                                                      int64_t latent_stride,
+                                                                      const __nv_bfloat16* __restrict__ k_pe,
+                                                                      int64_t k_pe_stride,
+                                                                      const int64_t* __restrict__ slot_mapping,
+                                                                      int64_t num_tokens, int D,
+                                                                      uint8_t* __restrict__ cache, int64_t num_slots,
+                                                                      int* __restrict__ status) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= num_tokens) return;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (lane == 0 && status) atomicOr(status, kErrBadBlock);
+        return;
+    }
+    const int lat_units = D / 8;  // 16-byte units of latent
+    uint4* dst = reinterpret_cast<uint4*>(cache + slot * static_cast<int64_t>(2 * (D + kP)));
+    const uint4* src_l = reinterpret_cast<const uint4*>(latent + t * latent_stride);
+    const uint4* src_r = reinterpret_cast<const uint4*>(k_pe + t * k_pe_stride);
+    for (int u = lane; u < lat_units; u += 32) dst[u] = __ldg(src_l + u);
+    if (lane < kP / 8) dst[lat_units + lane] = __ldg(src_r + lane);
+}
+
 __global__ void __launch_bounds__(256) cache_write_fp8_kernel(const __nv_bfloat16* __restrict__ latent,
                                                               int64_t latent_stride,
                                                               const __nv_bfloat16* __restrict__ k_pe,
@@ -162,6 +189,18 @@ __global__ void __launch_bounds__(256) gather_upconvert_fp8_kernel(const uint8_t
         out[2 * lane + 1] = c;
         if (lane < 8) out[64 + lane] = e;
     }
+}
+
+cudaError_t launch_cache_write_latent(const void* latent, int64_t latent_stride, const void* k_pe,
+                                      int64_t k_pe_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                                      void* cache, int64_t num_slots, int lat_dim, int* status,
+                                      cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int64_t blocks = (num_tokens + 7) / 8;
+    cache_write_bf16_latent_kernel<<<dim3(static_cast<unsigned>(blocks)), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(latent), latent_stride, static_cast<const __nv_bfloat16*>(k_pe), k_pe_stride,
+        slot_mapping, num_tokens, lat_dim, static_cast<uint8_t*>(cache), num_slots, status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gather_upconvert(const void* cache, int64_t num_slots, int page_size, const int32_t* block_table,

@@ -239,8 +239,8 @@ __device__ __forceinline__ void prefetch_request(const DecodeParams& p, int b, i
     const int HQg = req_rows_in_group(p, b, gy);
     const int64_t row0 = req_row0(p, b) + gy * 64;
     if (HQg > 0) {
-        prefetch_l2_bulk(p.q_lat + row0 * kD, static_cast<uint32_t>(HQg * kD * 2));
-        prefetch_l2_bulk(p.q_pe + row0 * kP, static_cast<uint32_t>(HQg * kP * 2));
+        prefetch_l2_bulk(p.q_lat + row0 * p.lat_dim, static_cast<uint32_t>(HQg * p.lat_dim * 2));
+        prefetch_l2_bulk(p.q_pe + row0 * p.rope_dim, static_cast<uint32_t>(HQg * p.rope_dim * 2));
     }
     const int T = max(__ldg(p.seq_lens + b), 0);
     const int64_t pages = (static_cast<int64_t>(T) + p.page_size - 1) / p.page_size;
@@ -1450,17 +1450,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // Nothing crosses between CTAs: a tile's shared memory is held from its load
 // to its value product only, with no exchange latency in between.
 
-template <int NP>
+template <int NP, int KB, bool PAIR = false>
 struct FoldCfg {
     static_assert(NP == 16 || NP == 32, "NP");
+    // KB K-blocks per tile and CTA: 128 KB latent values in two halves of 64 KB.
+    // PAIR: the two CTAs of a cluster take the latent's two halves (1792 = 2 x 896)
+    static_assert(PAIR ? (KB == 7 && NP == 16) : (KB == 2 || KB == 4 || (KB == 6 && NP == 16)), "latent width");
+    static constexpr int kDL = 128 * KB;                  // latent values this CTA holds
+    static constexpr int kD = PAIR ? 2 * kDL : kDL;       // the row's latent width
+    static constexpr int kHalf = 64 * KB;
     static constexpr int kTok = 64;                    // tokens per tile
     static constexpr int kBlkBytes = 128 * 128;        // a K-block: 64 dims x (64 + 64) rows, 128-B swizzled
     static constexpr int kRopeBytes = 128 * 64;        // 32 rope dims x 128 rows, 64-B swizzled
     // K-block slots (4 per tile) and rope slots (1 per tile, freed right after
     // S): at 32 rows a tenth K-block slot is worth more than a second rope slot
     // (the rope reload waits for one S, well inside a tile's time; 3% faster)
-    static constexpr int kRL = (NP == 16) ? 11 : 10;
-    static constexpr int kRR = (NP == 16) ? 2 : 1;
+    static constexpr int kRL = PAIR ? 9 : (KB == 4) ? ((NP == 16) ? 11 : 10) : (KB == 2 ? ((NP == 16) ? 11 : 10) : 10);
+    static constexpr int kRR = (KB == 4) ? ((NP == 16) ? 2 : 1) : 2;
+    // K-blocks [kb_lo(pp), kb_hi(pp)) of each tile belong to producer pp and PV issuer pp
+    static __host__ __device__ constexpr int kb_lo(int pp) { return pp ? (KB + 1) / 2 : 0; }
+    static __host__ __device__ constexpr int kb_hi(int pp) { return pp ? KB : (KB + 1) / 2; }
     // Producer warp 1 fills, and PV issuer 0 frees, K-blocks 0 and 1 of each
     // tile; warp 8 and issuer 1 K-blocks 2 and 3, all in one ring. A producer
     // orders a refill only by its own earlier waits (and the rope slots it
@@ -1468,9 +1477,9 @@ struct FoldCfg {
     // slot's last phase from the one before it; with 11 slots, or 10 and one
     // rope slot, those waits do prove the fill before last freed whichever
     // issuer runs behind (checked on a random-schedule model of the protocol).
-    static __device__ __forceinline__ int slot_of(int i, int kb) { return (4 * i + kb) % kRL; }
-    static __device__ __forceinline__ int fill_of(int i, int kb) { return (4 * i + kb) / kRL; }
-    static constexpr int kQBytes = 2 * NP * (4 * 128 + 64);
+    static __device__ __forceinline__ int slot_of(int i, int kb) { return (KB * i + kb) % kRL; }
+    static __device__ __forceinline__ int fill_of(int i, int kb) { return (KB * i + kb) / kRL; }
+    static constexpr int kQBytes = 2 * NP * (KB * 128 + 64);
     static constexpr int kNH = NP / 2;                 // softmax columns per thread
     static constexpr int kXBytes = 128 * kNH * 4;      // the partner lane's half scores
     static constexpr int kPBufs = 2;
@@ -1479,12 +1488,14 @@ struct FoldCfg {
     static constexpr int kOffQ = kOffRope + kRR * kRopeBytes;
     static constexpr int kOffX = (kOffQ + kQBytes + 1023) / 1024 * 1024;
     static constexpr int kOffP = kOffX + kXBytes;
-    static constexpr int kOffCtrl = kOffP + kPBufs * kPBytes;
+    static constexpr int kX2Bytes = PAIR ? 128 * kNH * 4 : 0;  // the peer CTA's partial scores
+    static constexpr int kOffX2 = kOffP + kPBufs * kPBytes;
+    static constexpr int kOffCtrl = kOffX2 + kX2Bytes;
     static constexpr int kSmemBytes = kOffCtrl + 3072 + 1024;  // + control block, alignment slack
     // TMEM: two O accumulators of 4 x NP columns (M-tile m at m * NP), then
     // two S buffers of 2 x NP columns
-    static constexpr int kColS = 8 * NP;
-    static constexpr int kTmemCols = NP == 16 ? 256 : 512;
+    static constexpr int kColS = 2 * KB * NP;
+    static constexpr int kTmemCols = (kColS + 4 * NP) <= 128 ? 128 : (kColS + 4 * NP) <= 256 ? 256 : 512;
     static constexpr uint32_t kPSwizzle = NP == 16 ? kSw32 : kSw64;  // one row of P = one swizzle atom
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(kColS + 4 * NP <= kTmemCols, "tmem");
@@ -1500,6 +1511,7 @@ struct FoldCtrl {
     // then complete a phase past that issuer, whose parity wait could never
     // end; tile t + 2's hand-off follows PV(t) of both issuers
     uint64_t p_full[2];
+    uint64_t x2full, x2free;         // CTA pair: the peer's partial scores landed / it has read ours
     uint32_t tmem_base;
     int abort;
     int t_begin, t_end, b0, j0;
@@ -1512,10 +1524,10 @@ struct FoldCtrl {
 };
 static_assert(sizeof(FoldCtrl) <= 3072, "control block");
 
-template <int NP>
+template <int NP, int KB, bool PAIR>
 __global__ void __launch_bounds__(288, 1)
     mla_decode_fold_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
-    using C = FoldCfg<NP>;
+    using C = FoldCfg<NP, KB, PAIR>;
     constexpr int kT = C::kTok;
     using It = TileItT<6>;
     extern __shared__ uint8_t smem_raw[];
@@ -1525,10 +1537,18 @@ __global__ void __launch_bounds__(288, 1)
     uint8_t* qs = smem + C::kOffQ;
     uint8_t* xbuf = smem + C::kOffX;
     uint8_t* pbufs = smem + C::kOffP;
+    uint8_t* x2buf = smem + C::kOffX2;
     FoldCtrl* ctrl = reinterpret_cast<FoldCtrl*>(smem + C::kOffCtrl);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.x, G = gridDim.x, gy = blockIdx.y;
+    // PAIR: a worker is a cluster of two CTAs, CTA r holding latent dims
+    // [r kDL, (r + 1) kDL) of every row (and, r = 0 only, the rope)
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int g = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int G = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int gy = blockIdx.y;
+    const int dbase = static_cast<int>(rank) * C::kDL;
+    const bool has_rope = !PAIR || rank == 0;
     if (threadIdx.x == 0) MLA_KTRACE(0);
 
     if (threadIdx.x == 0) {
@@ -1543,6 +1563,8 @@ __global__ void __launch_bounds__(288, 1)
         mbar_init(&ctrl->p_full[0], 1);
         mbar_init(&ctrl->p_full[1], 1);
         mbar_init(&ctrl->q_full, 1);
+        mbar_init(&ctrl->x2full, 1);  // + the peer's st.async bytes
+        mbar_init(&ctrl->x2free, 1);  // the peer's remote arrive
         ctrl->abort = 0;
         fence_mbar_init();
     }
@@ -1581,6 +1603,7 @@ __global__ void __launch_bounds__(288, 1)
         ctrl->m[c] = -INFINITY;
     }
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any remote traffic
     if (threadIdx.x == 0) {
         MLA_KTRACE(1);
         griddep_launch_dependents();  // the merge grid may be scheduled as CTAs retire
@@ -1588,7 +1611,7 @@ __global__ void __launch_bounds__(288, 1)
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
     const int ntiles = ctrl->t_end - ctrl->t_begin;
-    if (ntiles == 0 && ctrl->j0 > 0 && threadIdx.x >= 128 && threadIdx.x < 192) {
+    if (has_rope && ntiles == 0 && ctrl->j0 > 0 && threadIdx.x >= 128 && threadIdx.x < 192) {
         // an empty range strictly inside request b0 (more workers than tiles):
         // the merge of b0 counts this worker's slot, so mark it empty
         const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + ctrl->b0;
@@ -1602,7 +1625,7 @@ __global__ void __launch_bounds__(288, 1)
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint32_t idS = idesc_bf16(128, 2 * NP, false, false);
             const uint64_t dq = smem_desc(smem_u32(qs), 16, 1024, kSw128);
-            const uint64_t dqr = smem_desc(smem_u32(qs) + 8 * NP * 128, 16, 512, kSw64);
+            const uint64_t dqr = smem_desc(smem_u32(qs) + 2 * KB * NP * 128, 16, 512, kSw64);
             int seg = 0;
             for (int i = 0; i < ntiles; ++i) {
                 if (i == 0 || it.j == 0) {
@@ -1621,7 +1644,7 @@ __global__ void __launch_bounds__(288, 1)
                 const uint32_t tS = tmem + C::kColS + (i & 1) * 2 * NP;
                 bool ok = true;
                 int site = kSitePairFull;
-                for (int kb = 0; kb < 4 && ok; ++kb) {
+                for (int kb = 0; kb < KB && ok; ++kb) {
                     const int slot = C::slot_of(i, kb);
                     if (!mbar_wait(&ctrl->blk_full[slot], C::fill_of(i, kb) & 1, &ctrl->abort)) { ok = false; break; }
                     tc_fence_after();
@@ -1632,7 +1655,7 @@ __global__ void __launch_bounds__(288, 1)
                         umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4), idS, (kb | kk) != 0);
                 }
                 const int rr = i % C::kRR;
-                if (ok && !mbar_wait(&ctrl->rope_full[rr], (i / C::kRR) & 1, &ctrl->abort)) {
+                if (ok && has_rope && !mbar_wait(&ctrl->rope_full[rr], (i / C::kRR) & 1, &ctrl->abort)) {
                     ok = false;
                     site = kSiteRopeFull;
                 }
@@ -1643,11 +1666,13 @@ __global__ void __launch_bounds__(288, 1)
                 }
                 tc_fence_after();
                 MLA_TRACE_POINT(i, kTrSAllIn);
-                const uint64_t dr = smem_desc(smem_u32(rope_ring + rr * C::kRopeBytes), 16, 512, kSw64);
-                umma_bf16(tS, dr, dqr, idS, 1u);
-                umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
+                if (has_rope) {
+                    const uint64_t dr = smem_desc(smem_u32(rope_ring + rr * C::kRopeBytes), 16, 512, kSw64);
+                    umma_bf16(tS, dr, dqr, idS, 1u);
+                    umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
+                }
                 umma_commit(&ctrl->s_full[i & 1]);
-                umma_commit(&ctrl->rope_empty[rr]);
+                if (has_rope) umma_commit(&ctrl->rope_empty[rr]);
                 MLA_TRACE_POINT(i, kTrSIssued);
                 it.next(p.seq_lens, p.B);
             }
@@ -1666,7 +1691,7 @@ __global__ void __launch_bounds__(288, 1)
             for (int i = 0; i < ntiles; ++i) {
                 const bool new_seg = (i == 0) || (it.j == 0);
                 if (new_seg) ++seg;
-                const uint32_t tO = tmem + (seg & 1) * 4 * NP;
+                const uint32_t tO = tmem + (seg & 1) * KB * NP;
                 if (!mbar_wait(&ctrl->p_full[i & 1], (i >> 1) & 1, &ctrl->abort)) {
                     fail(p, ctrl, kErrWaitTimeout, kSitePFull, i);
                     report(p, kRolePV, kSitePFull, i);
@@ -1677,8 +1702,9 @@ __global__ void __launch_bounds__(288, 1)
                 const uint64_t dp = smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), C::kPBytes, p_sbo,
                                               C::kPSwizzle);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int kb = 2 * mt + q;
+                for (int q = 0; q < (KB + 1) / 2; ++q) {
+                    const int kb = C::kb_lo(mt) + q;
+                    if (kb >= C::kb_hi(mt)) break;
                     const int slot = C::slot_of(i, kb);
                     // tokens 16 kk .. 16 kk + 15: rows 16 kk .. of both halves
                     const uint64_t da = smem_desc(smem_u32(ring + slot * C::kBlkBytes), 8192, 1024, kSw128);
@@ -1725,8 +1751,9 @@ __global__ void __launch_bounds__(288, 1)
                 nx.next(p.seq_lens, p.B);
                 if (i + 1 < ntiles) y_next = run_slot(nx);
                 if (lane == 0) MLA_TRACE_POINT(i, kTrProdStart + 0 * pp);
-                for (int q = 0; q < 2; ++q) {
-                    const int kb = 2 * pp + q;
+                for (int q = 0; q < (KB + 1) / 2; ++q) {
+                    const int kb = C::kb_lo(pp) + q;
+                    if (kb >= C::kb_hi(pp)) break;
                     const int slot = C::slot_of(i, kb), fill = C::fill_of(i, kb);
                     if (fill > 0 &&
                         !__all_sync(0xffffffffu, mbar_wait(&ctrl->blk_empty[slot], (fill - 1) & 1, &ctrl->abort))) {
@@ -1742,11 +1769,11 @@ __global__ void __launch_bounds__(288, 1)
                         uint8_t* dst = ring + slot * C::kBlkBytes + lane * BR * 128;
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh)
-                            tma_load_2d(dst + hh * 8192, &maps.lat, &ctrl->blk_full[slot], 256 * hh + 64 * kb, y, pol);
+                            tma_load_2d(dst + hh * 8192, &maps.lat, &ctrl->blk_full[slot], dbase + C::kHalf * hh + 64 * kb, y, pol);
                     }
                 }
                 if (!ok) break;
-                {
+                if (has_rope) {
                     const int rr = i % C::kRR;
                     if (i >= C::kRR &&
                         !__all_sync(0xffffffffu, mbar_wait(&ctrl->rope_empty[rr], ((i / C::kRR) - 1) & 1, &ctrl->abort))) {
@@ -1760,7 +1787,7 @@ __global__ void __launch_bounds__(288, 1)
                     __syncwarp();
                     if (lane < nruns)
                         tma_load_2d(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
-                                    &ctrl->rope_full[rr], 512 + 32 * pp, y, pol);
+                                    &ctrl->rope_full[rr], C::kD + 32 * pp, y, pol);
                     if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrProdIssued);
                 }
                 it = nx;
@@ -1822,7 +1849,7 @@ __global__ void __launch_bounds__(288, 1)
                 tc_fence_after();
                 __syncwarp();
 #pragma unroll 1
-                for (int m4 = 0; m4 < 4; ++m4)
+                for (int m4 = 0; m4 < KB; ++m4)
 #pragma unroll 1
                     for (int c0 = 0; c0 < NP; c0 += 16) {
                         uint32_t o[16];
@@ -1842,15 +1869,18 @@ __global__ void __launch_bounds__(288, 1)
             auto issue_q = [&](int bq) {
                 const int y = static_cast<int>(req_row0(p, bq) + gy * 64);
                 const uint64_t pol = l2_policy_evict_first();
-                mbar_arrive_expect_tx(&ctrl->q_full, C::kQBytes);
+                mbar_arrive_expect_tx(&ctrl->q_full, has_rope ? C::kQBytes : C::kQBytes - 2 * NP * 64);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
+                for (int k = 0; k < KB; ++k)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh)
-                        tma_load_2d(qs + (k * 2 + hh) * NP * 128, &maps.q, &ctrl->q_full, 256 * hh + 64 * k, y, pol);
+                        tma_load_2d(qs + (k * 2 + hh) * NP * 128, &maps.q, &ctrl->q_full,
+                                    dbase + C::kHalf * hh + 64 * k, y, pol);
+                if (has_rope) {
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    tma_load_2d(qs + 8 * NP * 128 + hh * NP * 64, &maps.qpe, &ctrl->q_full, 32 * hh, y, pol);
+                    for (int hh = 0; hh < 2; ++hh)
+                        tma_load_2d(qs + 2 * KB * NP * 128 + hh * NP * 64, &maps.qpe, &ctrl->q_full, 32 * hh, y, pol);
+                }
             };
 
             // Row sums and maxima of segment sg, which just ended, into
@@ -1874,7 +1904,7 @@ __global__ void __launch_bounds__(288, 1)
             auto start_drain = [&](uint32_t src, int sg, int sb, bool sfinal, int shq) {
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + sb;
                 dr_row0 = req_row0(p, sb) + gy * 64;
-                if (st < NP && st < shq) {
+                if (st < NP && st < shq && rank == 0) {
                     const float lt = ctrl->dlt[sg & 1][st];
                     const float lv = lt > 0.f ? (ctrl->dm[sg & 1][st] + log2f(lt)) * kLn2 : -INFINITY;
                     if (sfinal) p.lse[dr_row0 + st] = lv;
@@ -1882,7 +1912,7 @@ __global__ void __launch_bounds__(288, 1)
                 }
                 dr_hq = shq;
                 dr_per_mt = max(1, (shq + kDC - 1) / kDC);
-                dr_left = shq > 0 ? 4 * dr_per_mt : 0;
+                dr_left = shq > 0 ? KB * dr_per_mt : 0;
                 dr_step = 0;
                 dr_b = sb;
                 dr_final = sfinal;
@@ -1899,7 +1929,7 @@ __global__ void __launch_bounds__(288, 1)
                 uint32_t o[kDC];
                 tmem_ld_x8(tmem + lane_base + dr_obuf + m4 * NP + c0, o);
                 // M-tile m4, lane st: latent dim 64 m4 + st (first half) or 256 + 64 m4 + st - 64
-                const int64_t d = (st < 64 ? 0 : 192) + 64 * m4 + st;
+                const int64_t d = dbase + (st < 64 ? 0 : C::kHalf - 64) + 64 * m4 + st;
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + dr_b;
 #pragma unroll
                 for (int cc = 0; cc < kDC; ++cc) {
@@ -1908,11 +1938,11 @@ __global__ void __launch_bounds__(288, 1)
                         const float lt = ctrl->dlt[dr_sg & 1][c];
                         const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
                         if (dr_final) {
-                            const int64_t idx = (dr_row0 + c) * kD + d;
+                            const int64_t idx = (dr_row0 + c) * C::kD + d;
                             if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
                             else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
                         } else {
-                            p.part_o[(pslot * 64 + c) * kD + d] = v;
+                            p.part_o[(pslot * 64 + c) * C::kD + d] = v;
                         }
                     }
                 }
@@ -1939,7 +1969,7 @@ __global__ void __launch_bounds__(288, 1)
                     // PV(t-1), the captured segment's last, is long done by now
                     group_wait(&ctrl->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, p, ctrl, kSiteOEpi, t);
                     tc_fence_after();
-                    start_drain(obuf ^ (4 * NP), seg - 1, cap_b, cap_final, cap_hq);
+                    start_drain(obuf ^ (KB * NP), seg - 1, cap_b, cap_final, cap_hq);
                 } else if (dr_left > 0) {
                     tc_fence_after();
                     drain_step();
@@ -2001,7 +2031,7 @@ __global__ void __launch_bounds__(288, 1)
                     seg_hq = req_rows_in_group(p, b, gy);
                     seg_has_pv = false;
                     ++seg;
-                    obuf = (seg & 1) * 4 * NP;
+                    obuf = (seg & 1) * KB * NP;
                 } else {
                     named_bar_sync(1, 128);
                 }
@@ -2015,6 +2045,33 @@ __global__ void __launch_bounds__(288, 1)
                     x[4 * u + 1] = __uint_as_float(own_s(4 * u + 1)) + v.y;
                     x[4 * u + 2] = __uint_as_float(own_s(4 * u + 2)) + v.z;
                     x[4 * u + 3] = __uint_as_float(own_s(4 * u + 3)) + v.w;
+                }
+                if constexpr (PAIR) {
+                    // the other CTA of the pair holds the other latent half: add its
+                    // partial scores of this thread's token and columns (row st of
+                    // each CTA's x2buf, written by st.async), then hand the buffer
+                    // back once every thread has read it. Both CTAs add the same two
+                    // values, so their scores, and every softmax decision, agree.
+                    const uint32_t peer = rank ^ 1u;
+                    if (i > 0) group_wait(&ctrl->x2free, (i - 1) & 1, p, ctrl, kSiteXFree, i, true);
+                    if (st == 0) mbar_arrive_expect_tx(&ctrl->x2full, C::kX2Bytes);
+                    const uint32_t dst = mapa_shared(smem_u32(x2buf + st * NH * 4), peer);
+                    const uint32_t bar = mapa_shared(smem_u32(&ctrl->x2full), peer);
+#pragma unroll
+                    for (int u = 0; u < NH / 4; ++u)
+                        st_async_v4(dst + 16 * u, __float_as_uint(x[4 * u]), __float_as_uint(x[4 * u + 1]),
+                                    __float_as_uint(x[4 * u + 2]), __float_as_uint(x[4 * u + 3]), bar);
+                    group_wait(&ctrl->x2full, i & 1, p, ctrl, kSiteXFull, i, true);
+#pragma unroll
+                    for (int u = 0; u < NH / 4; ++u) {
+                        const float4 v = *reinterpret_cast<const float4*>(x2buf + st * NH * 4 + 16 * u);
+                        x[4 * u] += v.x;
+                        x[4 * u + 1] += v.y;
+                        x[4 * u + 2] += v.z;
+                        x[4 * u + 3] += v.w;
+                    }
+                    named_bar_sync(1, 128);
+                    if (st == 0) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&ctrl->x2free), peer));
                 }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXRead);
                 const int tok = j * kT + tt;
@@ -2114,7 +2171,7 @@ __global__ void __launch_bounds__(288, 1)
                     // the row in the four K-blocks (rotated units: no bank conflicts)
                     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < KB; ++q) {
                         uint8_t* row = ring + C::slot_of(i, q) * C::kBlkBytes + st * 128;
 #pragma unroll
                         for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(row + (((u + st) & 7) << 4)) = z;
@@ -2154,6 +2211,7 @@ __global__ void __launch_bounds__(288, 1)
         }
     }
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();  // no remote traffic into this CTA after here
     if (threadIdx.x == 0) MLA_KTRACE(3);
     if (warp == 0) {
         __syncwarp();
@@ -2220,9 +2278,12 @@ __device__ __forceinline__ void merge_row(const float* po, int64_t o_stride, con
 // across workers g0..g1 combine their partial slots g + b; rows of empty
 // requests get (0, -inf). Block (0, 0) also folds the per-CTA status records
 // of the decode grid into the workspace header.
-template <int RPB, int GRP>
+// VP float4 columns per thread: thread t of a row owns dims 4t + 512v, v < VP,
+// below the latent width (VP = 2 for 768).
+template <int RPB, int GRP, int VP>
 __global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const DecodeParams p, int G, int nrec) {
     constexpr int kThreads = 128 * RPB * GRP;
+    const int64_t D = p.lat_dim;
     MLA_MTRACE(0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int RB = (min(64, p.HQ) + RPB - 1) / RPB;  // blocks per (request, row group)
@@ -2233,7 +2294,7 @@ __global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const
     // cost coordinate of request b's first tile, and the total cost (the
     // decode kernel's work split)
     __shared__ long long red_pre[kThreads / 32], red_tot[kThreads / 32];
-    __shared__ float4 part[GRP > 1 ? GRP - 1 : 1][128];
+    __shared__ float4 part[GRP > 1 ? GRP - 1 : 1][VP][128];
     long long pre = 0, tot = 0;
     for (int i = tid; i < p.B; i += kThreads) {
         const long long tl = (max(__ldg(p.seq_lens + i), 0) + (1 << p.tile_shift) - 1) >> p.tile_shift;
@@ -2285,7 +2346,12 @@ __global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const
     const int tiles_b = (max(__ldg(p.seq_lens + b), 0) + (1 << p.tile_shift) - 1) >> p.tile_shift;
     const int64_t row = req_row0(p, b) + gy * 64 + n;
     const int d = 4 * t;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool dv[VP];
+#pragma unroll
+    for (int v = 0; v < VP; ++v) dv[v] = d + 512 * v < D;
+    float4 acc[VP];
+#pragma unroll
+    for (int v = 0; v < VP; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = -INFINITY;
     if (tiles_b > 0) {
         // the workers holding the first and last tile: the largest g with
@@ -2296,16 +2362,19 @@ __global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const
         const int nseg = static_cast<int>(g1 - g0 + 1);
         const int64_t slot0 = static_cast<int64_t>(gy) * p.SPG + g0 + b;
         const float* pl = p.part_lse + slot0 * 64 + n;
-        const float* po = p.part_o + (slot0 * 64 + n) * kD + d;
+        const float* po = p.part_o + (slot0 * 64 + n) * D + d;
         // this group's slots k = grp, grp + GRP, ...: the first kSpec of them are
         // requested before the weights are known, so the loads overlap the LSE
         // round trip (empty slots hold stale values and get weight 0)
         constexpr int kSpec = GRP > 1 ? 4 : 8;
         const int nmine = nseg > grp ? (nseg - grp + GRP - 1) / GRP : 0;
-        float4 ov[kSpec];
+        float4 ov[kSpec][VP];
 #pragma unroll
         for (int k = 0; k < kSpec; ++k)
-            if (k < nmine) ov[k] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(grp + GRP * k) * 64 * kD);
+#pragma unroll
+            for (int v = 0; v < VP; ++v)
+                if (k < nmine && dv[v])
+                    ov[k][v] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(grp + GRP * k) * 64 * D + 512 * v);
         // the slot LSEs, 32 at a time, one per lane (every warp computes the
         // same weights)
         float mx = -INFINITY;
@@ -2319,14 +2388,18 @@ __global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const
                 ws += v != -INFINITY ? expf(v - mx) : 0.f;
             }
             L = mx + logf(warp_sum(ws));
-            auto add = [&](int k, const float4& o) {
-                const float v = pl[k * 64];
-                const float w = v != -INFINITY ? expf(v - L) : 0.f;
+            auto add = [&](int k, const float4 (&o)[VP]) {
+                const float lv = pl[k * 64];
+                const float w = lv != -INFINITY ? expf(lv - L) : 0.f;
                 if (w != 0.f) {
-                    acc.x += w * o.x;
-                    acc.y += w * o.y;
-                    acc.z += w * o.z;
-                    acc.w += w * o.w;
+#pragma unroll
+                    for (int v = 0; v < VP; ++v) {
+                        if (!dv[v]) continue;
+                        acc[v].x += w * o[v].x;
+                        acc[v].y += w * o[v].y;
+                        acc[v].z += w * o[v].z;
+                        acc[v].w += w * o[v].w;
+                    }
                 }
             };
 #pragma unroll
@@ -2334,11 +2407,14 @@ __global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const
                 if (k < nmine) add(grp + GRP * k, ov[k]);
             // the rest, 8 loads in flight at a time
             for (int k0 = kSpec; k0 < nmine; k0 += 8) {
-                float4 o8[8];
+                float4 o8[8][VP];
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    if (k0 + k < nmine)
-                        o8[k] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(grp + GRP * (k0 + k)) * 64 * kD);
+#pragma unroll
+                    for (int v = 0; v < VP; ++v)
+                        if (k0 + k < nmine && dv[v])
+                            o8[k][v] = *reinterpret_cast<const float4*>(
+                                po + static_cast<int64_t>(grp + GRP * (k0 + k)) * 64 * D + 512 * v);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     if (k0 + k < nmine) add(grp + GRP * (k0 + k), o8[k]);
@@ -2348,23 +2424,32 @@ __global__ void __launch_bounds__(128 * RPB * GRP) mla_decode_merge_kernel(const
     if constexpr (GRP > 1) {
         // the groups' sums (every group has L; the empty-request path too). The
         // block has one row, so every return above was taken by all of it.
-        if (grp > 0) part[grp - 1][t] = acc;
+        if (grp > 0) {
+#pragma unroll
+            for (int v = 0; v < VP; ++v) part[grp - 1][v][t] = acc[v];
+        }
         __syncthreads();
         if (grp > 0) return;
 #pragma unroll
-        for (int q = 0; q < GRP - 1; ++q) {
-            const float4 o = part[q][t];
-            acc.x += o.x;
-            acc.y += o.y;
-            acc.z += o.z;
-            acc.w += o.w;
-        }
+        for (int q = 0; q < GRP - 1; ++q)
+#pragma unroll
+            for (int v = 0; v < VP; ++v) {
+                const float4 o = part[q][v][t];
+                acc[v].x += o.x;
+                acc[v].y += o.y;
+                acc[v].z += o.z;
+                acc[v].w += o.w;
+            }
     }
-    if (p.out_f32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * kD + d) = acc;
-    } else {
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * kD + d) =
-            make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+#pragma unroll
+    for (int v = 0; v < VP; ++v) {
+        if (!dv[v]) continue;
+        if (p.out_f32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * D + d + 512 * v) = acc[v];
+        } else {
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * D + d + 512 * v) =
+                make_uint2(pack_bf16x2(acc[v].x, acc[v].y), pack_bf16x2(acc[v].z, acc[v].w));
+        }
     }
     if (t == 0) p.lse[row] = L;
     MLA_MTRACE(1);
@@ -2410,8 +2495,14 @@ static cudaError_t launch_decode_merge(const DecodeParams& p, int G, int nrec, i
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg =
         pdl_config(dim3(static_cast<unsigned>(p.B) * RB, GY), wide ? 512 : 256, 0, stream, attr);
-    return wide ? cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<1, 4>, p, G, nrec)
-                : cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<2, 1>, p, G, nrec);
+    if (p.lat_dim > 1024)
+        return wide ? cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<1, 4, 4>, p, G, nrec)
+                    : cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<2, 1, 4>, p, G, nrec);
+    if (p.lat_dim > 512)
+        return wide ? cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<1, 4, 2>, p, G, nrec)
+                    : cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<2, 1, 2>, p, G, nrec);
+    return wide ? cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<1, 4, 1>, p, G, nrec)
+                : cudaLaunchKernelEx(&cfg, mla_decode_merge_kernel<2, 1, 1>, p, G, nrec);
 }
 
 template <int NP, bool LSU, int KIND>
@@ -2477,48 +2568,96 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP,
     return launch_decode_merge(p, G, 2 * G * GY, GY, stream);
 }
 
-template <int NP>
+template <int NP, int KB, bool PAIR = false>
 struct FoldVariant {
+    using C = FoldCfg<NP, KB, PAIR>;
     // Set the shared-memory attribute (once per device) and return how many
-    // CTAs fit on the device at once.
-    static int max_ctas() {
+    // workers (CTAs, or clusters of two) fit on the device at once.
+    static int max_workers() {
         static int done[64] = {0};
-        static int ctas[64] = {0};
+        static int workers[64] = {0};
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return -1;
         if (!done[dev]) {
-            auto k = mla_decode_fold_kernel<NP>;
-            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, FoldCfg<NP>::kSmemBytes) != cudaSuccess)
+            auto k = mla_decode_fold_kernel<NP, KB, PAIR>;
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
                 return -1;
-            int per_sm = 0, sms = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 288, FoldCfg<NP>::kSmemBytes) != cudaSuccess ||
-                per_sm <= 0)
-                return -1;
-            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return -1;
-            ctas[dev] = per_sm * sms;
+            if constexpr (PAIR) {
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.gridDim = dim3(2, 1, 1);
+                cfg.blockDim = dim3(288, 1, 1);
+                cfg.dynamicSmemBytes = C::kSmemBytes;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) return -1;
+                workers[dev] = n;
+            } else {
+                int per_sm = 0, sms = 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 288, C::kSmemBytes) != cudaSuccess ||
+                    per_sm <= 0)
+                    return -1;
+                if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+                    return -1;
+                workers[dev] = per_sm * sms;
+            }
             done[dev] = 1;
         }
-        return ctas[dev];
+        return workers[dev];
     }
 
     static cudaError_t launch(const DecodeMaps& maps, const DecodeParams& p, int W, int GY, cudaStream_t stream) {
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = pdl_config(dim3(W, GY), 288, FoldCfg<NP>::kSmemBytes, stream, attr);
-        return cudaLaunchKernelEx(&cfg, mla_decode_fold_kernel<NP>, maps, p);
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = pdl_config(dim3(PAIR ? 2 * W : W, GY), 288, C::kSmemBytes, stream, attr);
+        if constexpr (PAIR) {
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = 2;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
+        }
+        return cudaLaunchKernelEx(&cfg, mla_decode_fold_kernel<NP, KB, PAIR>, maps, p);
     }
 };
 
-int decode_fold_ctas(int NP, int requested_ctas) {
-    const int mx = NP == 16 ? FoldVariant<16>::max_ctas() : FoldVariant<32>::max_ctas();
+// The folded-tile variants: query rows padded to NP, latent width D (K-blocks
+// per tile 128 / D; 1792 splits the latent over a CTA pair).
+#define MLA_FOLD(NPV, DV, EXPR)                                                                    \
+    (DV == 512 ? (NPV == 16 ? EXPR(16, 4, false) : EXPR(32, 4, false))                            \
+               : DV == 256 ? (NPV == 16 ? EXPR(16, 2, false) : EXPR(32, 2, false))                \
+                           : DV == 768 ? EXPR(16, 6, false) : EXPR(16, 7, true))
+
+bool fold_supported(int NP, int lat_dim) {
+    return (lat_dim == 512 || lat_dim == 256) ? (NP == 16 || NP == 32)
+                                              : ((lat_dim == 768 || lat_dim == 1792) && NP == 16);
+}
+
+bool fold_is_pair(int lat_dim) { return lat_dim == 1792; }
+
+int decode_fold_ctas(int NP, int lat_dim, int requested_ctas) {
+    if (!fold_supported(NP, lat_dim)) return -1;
+#define MLA_FOLD_WORKERS(a, b, c) FoldVariant<a, b, c>::max_workers()
+    const int mx = MLA_FOLD(NP, lat_dim, MLA_FOLD_WORKERS);
+#undef MLA_FOLD_WORKERS
     if (mx <= 0) return -1;
-    return requested_ctas > 0 ? requested_ctas : mx;
+    if (requested_ctas <= 0) return mx;
+    return fold_is_pair(lat_dim) ? (requested_ctas >= 4 ? requested_ctas / 2 : 1) : requested_ctas;
 }
 
 cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int W, int GY,
                                cudaStream_t stream) {
-    cudaError_t e = NP == 16 ? FoldVariant<16>::launch(maps, p, W, GY, stream) : FoldVariant<32>::launch(maps, p, W, GY, stream);
+    if (!fold_supported(NP, p.lat_dim)) return cudaErrorInvalidValue;
+#define MLA_FOLD_LAUNCH(a, b, c) FoldVariant<a, b, c>::launch(maps, p, W, GY, stream)
+    cudaError_t e = MLA_FOLD(NP, p.lat_dim, MLA_FOLD_LAUNCH);
+#undef MLA_FOLD_LAUNCH
     if (e != cudaSuccess) return e;
-    return launch_decode_merge(p, W, W * GY, GY, stream);
+    // status records: one per CTA
+    return launch_decode_merge(p, W, (fold_is_pair(p.lat_dim) ? 2 * W : W) * GY, GY, stream);
 }
 
 cudaError_t launch_merge_lse(const float* part_o, const float* part_lse, int S, int64_t N, void* out, int out_f32,

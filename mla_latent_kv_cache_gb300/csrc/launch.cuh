@@ -24,7 +24,7 @@ struct DecodeParams {
     float* lse;
     int* status;       // workspace header: status summary written by the merge step
     int* rec;          // [CTAs][kStatusRecWords] per-CTA status records
-    float* part_o;     // [GY][SPG][64][512] fp32 partial outputs
+    float* part_o;     // [GY][SPG][64][lat_dim] fp32 partial outputs
     float* part_lse;   // [GY][SPG][64] fp32 partial LSEs
     float scale_log2;  // softmax scale * log2(e)
     int page_size;
@@ -37,11 +37,17 @@ struct DecodeParams {
     int test_hold;     // test hooks: 1 = withhold the first hand-off to the PV issuers,
                        // 2 = hold one PV issuer ~20 us after each of its first 32 tiles
     const int32_t* cu_q;  // [B + 1] prefix sums of query tokens per request, or null: Qt each
+    int lat_dim;       // latent width D: 512 (576-value rows), or 256 / 768 / 1792 (folded tiles, bf16)
+    int rope_dim;      // rotary width P: 64
 };
 
 cudaError_t launch_cache_write(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
                                const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots,
                                int kind, int* status, cudaStream_t stream);
+// bf16 rows of another latent width D (2 (D + 64) bytes) (mla_cache_write_latent).
+cudaError_t launch_cache_write_latent(const void* latent, int64_t latent_stride, const void* k_pe,
+                                      int64_t k_pe_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                                      void* cache, int64_t num_slots, int lat_dim, int* status, cudaStream_t stream);
 // Context gather of an fp8_ds_mla pool into bf16 rows (mla_gather_upconvert).
 cudaError_t launch_gather_upconvert(const void* cache, int64_t num_slots, int page_size, const int32_t* block_table,
                                     int64_t bt_stride, const int32_t* cu_seq_lens, int B, int64_t num_rows, void* dst,
@@ -58,9 +64,15 @@ struct DecodeMaps {
     CUtensorMap lat, aux, rope, q, qpe;
 };
 
-// CTAs of the folded-tile decode kernel (bf16 pools, page_size % 8 == 0, at
-// most 32 query rows): the number that fit at once, or requested_ctas.
-int decode_fold_ctas(int NP, int requested_ctas);
+// Whether the folded-tile kernel has a variant for NP query rows and this
+// latent width.
+bool fold_supported(int NP, int lat_dim);
+// Whether that variant's workers are clusters of two CTAs (latent 1792).
+bool fold_is_pair(int lat_dim);
+// Workers of the folded-tile decode kernel (bf16 pools, page_size % 8 == 0, at
+// most 32 query rows): the number that fit at once, or what requested_ctas
+// CTAs make.
+int decode_fold_ctas(int NP, int lat_dim, int requested_ctas);
 cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int W, int GY,
                                cudaStream_t stream);
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,

@@ -211,8 +211,10 @@ def batched(device="cpu", seed: int = 2) -> Workload:
                 seed=seed, device=device)
 
 
-def long(device="cpu", seed: int = 3) -> Workload:
-    return make("long", B=4, Hq=32, Qt=1, page_size=64, seq_lens=[262144] * 4, num_blocks=16384,
+def long(device="cpu", seed: int = 3, B: int = 4) -> Workload:
+    """B requests of 262,144 tokens (4 in the named workload; fewer give a
+    cut-down copy of the same shape for profiling)."""
+    return make("long", B=B, Hq=32, Qt=1, page_size=64, seq_lens=[262144] * B, num_blocks=4096 * B,
                 seed=seed, device=device)
 
 
@@ -242,8 +244,10 @@ def mtp(device="cpu", seed: int = 4) -> Workload:
                 num_blocks=nb, min_block=first, force_block=nb - 1, seed=seed, device=device)
 
 
-def fp8(device="cpu", seed: int = 5) -> Workload:
-    return make("fp8", B=64, Hq=64, Qt=1, page_size=64, seq_lens=[32768] * 64, num_blocks=32768,
+def fp8(device="cpu", seed: int = 5, B: int = 64) -> Workload:
+    """B requests of 32,768 tokens (64 in the named workload; fewer give a
+    cut-down copy of the same shape for profiling)."""
+    return make("fp8", B=B, Hq=64, Qt=1, page_size=64, seq_lens=[32768] * B, num_blocks=512 * B,
                 kind=KIND_FP8, write_all=True, seed=seed, device=device)
 
 

@@ -21,8 +21,10 @@ The model reports:
 - a deadlock, where nothing can move (on the GPU, the bounded wait gives up).
 
 Ring layout: tile i has KB blocks; block kb is the u = KB * i + kb-th use of
-the ring, slot u % R. With two producers, producer p loads blocks
-[p KB/2, (p+1) KB/2). PV issuer m frees the same blocks. The rope ring has RR
+the ring, slot u % R. With two producers, producer 0 loads blocks
+[0, ceil(KB/2)) and producer 1 the rest (an odd KB gives producer 0 one
+more). PV issuer m frees the blocks producer m loads (with one producer,
+the same split). The rope ring has RR
 slots, one per tile, and every producer loads a part of each. The softmax
 waits for PV(i - PB) before it writes P(i) into buffer i % PB. It waits for
 PV(i - 1) as well on a random 30% of tiles, standing for an O rescale. It
@@ -75,12 +77,16 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
     errors: list[str] = []
     landings = []                                  # TMA completions, any order
     commits = {"S": [], "PV0": [], "PV1": []}     # tcgen05 commits, in order per thread
-    per_prod = KB // producers
+    half = (KB + 1) // 2
+
+    def blocks(m):
+        # the blocks of producer / PV issuer m: [0, half) and [half, KB)
+        return range(0, half) if m == 0 else range(half, KB)
 
     def producer(pp):
+        mine = range(KB) if producers == 1 else blocks(pp)
         for i in range(N):
-            for q in range(per_prod):
-                kb = pp * per_prod + q
+            for kb in mine:
                 u = KB * i + kb
                 s, f = u % R, u // R
                 if f > 0:
@@ -152,8 +158,7 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
             if pbuf[i % PB] != i:
                 errors.append(f"PV{mt}({i}) read P of tile {pbuf[i % PB]}")
             reads = pbuf_reads[i % PB]
-            for q in range(KB // 2):
-                kb = mt * (KB // 2) + q
+            for kb in blocks(mt):
                 s = (KB * i + kb) % R
                 if slot_data[s] != (i, kb):
                     errors.append(f"PV{mt}({i}) block {kb} read {slot_data[s]}")

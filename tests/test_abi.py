@@ -64,6 +64,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.mla_decode(*bad) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_lse(16, 16, -1, 4, 16, 0, 16, None) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_merge_lse(16, 16, 2, 0, 16, 0, 16, None) == m.MLA_OK
+    # other latent widths: only 256 / 512 / 768 / 1792
+    assert lib.mla_cache_write_latent(16, 384, 16, 64, 16, 4, 16, 10, 384, None, None) == m.MLA_ERR_UNSUPPORTED
+    assert lib.mla_cache_write_latent(16, 200, 16, 64, 16, 4, 16, 10, 256, None, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_latent_workspace_bytes(4, 1, 16, 300, 8) == 0
+    assert lib.mla_decode_latent_workspace_bytes(4, 1, 16, 768, 8) > lib.mla_decode_workspace_bytes(4, 1, 16, 8)
+    lat = [16, 16, 16, 384, 100, 16, 16, 4, 16, 2, 1, 8, 0.1, 16, 0, 16, 256, 1 << 20, 0, None]
+    assert lib.mla_decode_latent(*lat) == m.MLA_ERR_UNSUPPORTED
     assert lib.mla_static_scratch_status(None, 12, None) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_static_scratch_status(16, 0, None) == m.MLA_ERR_INVALID_ARG
     assert lib.mla_static_scratch_status(16, 13, None) == m.MLA_ERR_INVALID_ARG

@@ -23,6 +23,10 @@ SKEWS = [None, {"PV0": 0.02}, {"PV1": 0.02}, {"PV0": 0.01, "LD1": 0.2}, {"PV1": 
 SHAPES = [
     ("folded 16 rows", 4, 11, 2, 2, 2),
     ("folded 32 rows", 4, 10, 1, 2, 2),
+    ("folded latent 256, 16 rows", 2, 11, 2, 2, 2),
+    ("folded latent 256, 32 rows", 2, 10, 2, 2, 2),
+    ("folded latent 768, 16 rows", 6, 10, 2, 2, 2),
+    ("folded latent 1792 (one CTA of a pair), 16 rows", 7, 9, 2, 2, 2),
     ("cluster TMA 16 rows", 2, 5, 3, 1, 2),
     ("cluster TMA 32 rows", 2, 5, 2, 1, 2),
     ("cluster TMA 64 rows", 2, 4, 1, 1, 1),
