@@ -223,9 +223,9 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     // pages whose rows cannot be fetched as 8-row TMA boxes go through the
     // load/convert warps
     const bool lsu = (page_size % 8) != 0;
-    // bf16 pools with up to 32 query rows: folded 64-token tiles, one CTA per
-    // worker; otherwise 128-token tiles split over clusters of two CTAs
-    const bool fold = !lsu && cache_kind == MLA_CACHE_BF16_576 && NP <= 32;
+    // bf16 pools: folded 64-token tiles, one CTA per worker; fp8 pools and
+    // odd page sizes: 128-token tiles split over clusters of two CTAs
+    const bool fold = !lsu && cache_kind == MLA_CACHE_BF16_576;
     // other latent widths: bf16 rows of D + 64 values, folded tiles only
     if (D != 512 && (!fold || !mla::fold_supported(NP, D))) return MLA_ERR_UNSUPPORTED;
     const int nctas = ws_ctas(num_ctas, di.sms);  // what the workspace holds records and slots for
@@ -335,8 +335,10 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     p.SPG = W + B;
     // what a request boundary costs a worker, in tiles (measured on the
     // cluster kernel: about one and a half 128-token tiles at 16 query rows;
-    // the 64-row drain is four times larger; folded tiles are half as long)
-    p.wseg = (NP == 16 ? 2 : NP == 32 ? 4 : 8) * (fold ? 2 : 1);
+    // the 64-row drain is four times larger; folded tiles are half as long;
+    // at 64 rows the folded kernel drains a finished segment before the next
+    // one's first value product, about two tiles' time)
+    p.wseg = fold ? (NP == 16 ? 4 : NP == 32 ? 8 : 4) : (NP == 16 ? 2 : NP == 32 ? 4 : 8);
     p.test_hold = g_test_hold.exchange(0);
     p.cu_q = cu_q;
     p.lat_dim = D;

@@ -1452,7 +1452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 
 template <int NP, int KB, bool PAIR = false>
 struct FoldCfg {
-    static_assert(NP == 16 || NP == 32, "NP");
+    static_assert(NP == 16 || NP == 32 || (NP == 64 && KB == 4 && !PAIR), "NP");
     // KB K-blocks per tile and CTA: 128 KB latent values in two halves of 64 KB.
     // PAIR: the two CTAs of a cluster take the latent's two halves (1792 = 2 x 896)
     static_assert(PAIR ? (KB == 7 && NP == 16) : (KB == 2 || KB == 4 || (KB == 6 && NP == 16)), "latent width");
@@ -1465,7 +1465,11 @@ struct FoldCfg {
     // K-block slots (4 per tile) and rope slots (1 per tile, freed right after
     // S): at 32 rows a tenth K-block slot is worth more than a second rope slot
     // (the rope reload waits for one S, well inside a tile's time; 3% faster)
-    static constexpr int kRL = PAIR ? 9 : (KB == 4) ? ((NP == 16) ? 11 : 10) : (KB == 2 ? ((NP == 16) ? 11 : 10) : 10);
+    // At 64 query rows Q takes 72 KB. Eight K-block slots (two tiles, so that
+    // tile i's loads wait for PV(i - 2), not PV(i - 1)) and one rope slot fit
+    // beside one P buffer and a quarter-width exchange buffer.
+    static constexpr int kRL = PAIR ? 9 : (KB == 4) ? ((NP == 16) ? 11 : NP == 32 ? 10 : 8)
+                                                    : (KB == 2 ? ((NP == 16) ? 11 : 10) : 10);
     static constexpr int kRR = (KB == 4) ? ((NP == 16) ? 2 : 1) : 2;
     // K-blocks [kb_lo(pp), kb_hi(pp)) of each tile belong to producer pp and PV issuer pp
     static __host__ __device__ constexpr int kb_lo(int pp) { return pp ? (KB + 1) / 2 : 0; }
@@ -1481,8 +1485,13 @@ struct FoldCfg {
     static __device__ __forceinline__ int fill_of(int i, int kb) { return (KB * i + kb) / kRL; }
     static constexpr int kQBytes = 2 * NP * (KB * 128 + 64);
     static constexpr int kNH = NP / 2;                 // softmax columns per thread
-    static constexpr int kXBytes = 128 * kNH * 4;      // the partner lane's half scores
-    static constexpr int kPBufs = 2;
+    // the partner lane's half scores, kXR columns at a time (at 64 rows in four
+    // rounds of 8, so the buffer takes 4 KB)
+    static constexpr int kXR = NP == 64 ? 8 : kNH;
+    static constexpr int kXBytes = 128 * kXR * 4;
+    // one P buffer at 64 rows: the softmax writes P(i) once PV(i - 1) has
+    // read P(i - 1), which a tile's softmax outlasts
+    static constexpr int kPBufs = NP == 64 ? 1 : 2;
     static constexpr int kPBytes = kTok * NP * 2;      // P [64 tokens][NP] bf16, MN-major
     static constexpr int kOffRope = kRL * kBlkBytes;
     static constexpr int kOffQ = kOffRope + kRR * kRopeBytes;
@@ -1491,12 +1500,16 @@ struct FoldCfg {
     static constexpr int kX2Bytes = PAIR ? 128 * kNH * 4 : 0;  // the peer CTA's partial scores
     static constexpr int kOffX2 = kOffP + kPBufs * kPBytes;
     static constexpr int kOffCtrl = kOffX2 + kX2Bytes;
-    static constexpr int kSmemBytes = kOffCtrl + 3072 + 1024;  // + control block, alignment slack
-    // TMEM: two O accumulators of 4 x NP columns (M-tile m at m * NP), then
-    // two S buffers of 2 x NP columns
-    static constexpr int kColS = 2 * KB * NP;
+    static constexpr int kSmemBytes = kOffCtrl + 3584 + 1024;  // + control block, alignment slack
+    // TMEM: two O accumulators of KB x NP columns (M-tile m at m * NP; one at
+    // 64 rows, where two would leave no room for S), then two S buffers of
+    // 2 x NP columns. With one accumulator a finished segment is drained
+    // before the next segment's first value product.
+    static constexpr bool kOneO = NP == 64;
+    static constexpr int kColS = (kOneO ? 1 : 2) * KB * NP;
     static constexpr int kTmemCols = (kColS + 4 * NP) <= 128 ? 128 : (kColS + 4 * NP) <= 256 ? 256 : 512;
-    static constexpr uint32_t kPSwizzle = NP == 16 ? kSw32 : kSw64;  // one row of P = one swizzle atom
+    // one row of P = one swizzle atom
+    static constexpr uint32_t kPSwizzle = NP == 16 ? kSw32 : NP == 32 ? kSw64 : kSw128;
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(kColS + 4 * NP <= kTmemCols, "tmem");
 };
@@ -1518,11 +1531,11 @@ struct FoldCtrl {
     int colvis[64];                  // uniform verify length: query row -> trailing tokens it may not see
     alignas(16) float m[64];         // running max per row (log2 units)
     alignas(16) float alpha[64];
-    alignas(16) float red[4][32];    // per-warp column reductions (at most 32 columns here)
-    alignas(16) float dlt[2][32];    // row sums of a finished segment, by segment parity
-    float dm[2][32];                 // and its row maxima
+    alignas(16) float red[4][64];    // per-warp column reductions
+    alignas(16) float dlt[2][64];    // row sums of a finished segment, by segment parity
+    float dm[2][64];                 // and its row maxima
 };
-static_assert(sizeof(FoldCtrl) <= 3072, "control block");
+static_assert(sizeof(FoldCtrl) <= 3584, "control block");
 
 template <int NP, int KB, bool PAIR>
 __global__ void __launch_bounds__(288, 1)
@@ -1691,7 +1704,7 @@ __global__ void __launch_bounds__(288, 1)
             for (int i = 0; i < ntiles; ++i) {
                 const bool new_seg = (i == 0) || (it.j == 0);
                 if (new_seg) ++seg;
-                const uint32_t tO = tmem + (seg & 1) * KB * NP;
+                const uint32_t tO = tmem + (C::kOneO ? 0 : (seg & 1) * KB * NP);
                 if (!mbar_wait(&ctrl->p_full[i & 1], (i >> 1) & 1, &ctrl->abort)) {
                     fail(p, ctrl, kErrWaitTimeout, kSitePFull, i);
                     report(p, kRolePV, kSitePFull, i);
@@ -1812,7 +1825,8 @@ __global__ void __launch_bounds__(288, 1)
             const int own0 = hf * NH;
             // exchange rows of NH floats, 16-byte units swizzled by row; thread st
             // writes row st ^ 64 and reads row st (same swizzle: bit 6 is not in it)
-            const int xs = (NH == 16) ? ((st >> 1) & 3) : ((st >> 2) & 1);
+            constexpr int XR = C::kXR;
+            const int xs = (XR == 16) ? ((st >> 1) & 3) : ((st >> 2) & 1);
             It it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             // the current segment's verify length and its rows in this row group
@@ -1994,14 +2008,37 @@ __global__ void __launch_bounds__(288, 1)
                 tc_fence_after();
                 __syncwarp();
                 // this lane's half of the scores: columns [hf NP, hf NP + NP) (a TMEM
-                // load takes one column address per warp: hf is the same in the warp)
-                uint32_t sr[NP];
-                tmem_ld_np<NP>(tmem + lane_base + C::kColS + (i & 1) * 2 * NP + hf * NP, sr);
-                tc_fence_before();
+                // load takes one column address per warp: hf is the same in the warp).
+                // It keeps the NH columns [own0, own0 + NH) and writes the other NH
+                // into its partner's exchange row.
+                const uint32_t s_addr = tmem + lane_base + C::kColS + (i & 1) * 2 * NP + hf * NP;
+                uint32_t own[NH];
+                // partner columns [base, base + XR) into exchange row st ^ 64
+                auto put_x = [&](auto&& snd, int base) {
+#pragma unroll
+                    for (int u = 0; u < XR / 4; ++u)
+                        *reinterpret_cast<uint4*>(xbuf + (st ^ 64) * XR * 4 + ((u ^ xs) << 4)) =
+                            make_uint4(snd(base + 4 * u), snd(base + 4 * u + 1), snd(base + 4 * u + 2),
+                                       snd(base + 4 * u + 3));
+                };
+                uint32_t sv[NP == 64 ? NH : 1];
+                if constexpr (NP == 64) {
+                    // two loads of 32 columns, the partner's first; the exchange goes in
+                    // rounds of XR columns
+                    tmem_ld_x32(s_addr + (hf ? 0 : NH), sv);
+                    put_x([&](int k) -> uint32_t { return sv[k]; }, 0);
+                    tmem_ld_x32(s_addr + (hf ? NH : 0), own);
+                    tc_fence_before();
+                } else {
+                    uint32_t sr[NP];
+                    tmem_ld_np<NP>(s_addr, sr);
+                    tc_fence_before();
+                    // compile-time indices so sr[] stays in registers
+#pragma unroll
+                    for (int k = 0; k < NH; ++k) own[k] = hf ? sr[NH + k] : sr[k];
+                    put_x([&](int k) -> uint32_t { return hf ? sr[k] : sr[NH + k]; }, 0);
+                }
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmTmemLd);
-                // own / partner columns, compile-time indices so sr[] stays in registers
-                auto own_s = [&](int k) -> uint32_t { return hf ? sr[NH + k] : sr[k]; };
-                auto snd_s = [&](int k) -> uint32_t { return hf ? sr[k] : sr[NH + k]; };
                 if (st == 0 && (i == 0 || j == 0) && !last_of_seg) {
                     // warm L2 with the next request's queries and page list
                     It nx = it;
@@ -2009,10 +2046,6 @@ __global__ void __launch_bounds__(288, 1)
                     nx.next(p.seq_lens, p.B);
                     if (nx.b < p.B) prefetch_request(p, nx.b, gy);
                 }
-#pragma unroll
-                for (int u = 0; u < NH / 4; ++u)
-                    *reinterpret_cast<uint4*>(xbuf + (st ^ 64) * NH * 4 + ((u ^ xs) << 4)) =
-                        make_uint4(snd_s(4 * u), snd_s(4 * u + 1), snd_s(4 * u + 2), snd_s(4 * u + 3));
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmSent);
                 if (i > 0 && j == 0) {
                     // the previous segment ended with tile i-1: finish the older
@@ -2023,28 +2056,51 @@ __global__ void __launch_bounds__(288, 1)
                         tc_fence_before();
                     }
                     capture(seg);  // its barriers also order the exchange rows
-                    pend = true;
-                    cap_b = pend_b;
-                    cap_final = pend_final;
-                    cap_hq = seg_hq;
+                    if constexpr (C::kOneO) {
+                        // one accumulator: the ended segment's O (its last value product
+                        // is PV(i - 1)) is written out before PV(i) may start this one
+                        group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteOEpi, i);
+                        tc_fence_after();
+                        if (!ctrl->abort) {
+                            start_drain(0u, seg, pend_b, pend_final, seg_hq);
+                            while (dr_left > 0) drain_step();
+                        }
+                        tc_fence_before();
+                    } else {
+                        pend = true;
+                        cap_b = pend_b;
+                        cap_final = pend_final;
+                        cap_hq = seg_hq;
+                    }
                     seg_qt = req_qt(p, b);
                     seg_hq = req_rows_in_group(p, b, gy);
                     seg_has_pv = false;
                     ++seg;
-                    obuf = (seg & 1) * KB * NP;
+                    obuf = C::kOneO ? 0u : static_cast<uint32_t>((seg & 1) * KB * NP);
                 } else {
                     named_bar_sync(1, 128);
                 }
                 if (st == 0) mbar_arrive(&ctrl->s_free[i & 1]);  // every thread has read S(i)
                 if (st == 0) MLA_TRACE_POINT(i, kTrSmXFull);
                 float x[NH];
+                // own columns [base, base + XR) plus the partner's half of them
+                auto read_x = [&](int base) {
 #pragma unroll
-                for (int u = 0; u < NH / 4; ++u) {
-                    const float4 v = *reinterpret_cast<const float4*>(xbuf + st * NH * 4 + ((u ^ xs) << 4));
-                    x[4 * u] = __uint_as_float(own_s(4 * u)) + v.x;
-                    x[4 * u + 1] = __uint_as_float(own_s(4 * u + 1)) + v.y;
-                    x[4 * u + 2] = __uint_as_float(own_s(4 * u + 2)) + v.z;
-                    x[4 * u + 3] = __uint_as_float(own_s(4 * u + 3)) + v.w;
+                    for (int u = 0; u < XR / 4; ++u) {
+                        const float4 v = *reinterpret_cast<const float4*>(xbuf + st * XR * 4 + ((u ^ xs) << 4));
+                        x[base + 4 * u] = __uint_as_float(own[base + 4 * u]) + v.x;
+                        x[base + 4 * u + 1] = __uint_as_float(own[base + 4 * u + 1]) + v.y;
+                        x[base + 4 * u + 2] = __uint_as_float(own[base + 4 * u + 2]) + v.z;
+                        x[base + 4 * u + 3] = __uint_as_float(own[base + 4 * u + 3]) + v.w;
+                    }
+                };
+                read_x(0);
+#pragma unroll
+                for (int r = XR; r < NH; r += XR) {
+                    named_bar_sync(1, 128);  // every thread has read the last round
+                    put_x([&](int k) -> uint32_t { return sv[k]; }, r);
+                    named_bar_sync(1, 128);
+                    read_x(r);
                 }
                 if constexpr (PAIR) {
                     // the other CTA of the pair holds the other latent half: add its
@@ -2628,13 +2684,14 @@ struct FoldVariant {
 // The folded-tile variants: query rows padded to NP, latent width D (K-blocks
 // per tile 128 / D; 1792 splits the latent over a CTA pair).
 #define MLA_FOLD(NPV, DV, EXPR)                                                                    \
-    (DV == 512 ? (NPV == 16 ? EXPR(16, 4, false) : EXPR(32, 4, false))                            \
+    (DV == 512 ? (NPV == 16 ? EXPR(16, 4, false) : NPV == 32 ? EXPR(32, 4, false) : EXPR(64, 4, false)) \
                : DV == 256 ? (NPV == 16 ? EXPR(16, 2, false) : EXPR(32, 2, false))                \
                            : DV == 768 ? EXPR(16, 6, false) : EXPR(16, 7, true))
 
 bool fold_supported(int NP, int lat_dim) {
-    return (lat_dim == 512 || lat_dim == 256) ? (NP == 16 || NP == 32)
-                                              : ((lat_dim == 768 || lat_dim == 1792) && NP == 16);
+    return lat_dim == 512   ? (NP == 16 || NP == 32 || NP == 64)
+           : lat_dim == 256 ? (NP == 16 || NP == 32)
+                            : ((lat_dim == 768 || lat_dim == 1792) && NP == 16);
 }
 
 bool fold_is_pair(int lat_dim) { return lat_dim == 1792; }

@@ -24,8 +24,10 @@ def _lib():
     yield
 
 
-def test_bounded_wait_reports_and_context_survives():
-    wl = W.make("hold", B=3, Hq=16, Qt=1, page_size=16, seq_lens=[700, 1500, 300], seed=91, device=DEV)
+@pytest.mark.parametrize("Qt", [1, 4])
+def test_bounded_wait_reports_and_context_survives(Qt):
+    # 16 query rows, and 64 (the folded kernel with one O accumulator)
+    wl = W.make("hold", B=3, Hq=16, Qt=Qt, page_size=16, seq_lens=[700, 1500, 300], seed=91, device=DEV)
     m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
     m.test_hold_next_decode()
     out, lse, ws = m.decode(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens,

@@ -24,7 +24,8 @@ def _lib():
 @pytest.mark.parametrize("shape", [
     dict(Hq=16, Qt=1, page_size=16, kind=0),   # folded tiles, 16 rows
     dict(Hq=16, Qt=2, page_size=64, kind=0),   # folded tiles, 32 rows
-    dict(Hq=16, Qt=4, page_size=16, kind=0),   # cluster kernel, 64 rows
+    dict(Hq=16, Qt=4, page_size=16, kind=0),   # folded tiles, 64 rows
+    dict(Hq=16, Qt=4, page_size=5, kind=0),    # cluster kernel (load/convert warps), 64 rows
     dict(Hq=64, Qt=1, page_size=64, kind=1),   # fp8 pool
 ])
 def test_decode_step_replays_from_a_cuda_graph(shape):

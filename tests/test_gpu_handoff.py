@@ -30,11 +30,12 @@ def _lib():
 
 
 CASES = [
-    # name, kind, Hq, page size: the folded-tile kernel at 16 and 32 query
-    # rows, the cluster kernel (fp8 pool) at 16, and its load/convert-warp
+    # name, kind, Hq, page size: the folded-tile kernel at 16, 32 and 64
+    # query rows, the cluster kernel (fp8 pool) at 16, and its load/convert-warp
     # variants (pages that are not a multiple of 8 rows) at 16 and 32
     ("fold16", W.KIND_BF16, 16, 16),
     ("fold32", W.KIND_BF16, 32, 64),
+    ("fold64", W.KIND_BF16, 64, 16),
     ("cluster16_fp8", W.KIND_FP8, 16, 64),
     ("lsu16", W.KIND_BF16, 16, 3),
     ("lsu32", W.KIND_BF16, 32, 5),

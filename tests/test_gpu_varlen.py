@@ -40,7 +40,8 @@ CASES = [
     # (Hq, verify lengths, page size, kind, num_ctas)
     (8, [1, 2, 2, 1, 2, 1, 1], 16, 0, 0),    # folded tiles, 16 rows
     (16, [2, 1, 1, 2, 2, 1, 2], 64, 0, 5),   # folded tiles, 32 rows
-    (16, [4, 1, 3, 2, 4, 1, 2], 16, 0, 0),   # cluster kernel, 64 rows
+    (16, [4, 1, 3, 2, 4, 1, 2], 16, 0, 0),   # folded tiles, 64 rows
+    (16, [4, 1, 3, 2, 4, 1, 2], 8, 0, 9),    # folded tiles, 64 rows, requests cut across workers
     (16, [6, 1, 5, 2, 3, 6, 1], 16, 0, 7),   # 96 rows: two row groups
     (16, [3, 4, 1, 2, 4, 2, 1], 64, 1, 0),   # fp8 pool, 64 rows
 ]
