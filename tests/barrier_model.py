@@ -25,7 +25,9 @@ the ring, slot u % R. With two producers, producer 0 loads blocks
 [0, ceil(KB/2)) and producer 1 the rest (an odd KB gives producer 0 one
 more). PV issuer m frees the blocks producer m loads (with one producer,
 the same split). The rope ring has RR
-slots, one per tile, and every producer loads a part of each. The softmax
+slots, one per tile, and every producer loads a part of each; the S issuer
+reads it last and frees it with its final commit, or (rope_first) reads it
+first and frees it with a commit of its own before the tile's blocks. The softmax
 waits for PV(i - PB) before it writes P(i) into buffer i % PB. It waits for
 PV(i - 1) as well on a random 30% of tiles, standing for an O rescale. It
 hands tile i to the PV issuers through hand-off barrier i % H."""
@@ -60,7 +62,7 @@ class Bar:
 
 
 def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int, N: int = 40,
-        weights: dict | None = None) -> list[str]:
+        weights: dict | None = None, rope_first: bool = False) -> list[str]:
     """One random schedule; returns the problems found (empty when none)."""
     rnd = random.Random(seed)
     blk_full = [Bar(1) for _ in range(R)]
@@ -116,20 +118,29 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
         for i in range(N):
             if i >= 2:
                 yield lambda i=i: s_free[i & 1].passes(((i - 2) >> 1) & 1)
+            rr = i % RR
+            if rope_first:
+                # the rope's products first; its slot is released once they are done
+                yield lambda rr=rr, i=i: rope_full[rr].passes((i // RR) & 1)
+                if rope_data[rr] != i:
+                    errors.append(f"S({i}) rope read tile {rope_data[rr]}")
+                commits["S"].append(lambda rr=rr: rope_empty[rr].arrive_expect())
+                yield None
             for kb in range(KB):
                 u = KB * i + kb
                 yield lambda s=u % R, f=u // R: blk_full[s].passes(f & 1)
                 if slot_data[u % R] != (i, kb):
                     errors.append(f"S({i}) block {kb} read {slot_data[u % R]}")
-            rr = i % RR
-            yield lambda rr=rr, i=i: rope_full[rr].passes((i // RR) & 1)
-            if rope_data[rr] != i:
-                errors.append(f"S({i}) rope read tile {rope_data[rr]}")
+            if not rope_first:
+                yield lambda rr=rr, i=i: rope_full[rr].passes((i // RR) & 1)
+                if rope_data[rr] != i:
+                    errors.append(f"S({i}) rope read tile {rope_data[rr]}")
 
             def done(i=i, rr=rr):
                 s_buf[i & 1] = i
                 s_full[i & 1].arrive_expect()
-                rope_empty[rr].arrive_expect()
+                if not rope_first:
+                    rope_empty[rr].arrive_expect()
             commits["S"].append(done)
             yield None
 
