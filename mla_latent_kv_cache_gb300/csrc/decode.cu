@@ -1484,11 +1484,15 @@ struct FoldCfg {
     static __device__ __forceinline__ int slot_of(int i, int kb) { return (KB * i + kb) % kRL; }
     static __device__ __forceinline__ int fill_of(int i, int kb) { return (KB * i + kb) / kRL; }
     static constexpr int kQBytes = 2 * NP * (KB * 128 + 64);
-    static constexpr int kNH = NP / 2;                 // softmax columns per thread
-    // the partner lane's half scores, kXR columns at a time (at 64 rows in four
-    // rounds of 8, so the buffer takes 4 KB)
-    static constexpr int kXR = NP == 64 ? 8 : kNH;
-    static constexpr int kXBytes = 128 * kXR * 4;
+    // Softmax groups: at 64 rows two groups of four warps, each owning 32 of
+    // the query columns (two warps per scheduler, half the work per thread)
+    static constexpr int kSG = NP == 64 ? 2 : 1;
+    static constexpr int kGW = NP / kSG;               // columns per group
+    static constexpr int kNH = kGW / 2;                // softmax columns per thread
+    // the partner lane's half scores, kXR columns at a time (at 64 rows four
+    // rounds of 4 per group, so the two groups' buffers take 4 KB)
+    static constexpr int kXR = NP == 64 ? 4 : kNH;
+    static constexpr int kXBytes = kSG * 128 * kXR * 4;
     // one P buffer at 64 rows: the softmax writes P(i) once PV(i - 1) has
     // read P(i - 1), which a tile's softmax outlasts
     static constexpr int kPBufs = NP == 64 ? 1 : 2;
@@ -1537,8 +1541,13 @@ struct FoldCtrl {
 };
 static_assert(sizeof(FoldCtrl) <= 3584, "control block");
 
+// Threads of the folded-tile kernel: 9 warps, plus a second softmax group of
+// 4 at 64 query rows.
+template <int NP>
+constexpr int fold_threads() { return NP == 64 ? 416 : 288; }
+
 template <int NP, int KB, bool PAIR>
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(fold_threads<NP>(), 1)
     mla_decode_fold_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     using C = FoldCfg<NP, KB, PAIR>;
     constexpr int kT = C::kTok;
@@ -1570,11 +1579,11 @@ __global__ void __launch_bounds__(288, 1)
         for (int i = 0; i < C::kRR; ++i) { mbar_init(&ctrl->rope_full[i], 2); mbar_init(&ctrl->rope_empty[i], 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->s_full[i], 1);
-            mbar_init(&ctrl->s_free[i], 1);
+            mbar_init(&ctrl->s_free[i], C::kSG);  // one arrive per softmax group
             mbar_init(&ctrl->o_done[i], 2);  // one commit per PV issuer
         }
-        mbar_init(&ctrl->p_full[0], 1);
-        mbar_init(&ctrl->p_full[1], 1);
+        mbar_init(&ctrl->p_full[0], C::kSG);
+        mbar_init(&ctrl->p_full[1], C::kSG);
         mbar_init(&ctrl->q_full, 1);
         mbar_init(&ctrl->x2full, 1);  // + the peer's st.async bytes
         mbar_init(&ctrl->x2free, 1);  // the peer's remote arrive
@@ -1810,23 +1819,32 @@ __global__ void __launch_bounds__(288, 1)
                 report(p, pp ? kRoleLsu0 : kRoleTma, fsite, ftile);  // no load/convert warps here: their slot
             }
             if (bad) atomicOr(status_rec(p), kErrBadBlock);
-        } else if (warp >= 4 && warp < 8) {
+        } else if ((warp >= 4 && warp < 8) || warp >= 9) {
             // ------------------------------------------ softmax + epilogue
-            // Thread st reads TMEM lane st = A row st: half hf of token tt (warps
-            // 4, 5 the first halves, 6, 7 the second). It keeps columns [own0,
-            // own0 + NH) and hands the other NH partial scores to its partner
-            // st ^ 64, the other half of the same token.
-            const int st = threadIdx.x - 128;
-            const int sw = warp - 4;
+            // Thread st reads TMEM lane st = A row st: half hf of token tt (lane
+            // quadrants 0, 1 the first halves, 2, 3 the second). Softmax group grp
+            // (warps 4..7, and at 64 rows 9..12) owns query columns [cg0, cg0 +
+            // GW): the thread keeps [own0, own0 + NH) and hands the group's other
+            // NH partial scores to its partner st ^ 64, the other half of the same
+            // token.
+            const int grp = warp >= 9 ? 1 : 0;
+            const int sw = warp & 3;  // TMEM lane quadrant
+            const int st = sw * 32 + lane;
             const int hf = sw >> 1;
             const int tt = st & 63;
             const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-            constexpr int NH = C::kNH;
-            const int own0 = hf * NH;
-            // exchange rows of NH floats, 16-byte units swizzled by row; thread st
-            // writes row st ^ 64 and reads row st (same swizzle: bit 6 is not in it)
+            constexpr int NH = C::kNH, GW = C::kGW;
+            const int cg0 = grp * GW;
+            const int own0 = cg0 + hf * NH;
+            const int par0 = cg0 + (hf ? 0 : NH);  // the partner's columns
+            const int bsync = grp ? 3 : 1, bvote = grp ? 4 : 2;  // the group's named barriers
+            const bool lead = grp == 0 && st == 0;  // once-per-CTA work of the tile
+            // exchange rows of XR floats (the group's own rows), 16-byte units
+            // swizzled by row; thread st writes row st ^ 64 and reads row st (same
+            // swizzle: bit 6 is not in it)
             constexpr int XR = C::kXR;
-            const int xs = (XR == 16) ? ((st >> 1) & 3) : ((st >> 2) & 1);
+            uint8_t* xg = xbuf + grp * 128 * XR * 4;
+            const int xs = (XR == 16) ? ((st >> 1) & 3) : (XR == 8) ? ((st >> 2) & 1) : 0;
             It it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             // the current segment's verify length and its rows in this row group
@@ -1853,19 +1871,19 @@ __global__ void __launch_bounds__(288, 1)
             auto red_store = [&](int c, float v, float ident) {
                 if (lane == 0) {
                     ctrl->red[sw][own0 + c] = v;
-                    ctrl->red[sw][(NH - own0) + c] = ident;
+                    ctrl->red[sw][par0 + c] = ident;
                 }
             };
 
-            // O columns [0, NP) of accumulator ob, all four M-tiles, times alpha
-            // (the caller has waited for the last PV into it)
+            // O columns [cg0, cg0 + GW) of accumulator ob, all M-tiles, times
+            // alpha (the caller has waited for the last PV into it)
             auto rescale_o = [&](uint32_t ob) {
                 tc_fence_after();
                 __syncwarp();
 #pragma unroll 1
                 for (int m4 = 0; m4 < KB; ++m4)
 #pragma unroll 1
-                    for (int c0 = 0; c0 < NP; c0 += 16) {
+                    for (int c0 = cg0; c0 < cg0 + GW; c0 += 16) {
                         uint32_t o[16];
                         tmem_ld_x16(tmem + lane_base + ob + m4 * NP + c0, o);
 #pragma unroll
@@ -1902,15 +1920,16 @@ __global__ void __launch_bounds__(288, 1)
             auto capture = [&](int sg) {
 #pragma unroll
                 for (int c = 0; c < NH; ++c) red_store(c, warp_sum(l[c]), 0.f);
-                named_bar_sync(1, 128);
-                if (st < NP) {
-                    ctrl->dlt[sg & 1][st] = ctrl->red[0][st] + ctrl->red[1][st] + ctrl->red[2][st] + ctrl->red[3][st];
-                    ctrl->dm[sg & 1][st] = ctrl->m[st];
-                    ctrl->m[st] = -INFINITY;
+                named_bar_sync(bsync, 128);
+                if (st < GW) {
+                    const int c = cg0 + st;
+                    ctrl->dlt[sg & 1][c] = ctrl->red[0][c] + ctrl->red[1][c] + ctrl->red[2][c] + ctrl->red[3][c];
+                    ctrl->dm[sg & 1][c] = ctrl->m[c];
+                    ctrl->m[c] = -INFINITY;
                 }
 #pragma unroll
                 for (int c = 0; c < NH; ++c) l[c] = 0.f;
-                named_bar_sync(1, 128);
+                named_bar_sync(bsync, 128);
             };
 
             // The captured segment sg (accumulator src) has had its last PV:
@@ -1918,15 +1937,17 @@ __global__ void __launch_bounds__(288, 1)
             auto start_drain = [&](uint32_t src, int sg, int sb, bool sfinal, int shq) {
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + sb;
                 dr_row0 = req_row0(p, sb) + gy * 64;
-                if (st < NP && st < shq && rank == 0) {
-                    const float lt = ctrl->dlt[sg & 1][st];
-                    const float lv = lt > 0.f ? (ctrl->dm[sg & 1][st] + log2f(lt)) * kLn2 : -INFINITY;
-                    if (sfinal) p.lse[dr_row0 + st] = lv;
-                    else p.part_lse[pslot * 64 + st] = lv;
+                if (st < GW && cg0 + st < shq && rank == 0) {
+                    const int c = cg0 + st;
+                    const float lt = ctrl->dlt[sg & 1][c];
+                    const float lv = lt > 0.f ? (ctrl->dm[sg & 1][c] + log2f(lt)) * kLn2 : -INFINITY;
+                    if (sfinal) p.lse[dr_row0 + c] = lv;
+                    else p.part_lse[pslot * 64 + c] = lv;
                 }
                 dr_hq = shq;
-                dr_per_mt = max(1, (shq + kDC - 1) / kDC);
-                dr_left = shq > 0 ? KB * dr_per_mt : 0;
+                const int gq = min(GW, max(0, shq - cg0));  // the segment's rows in this group's columns
+                dr_per_mt = max(1, (gq + kDC - 1) / kDC);
+                dr_left = gq > 0 ? KB * dr_per_mt : 0;
                 dr_step = 0;
                 dr_b = sb;
                 dr_final = sfinal;
@@ -1939,7 +1960,7 @@ __global__ void __launch_bounds__(288, 1)
             // rows (a whole request) or this worker's partial slot.
             auto drain_step = [&]() {
                 const int m4 = dr_step / dr_per_mt;
-                const int c0 = (dr_step - m4 * dr_per_mt) * kDC;
+                const int c0 = cg0 + (dr_step - m4 * dr_per_mt) * kDC;
                 uint32_t o[kDC];
                 tmem_ld_x8(tmem + lane_base + dr_obuf + m4 * NP + c0, o);
                 // M-tile m4, lane st: latent dim 64 m4 + st (first half) or 256 + 64 m4 + st - 64
@@ -1972,10 +1993,13 @@ __global__ void __launch_bounds__(288, 1)
             auto finish = [&](int t) -> bool {
                 if (ctrl->abort) return false;  // same value in every thread after the last barrier
                 if (st == 0) {
-                    // the test hook withholds tile 0, so the PV issuers' bounded wait
-                    // gives up and every role leaves through the abort path
-                    MLA_TRACE_POINT(t, kTrSmPArrive);
-                    MLA_TTRACE(t);
+                    // (one arrive per group) the test hook withholds tile 0, so the PV
+                    // issuers' bounded wait gives up and every role leaves through the
+                    // abort path
+                    if (lead) {
+                        MLA_TRACE_POINT(t, kTrSmPArrive);
+                        MLA_TTRACE(t);
+                    }
                     if (!(p.test_hold == 1 && t == 0)) mbar_arrive(&ctrl->p_full[t & 1]);
                 }
                 seg_has_pv = true;
@@ -1992,14 +2016,14 @@ __global__ void __launch_bounds__(288, 1)
                 return true;
             };
 
-            if (st == 0) issue_q(it.b);
+            if (lead) issue_q(it.b);
             bool alive = true;
             for (int i = 0; i < ntiles; ++i) {
                 const int b = it.b, j = it.j, T = it.T;
                 const bool last_of_seg = (j == it.tiles - 1) || (i == ntiles - 1);
                 group_wait(&ctrl->s_full[i & 1], (i >> 1) & 1, p, ctrl, kSiteSFull, i);
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmSFull);
-                if (st == 0 && last_of_seg && i + 1 < ntiles) {
+                if (lead) MLA_TRACE_POINT(i, kTrSmSFull);
+                if (lead && last_of_seg && i + 1 < ntiles) {
                     // S(i) is complete, so Q may be replaced by the next request's
                     It nx = it;
                     nx.next(p.seq_lens, p.B);
@@ -2007,46 +2031,37 @@ __global__ void __launch_bounds__(288, 1)
                 }
                 tc_fence_after();
                 __syncwarp();
-                // this lane's half of the scores: columns [hf NP, hf NP + NP) (a TMEM
-                // load takes one column address per warp: hf is the same in the warp).
-                // It keeps the NH columns [own0, own0 + NH) and writes the other NH
-                // into its partner's exchange row.
-                const uint32_t s_addr = tmem + lane_base + C::kColS + (i & 1) * 2 * NP + hf * NP;
+                // this lane's half of the scores: the group's columns of [hf NP, hf NP +
+                // NP) (a TMEM load takes one column address per warp: hf is the same
+                // in the warp). It keeps the NH columns [own0, own0 + NH) and writes
+                // the other NH into its partner's exchange row, XR at a time.
+                const uint32_t s_addr = tmem + lane_base + C::kColS + (i & 1) * 2 * NP + hf * NP + cg0;
+                uint32_t sr[GW];
+                tmem_ld_np<GW>(s_addr, sr);
+                tc_fence_before();
                 uint32_t own[NH];
+                // compile-time indices so sr[] stays in registers
+#pragma unroll
+                for (int k = 0; k < NH; ++k) own[k] = hf ? sr[NH + k] : sr[k];
+                auto snd = [&](int k) -> uint32_t { return hf ? sr[k] : sr[NH + k]; };
                 // partner columns [base, base + XR) into exchange row st ^ 64
-                auto put_x = [&](auto&& snd, int base) {
+                auto put_x = [&](int base) {
 #pragma unroll
                     for (int u = 0; u < XR / 4; ++u)
-                        *reinterpret_cast<uint4*>(xbuf + (st ^ 64) * XR * 4 + ((u ^ xs) << 4)) =
+                        *reinterpret_cast<uint4*>(xg + (st ^ 64) * XR * 4 + ((u ^ xs) << 4)) =
                             make_uint4(snd(base + 4 * u), snd(base + 4 * u + 1), snd(base + 4 * u + 2),
                                        snd(base + 4 * u + 3));
                 };
-                uint32_t sv[NP == 64 ? NH : 1];
-                if constexpr (NP == 64) {
-                    // two loads of 32 columns, the partner's first; the exchange goes in
-                    // rounds of XR columns
-                    tmem_ld_x32(s_addr + (hf ? 0 : NH), sv);
-                    put_x([&](int k) -> uint32_t { return sv[k]; }, 0);
-                    tmem_ld_x32(s_addr + (hf ? NH : 0), own);
-                    tc_fence_before();
-                } else {
-                    uint32_t sr[NP];
-                    tmem_ld_np<NP>(s_addr, sr);
-                    tc_fence_before();
-                    // compile-time indices so sr[] stays in registers
-#pragma unroll
-                    for (int k = 0; k < NH; ++k) own[k] = hf ? sr[NH + k] : sr[k];
-                    put_x([&](int k) -> uint32_t { return hf ? sr[k] : sr[NH + k]; }, 0);
-                }
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmTmemLd);
-                if (st == 0 && (i == 0 || j == 0) && !last_of_seg) {
+                put_x(0);
+                if (lead) MLA_TRACE_POINT(i, kTrSmTmemLd);
+                if (lead && (i == 0 || j == 0) && !last_of_seg) {
                     // warm L2 with the next request's queries and page list
                     It nx = it;
                     nx.j = nx.tiles - 1;
                     nx.next(p.seq_lens, p.B);
                     if (nx.b < p.B) prefetch_request(p, nx.b, gy);
                 }
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmSent);
+                if (lead) MLA_TRACE_POINT(i, kTrSmSent);
                 if (i > 0 && j == 0) {
                     // the previous segment ended with tile i-1: finish the older
                     // drain (its accumulator is the one this segment will use)
@@ -2078,16 +2093,16 @@ __global__ void __launch_bounds__(288, 1)
                     ++seg;
                     obuf = C::kOneO ? 0u : static_cast<uint32_t>((seg & 1) * KB * NP);
                 } else {
-                    named_bar_sync(1, 128);
+                    named_bar_sync(bsync, 128);
                 }
-                if (st == 0) mbar_arrive(&ctrl->s_free[i & 1]);  // every thread has read S(i)
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmXFull);
+                if (st == 0) mbar_arrive(&ctrl->s_free[i & 1]);  // every thread of the group has read S(i)
+                if (lead) MLA_TRACE_POINT(i, kTrSmXFull);
                 float x[NH];
                 // own columns [base, base + XR) plus the partner's half of them
                 auto read_x = [&](int base) {
 #pragma unroll
                     for (int u = 0; u < XR / 4; ++u) {
-                        const float4 v = *reinterpret_cast<const float4*>(xbuf + st * XR * 4 + ((u ^ xs) << 4));
+                        const float4 v = *reinterpret_cast<const float4*>(xg + st * XR * 4 + ((u ^ xs) << 4));
                         x[base + 4 * u] = __uint_as_float(own[base + 4 * u]) + v.x;
                         x[base + 4 * u + 1] = __uint_as_float(own[base + 4 * u + 1]) + v.y;
                         x[base + 4 * u + 2] = __uint_as_float(own[base + 4 * u + 2]) + v.z;
@@ -2097,9 +2112,9 @@ __global__ void __launch_bounds__(288, 1)
                 read_x(0);
 #pragma unroll
                 for (int r = XR; r < NH; r += XR) {
-                    named_bar_sync(1, 128);  // every thread has read the last round
-                    put_x([&](int k) -> uint32_t { return sv[k]; }, r);
-                    named_bar_sync(1, 128);
+                    named_bar_sync(bsync, 128);  // every thread has read the last round
+                    put_x(r);
+                    named_bar_sync(bsync, 128);
                     read_x(r);
                 }
                 if constexpr (PAIR) {
@@ -2126,10 +2141,10 @@ __global__ void __launch_bounds__(288, 1)
                         x[4 * u + 2] += v.z;
                         x[4 * u + 3] += v.w;
                     }
-                    named_bar_sync(1, 128);
+                    named_bar_sync(bsync, 128);
                     if (st == 0) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&ctrl->x2free), peer));
                 }
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmXRead);
+                if (lead) MLA_TRACE_POINT(i, kTrSmXRead);
                 const int tok = j * kT + tt;
                 const bool all_vis = (j * kT + kT + seg_qt - 1) <= T;
                 const float4* m4p = reinterpret_cast<const float4*>(ctrl->m + own0);
@@ -2161,23 +2176,23 @@ __global__ void __launch_bounds__(288, 1)
                             (x[4 * u + 2] > mv.z + kRescaleThreshold) | (x[4 * u + 3] > mv.w + kRescaleThreshold);
                 }
                 // (also: every thread has read its exchange row)
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmMath);
-                need = named_bar_or(2, 128, need);
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmBarOr);
+                if (lead) MLA_TRACE_POINT(i, kTrSmMath);
+                need = named_bar_or(bvote, 128, need);
+                if (lead) MLA_TRACE_POINT(i, kTrSmBarOr);
                 if (need) {
                     // column maxima over the tile's 64 tokens
 #pragma unroll
                     for (int c = 0; c < NH; ++c) red_store(c, warp_max(x[c]), -INFINITY);
-                    named_bar_sync(1, 128);
-                    if (st < NP) {
-                        const int c = st;
+                    named_bar_sync(bsync, 128);
+                    if (st < GW) {
+                        const int c = cg0 + st;
                         const float mt = fmaxf(fmaxf(ctrl->red[0][c], ctrl->red[1][c]), fmaxf(ctrl->red[2][c], ctrl->red[3][c]));
                         const float mo = ctrl->m[c];
                         const float mn = fmaxf(mo, mt);
                         ctrl->alpha[c] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
                         ctrl->m[c] = mn;
                     }
-                    named_bar_sync(1, 128);
+                    named_bar_sync(bsync, 128);
 #pragma unroll
                     for (int c = 0; c < NH; ++c) l[c] *= ctrl->alpha[own0 + c];
                     if (seg_has_pv) {
@@ -2200,7 +2215,7 @@ __global__ void __launch_bounds__(288, 1)
                         x[c] = pc;
                     }
                 }
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmExpLoop);
+                if (lead) MLA_TRACE_POINT(i, kTrSmExpLoop);
                 // the P buffer of this tile was last read by PV(i - kPBufs)
                 if (i >= C::kPBufs) {
                     const int jp = i - C::kPBufs;
@@ -2209,7 +2224,7 @@ __global__ void __launch_bounds__(288, 1)
                     okp = __shfl_sync(0xffffffffu, okp ? 1 : 0, 0) != 0;
                     if (!okp && lane == 0) fail(p, ctrl, kErrWaitTimeout, kSiteOPbuf, i);
                 }
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmExp);
+                if (lead) MLA_TRACE_POINT(i, kTrSmExp);
                 // P row tt, columns [own0, own0 + NH): NH / 8 16-byte units
                 const int pb = i % C::kPBufs;
                 uint8_t* prow = pbufs + pb * C::kPBytes + tt * NP * 2;
@@ -2221,7 +2236,7 @@ __global__ void __launch_bounds__(288, 1)
                                                pack_bf16x2(x[8 * u + 4], x[8 * u + 5]), pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
                     *reinterpret_cast<uint4*>(prow + ((un ^ sz) << 4)) = v;
                 }
-                if (j * kT + tt >= T) {
+                if (grp == 0 && j * kT + tt >= T) {
                     // this row's token is past the request: its bytes are stale (maybe
                     // NaN); P is 0 there, but 0 * NaN would still poison O, so clear
                     // the row in the four K-blocks (rotated units: no bank conflicts)
@@ -2233,10 +2248,10 @@ __global__ void __launch_bounds__(288, 1)
                         for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(row + (((u + st) & 7) << 4)) = z;
                     }
                 }
-                if (st == 0) MLA_TRACE_POINT(i, kTrSmPStore);
+                if (lead) MLA_TRACE_POINT(i, kTrSmPStore);
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_sync(1, 128);
+                named_bar_sync(bsync, 128);
                 if (!finish(i)) {
                     alive = false;
                     break;
@@ -2256,7 +2271,7 @@ __global__ void __launch_bounds__(288, 1)
                 while (dr_left > 0) drain_step();
                 capture(seg);
                 group_wait(&ctrl->o_done[il & 1], (il >> 1) & 1, p, ctrl, kSiteOFinal, il);
-                named_bar_sync(1, 128);
+                named_bar_sync(bsync, 128);
                 if (!ctrl->abort) {
                     tc_fence_after();
                     start_drain(obuf, seg, pend_b, pend_final, seg_hq);
@@ -2646,7 +2661,7 @@ struct FoldVariant {
                 attr[0].val.clusterDim.y = 1;
                 attr[0].val.clusterDim.z = 1;
                 cfg.gridDim = dim3(2, 1, 1);
-                cfg.blockDim = dim3(288, 1, 1);
+                cfg.blockDim = dim3(fold_threads<NP>(), 1, 1);
                 cfg.dynamicSmemBytes = C::kSmemBytes;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
@@ -2655,7 +2670,7 @@ struct FoldVariant {
                 workers[dev] = n;
             } else {
                 int per_sm = 0, sms = 0;
-                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 288, C::kSmemBytes) != cudaSuccess ||
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, fold_threads<NP>(), C::kSmemBytes) != cudaSuccess ||
                     per_sm <= 0)
                     return -1;
                 if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -2669,7 +2684,7 @@ struct FoldVariant {
 
     static cudaError_t launch(const DecodeMaps& maps, const DecodeParams& p, int W, int GY, cudaStream_t stream) {
         cudaLaunchAttribute attr[2];
-        cudaLaunchConfig_t cfg = pdl_config(dim3(PAIR ? 2 * W : W, GY), 288, C::kSmemBytes, stream, attr);
+        cudaLaunchConfig_t cfg = pdl_config(dim3(PAIR ? 2 * W : W, GY), fold_threads<NP>(), C::kSmemBytes, stream, attr);
         if constexpr (PAIR) {
             attr[1].id = cudaLaunchAttributeClusterDimension;
             attr[1].val.clusterDim.x = 2;
