@@ -369,7 +369,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <int NP>
 __device__ __forceinline__ void tmem_ld_np(uint32_t taddr, uint32_t (&r)[NP]) {
-    if constexpr (NP == 16) tmem_ld_x16(taddr, r);
+    if constexpr (NP == 8) tmem_ld_x8(taddr, r);
+    else if constexpr (NP == 16) tmem_ld_x16(taddr, r);
     else if constexpr (NP == 32) tmem_ld_x32(taddr, r);
     else tmem_ld_x64(taddr, r);
 }
@@ -1484,15 +1485,18 @@ struct FoldCfg {
     static __device__ __forceinline__ int slot_of(int i, int kb) { return (KB * i + kb) % kRL; }
     static __device__ __forceinline__ int fill_of(int i, int kb) { return (KB * i + kb) / kRL; }
     static constexpr int kQBytes = 2 * NP * (KB * 128 + 64);
-    // Softmax groups: at 64 rows two groups of four warps, each owning 32 of
-    // the query columns (two warps per scheduler, half the work per thread)
-    static constexpr int kSG = NP == 64 ? 2 : 1;
+    // Softmax groups: at 32 and 64 rows of the 576-wide row two groups of four
+    // warps, each owning half of the query columns (two warps per scheduler,
+    // half the work per thread)
+    static constexpr int kSG = (NP == 64 || (NP == 32 && KB == 4 && !PAIR)) ? 2 : 1;
     static constexpr int kGW = NP / kSG;               // columns per group
     static constexpr int kNH = kGW / 2;                // softmax columns per thread
     // the partner lane's half scores, kXR columns at a time (at 64 rows four
     // rounds of 4 per group, so the two groups' buffers take 4 KB)
     static constexpr int kXR = NP == 64 ? 4 : kNH;
     static constexpr int kXBytes = kSG * 128 * kXR * 4;
+    // 9 warps, plus the second softmax group's 4
+    static constexpr int kThreads = 288 + 128 * (kSG - 1);
     // one P buffer at 64 rows: the softmax writes P(i) once PV(i - 1) has
     // read P(i - 1), which a tile's softmax outlasts
     static constexpr int kPBufs = NP == 64 ? 1 : 2;
@@ -1541,13 +1545,8 @@ struct FoldCtrl {
 };
 static_assert(sizeof(FoldCtrl) <= 3584, "control block");
 
-// Threads of the folded-tile kernel: 9 warps, plus a second softmax group of
-// 4 at 64 query rows.
-template <int NP>
-constexpr int fold_threads() { return NP == 64 ? 416 : 288; }
-
 template <int NP, int KB, bool PAIR>
-__global__ void __launch_bounds__(fold_threads<NP>(), 1)
+__global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
     mla_decode_fold_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     using C = FoldCfg<NP, KB, PAIR>;
     constexpr int kT = C::kTok;
@@ -2661,7 +2660,7 @@ struct FoldVariant {
                 attr[0].val.clusterDim.y = 1;
                 attr[0].val.clusterDim.z = 1;
                 cfg.gridDim = dim3(2, 1, 1);
-                cfg.blockDim = dim3(fold_threads<NP>(), 1, 1);
+                cfg.blockDim = dim3(C::kThreads, 1, 1);
                 cfg.dynamicSmemBytes = C::kSmemBytes;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
@@ -2670,7 +2669,7 @@ struct FoldVariant {
                 workers[dev] = n;
             } else {
                 int per_sm = 0, sms = 0;
-                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, fold_threads<NP>(), C::kSmemBytes) != cudaSuccess ||
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, C::kThreads, C::kSmemBytes) != cudaSuccess ||
                     per_sm <= 0)
                     return -1;
                 if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -2684,7 +2683,7 @@ struct FoldVariant {
 
     static cudaError_t launch(const DecodeMaps& maps, const DecodeParams& p, int W, int GY, cudaStream_t stream) {
         cudaLaunchAttribute attr[2];
-        cudaLaunchConfig_t cfg = pdl_config(dim3(PAIR ? 2 * W : W, GY), fold_threads<NP>(), C::kSmemBytes, stream, attr);
+        cudaLaunchConfig_t cfg = pdl_config(dim3(PAIR ? 2 * W : W, GY), C::kThreads, C::kSmemBytes, stream, attr);
         if constexpr (PAIR) {
             attr[1].id = cudaLaunchAttributeClusterDimension;
             attr[1].val.clusterDim.x = 2;
