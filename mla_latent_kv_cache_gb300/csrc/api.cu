@@ -229,7 +229,7 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     // other latent widths: bf16 rows of D + 64 values, folded tiles only
     if (D != 512 && (!fold || !mla::fold_supported(NP, D))) return MLA_ERR_UNSUPPORTED;
     const int nctas = ws_ctas(num_ctas, di.sms);  // what the workspace holds records and slots for
-    int W = fold ? mla::decode_fold_ctas(NP, D, num_ctas) : mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
+    int W = fold ? mla::decode_fold_ctas(NP, D, GY, num_ctas) : mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
     if (W <= 0) return MLA_ERR_CUDA;
     W = std::min(W, (fold && !mla::fold_is_pair(D)) ? nctas : nctas / 2);
     const int tile = fold ? 64 : 128;

@@ -1533,6 +1533,7 @@ struct FoldCtrl {
     // end; tile t + 2's hand-off follows PV(t) of both issuers
     uint64_t p_full[2];
     uint64_t x2full, x2free;         // CTA pair: the peer's partial scores landed / it has read ours
+    uint64_t fin[3];                 // the S and PV issuers' products have all completed (at exit)
     uint32_t tmem_base;
     int abort;
     int t_begin, t_end, b0, j0;
@@ -1545,10 +1546,17 @@ struct FoldCtrl {
 };
 static_assert(sizeof(FoldCtrl) <= 3584, "control block");
 
-template <int NP, int KB, bool PAIR>
+// MC: the two row groups of a worker (query rows 0..63 and 64..127 of each
+// request) are the two CTAs of a cluster; each CTA loads half of every tile's
+// boxes with multicast, so each cached row crosses HBM once for both groups,
+// and a ring slot is refilled only when both CTAs' value products have
+// released it.
+template <int NP, int KB, bool PAIR, bool MC>
 __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
     mla_decode_fold_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
+    static_assert(!MC || (NP == 64 && !PAIR), "row-group pairs are 64-row CTAs");
     using C = FoldCfg<NP, KB, PAIR>;
+    constexpr uint16_t kPairMask = 0x3;
     constexpr int kT = C::kTok;
     using It = TileItT<6>;
     extern __shared__ uint8_t smem_raw[];
@@ -1570,12 +1578,22 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
     const int gy = blockIdx.y;
     const int dbase = static_cast<int>(rank) * C::kDL;
     const bool has_rope = !PAIR || rank == 0;
+    // MC: which half of every box pair (and which rope half) this CTA issues
+    const int mrank = MC ? static_cast<int>(cluster_ctarank()) : 0;
     if (threadIdx.x == 0) MLA_KTRACE(0);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kRL; ++i) { mbar_init(&ctrl->blk_full[i], 1); mbar_init(&ctrl->blk_empty[i], 1); }
-        // a rope slot is filled by both producer warps (one half each)
-        for (int i = 0; i < C::kRR; ++i) { mbar_init(&ctrl->rope_full[i], 2); mbar_init(&ctrl->rope_empty[i], 1); }
+        // MC: a slot is released by the value products of both CTAs
+        for (int i = 0; i < C::kRL; ++i) {
+            mbar_init(&ctrl->blk_full[i], 1);
+            mbar_init(&ctrl->blk_empty[i], MC ? 2 : 1);
+        }
+        // a rope slot is armed by both producer warps (one half each)
+        for (int i = 0; i < C::kRR; ++i) {
+            mbar_init(&ctrl->rope_full[i], 2);
+            mbar_init(&ctrl->rope_empty[i], MC ? 2 : 1);
+        }
+        for (int i = 0; i < 3; ++i) mbar_init(&ctrl->fin[i], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->s_full[i], 1);
             mbar_init(&ctrl->s_free[i], C::kSG);  // one arrive per softmax group
@@ -1624,7 +1642,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
         ctrl->m[c] = -INFINITY;
     }
     __syncthreads();
-    if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any remote traffic
+    if constexpr (PAIR || MC) cluster_sync_all();  // the peer's barriers exist before any remote traffic
     if (threadIdx.x == 0) {
         MLA_KTRACE(1);
         griddep_launch_dependents();  // the merge grid may be scheduled as CTAs retire
@@ -1693,10 +1711,16 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                     umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
                 }
                 umma_commit(&ctrl->s_full[i & 1]);
-                if (has_rope) umma_commit(&ctrl->rope_empty[rr]);
+                if (has_rope) {
+                    if constexpr (MC) umma_commit_mc(&ctrl->rope_empty[rr], kPairMask);
+                    else umma_commit(&ctrl->rope_empty[rr]);
+                }
                 MLA_TRACE_POINT(i, kTrSIssued);
                 it.next(p.seq_lens, p.B);
             }
+            // every product issued here completes before the CTA may release
+            // TMEM or exit (on the abort path some are still running)
+            drain_mma(&ctrl->fin[0]);
         } else if ((warp == 3 || warp == 2) && lane == 0) {
             // ------------------------------------------------- PV issuers
             // issuer mt takes K-blocks 2 mt and 2 mt + 1: M-tile kb reads K-block
@@ -1733,13 +1757,15 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(tO + kb * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
                                   (new_seg && kk == 0) ? 0u : 1u);
-                    umma_commit(&ctrl->blk_empty[slot]);
+                    if constexpr (MC) umma_commit_mc(&ctrl->blk_empty[slot], kPairMask);
+                    else umma_commit(&ctrl->blk_empty[slot]);
                 }
                 umma_commit(&ctrl->o_done[i & 1]);
                 if (p.test_hold == 2 && mt == 1 && i < 32) spin_for_ns(20000);  // test hook: a lagging issuer
                 if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssued);
                 it.next(p.seq_lens, p.B);
             }
+            drain_mma(&ctrl->fin[1 + mt]);
         } else if (warp == 1 || warp == 8) {
             // ------------------------------------------------- TMA producers
             // Warp 1 loads K-blocks 0, 1 and the first rope half of every tile,
@@ -1763,6 +1789,10 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                 return lane < nr ? static_cast<int>(token_slot(p, btr, t.j * kT + lane * BR, bad)) : 0;
             };
             int y_next = run_slot(it);
+            // K-block fills (tile-major, this warp's K-blocks) and rope fills (tiles)
+            // whose barriers this warp has armed: at exit it waits for those fills
+            // to land, so that no copy arrives after the CTA is gone
+            int armed = 0, rope_armed = 0;
             for (int i = 0; i < ntiles && ok; ++i) {
                 const int valid = min(kT, it.T - it.j * kT);
                 const int nruns = (valid + BR - 1) / BR;
@@ -1784,14 +1814,32 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                         break;
                     }
                     if (lane == 0 && q == 0) MLA_TRACE_POINT(i, kTrEpiStart + pp);  // slot free
+                    if constexpr (MC) {
+                        // a peer that has given up may leave at any time: send it nothing more
+                        if (__shfl_sync(0xffffffffu, lane == 0 ? peer_aborted(&ctrl->abort, mrank ^ 1) : 0, 0)) {
+                            ok = false;
+                            fsite = kSiteTmaPairEmpty;
+                            ftile = i;
+                            break;
+                        }
+                    }
                     if (lane == 0) mbar_arrive_expect_tx(&ctrl->blk_full[slot], 2 * run_bytes);
                     __syncwarp();
                     if (lane < nruns) {
                         uint8_t* dst = ring + slot * C::kBlkBytes + lane * BR * 128;
+                        if constexpr (MC) {
+                            // this CTA's half of the pair, into both CTAs
+                            const int hh = mrank;
+                            tma_load_2d_mc(dst + hh * 8192, &maps.lat, &ctrl->blk_full[slot], C::kHalf * hh + 64 * kb, y,
+                                           kPairMask, pol);
+                        } else {
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh)
-                            tma_load_2d(dst + hh * 8192, &maps.lat, &ctrl->blk_full[slot], dbase + C::kHalf * hh + 64 * kb, y, pol);
+                            for (int hh = 0; hh < 2; ++hh)
+                                tma_load_2d(dst + hh * 8192, &maps.lat, &ctrl->blk_full[slot],
+                                            dbase + C::kHalf * hh + 64 * kb, y, pol);
+                        }
                     }
+                    armed = i * (C::kb_hi(pp) - C::kb_lo(pp)) + q + 1;
                 }
                 if (!ok) break;
                 if (has_rope) {
@@ -1806,9 +1854,18 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                     if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrEpiStored);  // K-blocks issued, rope slot free
                     if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], run_bytes / 2);
                     __syncwarp();
-                    if (lane < nruns)
-                        tma_load_2d(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
-                                    &ctrl->rope_full[rr], C::kD + 32 * pp, y, pol);
+                    rope_armed = i + 1;
+                    if (lane < nruns) {
+                        if constexpr (MC) {
+                            // rope half pp comes from the CTA of rank pp, into both CTAs
+                            if (pp == mrank)
+                                tma_load_2d_mc(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
+                                               &ctrl->rope_full[rr], C::kD + 32 * pp, y, kPairMask, pol);
+                        } else {
+                            tma_load_2d(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
+                                        &ctrl->rope_full[rr], C::kD + 32 * pp, y, pol);
+                        }
+                    }
                     if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrProdIssued);
                 }
                 it = nx;
@@ -1816,6 +1873,36 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
             if (!ok && lane == 0) {
                 fail(p, ctrl, kErrWaitTimeout, fsite, ftile);
                 report(p, pp ? kRoleLsu0 : kRoleTma, fsite, ftile);  // no load/convert warps here: their slot
+            }
+            if (lane == 0 && ctrl->abort) {
+                // Abort path: copies this warp armed may still be in flight; let them
+                // land before the CTA leaves (on the normal path every fill has been
+                // consumed by S). The last fill of each slot this warp armed, newest
+                // first; a slot the other producer refilled later (a shared ring)
+                // cannot be told apart by parity and waits out the deadline, which
+                // is one for all of them.
+                volatile int never = 0;
+                const unsigned long long t0 = globaltimer_ns();
+                const int nk = C::kb_hi(pp) - C::kb_lo(pp);
+                uint32_t seen = 0;
+                for (int a = armed - 1; a >= 0 && a >= armed - 2 * C::kRL; --a) {
+                    const int t = a / nk, kb = C::kb_lo(pp) + a % nk;
+                    const int slot = C::slot_of(t, kb);
+                    if (seen & (1u << slot)) continue;
+                    seen |= 1u << slot;
+                    while (!mbar_try_wait(&ctrl->blk_full[slot], C::fill_of(t, kb) & 1) && !never &&
+                           globaltimer_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
+                seen = 0;
+                for (int t = rope_armed - 1; t >= 0 && t >= rope_armed - 4; --t) {
+                    const int rr = t % C::kRR;
+                    if (seen & (1u << rr)) continue;
+                    seen |= 1u << rr;
+                    while (!mbar_try_wait(&ctrl->rope_full[rr], (t / C::kRR) & 1) && !never &&
+                           globaltimer_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
             }
             if (bad) atomicOr(status_rec(p), kErrBadBlock);
         } else if ((warp >= 4 && warp < 8) || warp >= 9) {
@@ -2281,7 +2368,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
         }
     }
     __syncthreads();
-    if constexpr (PAIR) cluster_sync_all();  // no remote traffic into this CTA after here
+    if constexpr (PAIR || MC) cluster_sync_all();  // no remote traffic into this CTA after here
     if (threadIdx.x == 0) MLA_KTRACE(3);
     if (warp == 0) {
         __syncwarp();
@@ -2638,9 +2725,18 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP,
     return launch_decode_merge(p, G, 2 * G * GY, GY, stream);
 }
 
-template <int NP, int KB, bool PAIR = false>
+template <int NP, int KB, bool PAIR = false, bool MC = false>
 struct FoldVariant {
     using C = FoldCfg<NP, KB, PAIR>;
+    static constexpr bool kCluster = PAIR || MC;
+    // cluster shape: the latent halves of a row (PAIR) side by side in x, the
+    // two row groups (MC) in y
+    static void cluster_attr(cudaLaunchAttribute& a) {
+        a.id = cudaLaunchAttributeClusterDimension;
+        a.val.clusterDim.x = PAIR ? 2 : 1;
+        a.val.clusterDim.y = MC ? 2 : 1;
+        a.val.clusterDim.z = 1;
+    }
     // Set the shared-memory attribute (once per device) and return how many
     // workers (CTAs, or clusters of two) fit on the device at once.
     static int max_workers() {
@@ -2649,17 +2745,14 @@ struct FoldVariant {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return -1;
         if (!done[dev]) {
-            auto k = mla_decode_fold_kernel<NP, KB, PAIR>;
+            auto k = mla_decode_fold_kernel<NP, KB, PAIR, MC>;
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
                 return -1;
-            if constexpr (PAIR) {
+            if constexpr (kCluster) {
                 cudaLaunchConfig_t cfg = {};
                 cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = 2;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.gridDim = dim3(2, 1, 1);
+                cluster_attr(attr[0]);
+                cfg.gridDim = dim3(PAIR ? 2 : 1, MC ? 2 : 1, 1);
                 cfg.blockDim = dim3(C::kThreads, 1, 1);
                 cfg.dynamicSmemBytes = C::kSmemBytes;
                 cfg.attrs = attr;
@@ -2684,23 +2777,23 @@ struct FoldVariant {
     static cudaError_t launch(const DecodeMaps& maps, const DecodeParams& p, int W, int GY, cudaStream_t stream) {
         cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = pdl_config(dim3(PAIR ? 2 * W : W, GY), C::kThreads, C::kSmemBytes, stream, attr);
-        if constexpr (PAIR) {
-            attr[1].id = cudaLaunchAttributeClusterDimension;
-            attr[1].val.clusterDim.x = 2;
-            attr[1].val.clusterDim.y = 1;
-            attr[1].val.clusterDim.z = 1;
+        if constexpr (kCluster) {
+            cluster_attr(attr[1]);
             cfg.numAttrs = 2;
         }
-        return cudaLaunchKernelEx(&cfg, mla_decode_fold_kernel<NP, KB, PAIR>, maps, p);
+        return cudaLaunchKernelEx(&cfg, mla_decode_fold_kernel<NP, KB, PAIR, MC>, maps, p);
     }
 };
 
 // The folded-tile variants: query rows padded to NP, latent width D (K-blocks
-// per tile 128 / D; 1792 splits the latent over a CTA pair).
-#define MLA_FOLD(NPV, DV, EXPR)                                                                    \
-    (DV == 512 ? (NPV == 16 ? EXPR(16, 4, false) : NPV == 32 ? EXPR(32, 4, false) : EXPR(64, 4, false)) \
-               : DV == 256 ? (NPV == 16 ? EXPR(16, 2, false) : EXPR(32, 2, false))                \
-                           : DV == 768 ? EXPR(16, 6, false) : EXPR(16, 7, true))
+// per tile 128 / D; 1792 splits the latent over a CTA pair); at 65 to 128
+// query rows of the 576-wide row the two row groups share each tile (MC).
+#define MLA_FOLD(NPV, DV, MCV, EXPR)                                                                          \
+    (DV == 512 ? (NPV == 16 ? EXPR(16, 4, false, false)                                                        \
+                            : NPV == 32 ? EXPR(32, 4, false, false)                                            \
+                                        : (MCV ? EXPR(64, 4, false, true) : EXPR(64, 4, false, false)))       \
+               : DV == 256 ? (NPV == 16 ? EXPR(16, 2, false, false) : EXPR(32, 2, false, false))              \
+                           : DV == 768 ? EXPR(16, 6, false, false) : EXPR(16, 7, true, false))
 
 bool fold_supported(int NP, int lat_dim) {
     return lat_dim == 512   ? (NP == 16 || NP == 32 || NP == 64)
@@ -2710,21 +2803,27 @@ bool fold_supported(int NP, int lat_dim) {
 
 bool fold_is_pair(int lat_dim) { return lat_dim == 1792; }
 
-int decode_fold_ctas(int NP, int lat_dim, int requested_ctas) {
+bool fold_is_row_pair(int NP, int lat_dim, int GY) { return NP == 64 && lat_dim == 512 && GY == 2; }
+
+int decode_fold_ctas(int NP, int lat_dim, int GY, int requested_ctas) {
     if (!fold_supported(NP, lat_dim)) return -1;
-#define MLA_FOLD_WORKERS(a, b, c) FoldVariant<a, b, c>::max_workers()
-    const int mx = MLA_FOLD(NP, lat_dim, MLA_FOLD_WORKERS);
+    const bool mc = fold_is_row_pair(NP, lat_dim, GY);
+#define MLA_FOLD_WORKERS(a, b, c, d) FoldVariant<a, b, c, d>::max_workers()
+    const int mx = MLA_FOLD(NP, lat_dim, mc, MLA_FOLD_WORKERS);
 #undef MLA_FOLD_WORKERS
     if (mx <= 0) return -1;
     if (requested_ctas <= 0) return mx;
-    return fold_is_pair(lat_dim) ? (requested_ctas >= 4 ? requested_ctas / 2 : 1) : requested_ctas;
+    if (fold_is_pair(lat_dim)) return requested_ctas >= 4 ? requested_ctas / 2 : 1;
+    if (mc) return requested_ctas >= 2 ? requested_ctas / 2 : 1;  // the grid has GY = 2 CTAs per worker
+    return requested_ctas;
 }
 
 cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int W, int GY,
                                cudaStream_t stream) {
     if (!fold_supported(NP, p.lat_dim)) return cudaErrorInvalidValue;
-#define MLA_FOLD_LAUNCH(a, b, c) FoldVariant<a, b, c>::launch(maps, p, W, GY, stream)
-    cudaError_t e = MLA_FOLD(NP, p.lat_dim, MLA_FOLD_LAUNCH);
+    const bool mc = fold_is_row_pair(NP, p.lat_dim, GY);
+#define MLA_FOLD_LAUNCH(a, b, c, d) FoldVariant<a, b, c, d>::launch(maps, p, W, GY, stream)
+    cudaError_t e = MLA_FOLD(NP, p.lat_dim, mc, MLA_FOLD_LAUNCH);
 #undef MLA_FOLD_LAUNCH
     if (e != cudaSuccess) return e;
     // status records: one per CTA

@@ -69,10 +69,11 @@ struct DecodeMaps {
 bool fold_supported(int NP, int lat_dim);
 // Whether that variant's workers are clusters of two CTAs (latent 1792).
 bool fold_is_pair(int lat_dim);
-// Workers of the folded-tile decode kernel (bf16 pools, page_size % 8 == 0, at
-// most 32 query rows): the number that fit at once, or what requested_ctas
-// CTAs make.
-int decode_fold_ctas(int NP, int lat_dim, int requested_ctas);
+// Workers of the folded-tile decode kernel (bf16 pools, page_size % 8 == 0)
+// for GY row groups: the number that fit at once, or what requested_ctas CTAs
+// make (a worker is a cluster of two for latent 1792, and for 65..128 query
+// rows of the 576-wide row, whose two row groups share each tile).
+int decode_fold_ctas(int NP, int lat_dim, int GY, int requested_ctas);
 cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int W, int GY,
                                cudaStream_t stream);
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,

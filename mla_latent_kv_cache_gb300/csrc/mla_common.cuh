@@ -139,6 +139,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
+// Reads the int at the offset of `flag` in CTA `rank` of the cluster.
+__device__ __forceinline__ int peer_aborted(volatile int* flag, uint32_t rank) {
+    int v;
+    asm volatile("ld.shared::cluster.relaxed.cluster.s32 %0, [%1];" : "=r"(v)
+                 : "r"(mapa_shared(smem_u32(const_cast<int*>(flag)), rank))
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -229,6 +238,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// tma_load_2d delivered to every CTA of the cluster named in cta_mask, at the
+// same shared-memory offset, each copy counted on that CTA's mbarrier at the
+// offset of `bar`.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                               uint16_t cta_mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
+        : "memory");
+}
+
 // Bulk prefetch of [addr, addr + bytes) into L2 (bytes a multiple of 16).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* addr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(addr)), "r"(bytes)
@@ -289,6 +310,24 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// umma_commit that arrives on the mbarrier at the offset of `bar` in every
+// CTA of the cluster named in cta_mask.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Waits (bounded, whatever the abort flag says) until every tcgen05.mma this
+// thread has issued is complete, through a one-use mbarrier of count 1.
+__device__ __forceinline__ void drain_mma(uint64_t* bar) {
+    umma_commit(bar);
+    volatile int never = 0;
+    mbar_wait(bar, 0, &never);
 }
 
 #include "tmem_ldst.inc"

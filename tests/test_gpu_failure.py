@@ -24,9 +24,10 @@ def _lib():
     yield
 
 
-@pytest.mark.parametrize("Qt", [1, 4])
+@pytest.mark.parametrize("Qt", [1, 4, 8])
 def test_bounded_wait_reports_and_context_survives(Qt):
-    # 16 query rows, and 64 (the folded kernel with one O accumulator)
+    # 16 query rows, 64 (the folded kernel with one O accumulator) and 128
+    # (two row groups as a CTA pair sharing multicast tiles)
     wl = W.make("hold", B=3, Hq=16, Qt=Qt, page_size=16, seq_lens=[700, 1500, 300], seed=91, device=DEV)
     m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
     m.test_hold_next_decode()

@@ -25,6 +25,7 @@ def _lib():
     dict(Hq=16, Qt=1, page_size=16, kind=0),   # folded tiles, 16 rows
     dict(Hq=16, Qt=2, page_size=64, kind=0),   # folded tiles, 32 rows
     dict(Hq=16, Qt=4, page_size=16, kind=0),   # folded tiles, 64 rows
+    dict(Hq=16, Qt=8, page_size=16, kind=0),   # 128 rows: a CTA pair on multicast tiles
     dict(Hq=16, Qt=4, page_size=5, kind=0),    # cluster kernel (load/convert warps), 64 rows
     dict(Hq=64, Qt=1, page_size=64, kind=1),   # fp8 pool
 ])

@@ -199,7 +199,8 @@ def test_decode_page_sizes_ragged(page_size):
     check_decode(out, lse, o, l, rows, what=f"page_size={page_size}")
 
 
-@pytest.mark.parametrize("Hq,Qt", [(16, 4), (8, 3), (32, 1), (64, 1), (80, 1), (20, 4)])
+@pytest.mark.parametrize("Hq,Qt", [(16, 4), (8, 3), (32, 1), (64, 1), (80, 1), (20, 4), (16, 8), (32, 3), (128, 1),
+                                   (48, 3)])
 def test_decode_row_shapes_and_causal(Hq, Qt):
     sl = [0, 1, 2, 3, 5, 130, 400]
     wl = W.make("rows", B=len(sl), Hq=Hq, Qt=Qt, page_size=16, seq_lens=sl, seed=40 + Hq + Qt, device=DEV)

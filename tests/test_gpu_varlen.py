@@ -42,7 +42,9 @@ CASES = [
     (16, [2, 1, 1, 2, 2, 1, 2], 64, 0, 5),   # folded tiles, 32 rows
     (16, [4, 1, 3, 2, 4, 1, 2], 16, 0, 0),   # folded tiles, 64 rows
     (16, [4, 1, 3, 2, 4, 1, 2], 8, 0, 9),    # folded tiles, 64 rows, requests cut across workers
-    (16, [6, 1, 5, 2, 3, 6, 1], 16, 0, 7),   # 96 rows: two row groups
+    (16, [6, 1, 5, 2, 3, 6, 1], 16, 0, 7),   # 96 rows: two row groups sharing each tile (a CTA pair)
+    (16, [8, 1, 7, 3, 8, 5, 8], 16, 0, 0),   # 1 + 7 drafts: 128 rows, one cache read per request
+    (16, [8, 2, 8, 1, 6, 8, 4], 64, 0, 11),  # the same with 64-token pages, requests cut across pairs
     (16, [3, 4, 1, 2, 4, 2, 1], 64, 1, 0),   # fp8 pool, 64 rows
 ]
 
@@ -50,6 +52,7 @@ CASES = [
 @pytest.mark.parametrize("Hq,qlens,page_size,kind,num_ctas", CASES)
 def test_decode_varlen_matches_the_oracle(Hq, qlens, page_size, kind, num_ctas):
     sl = [700, 2, 1500, 0, 257, 3, 64 * 5 + 1]   # requests shorter than their step, and an empty one
+    assert len(qlens) == len(sl)  # one verify length per request (checked before any device indexing)
     qmax = max(qlens)
     wl = W.make("varlen", B=len(sl), Hq=Hq, Qt=qmax, page_size=page_size, seq_lens=sl, kind=kind,
                 write_all=(kind == 1), seed=300 + Hq + page_size + kind, device=DEV)
