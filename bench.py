@@ -52,6 +52,8 @@ CONFIG_TEXT = {
     "fp8": "B=64 Hq=64 seq 32768 page 64 fp8_ds_mla (656 B rows)",
     "verify": "the mtp workload with a verify length of its own per request, U{1..4} (seeded): "
               "mla_decode_varlen",
+    "verify8": "the mtp pool and requests with verify steps of 1 + k tokens, k U{0..7} per request (seeded; up "
+               "to 128 query rows a request, one cache read each): mla_decode_varlen",
     "gather": "fp8_ds_mla pool of the fp8 workload (B=64 x 32768 tokens, page 64) gathered into "
               "[2097152, 576] bf16 rows",
 }
@@ -217,21 +219,21 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
-def verify_qlens(B, rank=0):
-    """The verify workload's per-request verify lengths, U{1..4} (seeded)."""
+def verify_qlens(B, rank=0, qmax=4):
+    """The verify workloads' per-request verify lengths, U{1..qmax} (seeded)."""
     import numpy as np
-    return np.random.default_rng(7 + 1000 * rank).integers(1, 5, size=B)
+    return np.random.default_rng(7 + 1000 * rank).integers(1, qmax + 1, size=B)
 
 
 WORKLOAD_SEED = {"tiny": 1, "batched": 2, "long": 3, "mtp": 4, "fp8": 5}
 # workloads measured beside the headline one and reported in its line
-SIDE_WORKLOADS = ("long", "fp8", "batched", "tiny", "verify")
+SIDE_WORKLOADS = ("long", "fp8", "batched", "tiny", "verify", "verify8")
 
 
 def config_dict(name, ctx_tokens, cache_bytes, row_bytes, ws_):
     """The `config` object of a decode line; both arms use it, so the
     reference arm's line names the same workload in the same words."""
-    varlen = name == "verify"
+    varlen = name.startswith("verify")
     return {"workload": name, "shape": CONFIG_TEXT[name], "context_tokens": ctx_tokens,
             "cache_bytes_per_step": cache_bytes, "row_bytes": row_bytes,
             "l2": "flushed before every step (256 MiB write, outside the timed events)",
@@ -245,8 +247,8 @@ def build_workload(name, dev, rank=0, requests=None):
     requests), seeded per rank. `requests` (long and fp8 only) keeps that
     many of their equal-length requests: a cut-down copy for profiling."""
     from mla_latent_kv_cache_gb300 import workloads as W
-    base = "mtp" if name == "verify" else name
-    kw = {}
+    base = "mtp" if name.startswith("verify") else name
+    kw = {"Qt": 8} if name == "verify8" else {}
     if requests is not None:
         if base not in ("long", "fp8"):
             raise SystemExit("--requests applies to the long and fp8 workloads only")
@@ -263,14 +265,14 @@ def measure_gpu(name, args, dev, rank, ws_, clock_csv=None):
     import torch.distributed as dist
     import mla_latent_kv_cache_gb300 as m
 
-    varlen = name == "verify"
+    varlen = name.startswith("verify")
     wl = build_workload(name, dev, rank, args.requests if name == args.config else None)
     cu_q = None
     q_lat_s, q_pe_s = wl.q_lat, wl.q_pe  # the step's query rows
     if varlen:
         # per-request verify lengths U{1..4}: request b's queries are the first
         # q_len_b of its four query rows
-        qlens = verify_qlens(wl.B, rank)
+        qlens = verify_qlens(wl.B, rank, wl.Qt)
         pick = torch.tensor([b * wl.Qt + t for b in range(wl.B) for t in range(int(qlens[b]))], dtype=torch.int64,
                             device=dev)
         q_lat_s = wl.q_lat[pick].contiguous()
@@ -724,7 +726,7 @@ def _oracle_run(wl, prep, cap=None, qt=None):
 
 def _qt_for(config, wl):
     """Per-request verify lengths of the workload (None: wl.Qt for all)."""
-    return verify_qlens(wl.B) if config == "verify" else None
+    return verify_qlens(wl.B, 0, wl.Qt) if config.startswith("verify") else None
 
 
 def oracle_sample(config, wl, budget_s=15.0):

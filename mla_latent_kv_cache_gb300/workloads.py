@@ -237,11 +237,14 @@ def mtp_seq_lens(seed: int = 4) -> np.ndarray:
             return sl
 
 
-def mtp(device="cpu", seed: int = 4) -> Workload:
+def mtp(device="cpu", seed: int = 4, Qt: int = 4) -> Workload:
+    """The large-pool verify workload; Qt = 4 (1 + 3 drafts) as named, or a
+    longer step (1 + 7 drafts: Qt = 8) on the same pool and requests."""
     nb = MTP_POOL_SLOTS // MTP_PAGE            # 612,500 pages
     first = -(-INT32_WRAP_SLOT // MTP_PAGE)    # 233,017: first page wholly above the wrap slot
-    return make("mtp", B=128, Hq=16, Qt=4, page_size=MTP_PAGE, seq_lens=mtp_seq_lens(seed),
-                num_blocks=nb, min_block=first, force_block=nb - 1, seed=seed, device=device)
+    return make("mtp" if Qt == 4 else f"mtp_q{Qt}", B=128, Hq=16, Qt=Qt, page_size=MTP_PAGE,
+                seq_lens=mtp_seq_lens(seed), num_blocks=nb, min_block=first, force_block=nb - 1, seed=seed,
+                device=device)
 
 
 def fp8(device="cpu", seed: int = 5, B: int = 64) -> Workload:
