@@ -223,13 +223,16 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     // pages whose rows cannot be fetched as 8-row TMA boxes go through the
     // load/convert warps
     const bool lsu = (page_size % 8) != 0;
-    // bf16 pools: folded 64-token tiles, one CTA per worker; fp8 pools and
-    // odd page sizes: 128-token tiles split over clusters of two CTAs
-    const bool fold = !lsu && cache_kind == MLA_CACHE_BF16_576;
+    // bf16 pools, and fp8 pools at 33..64 query rows: folded 64-token tiles,
+    // one CTA per worker (or a CTA pair, see decode_fold_ctas); other fp8
+    // pools and odd page sizes: 128-token tiles split over clusters of two
+    // CTAs
+    const bool fold = !lsu && (cache_kind == MLA_CACHE_BF16_576 || mla::fold_supported(NP, D, cache_kind, GY));
     // other latent widths: bf16 rows of D + 64 values, folded tiles only
-    if (D != 512 && (!fold || !mla::fold_supported(NP, D))) return MLA_ERR_UNSUPPORTED;
+    if (D != 512 && (!fold || !mla::fold_supported(NP, D, cache_kind, GY))) return MLA_ERR_UNSUPPORTED;
     const int nctas = ws_ctas(num_ctas, di.sms);  // what the workspace holds records and slots for
-    int W = fold ? mla::decode_fold_ctas(NP, D, GY, num_ctas) : mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
+    int W = fold ? mla::decode_fold_ctas(NP, D, cache_kind, GY, num_ctas)
+                 : mla::decode_clusters(NP, lsu, cache_kind, num_ctas);
     if (W <= 0) return MLA_ERR_CUDA;
     W = std::min(W, (fold && !mla::fold_is_pair(D)) ? nctas : nctas / 2);
     const int tile = fold ? 64 : 128;
@@ -284,7 +287,9 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
             // bytes of the 656-byte row: codes [0, 512), scales [512, 528)
             cuuint64_t gdim[2] = {row_bytes, static_cast<cuuint64_t>(num_slots)};
             cuuint64_t gstride[1] = {row_bytes};
-            cuuint32_t box_codes[2] = {256u, static_cast<cuuint32_t>(br)};
+            // folded tiles take 64 code bytes of a row per box (one K-block's
+            // half), the cluster kernel 256 (a CTA's half of the row)
+            cuuint32_t box_codes[2] = {fold ? 64u : 256u, static_cast<cuuint32_t>(br)};
             cuuint32_t box_scales[2] = {16u, static_cast<cuuint32_t>(br)};
             r = enc(&tmap_lat, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), gdim, gstride, box_codes,
                     estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -343,7 +348,7 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     p.cu_q = cu_q;
     p.lat_dim = D;
     p.rope_dim = mla::kP;
-    cudaError_t e = fold ? mla::launch_decode_fold(maps, p, NP, W, GY, s)
+    cudaError_t e = fold ? mla::launch_decode_fold(maps, p, NP, cache_kind, W, GY, s)
                          : mla::launch_decode(maps, p, NP, lsu, cache_kind, W, GY, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -1451,9 +1451,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // Nothing crosses between CTAs: a tile's shared memory is held from its load
 // to its value product only, with no exchange latency in between.
 
-template <int NP, int KB, bool PAIR = false>
+template <int NP, int KB, bool PAIR = false, int KIND = 0>
 struct FoldCfg {
     static_assert(NP == 16 || NP == 32 || (NP == 64 && KB == 4 && !PAIR), "NP");
+    // KIND 1: fp8_ds_mla rows (656 bytes), at 64 query rows of the 576-wide row
+    static_assert(KIND == 0 || (NP == 64 && KB == 4 && !PAIR), "fp8 rows");
     // KB K-blocks per tile and CTA: 128 KB latent values in two halves of 64 KB.
     // PAIR: the two CTAs of a cluster take the latent's two halves (1792 = 2 x 896)
     static_assert(PAIR ? (KB == 7 && NP == 16) : (KB == 2 || KB == 4 || (KB == 6 && NP == 16)), "latent width");
@@ -1496,7 +1498,16 @@ struct FoldCfg {
     static constexpr int kXR = NP == 64 ? 4 : kNH;
     static constexpr int kXBytes = kSG * 128 * kXR * 4;
     // 9 warps, plus the second softmax group's 4
-    static constexpr int kThreads = 288 + 128 * (kSG - 1);
+    // fp8 rows: four expand warps (one per K-block of a tile) widen the e4m3
+    // codes into bf16; the pools' 64-token pages make few boxes a tile, so one
+    // producer warp issues them all and the second producer warp is an
+    // expander (four warps to a scheduler at most: 128 registers a thread)
+    static constexpr int kExpandWarps = KIND == 1 ? 4 : 0;
+    static constexpr int kProducers = KIND == 1 ? 1 : 2;
+    static constexpr int kThreads = 288 + 128 * (kSG - 1) + 32 * (kExpandWarps - (kProducers == 1 ? 1 : 0));
+    // K-blocks [kb_lo(pp), kb_hi(pp)) of each tile: producer pp (and PV issuer pp)
+    static __host__ __device__ constexpr int prod_lo(int pp) { return kProducers == 1 ? 0 : kb_lo(pp); }
+    static __host__ __device__ constexpr int prod_hi(int pp) { return kProducers == 1 ? KB : kb_hi(pp); }
     // one P buffer at 64 rows: the softmax writes P(i) once PV(i - 1) has
     // read P(i - 1), which a tile's softmax outlasts
     static constexpr int kPBufs = NP == 64 ? 1 : 2;
@@ -1507,7 +1518,11 @@ struct FoldCfg {
     static constexpr int kOffP = kOffX + kXBytes;
     static constexpr int kX2Bytes = PAIR ? 128 * kNH * 4 : 0;  // the peer CTA's partial scores
     static constexpr int kOffX2 = kOffP + kPBufs * kPBytes;
-    static constexpr int kOffCtrl = kOffX2 + kX2Bytes;
+    // fp8 rows: each tile's 64 rows of four fp32 block scales, in two slots
+    // (tile i in slot i % 2)
+    static constexpr int kScaleBytes = KIND == 1 ? kTok * 16 : 0;
+    static constexpr int kOffScale = kOffX2 + kX2Bytes;
+    static constexpr int kOffCtrl = kOffScale + 2 * kScaleBytes;
     static constexpr int kSmemBytes = kOffCtrl + 3584 + 1024;  // + control block, alignment slack
     // TMEM: two O accumulators of KB x NP columns (M-tile m at m * NP; one at
     // 64 rows, where two would leave no room for S), then two S buffers of
@@ -1534,6 +1549,8 @@ struct FoldCtrl {
     uint64_t p_full[2];
     uint64_t x2full, x2free;         // CTA pair: the peer's partial scores landed / it has read ours
     uint64_t fin[3];                 // the S and PV issuers' products have all completed (at exit)
+    uint64_t raw_full[8];            // fp8 rows: a K-block's codes landed in the upper half of its slot
+    uint64_t scale_full[2], scale_empty[2];  // fp8 rows: a tile's block scales landed / both expanders done
     uint32_t tmem_base;
     int abort;
     int t_begin, t_end, b0, j0;
@@ -1551,11 +1568,19 @@ static_assert(sizeof(FoldCtrl) <= 3584, "control block");
 // boxes with multicast, so each cached row crosses HBM once for both groups,
 // and a ring slot is refilled only when both CTAs' value products have
 // released it.
-template <int NP, int KB, bool PAIR, bool MC>
-__global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
+// KIND 1: fp8_ds_mla rows. TMA lands each K-block's e4m3 codes in the upper
+// half of its slot and each tile's block scales in a scale slot; two expand
+// warps widen the codes into the bf16 layout the products read, in place.
+template <int NP, int KB, bool PAIR, bool MC, int KIND>
+__global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
     mla_decode_fold_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     static_assert(!MC || (NP == 64 && !PAIR), "row-group pairs are 64-row CTAs");
-    using C = FoldCfg<NP, KB, PAIR>;
+    static_assert(!(MC && KIND == 1), "fp8 rows: one row group per worker");
+    using C = FoldCfg<NP, KB, PAIR, KIND>;
+    // first expand warp (fp8 rows), after the softmax groups
+    constexpr int kExp0 = 9 + 4 * (C::kSG - 1);
+    // the rope's element column in a row: after the latent (bf16), or at byte 528 (fp8)
+    constexpr int kRopeX = KIND == 1 ? 264 : C::kD;
     constexpr uint16_t kPairMask = 0x3;
     constexpr int kT = C::kTok;
     using It = TileItT<6>;
@@ -1567,6 +1592,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
     uint8_t* xbuf = smem + C::kOffX;
     uint8_t* pbufs = smem + C::kOffP;
     uint8_t* x2buf = smem + C::kOffX2;
+    uint8_t* scales = smem + C::kOffScale;
     FoldCtrl* ctrl = reinterpret_cast<FoldCtrl*>(smem + C::kOffCtrl);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1590,10 +1616,17 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
         }
         // a rope slot is armed by both producer warps (one half each)
         for (int i = 0; i < C::kRR; ++i) {
-            mbar_init(&ctrl->rope_full[i], 2);
+            mbar_init(&ctrl->rope_full[i], C::kProducers);
             mbar_init(&ctrl->rope_empty[i], MC ? 2 : 1);
         }
         for (int i = 0; i < 3; ++i) mbar_init(&ctrl->fin[i], 1);
+        if constexpr (KIND == 1) {
+            for (int i = 0; i < C::kRL; ++i) mbar_init(&ctrl->raw_full[i], 1);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&ctrl->scale_full[i], 1);
+                mbar_init(&ctrl->scale_empty[i], C::kExpandWarps);
+            }
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctrl->s_full[i], 1);
             mbar_init(&ctrl->s_free[i], C::kSG);  // one arrive per softmax group
@@ -1766,7 +1799,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                 it.next(p.seq_lens, p.B);
             }
             drain_mma(&ctrl->fin[1 + mt]);
-        } else if (warp == 1 || warp == 8) {
+        } else if (warp == 1 || (warp == 8 && C::kProducers == 2)) {
             // ------------------------------------------------- TMA producers
             // Warp 1 loads K-blocks 0, 1 and the first rope half of every tile,
             // warp 8 K-blocks 2, 3 and the second rope half (with 16-token pages a
@@ -1792,7 +1825,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
             // K-block fills (tile-major, this warp's K-blocks) and rope fills (tiles)
             // whose barriers this warp has armed: at exit it waits for those fills
             // to land, so that no copy arrives after the CTA is gone
-            int armed = 0, rope_armed = 0;
+            int armed = 0, rope_armed = 0, scale_armed = 0;
             for (int i = 0; i < ntiles && ok; ++i) {
                 const int valid = min(kT, it.T - it.j * kT);
                 const int nruns = (valid + BR - 1) / BR;
@@ -1802,9 +1835,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                 nx.next(p.seq_lens, p.B);
                 if (i + 1 < ntiles) y_next = run_slot(nx);
                 if (lane == 0) MLA_TRACE_POINT(i, kTrProdStart + 0 * pp);
-                for (int q = 0; q < (KB + 1) / 2; ++q) {
-                    const int kb = C::kb_lo(pp) + q;
-                    if (kb >= C::kb_hi(pp)) break;
+                for (int q = 0; q < C::prod_hi(pp) - C::prod_lo(pp); ++q) {
+                    const int kb = C::prod_lo(pp) + q;
                     const int slot = C::slot_of(i, kb), fill = C::fill_of(i, kb);
                     if (fill > 0 &&
                         !__all_sync(0xffffffffu, mbar_wait(&ctrl->blk_empty[slot], (fill - 1) & 1, &ctrl->abort))) {
@@ -1823,6 +1855,21 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                             break;
                         }
                     }
+                    if constexpr (KIND == 1) {
+                        // the codes of both halves (64 bytes a row each) into the slot's
+                        // upper half: first-half rows at 8 KB, second-half rows at 12 KB
+                        if (lane == 0) mbar_arrive_expect_tx(&ctrl->raw_full[slot], 2u * nruns * BR * 64);
+                        __syncwarp();
+                        if (lane < nruns) {
+                            uint8_t* dst = ring + slot * C::kBlkBytes + 8192 + lane * BR * 64;
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh)
+                                tma_load_2d(dst + hh * 4096, &maps.lat, &ctrl->raw_full[slot], 256 * hh + 64 * kb, y,
+                                            pol);
+                        }
+                        armed = i * (C::prod_hi(pp) - C::prod_lo(pp)) + q + 1;
+                        continue;
+                    }
                     if (lane == 0) mbar_arrive_expect_tx(&ctrl->blk_full[slot], 2 * run_bytes);
                     __syncwarp();
                     if (lane < nruns) {
@@ -1839,9 +1886,29 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                                             dbase + C::kHalf * hh + 64 * kb, y, pol);
                         }
                     }
-                    armed = i * (C::kb_hi(pp) - C::kb_lo(pp)) + q + 1;
+                    armed = i * (C::prod_hi(pp) - C::prod_lo(pp)) + q + 1;
                 }
                 if (!ok) break;
+                if constexpr (KIND == 1) {
+                    if (pp == 0) {
+                        // the tile's block scales, 16 bytes a row, once both expanders
+                        // are done with the slot's tile before last
+                        const int sb = i & 1;
+                        if (i >= 2 &&
+                            !__all_sync(0xffffffffu, mbar_wait(&ctrl->scale_empty[sb], ((i >> 1) - 1) & 1, &ctrl->abort))) {
+                            ok = false;
+                            fsite = kSiteRawFull;
+                            ftile = i;
+                            break;
+                        }
+                        if (lane == 0) mbar_arrive_expect_tx(&ctrl->scale_full[sb], static_cast<uint32_t>(nruns * BR * 16));
+                        __syncwarp();
+                        scale_armed = i + 1;
+                        if (lane < nruns)
+                            tma_load_2d(scales + sb * C::kScaleBytes + lane * BR * 16, &maps.aux, &ctrl->scale_full[sb], 512,
+                                        y, pol);
+                    }
+                }
                 if (has_rope) {
                     const int rr = i % C::kRR;
                     if (i >= C::kRR &&
@@ -1852,18 +1919,26 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                         break;
                     }
                     if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrEpiStored);  // K-blocks issued, rope slot free
-                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], run_bytes / 2);
+                    // rope half pp (each producer one half; a single producer both)
+                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], C::kProducers == 1 ? run_bytes : run_bytes / 2);
                     __syncwarp();
                     rope_armed = i + 1;
-                    if (lane < nruns) {
+                    if constexpr (C::kProducers == 1) {
+                        if (lane < nruns) {
+#pragma unroll
+                            for (int rh = 0; rh < 2; ++rh)
+                                tma_load_2d(rope_ring + rr * C::kRopeBytes + rh * 4096 + lane * BR * 64, &maps.rope,
+                                            &ctrl->rope_full[rr], kRopeX + 32 * rh, y, pol);
+                        }
+                    } else if (lane < nruns) {
                         if constexpr (MC) {
                             // rope half pp comes from the CTA of rank pp, into both CTAs
                             if (pp == mrank)
                                 tma_load_2d_mc(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
-                                               &ctrl->rope_full[rr], C::kD + 32 * pp, y, kPairMask, pol);
+                                               &ctrl->rope_full[rr], kRopeX + 32 * pp, y, kPairMask, pol);
                         } else {
                             tma_load_2d(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
-                                        &ctrl->rope_full[rr], C::kD + 32 * pp, y, pol);
+                                        &ctrl->rope_full[rr], kRopeX + 32 * pp, y, pol);
                         }
                     }
                     if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrProdIssued);
@@ -1883,17 +1958,21 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                 // is one for all of them.
                 volatile int never = 0;
                 const unsigned long long t0 = globaltimer_ns();
-                const int nk = C::kb_hi(pp) - C::kb_lo(pp);
+                const int nk = C::prod_hi(pp) - C::prod_lo(pp);
                 uint32_t seen = 0;
                 for (int a = armed - 1; a >= 0 && a >= armed - 2 * C::kRL; --a) {
-                    const int t = a / nk, kb = C::kb_lo(pp) + a % nk;
+                    const int t = a / nk, kb = C::prod_lo(pp) + a % nk;
                     const int slot = C::slot_of(t, kb);
                     if (seen & (1u << slot)) continue;
                     seen |= 1u << slot;
-                    while (!mbar_try_wait(&ctrl->blk_full[slot], C::fill_of(t, kb) & 1) && !never &&
-                           globaltimer_ns() - t0 < kWaitLimitNs) {
+                    uint64_t* full = KIND == 1 ? &ctrl->raw_full[slot] : &ctrl->blk_full[slot];
+                    while (!mbar_try_wait(full, C::fill_of(t, kb) & 1) && !never && globaltimer_ns() - t0 < kWaitLimitNs) {
                     }
                 }
+                for (int t = scale_armed - 1; t >= 0 && t >= scale_armed - 2; --t)
+                    while (!mbar_try_wait(&ctrl->scale_full[t & 1], (t >> 1) & 1) && !never &&
+                           globaltimer_ns() - t0 < kWaitLimitNs) {
+                    }
                 seen = 0;
                 for (int t = rope_armed - 1; t >= 0 && t >= rope_armed - 4; --t) {
                     const int rr = t % C::kRR;
@@ -1905,7 +1984,76 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR>::kThreads, 1)
                 }
             }
             if (bad) atomicOr(status_rec(p), kErrBadBlock);
-        } else if ((warp >= 4 && warp < 8) || warp >= 9) {
+        } else if (KIND == 1 && (warp >= kExp0 || warp == 8)) {
+            // ------------------------------------------- expand warps (fp8 rows)
+            // Warp e widens K-block e of every tile: the codes TMA
+            // landed in the upper half of the slot (first-half rows at 8 KB + 64 t,
+            // second-half rows at 12 KB + 64 t for token t) become bf16 rows of the
+            // 128-byte-swizzled layout S and PV read, each code times its token's
+            // scale of the 128-value block it belongs to (one fp32 multiply, bf16
+            // round to nearest even). A second-half row overwrites codes, so every
+            // lane holds its codes in registers before any row is written.
+            const int e = warp == 8 ? 0 : warp - kExp0 + 1;  // K-block e of every tile
+            bool ok = true;
+            int fsite = 0, ftile = 0;
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int sb = i & 1;
+                if (!mbar_wait(&ctrl->scale_full[sb], (i >> 1) & 1, &ctrl->abort)) {
+                    ok = false;
+                    fsite = kSiteRawFull;
+                    ftile = i;
+                    break;
+                }
+                const uint8_t* sc = scales + sb * C::kScaleBytes;
+                for (int q = 0; q < KB / (C::kExpandWarps > 0 ? C::kExpandWarps : 1); ++q) {
+                    const int kb = e + q;
+                    const int slot = C::slot_of(i, kb);
+                    if (!mbar_wait(&ctrl->raw_full[slot], C::fill_of(i, kb) & 1, &ctrl->abort)) {
+                        ok = false;
+                        fsite = kSiteRawFull;
+                        ftile = i;
+                        break;
+                    }
+                    if (lane == 0 && e == 0 && q == 0) MLA_TRACE_POINT(i, kTrSmXFree);  // codes landed
+                    uint8_t* blk = ring + slot * C::kBlkBytes;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 cd[2][4];
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const uint4* src = reinterpret_cast<const uint4*>(blk + 8192 + h * 4096 + (lane + 32 * k) * 64);
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) cd[k][u] = src[u];
+                        }
+                        __syncwarp();  // every lane's codes are in registers
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int t = lane + 32 * k, r = 64 * h + t;
+                            const float scale = *reinterpret_cast<const float*>(sc + t * 16 + 4 * (2 * h + (kb >> 1)));
+                            uint8_t* row = blk + r * 128;
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                uint4 lo, hi;
+                                dequant16(cd[k][u], scale, lo, hi);
+                                *reinterpret_cast<uint4*>(row + (((2 * u) ^ (r & 7)) << 4)) = lo;
+                                *reinterpret_cast<uint4*>(row + (((2 * u + 1) ^ (r & 7)) << 4)) = hi;
+                            }
+                        }
+                        __syncwarp();  // the first halves' codes are consumed before h = 1 writes over them
+                    }
+                    fence_proxy_async_smem();  // the products read these rows through the async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctrl->blk_full[slot]);
+                }
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(&ctrl->scale_empty[sb]);
+                if (lane == 0) MLA_TRACE_POINT(i, e == 0 ? kTrEpiEnd : kTrEpiHalf);  // expander e done with tile i
+            }
+            if (!ok && lane == 0) {
+                fail(p, ctrl, kErrWaitTimeout, fsite, ftile);
+                report(p, kRoleLsu0 + 1, fsite, ftile);
+            }
+        } else if ((warp >= 4 && warp < 8) || (warp >= 9 && warp < kExp0)) {
             // ------------------------------------------ softmax + epilogue
             // Thread st reads TMEM lane st = A row st: half hf of token tt (lane
             // quadrants 0, 1 the first halves, 2, 3 the second). Softmax group grp
@@ -2725,9 +2873,9 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP,
     return launch_decode_merge(p, G, 2 * G * GY, GY, stream);
 }
 
-template <int NP, int KB, bool PAIR = false, bool MC = false>
+template <int NP, int KB, bool PAIR = false, bool MC = false, int KIND = 0>
 struct FoldVariant {
-    using C = FoldCfg<NP, KB, PAIR>;
+    using C = FoldCfg<NP, KB, PAIR, KIND>;
     static constexpr bool kCluster = PAIR || MC;
     // cluster shape: the latent halves of a row (PAIR) side by side in x, the
     // two row groups (MC) in y
@@ -2745,7 +2893,7 @@ struct FoldVariant {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return -1;
         if (!done[dev]) {
-            auto k = mla_decode_fold_kernel<NP, KB, PAIR, MC>;
+            auto k = mla_decode_fold_kernel<NP, KB, PAIR, MC, KIND>;
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
                 return -1;
             if constexpr (kCluster) {
@@ -2781,21 +2929,24 @@ struct FoldVariant {
             cluster_attr(attr[1]);
             cfg.numAttrs = 2;
         }
-        return cudaLaunchKernelEx(&cfg, mla_decode_fold_kernel<NP, KB, PAIR, MC>, maps, p);
+        return cudaLaunchKernelEx(&cfg, mla_decode_fold_kernel<NP, KB, PAIR, MC, KIND>, maps, p);
     }
 };
 
 // The folded-tile variants: query rows padded to NP, latent width D (K-blocks
 // per tile 128 / D; 1792 splits the latent over a CTA pair); at 65 to 128
-// query rows of the 576-wide row the two row groups share each tile (MC).
-#define MLA_FOLD(NPV, DV, MCV, EXPR)                                                                          \
-    (DV == 512 ? (NPV == 16 ? EXPR(16, 4, false, false)                                                        \
-                            : NPV == 32 ? EXPR(32, 4, false, false)                                            \
-                                        : (MCV ? EXPR(64, 4, false, true) : EXPR(64, 4, false, false)))       \
-               : DV == 256 ? (NPV == 16 ? EXPR(16, 2, false, false) : EXPR(32, 2, false, false))              \
-                           : DV == 768 ? EXPR(16, 6, false, false) : EXPR(16, 7, true, false))
+// query rows of the 576-wide row the two row groups share each tile (MC);
+// fp8_ds_mla rows (KINDV 1) at 64 rows.
+#define MLA_FOLD(NPV, DV, MCV, KINDV, EXPR)                                                                   \
+    (DV == 512 ? (NPV == 16 ? EXPR(16, 4, false, false, 0)                                                     \
+                            : NPV == 32 ? EXPR(32, 4, false, false, 0)                                         \
+                                        : (MCV ? EXPR(64, 4, false, true, 0)                                   \
+                                               : KINDV ? EXPR(64, 4, false, false, 1) : EXPR(64, 4, false, false, 0))) \
+               : DV == 256 ? (NPV == 16 ? EXPR(16, 2, false, false, 0) : EXPR(32, 2, false, false, 0))        \
+                           : DV == 768 ? EXPR(16, 6, false, false, 0) : EXPR(16, 7, true, false, 0))
 
-bool fold_supported(int NP, int lat_dim) {
+bool fold_supported(int NP, int lat_dim, int kind, int GY) {
+    if (kind == 1) return lat_dim == 512 && NP == 64 && GY == 1;
     return lat_dim == 512   ? (NP == 16 || NP == 32 || NP == 64)
            : lat_dim == 256 ? (NP == 16 || NP == 32)
                             : ((lat_dim == 768 || lat_dim == 1792) && NP == 16);
@@ -2805,11 +2956,11 @@ bool fold_is_pair(int lat_dim) { return lat_dim == 1792; }
 
 bool fold_is_row_pair(int NP, int lat_dim, int GY) { return NP == 64 && lat_dim == 512 && GY == 2; }
 
-int decode_fold_ctas(int NP, int lat_dim, int GY, int requested_ctas) {
-    if (!fold_supported(NP, lat_dim)) return -1;
-    const bool mc = fold_is_row_pair(NP, lat_dim, GY);
-#define MLA_FOLD_WORKERS(a, b, c, d) FoldVariant<a, b, c, d>::max_workers()
-    const int mx = MLA_FOLD(NP, lat_dim, mc, MLA_FOLD_WORKERS);
+int decode_fold_ctas(int NP, int lat_dim, int kind, int GY, int requested_ctas) {
+    if (!fold_supported(NP, lat_dim, kind, GY)) return -1;
+    const bool mc = kind == 0 && fold_is_row_pair(NP, lat_dim, GY);
+#define MLA_FOLD_WORKERS(a, b, c, d, e) FoldVariant<a, b, c, d, e>::max_workers()
+    const int mx = MLA_FOLD(NP, lat_dim, mc, kind == 1, MLA_FOLD_WORKERS);
 #undef MLA_FOLD_WORKERS
     if (mx <= 0) return -1;
     if (requested_ctas <= 0) return mx;
@@ -2818,12 +2969,12 @@ int decode_fold_ctas(int NP, int lat_dim, int GY, int requested_ctas) {
     return requested_ctas;
 }
 
-cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int W, int GY,
+cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int kind, int W, int GY,
                                cudaStream_t stream) {
-    if (!fold_supported(NP, p.lat_dim)) return cudaErrorInvalidValue;
-    const bool mc = fold_is_row_pair(NP, p.lat_dim, GY);
-#define MLA_FOLD_LAUNCH(a, b, c, d) FoldVariant<a, b, c, d>::launch(maps, p, W, GY, stream)
-    cudaError_t e = MLA_FOLD(NP, p.lat_dim, mc, MLA_FOLD_LAUNCH);
+    if (!fold_supported(NP, p.lat_dim, kind, GY)) return cudaErrorInvalidValue;
+    const bool mc = kind == 0 && fold_is_row_pair(NP, p.lat_dim, GY);
+#define MLA_FOLD_LAUNCH(a, b, c, d, e) FoldVariant<a, b, c, d, e>::launch(maps, p, W, GY, stream)
+    cudaError_t e = MLA_FOLD(NP, p.lat_dim, mc, kind == 1, MLA_FOLD_LAUNCH);
 #undef MLA_FOLD_LAUNCH
     if (e != cudaSuccess) return e;
     // status records: one per CTA

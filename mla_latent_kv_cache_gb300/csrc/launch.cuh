@@ -64,17 +64,17 @@ struct DecodeMaps {
     CUtensorMap lat, aux, rope, q, qpe;
 };
 
-// Whether the folded-tile kernel has a variant for NP query rows and this
-// latent width.
-bool fold_supported(int NP, int lat_dim);
+// Whether the folded-tile kernel has a variant for NP query rows, this latent
+// width, cache kind and number of row groups.
+bool fold_supported(int NP, int lat_dim, int kind, int GY);
 // Whether that variant's workers are clusters of two CTAs (latent 1792).
 bool fold_is_pair(int lat_dim);
 // Workers of the folded-tile decode kernel (bf16 pools, page_size % 8 == 0)
 // for GY row groups: the number that fit at once, or what requested_ctas CTAs
 // make (a worker is a cluster of two for latent 1792, and for 65..128 query
 // rows of the 576-wide row, whose two row groups share each tile).
-int decode_fold_ctas(int NP, int lat_dim, int GY, int requested_ctas);
-cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int W, int GY,
+int decode_fold_ctas(int NP, int lat_dim, int kind, int GY, int requested_ctas);
+cudaError_t launch_decode_fold(const DecodeMaps& maps, const DecodeParams& p, int NP, int kind, int W, int GY,
                                cudaStream_t stream);
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeParams& p, int NP, bool lsu, int kind, int G, int GY,
                           cudaStream_t stream);

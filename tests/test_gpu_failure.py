@@ -24,11 +24,13 @@ def _lib():
     yield
 
 
-@pytest.mark.parametrize("Qt", [1, 4, 8])
-def test_bounded_wait_reports_and_context_survives(Qt):
-    # 16 query rows, 64 (the folded kernel with one O accumulator) and 128
-    # (two row groups as a CTA pair sharing multicast tiles)
-    wl = W.make("hold", B=3, Hq=16, Qt=Qt, page_size=16, seq_lens=[700, 1500, 300], seed=91, device=DEV)
+@pytest.mark.parametrize("Qt,kind", [(1, 0), (4, 0), (8, 0), (4, 1)])
+def test_bounded_wait_reports_and_context_survives(Qt, kind):
+    # 16 query rows, 64 (the folded kernel with one O accumulator), 128 (two
+    # row groups as a CTA pair sharing multicast tiles), and an fp8 pool at 64
+    # rows (expand warps)
+    wl = W.make("hold", B=3, Hq=16, Qt=Qt, page_size=16, seq_lens=[700, 1500, 300], seed=91, device=DEV, kind=kind,
+                write_all=(kind == 1))
     m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
     m.test_hold_next_decode()
     out, lse, ws = m.decode(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens,
@@ -50,5 +52,6 @@ def test_bounded_wait_reports_and_context_survives(Qt):
     torch.cuda.synchronize()
     assert m.device_status(ws) == 0
     o = out.cpu().numpy()[c["rows"]].astype(np.float64)
-    assert np.all(np.abs(o - ref_o) <= 1e-2 + 2e-2 * np.abs(ref_o))
-    assert np.abs(lse.cpu().numpy()[c["rows"]] - ref_l).max() <= 1e-3
+    tol = (1e-2 + 2e-2 * np.abs(ref_o)) if kind == 0 else 5e-2
+    assert np.all(np.abs(o - ref_o) <= tol)
+    assert np.abs(lse.cpu().numpy()[c["rows"]] - ref_l).max() <= (1e-3 if kind == 0 else 5e-2)

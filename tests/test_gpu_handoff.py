@@ -37,6 +37,7 @@ CASES = [
     ("fold32", W.KIND_BF16, 32, 64),
     ("fold64", W.KIND_BF16, 64, 16),
     ("fold128_pair", W.KIND_BF16, 128, 16),
+    ("fold64_fp8", W.KIND_FP8, 64, 64),
     ("cluster16_fp8", W.KIND_FP8, 16, 64),
     ("lsu16", W.KIND_BF16, 16, 3),
     ("lsu32", W.KIND_BF16, 32, 5),

@@ -226,12 +226,15 @@ def test_many_request_boundaries(rows, num_ctas):
     check_decode(out, lse, o, l, rr, what=f"rows={rows} ctas={num_ctas}")
 
 
-@pytest.mark.parametrize("num_ctas", [4, 0])
-def test_fp8_split_columns_boundaries(num_ctas):
-    """fp8 pool (TMA + in-place expansion) with 64 rows and ragged requests."""
+@pytest.mark.parametrize("num_ctas,page_size,Hq,Qt", [(4, 64, 64, 1), (0, 64, 64, 1), (7, 16, 16, 4), (40, 8, 64, 1),
+                                                     (3, 32, 16, 3)])
+def test_fp8_64_rows_boundaries(num_ctas, page_size, Hq, Qt):
+    """fp8 pools at 33..64 query rows (folded tiles: TMA-landed codes widened
+    in place by the expand warps) with ragged requests, tile and page
+    boundaries, requests cut across workers."""
     sl = [0, 1, 64, 65, 127, 300, 900, 2049, 5]
-    wl = W.make("fp8b", B=len(sl), Hq=64, Qt=1, page_size=64, seq_lens=sl, kind=W.KIND_FP8, write_all=True,
-                seed=77 + num_ctas, device=DEV)
+    wl = W.make("fp8b", B=len(sl), Hq=Hq, Qt=Qt, page_size=page_size, seq_lens=sl, kind=W.KIND_FP8, write_all=True,
+                seed=77 + num_ctas + page_size, device=DEV)
     o, l, rr = oracle_step(wl, range(wl.B))
     out, lse = run_step(wl, num_ctas=num_ctas)
     check_decode(out, lse, o, l, rr, kind=1, what=f"fp8 ctas={num_ctas}")
