@@ -54,6 +54,8 @@ CONFIG_TEXT = {
               "mla_decode_varlen",
     "verify8": "the mtp pool and requests with verify steps of 1 + k tokens, k U{0..7} per request (seeded; up "
                "to 128 query rows a request, one cache read each): mla_decode_varlen",
+    "latent768": "the batched shape (B=64 Hq=16 seq U{1024..8192} page 16) over bf16 rows [latent 768 | rope 64] "
+                 "(1664 B): mla_cache_write_latent + mla_decode_latent",
     "gather": "fp8_ds_mla pool of the fp8 workload (B=64 x 32768 tokens, page 64) gathered into "
               "[2097152, 576] bf16 rows",
 }
@@ -227,17 +229,19 @@ def verify_qlens(B, rank=0, qmax=4):
 
 WORKLOAD_SEED = {"tiny": 1, "batched": 2, "long": 3, "mtp": 4, "fp8": 5}
 # workloads measured beside the headline one and reported in its line
-SIDE_WORKLOADS = ("long", "fp8", "batched", "tiny", "verify", "verify8")
+SIDE_WORKLOADS = ("long", "fp8", "batched", "tiny", "verify", "verify8", "latent768")
 
 
 def config_dict(name, ctx_tokens, cache_bytes, row_bytes, ws_):
     """The `config` object of a decode line; both arms use it, so the
     reference arm's line names the same workload in the same words."""
     varlen = name.startswith("verify")
+    lat = name.startswith("latent")
     return {"workload": name, "shape": CONFIG_TEXT[name], "context_tokens": ctx_tokens,
             "cache_bytes_per_step": cache_bytes, "row_bytes": row_bytes,
             "l2": "flushed before every step (256 MiB write, outside the timed events)",
-            "step": "mla_cache_write of the step's new rows + " + ("mla_decode_varlen" if varlen else "mla_decode")
+            "step": ("mla_cache_write_latent" if lat else "mla_cache_write") + " of the step's new rows + "
+                    + ("mla_decode_varlen" if varlen else "mla_decode_latent" if lat else "mla_decode")
                     + " (decode + split merge)",
             "parallelism": f"replicas x{ws_} (requests are independent)"}
 
@@ -247,6 +251,8 @@ def build_workload(name, dev, rank=0, requests=None):
     requests), seeded per rank. `requests` (long and fp8 only) keeps that
     many of their equal-length requests: a cut-down copy for profiling."""
     from mla_latent_kv_cache_gb300 import workloads as W
+    if name.startswith("latent"):
+        return W.latent(int(name[len("latent"):]), device=dev, seed=WORKLOAD_SEED["batched"] + 1000 * rank)
     base = "mtp" if name.startswith("verify") else name
     kw = {"Qt": 8} if name == "verify8" else {}
     if requests is not None:
@@ -296,9 +302,11 @@ def measure_gpu(name, args, dev, rank, ws_, clock_csv=None):
     ctx_tokens = wl.context_tokens()
     B, Qt, Hq = wl.B, wl.Qt, wl.Hq
     R = q_lat_s.shape[0]  # query tokens of the step
-    out = torch.empty((R, Hq, 512), dtype=torch.bfloat16, device=dev)
+    D = wl.lat_dim
+    lat = D != 512
+    out = torch.empty((R, Hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((R, Hq), dtype=torch.float32, device=dev)
-    wsb = m.mla_decode_workspace_bytes(B, Qt, Hq, 0)
+    wsb = m.mla_decode_latent_workspace_bytes(B, Qt, Hq, D, 0) if lat else m.mla_decode_workspace_bytes(B, Qt, Hq, 0)
     workspace = torch.empty((wsb,), dtype=torch.uint8, device=dev)
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -311,11 +319,16 @@ def measure_gpu(name, args, dev, rank, ws_, clock_csv=None):
     def decode(q_lat, q_pe, bt, sl, cq, o, l):
         if varlen:
             m.mla_decode_varlen(q_lat, q_pe, wl.pool, wl.kind, wl.page_size, bt, sl, cq, Qt, wl.scale, o, l, workspace)
+        elif lat:
+            m.mla_decode_latent(q_lat, q_pe, wl.pool, D, wl.page_size, bt, sl, Qt, wl.scale, o, l, workspace)
         else:
             m.mla_decode(q_lat, q_pe, wl.pool, wl.kind, wl.page_size, bt, sl, Qt, wl.scale, o, l, workspace)
 
-    def write(lat, kpe, slots):
-        m.mla_cache_write(lat, kpe, slots, wl.pool, wl.kind, status=write_status)
+    def write(latent_rows, kpe, slots):
+        if lat:
+            m.mla_cache_write_latent(latent_rows, kpe, slots, wl.pool, D, status=write_status)
+        else:
+            m.mla_cache_write(latent_rows, kpe, slots, wl.pool, wl.kind, status=write_status)
 
     # clock sampling starts before the warm-up so its start-up is over before timing
     clocks = ClockSampler(torch.cuda.current_device(), clock_csv)
@@ -704,7 +717,8 @@ def _oracle_prepare(wl, b):
     from mla_latent_kv_cache_gb300 import workloads as W
     c = W.compact(wl, [b])
     pool = c["pool"].copy()
-    oracle.cache_write(c["w_latent"], c["w_k_pe"], c["w_slots"], pool, wl.kind)
+    if wl.lat_dim == 512:
+        oracle.cache_write(c["w_latent"], c["w_k_pe"], c["w_slots"], pool, wl.kind)
     return c, pool
 
 
@@ -712,6 +726,7 @@ def _oracle_run(wl, prep, cap=None, qt=None):
     """Time the oracle's decode of a prepared request (its first `cap`
     tokens when given; a verify step of `qt` tokens, its first qt query rows,
     when given); returns (bytes, seconds)."""
+    import numpy as np
     import oracle
     c, pool = prep
     sl = c["seq_lens"].copy()
@@ -719,8 +734,13 @@ def _oracle_run(wl, prep, cap=None, qt=None):
         sl[0] = min(int(sl[0]), int(cap))
     qt = wl.Qt if qt is None else int(qt)
     t0 = time.perf_counter()
-    oracle.decode(c["q_lat"][:qt], c["q_pe"][:qt], pool, wl.kind, wl.page_size, c["block_table"], sl, 1, qt, wl.Hq,
-                  wl.scale)
+    if wl.lat_dim != 512:
+        # other latent widths: the pool as it stands (a timing sample only)
+        oracle.decode_latent(c["q_lat"][:qt], c["q_pe"][:qt], pool.view(np.uint16), wl.lat_dim, 64, wl.page_size,
+                             c["block_table"], sl, 1, qt, wl.Hq, wl.scale)
+    else:
+        oracle.decode(c["q_lat"][:qt], c["q_pe"][:qt], pool, wl.kind, wl.page_size, c["block_table"], sl, 1, qt,
+                      wl.Hq, wl.scale)
     return int(sl[0]) * wl.row_bytes, time.perf_counter() - t0
 
 

@@ -168,16 +168,21 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *                failing CTA; words 4..11 where each of its roles gave up.
  *                Calls sharing a workspace must be ordered on one stream.
  *   num_ctas     CTAs sharing the token stream (0 = as many as fit on the
- *                device, one per SM). bf16 pools whose page_size is a multiple
- *                of 8 with at most 32 rows (Hq * q_len) per group: each CTA is
- *                a worker on 64-token tiles of whole rows. Otherwise CTAs work
- *                in clusters of two that split each token's 576 dims between
- *                them, num_ctas / 2 workers on 128-token tiles. The tiles of
- *                all requests are dealt out as equal contiguous ranges, one per
- *                worker; requests cut across workers are merged from fp32
- *                partials by a second kernel.
- * Limits: Hq * q_len rows are processed in groups of at most 64. Returns
- * MLA_ERR_UNSUPPORTED on a device other than sm_103 / sm_100 family.
+ *                device, one per SM). Pools whose page_size is a multiple of
+ *                8 (bf16 at any row count, fp8 at 33..64 rows): each CTA is a
+ *                worker on 64-token tiles of whole rows, except at 65..128
+ *                rows (Hq * q_len), where the two 64-row groups of a worker
+ *                are a cluster of two CTAs sharing each tile (num_ctas / 2
+ *                workers). fp8 pools at other row counts and page sizes that
+ *                are not a multiple of 8: clusters of two CTAs that split each
+ *                token's 576 dims between them, num_ctas / 2 workers on
+ *                128-token tiles. The tiles of all requests are dealt out as
+ *                equal contiguous ranges, one per worker; requests cut across
+ *                workers are merged from fp32 partials by a second kernel.
+ * Limits: Hq * q_len rows are processed in groups of at most 64; up to 128
+ * rows (bf16 pools, page_size a multiple of 8) the cache is read once per
+ * request, beyond that once per row group. Returns MLA_ERR_UNSUPPORTED on a
+ * device other than sm_103 / sm_100 family.
  */
 MLA_API int mla_decode(const void* q_lat, const void* q_pe, const void* cache, int cache_kind, int64_t num_slots,
                int page_size, const int32_t* block_table, int64_t block_table_stride, const int32_t* seq_lens,
@@ -238,7 +243,9 @@ MLA_API int mla_decode_latent(const void* q_lat, const void* q_pe, const void* c
  *   max_q_len       the largest q_len_b, >= 1. Rows are processed in groups of
  *                   64 as in mla_decode with q_len = max_q_len; the workspace
  *                   is mla_decode_workspace_bytes(B, max_q_len, Hq, num_ctas).
- * While max_q_len * Hq <= 64 every request's cache is read once.
+ * While max_q_len * Hq <= 64, and up to 128 for bf16 pools whose page_size
+ * is a multiple of 8 (two row groups sharing each tile), every request's
+ * cache is read once.
  */
 MLA_API int mla_decode_varlen(const void* q_lat, const void* q_pe, int64_t total_q_tokens, const void* cache,
                               int cache_kind, int64_t num_slots, int page_size, const int32_t* block_table,

@@ -8,19 +8,31 @@
 //   s_j = scale * (q_lat . c_j + q_pe . k_pe_j),  out = softmax(s) . c,
 //   lse = ln sum_j exp(s_j), over the tokens each query row may see.
 //
-// Work split ("stream-K" over 128-token tiles). The tiles of all requests are
-// concatenated and the clusters (one per SM pair) each take an equal
-// contiguous range, so every SM streams the same number of cache bytes
-// whatever the request lengths. The tiles of one request inside a range form
-// a segment; a segment covering its whole request writes the final output,
-// otherwise an fp32 partial (out, lse) that a second kernel merges. Query rows
-// (query token x head) are processed NP at a time (NP = 16, 32 or 64,
-// padded); gridDim.y covers more.
+// Two decode kernels share the work split, the split-KV partials and the
+// merge:
+//   mla_decode_fold_kernel  64-token tiles folded into two 288-value halves
+//                           (see "folded tiles" below): every pool whose page
+//                           size is a multiple of 8 rows, except fp8_ds_mla
+//                           pools at up to 32 or above 64 query rows.
+//   mla_decode_kernel       128-token tiles whose 576 dims are split over the
+//                           two CTAs of a cluster: those fp8 pools, and pages
+//                           that are not a multiple of 8 rows (load/convert
+//                           warps read them).
 //
-// Two CTAs per tile (a cluster of 2 on neighbouring SMs) split the 576 cached
-// dims: CTA r holds latent dims [256r, 256r+256) and rope dims
-// [512+32r, 512+32r+32), i.e. 72 KB of each 128-token tile, so two or more
-// tiles fit in shared memory and loads overlap compute. Per tile:
+// Work split ("stream-K" over tiles). The tiles of all requests are
+// concatenated and the workers (a CTA, or a cluster of two) each take an
+// equal contiguous range of the cost (a request boundary counts as a few
+// tiles), so every SM streams about the same number of cache bytes whatever
+// the request lengths. The tiles of one request inside a range form a
+// segment; a segment covering its whole request writes the final output,
+// otherwise an fp32 partial (out, lse) that a second kernel merges. Query
+// rows (query token x head) are processed in groups of at most 64 (NP = 16,
+// 32 or 64, padded); gridDim.y covers more.
+//
+// Cluster kernel. Two CTAs per tile (a cluster of 2 on neighbouring SMs)
+// split the 576 cached dims: CTA r holds latent dims [256r, 256r+256) and
+// rope dims [512+32r, 512+32r+32), i.e. 72 KB of each 128-token tile, so two
+// or more tiles fit in shared memory and loads overlap compute. Per tile:
 //   S_r^T[128 tok, NP] = C_r[128, 288] . Q_r^T        (UMMA M=128, into TMEM)
 //   S = S_0 + S_1       (each CTA sends its partial to the other through
 //                        distributed shared memory)
@@ -31,9 +43,9 @@
 // All query rows share one read of the cache (the pages' point that a verify
 // step must read the latent once per request).
 //
-// Warp roles in each CTA:
+// Warp roles of the cluster kernel's CTAs:
 //   warp 0      : TMEM allocation; lane 0 issues the S = C.Q^T MMAs
-//   warp 1      : TMA producer (bf16 pools, page_size % 8 == 0)
+//   warp 1      : TMA producer (page_size % 8 == 0)
 //   warp 2      : tile-range scan at start
 //   warp 3      : lane 0 issues the O += C^T.P MMAs
 //   warps 4..7  : softmax, P, output epilogue (thread t <-> token t <-> TMEM lane t)
@@ -1430,8 +1442,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 
 // ---------------------------------------------------------------- folded tiles
 //
-// bf16 pools, page sizes that are a multiple of 8, up to 32 query rows: one CTA
-// per worker and no cluster. A tile is 64 tokens of whole 576-value rows,
+// Pools whose page size is a multiple of 8 rows: bf16 at 1..128 query rows,
+// fp8_ds_mla at 33..64 (and bf16 rows of other latent widths). One CTA per
+// worker, except the two cases below that pair two CTAs in a cluster. A tile
+// is 64 tokens of whole rows,
 // held as the 128-row A operand of one UMMA: row t (t < 64) carries token t's
 // first half (latent [0, 256) and rope [512, 544)), row 64 + t its second half
 // (latent [256, 512) and rope [544, 576)). With the query rows stacked the same
@@ -1450,6 +1464,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // and the ring is in K-block slots that free one by one.
 // Nothing crosses between CTAs: a tile's shared memory is held from its load
 // to its value product only, with no exchange latency in between.
+//
+// Query rows: NP = 16, 32 or 64 a CTA. At 32 and 64 rows two softmax groups of
+// four warps each own half of the columns. At 64 rows Q takes 72 KB, so the
+// ring has eight K-block slots (two tiles), one P buffer and one O
+// accumulator (a finished segment is written out before the next segment's
+// first value product). 65..128 rows: the two 64-row groups of a worker run
+// as a cluster of two CTAs that share each tile through multicast TMA (each
+// issues half of the boxes into both), so the cache is read once per request.
+// fp8_ds_mla rows at 64 rows: TMA lands each K-block's e4m3 codes in the upper
+// half of its slot, four expand warps widen them into the bf16 layout in
+// place. Latent width 1792: the two latent halves of every row in the two
+// CTAs of a cluster, which add their partial scores.
 
 template <int NP, int KB, bool PAIR = false, int KIND = 0>
 struct FoldCfg {
@@ -2016,28 +2042,27 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     }
                     if (lane == 0 && e == 0 && q == 0) MLA_TRACE_POINT(i, kTrSmXFree);  // codes landed
                     uint8_t* blk = ring + slot * C::kBlkBytes;
+                    // Lane l takes a quarter (16 codes, 32 bf16 bytes) of row 8 it + l / 4
+                    // in each of eight steps: a warp-wide 16-byte load then covers 512
+                    // contiguous code bytes (no bank conflicts), and the two stores of
+                    // a step hit every bank group once.
+                    const int uq = lane & 3;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        uint4 cd[2][4];
+                        uint4 cd[8];
 #pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const uint4* src = reinterpret_cast<const uint4*>(blk + 8192 + h * 4096 + (lane + 32 * k) * 64);
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) cd[k][u] = src[u];
-                        }
+                        for (int it = 0; it < 8; ++it)
+                            cd[it] = *reinterpret_cast<const uint4*>(blk + 8192 + h * 4096 + it * 512 + lane * 16);
                         __syncwarp();  // every lane's codes are in registers
 #pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const int t = lane + 32 * k, r = 64 * h + t;
+                        for (int it = 0; it < 8; ++it) {
+                            const int t = 8 * it + (lane >> 2), r = 64 * h + t;
                             const float scale = *reinterpret_cast<const float*>(sc + t * 16 + 4 * (2 * h + (kb >> 1)));
+                            uint4 lo, hi;
+                            dequant16(cd[it], scale, lo, hi);
                             uint8_t* row = blk + r * 128;
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                uint4 lo, hi;
-                                dequant16(cd[k][u], scale, lo, hi);
-                                *reinterpret_cast<uint4*>(row + (((2 * u) ^ (r & 7)) << 4)) = lo;
-                                *reinterpret_cast<uint4*>(row + (((2 * u + 1) ^ (r & 7)) << 4)) = hi;
-                            }
+                            *reinterpret_cast<uint4*>(row + (((2 * uq) ^ (r & 7)) << 4)) = lo;
+                            *reinterpret_cast<uint4*>(row + (((2 * uq + 1) ^ (r & 7)) << 4)) = hi;
                         }
                         __syncwarp();  // the first halves' codes are consumed before h = 1 writes over them
                     }

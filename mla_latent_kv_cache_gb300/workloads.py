@@ -54,10 +54,11 @@ class Workload:
     w_k_pe: torch.Tensor          # [Tw, 64] bf16
     w_slots: torch.Tensor         # [Tw] int64 (-1 = skip)
     meta: dict = field(default_factory=dict)
+    lat_dim: int = D              # latent width of a bf16 row [latent | rope 64]
 
     @property
     def row_bytes(self) -> int:
-        return ROW_BYTES[self.kind]
+        return 2 * (self.lat_dim + P) if self.kind == KIND_BF16 else ROW_BYTES[self.kind]
 
     def context_tokens(self) -> int:
         return int(self.seq_lens.to(torch.int64).sum().item())
@@ -77,8 +78,9 @@ def _randn_bf16(shape, g, device) -> torch.Tensor:
     return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
-def _nan_pool(num_slots: int, kind: int, device) -> torch.Tensor:
-    pool = torch.empty((num_slots, ROW_BYTES[kind]), dtype=torch.uint8, device=device)
+def _nan_pool(num_slots: int, kind: int, device, lat_dim: int = D) -> torch.Tensor:
+    row_bytes = 2 * (lat_dim + P) if kind == KIND_BF16 else ROW_BYTES[kind]
+    pool = torch.empty((num_slots, row_bytes), dtype=torch.uint8, device=device)
     if kind == KIND_BF16:
         pool.view(torch.int16).fill_(0x7FC0)
     else:
@@ -119,9 +121,10 @@ def _fill_rows(pool: torch.Tensor, slots: torch.Tensor, g, device, rms_spread: f
                chunk: int = 1 << 20) -> None:
     """Write N(0,1) bf16 rows into `slots` of a bf16 pool, in chunks."""
     pv = pool.view(torch.bfloat16)
+    width = pv.shape[1]
     for s in range(0, slots.numel(), chunk):
         idx = slots[s:s + chunk]
-        rows = torch.randn((idx.numel(), W), generator=g, device=device, dtype=torch.float32)
+        rows = torch.randn((idx.numel(), width), generator=g, device=device, dtype=torch.float32)
         if rms_spread:
             f = torch.exp(rms_spread * (2 * torch.rand((idx.numel(), 1), generator=g, device=device) - 1))
             rows = rows * f
@@ -131,7 +134,7 @@ def _fill_rows(pool: torch.Tensor, slots: torch.Tensor, g, device, rms_spread: f
 def make(name: str, *, B: int, Hq: int, Qt: int, page_size: int, seq_lens, kind: int = KIND_BF16,
          num_blocks: int | None = None, min_block: int = 0, force_block: int | None = None,
          seed: int = 0, device="cpu", write_last: int | None = None, rms_spread: float = 0.0,
-         write_all: bool = False) -> Workload:
+         write_all: bool = False, lat_dim: int = D) -> Workload:
     """General builder.
 
     seq_lens     per-request context lengths, counting the Qt query tokens.
@@ -142,7 +145,9 @@ def make(name: str, *, B: int, Hq: int, Qt: int, page_size: int, seq_lens, kind:
     write_last   how many trailing tokens per request the step writes with the
                  cache-write kernel (default Qt; bf16 pools only).
     write_all    (fp8) every token's row is written by the cache-write kernel.
+    lat_dim      (bf16) latent width of a row [latent lat_dim | rope 64].
     """
+    assert lat_dim == D or kind == KIND_BF16
     g_np = np.random.default_rng(seed)
     sl = np.asarray(seq_lens, dtype=np.int64)
     need = int(sum((int(t) + page_size - 1) // page_size for t in sl))
@@ -164,9 +169,9 @@ def make(name: str, *, B: int, Hq: int, Qt: int, page_size: int, seq_lens, kind:
     g = _gen(seed, device)
     block_table = torch.from_numpy(bt_np).to(device)
     seq = torch.from_numpy(sl.astype(np.int32)).to(device)
-    q_lat = _randn_bf16((B * Qt, Hq, D), g, device)
+    q_lat = _randn_bf16((B * Qt, Hq, lat_dim), g, device)
     q_pe = _randn_bf16((B * Qt, Hq, P), g, device)
-    pool = _nan_pool(num_slots, kind, device)
+    pool = _nan_pool(num_slots, kind, device, lat_dim)
     slots = token_slots(block_table, seq, page_size)
 
     if kind == KIND_BF16:
@@ -182,7 +187,7 @@ def make(name: str, *, B: int, Hq: int, Qt: int, page_size: int, seq_lens, kind:
         assert write_all, "fp8 pools are written by the cache-write kernel"
         w_slots = slots
     Tw = w_slots.numel()
-    w_latent = _randn_bf16((Tw, D), g, device)
+    w_latent = _randn_bf16((Tw, lat_dim), g, device)
     w_k_pe = _randn_bf16((Tw, P), g, device)
     if rms_spread and Tw:
         f = torch.exp(rms_spread * (2 * torch.rand((Tw, 1), generator=g, device=device) - 1))
@@ -190,7 +195,7 @@ def make(name: str, *, B: int, Hq: int, Qt: int, page_size: int, seq_lens, kind:
     return Workload(name=name, kind=kind, B=B, Hq=Hq, Qt=Qt, page_size=page_size,
                     num_slots=num_slots, scale=SCALE, seq_lens=seq, block_table=block_table,
                     q_lat=q_lat, q_pe=q_pe, pool=pool, w_latent=w_latent, w_k_pe=w_k_pe,
-                    w_slots=w_slots, meta={"seed": seed, "num_blocks": num_blocks})
+                    w_slots=w_slots, meta={"seed": seed, "num_blocks": num_blocks}, lat_dim=lat_dim)
 
 
 # ------------------------------------------------------------ named configs
@@ -252,6 +257,13 @@ def fp8(device="cpu", seed: int = 5, B: int = 64) -> Workload:
     cut-down copy of the same shape for profiling)."""
     return make("fp8", B=B, Hq=64, Qt=1, page_size=64, seq_lens=[32768] * B, num_blocks=512 * B,
                 kind=KIND_FP8, write_all=True, seed=seed, device=device)
+
+
+def latent(D: int, device="cpu", seed: int = 2) -> Workload:
+    """The batched shape (B=64, Hq=16, seq U{1024..8192}, page 16) over bf16
+    rows of another latent width: [latent D | rope 64]."""
+    return make(f"latent{D}", B=64, Hq=16, Qt=1, page_size=16, seq_lens=batched_seq_lens(seed), seed=seed,
+                device=device, lat_dim=D)
 
 
 CONFIGS = {"tiny": tiny, "batched": batched, "long": long, "mtp": mtp, "fp8": fp8}
