@@ -97,8 +97,42 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_HEADERS = [os.path.join(ROOT, "mla_latent_kv_cache_gb300", "csrc", f)
+                  for f in ("launch.cuh", "mla_common.cuh", "tmem_ldst.inc")]
+
+
+def _code_only(text):
+    """C/C++ source with comments and blank space removed (string and
+    character literals kept), so that a comment edit keeps a capture valid."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sha(src=DECODE_SRC):
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    """Hash of the code (comments stripped) of a kernel file and the headers
+    it includes: a committed ncu traffic figure holds only while it matches."""
+    h = hashlib.sha256()
+    for f in [src] + KERNEL_HEADERS:
+        h.update(_code_only(open(f, encoding="utf-8").read()).encode())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(config):
