@@ -508,7 +508,8 @@ def run_gpu(args):
         entry = {"value": n["value"], "unit": "GB/s", "ms_per_step": n["ms_per_step"],
                  "decode_steps_per_s": n["decode_steps_per_s"], "ctx_tokens_per_s": n["ctx_tokens_per_s"],
                  "roofline": {"bound": "hbm", "achieved": round(n["achieved"], 1), "peak": peak,
-                              "frac": round(n["frac"], 4), "traffic": traffic_for(name)},
+                              "frac": round(n["frac"], 4), "traffic": traffic_for(name),
+                              "algorithmic_bytes_per_launch": rs["cache_bytes"]},
                  "e2e": n["e2e"], "config": config_dict(name, rs["ctx_tokens"], rs["cache_bytes"],
                                                         rs["wl"].row_bytes, ws_),
                  "clocks": rs["clk"], "step_times": step_time_summary(rs["step_times"]),

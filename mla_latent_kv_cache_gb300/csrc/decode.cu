@@ -70,7 +70,9 @@ namespace mla {
 enum TraceEvent : int {
     kTrProdStart = 0, kTrProdIssued, kTrSPair0, kTrSAllIn, kTrPvIssue, kTrSmSFull, kTrSmXFull, kTrSmPArrive,
     kTrSIssued = 8, kTrSmTmemLd, kTrSmXFree, kTrSmSent, kTrSmMath, kTrSmBarOr, kTrSmExp, kTrSmPStore, kTrPvIssued,
-    kTrSmXRead, kTrSmExpLoop, kTrEpiStart, kTrEpiRed, kTrEpiStored, kTrEpiEnd, kTrEpiHalf, kTrEvents = 24
+    kTrSmXRead, kTrSmExpLoop, kTrEpiStart, kTrEpiRed, kTrEpiStored, kTrEpiEnd, kTrEpiHalf,
+    kTrSKb1 = 24, kTrSKb2, kTrSKb3, kTrSRope, kTrProd1Start, kTrProd1Done, kTrProd0Done, kTrSmRescaled,
+    kTrEvents = 32
 };
 #ifdef MLA_TRACE
 __device__ unsigned long long g_trace[8][64][kTrEvents];
@@ -1719,6 +1721,11 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
     if (ntiles > 0) {
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------- S issuer
+            // The rope's two products come first and release the rope slot with
+            // a commit of their own: the producers load tile i + 1's rope as soon
+            // as S(i) has read this one, and with one rope slot a release at the
+            // end of S(i) would chain every tile's rope copy behind the previous
+            // tile's whole score product.
             It it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint32_t idS = idesc_bf16(128, 2 * NP, false, false);
@@ -1742,38 +1749,40 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 const uint32_t tS = tmem + C::kColS + (i & 1) * 2 * NP;
                 bool ok = true;
                 int site = kSitePairFull;
+                const int rr = i % C::kRR;
+                if (has_rope) {
+                    if (!mbar_wait(&ctrl->rope_full[rr], (i / C::kRR) & 1, &ctrl->abort)) {
+                        ok = false;
+                        site = kSiteRopeFull;
+                    } else {
+                        tc_fence_after();
+                        MLA_TRACE_POINT(i, kTrSRope);
+                        const uint64_t dr = smem_desc(smem_u32(rope_ring + rr * C::kRopeBytes), 16, 512, kSw64);
+                        umma_bf16(tS, dr, dqr, idS, 0u);
+                        umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
+                        if constexpr (MC) umma_commit_mc(&ctrl->rope_empty[rr], kPairMask);
+                        else umma_commit(&ctrl->rope_empty[rr]);
+                    }
+                }
                 for (int kb = 0; kb < KB && ok; ++kb) {
                     const int slot = C::slot_of(i, kb);
                     if (!mbar_wait(&ctrl->blk_full[slot], C::fill_of(i, kb) & 1, &ctrl->abort)) { ok = false; break; }
                     tc_fence_after();
                     if (kb == 0) MLA_TRACE_POINT(i, kTrSPair0);
+                    else if (kb < 4) MLA_TRACE_POINT(i, kTrSKb1 + kb - 1);
                     const uint64_t da = smem_desc(smem_u32(ring + slot * C::kBlkBytes), 16, 1024, kSw128);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4), idS, (kb | kk) != 0);
-                }
-                const int rr = i % C::kRR;
-                if (ok && has_rope && !mbar_wait(&ctrl->rope_full[rr], (i / C::kRR) & 1, &ctrl->abort)) {
-                    ok = false;
-                    site = kSiteRopeFull;
+                        umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4), idS,
+                                  (has_rope || (kb | kk) != 0) ? 1u : 0u);
                 }
                 if (!ok) {
                     fail(p, ctrl, kErrWaitTimeout, site, i);
                     report(p, kRoleS, site, i);
                     break;
                 }
-                tc_fence_after();
                 MLA_TRACE_POINT(i, kTrSAllIn);
-                if (has_rope) {
-                    const uint64_t dr = smem_desc(smem_u32(rope_ring + rr * C::kRopeBytes), 16, 512, kSw64);
-                    umma_bf16(tS, dr, dqr, idS, 1u);
-                    umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
-                }
                 umma_commit(&ctrl->s_full[i & 1]);
-                if (has_rope) {
-                    if constexpr (MC) umma_commit_mc(&ctrl->rope_empty[rr], kPairMask);
-                    else umma_commit(&ctrl->rope_empty[rr]);
-                }
                 MLA_TRACE_POINT(i, kTrSIssued);
                 it.next(p.seq_lens, p.B);
             }
@@ -1860,7 +1869,42 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 It nx = it;
                 nx.next(p.seq_lens, p.B);
                 if (i + 1 < ntiles) y_next = run_slot(nx);
-                if (lane == 0) MLA_TRACE_POINT(i, kTrProdStart + 0 * pp);
+                if (lane == 0) MLA_TRACE_POINT(i, pp ? kTrProd1Start : kTrProdStart);
+                if (has_rope) {
+                    const int rr = i % C::kRR;
+                    if (i >= C::kRR &&
+                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->rope_empty[rr], ((i / C::kRR) - 1) & 1, &ctrl->abort))) {
+                        ok = false;
+                        fsite = kSiteTmaRopeEmpty;
+                        ftile = i;
+                        break;
+                    }
+                    if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrEpiStored);  // rope slot free
+                    // rope half pp (each producer one half; a single producer both),
+                    // before the tile's K-blocks: its slot comes free first
+                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], C::kProducers == 1 ? run_bytes : run_bytes / 2);
+                    __syncwarp();
+                    rope_armed = i + 1;
+                    if constexpr (C::kProducers == 1) {
+                        if (lane < nruns) {
+#pragma unroll
+                            for (int rh = 0; rh < 2; ++rh)
+                                tma_load_2d(rope_ring + rr * C::kRopeBytes + rh * 4096 + lane * BR * 64, &maps.rope,
+                                            &ctrl->rope_full[rr], kRopeX + 32 * rh, y, pol);
+                        }
+                    } else if (lane < nruns) {
+                        if constexpr (MC) {
+                            // rope half pp comes from the CTA of rank pp, into both CTAs
+                            if (pp == mrank)
+                                tma_load_2d_mc(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
+                                               &ctrl->rope_full[rr], kRopeX + 32 * pp, y, kPairMask, pol);
+                        } else {
+                            tma_load_2d(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
+                                        &ctrl->rope_full[rr], kRopeX + 32 * pp, y, pol);
+                        }
+                    }
+                    if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrProdIssued);
+                }
                 for (int q = 0; q < C::prod_hi(pp) - C::prod_lo(pp); ++q) {
                     const int kb = C::prod_lo(pp) + q;
                     const int slot = C::slot_of(i, kb), fill = C::fill_of(i, kb);
@@ -1915,6 +1959,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     armed = i * (C::prod_hi(pp) - C::prod_lo(pp)) + q + 1;
                 }
                 if (!ok) break;
+                if (lane == 0) MLA_TRACE_POINT(i, pp ? kTrProd1Done : kTrProd0Done);
                 if constexpr (KIND == 1) {
                     if (pp == 0) {
                         // the tile's block scales, 16 bytes a row, once both expanders
@@ -1934,40 +1979,6 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                             tma_load_2d(scales + sb * C::kScaleBytes + lane * BR * 16, &maps.aux, &ctrl->scale_full[sb], 512,
                                         y, pol);
                     }
-                }
-                if (has_rope) {
-                    const int rr = i % C::kRR;
-                    if (i >= C::kRR &&
-                        !__all_sync(0xffffffffu, mbar_wait(&ctrl->rope_empty[rr], ((i / C::kRR) - 1) & 1, &ctrl->abort))) {
-                        ok = false;
-                        fsite = kSiteTmaRopeEmpty;
-                        ftile = i;
-                        break;
-                    }
-                    if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrEpiStored);  // K-blocks issued, rope slot free
-                    // rope half pp (each producer one half; a single producer both)
-                    if (lane == 0) mbar_arrive_expect_tx(&ctrl->rope_full[rr], C::kProducers == 1 ? run_bytes : run_bytes / 2);
-                    __syncwarp();
-                    rope_armed = i + 1;
-                    if constexpr (C::kProducers == 1) {
-                        if (lane < nruns) {
-#pragma unroll
-                            for (int rh = 0; rh < 2; ++rh)
-                                tma_load_2d(rope_ring + rr * C::kRopeBytes + rh * 4096 + lane * BR * 64, &maps.rope,
-                                            &ctrl->rope_full[rr], kRopeX + 32 * rh, y, pol);
-                        }
-                    } else if (lane < nruns) {
-                        if constexpr (MC) {
-                            // rope half pp comes from the CTA of rank pp, into both CTAs
-                            if (pp == mrank)
-                                tma_load_2d_mc(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
-                                               &ctrl->rope_full[rr], kRopeX + 32 * pp, y, kPairMask, pol);
-                        } else {
-                            tma_load_2d(rope_ring + rr * C::kRopeBytes + pp * 4096 + lane * BR * 64, &maps.rope,
-                                        &ctrl->rope_full[rr], kRopeX + 32 * pp, y, pol);
-                        }
-                    }
-                    if (lane == 0 && pp == 0) MLA_TRACE_POINT(i, kTrProdIssued);
                 }
                 it = nx;
             }
@@ -2459,6 +2470,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                         // every column (each thread its TMEM lane of the four M-tiles)
                         group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i);
                         rescale_o(obuf);
+                        if (lead) MLA_TRACE_POINT(i, kTrSmRescaled);
                     }
                 }
 #pragma unroll

@@ -27,7 +27,12 @@ more). PV issuer m frees the blocks producer m loads (with one producer,
 the same split). The rope ring has RR
 slots, one per tile, and every producer loads a part of each; the S issuer
 reads it last and frees it with its final commit, or (rope_first) reads it
-first and frees it with a commit of its own before the tile's blocks. The softmax
+first and frees it with a commit of its own before the tile's blocks, and
+then the producers load each tile's rope before its blocks. With expand (fp8
+rows) one producer lands each block's codes behind a raw barrier and each
+tile's scales in one of two scale slots; expander e widens block e of every
+tile in place once both have landed, then marks the block full, and the
+producer reloads a scale slot once every expander is done with it. The softmax
 waits for PV(i - PB) before it writes P(i) into buffer i % PB. It waits for
 PV(i - 1) as well on a random 30% of tiles, standing for an O rescale. It
 hands tile i to the PV issuers through hand-off barrier i % H."""
@@ -62,10 +67,15 @@ class Bar:
 
 
 def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int, N: int = 40,
-        weights: dict | None = None, rope_first: bool = False) -> list[str]:
+        weights: dict | None = None, rope_first: bool = False, expand: bool = False) -> list[str]:
     """One random schedule; returns the problems found (empty when none)."""
     rnd = random.Random(seed)
     blk_full = [Bar(1) for _ in range(R)]
+    raw_full = [Bar(1) for _ in range(R)]
+    # every expander releases a scale slot (a control may count fewer)
+    scale_full, scale_empty = [Bar(1), Bar(1)], [Bar(KB), Bar(KB)]
+    scale_data = [None, None]
+    raw_data = [None] * R
     blk_empty = [Bar(1) for _ in range(R)]
     rope_full = [Bar(producers) for _ in range(RR)]
     rope_empty = [Bar(1) for _ in range(RR)]
@@ -85,9 +95,23 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
         # the blocks of producer / PV issuer m: [0, half) and [half, KB)
         return range(0, half) if m == 0 else range(half, KB)
 
+    def load_rope(i):
+        rr = i % RR
+        if i >= RR:
+            yield lambda rr=rr, i=i: rope_empty[rr].passes(((i // RR) - 1) & 1)
+        rope_full[rr].arrive_expect(1, 1)
+
+        def land_rope(rr=rr, i=i):
+            rope_data[rr] = i
+            rope_full[rr].complete_tx(1)
+        landings.append(land_rope)
+        yield None
+
     def producer(pp):
         mine = range(KB) if producers == 1 else blocks(pp)
         for i in range(N):
+            if rope_first:
+                yield from load_rope(i)
             for kb in mine:
                 u = KB * i + kb
                 s, f = u % R, u // R
@@ -96,22 +120,46 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
                 if slot_held[s] is not None:
                     errors.append(f"load of tile {i} block {kb} over unfreed {slot_held[s]} in slot {s}")
                 slot_held[s] = (i, kb)
-                blk_full[s].arrive_expect(1, 1)
+                bar = raw_full[s] if expand else blk_full[s]
+                bar.arrive_expect(1, 1)
 
-                def land(s=s, i=i, kb=kb):
-                    slot_data[s] = (i, kb)
-                    blk_full[s].complete_tx(1)
+                def land(s=s, i=i, kb=kb, bar=bar):
+                    if expand:
+                        raw_data[s] = (i, kb)
+                    else:
+                        slot_data[s] = (i, kb)
+                    bar.complete_tx(1)
                 landings.append(land)
                 yield None
-            rr = i % RR
-            if i >= RR:
-                yield lambda rr=rr, i=i: rope_empty[rr].passes(((i // RR) - 1) & 1)
-            rope_full[rr].arrive_expect(1, 1)
+            if expand:
+                sb = i & 1
+                if i >= 2:
+                    yield lambda sb=sb, i=i: scale_empty[sb].passes(((i >> 1) - 1) & 1)
+                scale_full[sb].arrive_expect(1, 1)
 
-            def land_rope(rr=rr, i=i):
-                rope_data[rr] = i
-                rope_full[rr].complete_tx(1)
-            landings.append(land_rope)
+                def land_scales(sb=sb, i=i):
+                    scale_data[sb] = i
+                    scale_full[sb].complete_tx(1)
+                landings.append(land_scales)
+                yield None
+            if not rope_first:
+                yield from load_rope(i)
+
+    def expander(e):
+        for i in range(N):
+            sb = i & 1
+            yield lambda sb=sb, i=i: scale_full[sb].passes((i >> 1) & 1)
+            u = KB * i + e
+            s, f = u % R, u // R
+            yield lambda s=s, f=f: raw_full[s].passes(f & 1)
+            if raw_data[s] != (i, e):
+                errors.append(f"expander {e} tile {i} widened codes of {raw_data[s]}")
+            if scale_data[sb] != i:
+                errors.append(f"expander {e} tile {i} used the scales of tile {scale_data[sb]}")
+            slot_data[s] = (i, e)
+            blk_full[s].arrive_expect()
+            yield None
+            scale_empty[sb].arrive_expect()
             yield None
 
     def s_issuer():
@@ -189,6 +237,9 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
     actors = {"S": s_issuer(), "SM": softmax(), "PV0": pv(0), "PV1": pv(1)}
     for pp in range(producers):
         actors[f"LD{pp}"] = producer(pp)
+    if expand:
+        for e in range(KB):
+            actors[f"EX{e}"] = expander(e)
     weight = {k: (weights or {}).get(k, 1.0) for k in actors}
     waiting = {k: None for k in actors}
     finished_actors = set()

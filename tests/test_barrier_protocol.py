@@ -19,23 +19,26 @@ from barrier_model_pair import run_pair
 SKEWS = [None, {"PV0": 0.02}, {"PV1": 0.02}, {"PV0": 0.01, "LD1": 0.2}, {"PV1": 0.01, "LD0": 0.2},
          {"PV0": 0.005, "S": 3.0, "LD0": 3.0}]
 
-# (name, blocks per tile, ring slots, rope slots, producers, P buffers, rope read first: an
-#  order of the score product that the kernels do not use, measured slower, kept as a model case)
+# (name, blocks per tile, ring slots, rope slots, producers, P buffers, rope read first (the
+#  folded kernel's order: S reads the rope first and frees it early, the producers load it
+#  first), fp8 rows widened in place by one expander per block)
 SHAPES = [
-    ("folded 16 rows", 4, 11, 2, 2, 2, False),
-    ("folded 32 rows", 4, 10, 1, 2, 2, False),
-    ("folded 64 rows", 4, 8, 1, 2, 1, False),
-    ("folded latent 256, 16 rows", 2, 11, 2, 2, 2, False),
-    ("folded latent 256, 32 rows", 2, 10, 2, 2, 2, False),
-    ("folded latent 768, 16 rows", 6, 10, 2, 2, 2, False),
-    ("folded latent 1792 (one CTA of a pair), 16 rows", 7, 9, 2, 2, 2, False),
-    ("folded 64 rows, rope read first", 4, 8, 1, 2, 1, True),
-    ("cluster TMA 16 rows", 2, 5, 3, 1, 2, False),
-    ("cluster TMA 32 rows", 2, 5, 2, 1, 2, False),
-    ("cluster load/convert 16 rows", 2, 4, 3, 2, 2, False),
-    ("cluster load/convert 32 rows", 2, 4, 2, 2, 2, False),
-    ("cluster load/convert 64 rows", 2, 4, 1, 2, 1, False),
-    ("cluster fp8 64 rows", 2, 4, 1, 1, 1, False),
+    ("folded 16 rows", 4, 11, 2, 2, 2, True, False),
+    ("folded 32 rows", 4, 10, 1, 2, 2, True, False),
+    ("folded 64 rows", 4, 8, 1, 2, 1, True, False),
+    ("folded latent 256, 16 rows", 2, 11, 2, 2, 2, True, False),
+    ("folded latent 256, 32 rows", 2, 10, 2, 2, 2, True, False),
+    ("folded latent 768, 16 rows", 6, 10, 2, 2, 2, True, False),
+    ("folded latent 1792 (one CTA of a pair), 16 rows", 7, 9, 2, 2, 2, True, False),
+    ("folded fp8 64 rows", 4, 8, 1, 1, 1, True, True),
+    ("folded 64 rows, rope read last", 4, 8, 1, 2, 1, False, False),
+    ("folded fp8 64 rows, rope read last", 4, 8, 1, 1, 1, False, True),
+    ("cluster TMA 16 rows", 2, 5, 3, 1, 2, False, False),
+    ("cluster TMA 32 rows", 2, 5, 2, 1, 2, False, False),
+    ("cluster load/convert 16 rows", 2, 4, 3, 2, 2, False, False),
+    ("cluster load/convert 32 rows", 2, 4, 2, 2, 2, False, False),
+    ("cluster load/convert 64 rows", 2, 4, 1, 2, 1, False, False),
+    ("cluster fp8 64 rows", 2, 4, 1, 1, 1, False, False),
 ]
 
 
@@ -49,9 +52,9 @@ def failures(seeds, **shape):
     return out
 
 
-@pytest.mark.parametrize("name,KB,R,RR,producers,PB,rope_first", SHAPES, ids=[s[0] for s in SHAPES])
-def test_kernel_shapes_survive_skew(name, KB, R, RR, producers, PB, rope_first):
-    bad = failures(40, KB=KB, R=R, RR=RR, producers=producers, PB=PB, H=2, rope_first=rope_first)
+@pytest.mark.parametrize("name,KB,R,RR,producers,PB,rope_first,expand", SHAPES, ids=[s[0] for s in SHAPES])
+def test_kernel_shapes_survive_skew(name, KB, R, RR, producers, PB, rope_first, expand):
+    bad = failures(40, KB=KB, R=R, RR=RR, producers=producers, PB=PB, H=2, rope_first=rope_first, expand=expand)
     assert not bad, bad[:3]
 
 
