@@ -1468,10 +1468,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // to its value product only, with no exchange latency in between.
 //
 // Query rows: NP = 16, 32 or 64 a CTA. At 32 and 64 rows two softmax groups of
-// four warps each own half of the columns. At 64 rows Q takes 72 KB, so the
-// ring has eight K-block slots (two tiles), one P buffer and one O
-// accumulator (a finished segment is written out before the next segment's
-// first value product). 65..128 rows: the two 64-row groups of a worker run
+// four warps each own half of the columns (at 64 rows: half of the tile's
+// tokens, for every query). At 64 rows the score product is transposed, with
+// Q's latent part in TMEM as its A operand; the ring has twelve K-block slots
+// (three tiles), one S buffer, one P buffer and one O accumulator (a finished
+// segment is written out before the next segment's first value product).
+// 65..128 rows: the two 64-row groups of a worker run
 // as a cluster of two CTAs that share each tile through multicast TMA (each
 // issues half of the boxes into both), so the cache is read once per request.
 // fp8_ds_mla rows at 64 rows: TMA lands each K-block's e4m3 codes in the upper
@@ -1496,10 +1498,18 @@ struct FoldCfg {
     // K-block slots (4 per tile) and rope slots (1 per tile, freed right after
     // S): at 32 rows a tenth K-block slot is worth more than a second rope slot
     // (the rope reload waits for one S, well inside a tile's time; 3% faster)
-    // At 64 query rows Q takes 72 KB. Eight K-block slots (two tiles, so that
-    // tile i's loads wait for PV(i - 2), not PV(i - 1)) and one rope slot fit
-    // beside one P buffer and a quarter-width exchange buffer.
-    static constexpr int kRL = PAIR ? 9 : (KB == 4) ? ((NP == 16) ? 11 : NP == 32 ? 10 : 8)
+    // At 64 query rows only Q's rope part (8 KB) stays in shared memory: twelve
+    // K-block slots (three tiles, so that tile i's loads wait for PV(i - 3))
+    // and one rope slot fit beside one P buffer and a quarter-width exchange
+    // buffer.
+    // kTr: at 64 rows the score product runs transposed, S^T = Q K^T, with the
+    // latent part of Q as the A operand in TMEM (lanes 0..63: the queries'
+    // first latent halves, 64..127: their second halves) and the tile as B, so
+    // that Q's 64 KB leave shared memory for four more K-block slots (three
+    // tiles in flight). TMEM: O in columns [0, 256), Q in [256, 384), one S
+    // buffer in [384, 512).
+    static constexpr bool kTr = NP == 64;
+    static constexpr int kRL = PAIR ? 9 : (KB == 4) ? ((NP == 16) ? 11 : NP == 32 ? 10 : 12)
                                                     : (KB == 2 ? ((NP == 16) ? 11 : 10) : 10);
     static constexpr int kRR = (KB == 4) ? ((NP == 16) ? 2 : 1) : 2;
     // K-blocks [kb_lo(pp), kb_hi(pp)) of each tile belong to producer pp and PV issuer pp
@@ -1514,7 +1524,7 @@ struct FoldCfg {
     // issuer runs behind (checked on a random-schedule model of the protocol).
     static __device__ __forceinline__ int slot_of(int i, int kb) { return (KB * i + kb) % kRL; }
     static __device__ __forceinline__ int fill_of(int i, int kb) { return (KB * i + kb) / kRL; }
-    static constexpr int kQBytes = 2 * NP * (KB * 128 + 64);
+    static constexpr int kQBytes = kTr ? 2 * NP * 64 : 2 * NP * (KB * 128 + 64);  // kTr: the rope part only
     // Softmax groups: at 32 and 64 rows of the 576-wide row two groups of four
     // warps, each owning half of the query columns (two warps per scheduler,
     // half the work per thread)
@@ -1557,16 +1567,20 @@ struct FoldCfg {
     // 2 x NP columns. With one accumulator a finished segment is drained
     // before the next segment's first value product.
     static constexpr bool kOneO = NP == 64;
-    static constexpr int kColS = (kOneO ? 1 : 2) * KB * NP;
-    static constexpr int kTmemCols = (kColS + 4 * NP) <= 128 ? 128 : (kColS + 4 * NP) <= 256 ? 256 : 512;
+    static constexpr int kColQ = KB * NP;               // kTr: Q's latent values, 2 a column
+    static constexpr int kColS = kTr ? kColQ + 64 * KB / 2 : (kOneO ? 1 : 2) * KB * NP;
+    static constexpr int kSBufs = kTr ? 1 : 2;
+    static constexpr int kTmemCols = (kColS + kSBufs * 2 * NP) <= 128   ? 128
+                                     : (kColS + kSBufs * 2 * NP) <= 256 ? 256
+                                                                        : 512;
     // one row of P = one swizzle atom
     static constexpr uint32_t kPSwizzle = NP == 16 ? kSw32 : NP == 32 ? kSw64 : kSw128;
     static_assert(kSmemBytes <= 232448, "shared memory");
-    static_assert(kColS + 4 * NP <= kTmemCols, "tmem");
+    static_assert(kColS + kSBufs * 2 * NP <= kTmemCols, "tmem");
 };
 
 struct FoldCtrl {
-    uint64_t blk_full[11], blk_empty[11];
+    uint64_t blk_full[12], blk_empty[12];
     uint64_t rope_full[2], rope_empty[2];
     uint64_t s_full[2], s_free[2], o_done[2], q_full;
     // tile t's P hand-off to the two PV issuers is p_full[t & 1]: the softmax
@@ -1577,7 +1591,8 @@ struct FoldCtrl {
     uint64_t p_full[2];
     uint64_t x2full, x2free;         // CTA pair: the peer's partial scores landed / it has read ours
     uint64_t fin[3];                 // the S and PV issuers' products have all completed (at exit)
-    uint64_t raw_full[8];            // fp8 rows: a K-block's codes landed in the upper half of its slot
+    uint64_t raw_full[12];           // fp8 rows: a K-block's codes landed in the upper half of its slot
+    uint64_t q_tmem;                 // transposed scores: the softmax warps have written Q's latent part
     uint64_t scale_full[2], scale_empty[2];  // fp8 rows: a tile's block scales landed / both expanders done
     uint32_t tmem_base;
     int abort;
@@ -1660,6 +1675,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             mbar_init(&ctrl->s_free[i], C::kSG);  // one arrive per softmax group
             mbar_init(&ctrl->o_done[i], 2);  // one commit per PV issuer
         }
+        mbar_init(&ctrl->q_tmem, 4 * C::kSG);  // one arrive per softmax warp
         mbar_init(&ctrl->p_full[0], C::kSG);
         mbar_init(&ctrl->p_full[1], C::kSG);
         mbar_init(&ctrl->q_full, 1);
@@ -1730,23 +1746,28 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint32_t idS = idesc_bf16(128, 2 * NP, false, false);
             const uint64_t dq = smem_desc(smem_u32(qs), 16, 1024, kSw128);
-            const uint64_t dqr = smem_desc(smem_u32(qs) + 2 * KB * NP * 128, 16, 512, kSw64);
+            const uint64_t dqr = smem_desc(smem_u32(qs) + (C::kTr ? 0 : 2 * KB * NP * 128), 16, 512, kSw64);
             int seg = 0;
             for (int i = 0; i < ntiles; ++i) {
                 if (i == 0 || it.j == 0) {
-                    if (!mbar_wait(&ctrl->q_full, seg & 1, &ctrl->abort)) {
+                    // a new request: its Q (with kTr, the rope part here and the
+                    // latent part in TMEM, written by the softmax warps)
+                    if (!mbar_wait(&ctrl->q_full, seg & 1, &ctrl->abort) ||
+                        (C::kTr && !mbar_wait(&ctrl->q_tmem, seg & 1, &ctrl->abort))) {
                         fail(p, ctrl, kErrWaitTimeout, kSiteQFull, i);
                         report(p, kRoleS, kSiteQFull, i);
                         break;
                     }
                     ++seg;
                 }
-                if (i >= 2 && !mbar_wait(&ctrl->s_free[i & 1], ((i - 2) >> 1) & 1, &ctrl->abort)) {
+                // the softmax has read S(i - kSBufs) from the buffer S(i) writes
+                if (i >= C::kSBufs &&
+                    !mbar_wait(&ctrl->s_free[i % C::kSBufs], ((i / C::kSBufs) - 1) & 1, &ctrl->abort)) {
                     fail(p, ctrl, kErrWaitTimeout, kSiteSFree, i);
                     report(p, kRoleS, kSiteSFree, i);
                     break;
                 }
-                const uint32_t tS = tmem + C::kColS + (i & 1) * 2 * NP;
+                const uint32_t tS = tmem + C::kColS + (i % C::kSBufs) * 2 * NP;
                 bool ok = true;
                 int site = kSitePairFull;
                 const int rr = i % C::kRR;
@@ -1758,8 +1779,13 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                         tc_fence_after();
                         MLA_TRACE_POINT(i, kTrSRope);
                         const uint64_t dr = smem_desc(smem_u32(rope_ring + rr * C::kRopeBytes), 16, 512, kSw64);
-                        umma_bf16(tS, dr, dqr, idS, 0u);
-                        umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
+                        if constexpr (C::kTr) {
+                            umma_bf16(tS, dqr, dr, idS, 0u);
+                            umma_bf16(tS, dqr + 2, dr + 2, idS, 1u);
+                        } else {
+                            umma_bf16(tS, dr, dqr, idS, 0u);
+                            umma_bf16(tS, dr + 2, dqr + 2, idS, 1u);
+                        }
                         if constexpr (MC) umma_commit_mc(&ctrl->rope_empty[rr], kPairMask);
                         else umma_commit(&ctrl->rope_empty[rr]);
                     }
@@ -1772,9 +1798,13 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     else if (kb < 4) MLA_TRACE_POINT(i, kTrSKb1 + kb - 1);
                     const uint64_t da = smem_desc(smem_u32(ring + slot * C::kBlkBytes), 16, 1024, kSw128);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4), idS,
-                                  (has_rope || (kb | kk) != 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if constexpr (C::kTr)
+                            umma_bf16_ta(tS, tmem + C::kColQ + kb * 32 + kk * 8, da + ((kk * 32) >> 4), idS, 1u);
+                        else
+                            umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4), idS,
+                                      (has_rope || (kb | kk) != 0) ? 1u : 0u);
+                    }
                 }
                 if (!ok) {
                     fail(p, ctrl, kErrWaitTimeout, site, i);
@@ -1782,7 +1812,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     break;
                 }
                 MLA_TRACE_POINT(i, kTrSAllIn);
-                umma_commit(&ctrl->s_full[i & 1]);
+                umma_commit(&ctrl->s_full[i % C::kSBufs]);
                 MLA_TRACE_POINT(i, kTrSIssued);
                 it.next(p.seq_lens, p.B);
             }
@@ -1797,7 +1827,9 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             const int mt = warp == 3 ? 0 : 1;
             It it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
-            const uint32_t idPV = idesc_bf16(128, NP, true, true);
+            // P: [64 tokens][NP] (MN-major), or with kTr [NP queries][64 tokens]
+            // (K-major, a 128-byte row per query)
+            const uint32_t idPV = idesc_bf16(128, NP, true, !C::kTr);
             constexpr uint32_t p_sbo = 8 * NP * 2;
 
             int seg = -1;
@@ -1812,8 +1844,9 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 }
                 tc_fence_after();
                 if (mt == 0) MLA_TRACE_POINT(i, kTrPvIssue);
-                const uint64_t dp = smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), C::kPBytes, p_sbo,
-                                              C::kPSwizzle);
+                const uint64_t dp = C::kTr ? smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), 16, 1024, kSw128)
+                                           : smem_desc(smem_u32(pbufs + (i % C::kPBufs) * C::kPBytes), C::kPBytes,
+                                                       p_sbo, C::kPSwizzle);
 #pragma unroll
                 for (int q = 0; q < (KB + 1) / 2; ++q) {
                     const int kb = C::kb_lo(mt) + q;
@@ -1823,7 +1856,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     const uint64_t da = smem_desc(smem_u32(ring + slot * C::kBlkBytes), 8192, 1024, kSw128);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tO + kb * NP, da + ((kk * 2048) >> 4), dp + ((kk * 16 * NP * 2) >> 4), idPV,
+                        umma_bf16(tO + kb * NP, da + ((kk * 2048) >> 4),
+                                  dp + ((C::kTr ? kk * 32 : kk * 16 * NP * 2) >> 4), idPV,
                                   (new_seg && kk == 0) ? 0u : 1u);
                     if constexpr (MC) umma_commit_mc(&ctrl->blk_empty[slot], kPairMask);
                     else umma_commit(&ctrl->blk_empty[slot]);
@@ -2097,6 +2131,11 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             // GW): the thread keeps [own0, own0 + NH) and hands the group's other
             // NH partial scores to its partner st ^ 64, the other half of the same
             // token.
+            // kTr (64 rows, S^T): lane st holds half hf of query tt's scores and
+            // the columns are the tile's token halves, so the same exchange leaves
+            // the thread the whole scores of query tt for tokens [own0, own0 +
+            // NH); the four threads of a query (two halves, two groups) meet for
+            // its row maximum and sum, and O's columns stay the groups' queries.
             const int grp = warp >= 9 ? 1 : 0;
             const int sw = warp & 3;  // TMEM lane quadrant
             const int st = sw * 32 + lane;
@@ -2108,6 +2147,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             const int own0 = cg0 + hf * NH;
             const int par0 = cg0 + (hf ? 0 : NH);  // the partner's columns
             const int bsync = grp ? 3 : 1, bvote = grp ? 4 : 2;  // the group's named barriers
+            constexpr int kBarAll = 5, kBarAllOr = 6;             // both groups (kTr)
             const bool lead = grp == 0 && st == 0;  // once-per-CTA work of the tile
             // exchange rows of XR floats (the group's own rows), 16-byte units
             // swizzled by row; thread st writes row st ^ 64 and reads row st (same
@@ -2172,25 +2212,62 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 const int y = static_cast<int>(req_row0(p, bq) + gy * 64);
                 const uint64_t pol = l2_policy_evict_first();
                 mbar_arrive_expect_tx(&ctrl->q_full, has_rope ? C::kQBytes : C::kQBytes - 2 * NP * 64);
+                if constexpr (!C::kTr) {
 #pragma unroll
-                for (int k = 0; k < KB; ++k)
+                    for (int k = 0; k < KB; ++k)
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
-                        tma_load_2d(qs + (k * 2 + hh) * NP * 128, &maps.q, &ctrl->q_full,
-                                    dbase + C::kHalf * hh + 64 * k, y, pol);
+                        for (int hh = 0; hh < 2; ++hh)
+                            tma_load_2d(qs + (k * 2 + hh) * NP * 128, &maps.q, &ctrl->q_full,
+                                        dbase + C::kHalf * hh + 64 * k, y, pol);
+                }
                 if (has_rope) {
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh)
-                        tma_load_2d(qs + 2 * KB * NP * 128 + hh * NP * 64, &maps.qpe, &ctrl->q_full, 32 * hh, y, pol);
+                        tma_load_2d(qs + (C::kTr ? 0 : 2 * KB * NP * 128) + hh * NP * 64, &maps.qpe, &ctrl->q_full,
+                                    32 * hh, y, pol);
                 }
+            };
+
+            // kTr: Q's latent part of request bq into TMEM, the A operand of S^T:
+            // lane st holds half hf of query tt (latent dims 256 hf ..), group grp
+            // its columns [64 grp, 64 grp + 64) (dims 256 hf + 128 grp ..); padding
+            // rows are zeros. Called once S has read the previous request's Q.
+            auto write_q = [&](int bq) {
+                const bool v = tt < req_rows_in_group(p, bq, gy);
+                const __nv_bfloat16* src =
+                    p.q_lat + (req_row0(p, bq) + gy * 64 + (v ? tt : 0)) * static_cast<int64_t>(C::kD) + 256 * hf + 128 * grp;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 w = v ? __ldg(reinterpret_cast<const uint4*>(src + 32 * q4 + 8 * u)) : make_uint4(0, 0, 0, 0);
+                        r[4 * u] = w.x;
+                        r[4 * u + 1] = w.y;
+                        r[4 * u + 2] = w.z;
+                        r[4 * u + 3] = w.w;
+                    }
+                    tmem_st_x16(tmem + lane_base + C::kColQ + 64 * grp + 16 * q4, r);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->q_tmem);
             };
 
             // Row sums and maxima of segment sg, which just ended, into
             // dlt / dm [sg & 1]; fresh softmax state for the next segment.
             auto capture = [&](int sg) {
+                if constexpr (C::kTr) {
+                    // query tt's sum: this thread's tokens, the partner half's, the
+                    // other group's two
+                    ctrl->red[2 * grp + hf][tt] = l[0];
+                    named_bar_sync(kBarAll, 256);
+                } else {
 #pragma unroll
-                for (int c = 0; c < NH; ++c) red_store(c, warp_sum(l[c]), 0.f);
-                named_bar_sync(bsync, 128);
+                    for (int c = 0; c < NH; ++c) red_store(c, warp_sum(l[c]), 0.f);
+                    named_bar_sync(bsync, 128);
+                }
                 if (st < GW) {
                     const int c = cg0 + st;
                     ctrl->dlt[sg & 1][c] = ctrl->red[0][c] + ctrl->red[1][c] + ctrl->red[2][c] + ctrl->red[3][c];
@@ -2199,7 +2276,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 }
 #pragma unroll
                 for (int c = 0; c < NH; ++c) l[c] = 0.f;
-                named_bar_sync(bsync, 128);
+                if constexpr (C::kTr) named_bar_sync(kBarAll, 256);
+                else named_bar_sync(bsync, 128);
             };
 
             // The captured segment sg (accumulator src) has had its last PV:
@@ -2260,8 +2338,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
 
             // Hand tile t to the PV issuers, then start or advance the drain.
             // False when the group aborts.
-            auto finish = [&](int t) -> bool {
-                if (ctrl->abort) return false;  // same value in every thread after the last barrier
+            auto finish = [&](int t, bool aborted) -> bool {
+                if (aborted) return false;  // the same value in every thread of the group (kTr: of both)
                 if (st == 0) {
                     // (one arrive per group) the test hook withholds tile 0, so the PV
                     // issuers' bounded wait gives up and every role leaves through the
@@ -2287,11 +2365,12 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             };
 
             if (lead) issue_q(it.b);
+            if constexpr (C::kTr) write_q(it.b);
             bool alive = true;
             for (int i = 0; i < ntiles; ++i) {
                 const int b = it.b, j = it.j, T = it.T;
                 const bool last_of_seg = (j == it.tiles - 1) || (i == ntiles - 1);
-                group_wait(&ctrl->s_full[i & 1], (i >> 1) & 1, p, ctrl, kSiteSFull, i);
+                group_wait(&ctrl->s_full[i % C::kSBufs], (i / C::kSBufs) & 1, p, ctrl, kSiteSFull, i);
                 if (lead) MLA_TRACE_POINT(i, kTrSmSFull);
                 if (lead && last_of_seg && i + 1 < ntiles) {
                     // S(i) is complete, so Q may be replaced by the next request's
@@ -2305,7 +2384,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 // NP) (a TMEM load takes one column address per warp: hf is the same
                 // in the warp). It keeps the NH columns [own0, own0 + NH) and writes
                 // the other NH into its partner's exchange row, XR at a time.
-                const uint32_t s_addr = tmem + lane_base + C::kColS + (i & 1) * 2 * NP + hf * NP + cg0;
+                const uint32_t s_addr = tmem + lane_base + C::kColS + (i % C::kSBufs) * 2 * NP + hf * NP + cg0;
                 uint32_t sr[GW];
                 tmem_ld_np<GW>(s_addr, sr);
                 tc_fence_before();
@@ -2365,7 +2444,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 } else {
                     named_bar_sync(bsync, 128);
                 }
-                if (st == 0) mbar_arrive(&ctrl->s_free[i & 1]);  // every thread of the group has read S(i)
+                if (st == 0) mbar_arrive(&ctrl->s_free[i % C::kSBufs]);  // every thread of the group has read S(i)
                 if (lead) MLA_TRACE_POINT(i, kTrSmXFull);
                 float x[NH];
                 // own columns [base, base + XR) plus the partner's half of them
@@ -2418,7 +2497,24 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 const int tok = j * kT + tt;
                 const bool all_vis = (j * kT + kT + seg_qt - 1) <= T;
                 const float4* m4p = reinterpret_cast<const float4*>(ctrl->m + own0);
-                if (all_vis) {
+                if constexpr (C::kTr) {
+                    // x[c]: query tt, token j kT + own0 + c
+                    if (all_vis) {
+                        const bool qv = tt < seg_hq;
+#pragma unroll
+                        for (int c = 0; c < NH; ++c) x[c] = qv ? x[c] * p.scale_log2 : -INFINITY;
+                    } else if (p.cu_q) {
+                        const int r = gy * 64 + tt;
+                        const int lim = T - (seg_qt - 1 - r / p.Hq) - (j * kT + own0);  // visible: c < lim
+                        const bool qv = tt < seg_hq;
+#pragma unroll
+                        for (int c = 0; c < NH; ++c) x[c] = (qv && c < lim) ? x[c] * p.scale_log2 : -INFINITY;
+                    } else {
+                        const int lim = T - ctrl->colvis[tt] - (j * kT + own0);
+#pragma unroll
+                        for (int c = 0; c < NH; ++c) x[c] = (c < lim) ? x[c] * p.scale_log2 : -INFINITY;
+                    }
+                } else if (all_vis) {
 #pragma unroll
                     for (int c = 0; c < NH; ++c) x[c] = (own0 + c < seg_hq) ? x[c] * p.scale_log2 : -INFINITY;
                 } else {
@@ -2439,17 +2535,45 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     }
                 }
                 int need = 0;
+                if constexpr (C::kTr) {
+                    const float mq = ctrl->m[tt] + kRescaleThreshold;
 #pragma unroll
-                for (int u = 0; u < NH / 4; ++u) {
-                    const float4 mv = m4p[u];
-                    need |= (x[4 * u] > mv.x + kRescaleThreshold) | (x[4 * u + 1] > mv.y + kRescaleThreshold) |
-                            (x[4 * u + 2] > mv.z + kRescaleThreshold) | (x[4 * u + 3] > mv.w + kRescaleThreshold);
+                    for (int c = 0; c < NH; ++c) need |= x[c] > mq;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < NH / 4; ++u) {
+                        const float4 mv = m4p[u];
+                        need |= (x[4 * u] > mv.x + kRescaleThreshold) | (x[4 * u + 1] > mv.y + kRescaleThreshold) |
+                                (x[4 * u + 2] > mv.z + kRescaleThreshold) | (x[4 * u + 3] > mv.w + kRescaleThreshold);
+                    }
                 }
                 // (also: every thread has read its exchange row)
                 if (lead) MLA_TRACE_POINT(i, kTrSmMath);
-                need = named_bar_or(bvote, 128, need);
+                // kTr: a query's maximum involves both groups, and so does its O column
+                need = C::kTr ? named_bar_or(kBarAllOr, 256, need) : named_bar_or(bvote, 128, need);
                 if (lead) MLA_TRACE_POINT(i, kTrSmBarOr);
-                if (need) {
+                if (need && C::kTr) {
+                    // query tt's maximum over the tile: its four threads' maxima
+                    float mx = x[0];
+#pragma unroll
+                    for (int c = 1; c < NH; ++c) mx = fmaxf(mx, x[c]);
+                    ctrl->red[2 * grp + hf][tt] = mx;
+                    named_bar_sync(kBarAll, 256);
+                    if (grp == 0 && hf == 0) {
+                        const float mt = fmaxf(fmaxf(ctrl->red[0][tt], ctrl->red[1][tt]), fmaxf(ctrl->red[2][tt], ctrl->red[3][tt]));
+                        const float mo = ctrl->m[tt];
+                        const float mn = fmaxf(mo, mt);
+                        ctrl->alpha[tt] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
+                        ctrl->m[tt] = mn;
+                    }
+                    named_bar_sync(kBarAll, 256);
+                    l[0] *= ctrl->alpha[tt];
+                    if (seg_has_pv) {
+                        group_wait(&ctrl->o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p, ctrl, kSiteORescale, i);
+                        rescale_o(obuf);
+                        if (lead) MLA_TRACE_POINT(i, kTrSmRescaled);
+                    }
+                } else if (need) {
                     // column maxima over the tile's 64 tokens
 #pragma unroll
                     for (int c = 0; c < NH; ++c) red_store(c, warp_max(x[c]), -INFINITY);
@@ -2473,17 +2597,29 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                         if (lead) MLA_TRACE_POINT(i, kTrSmRescaled);
                     }
                 }
+                if constexpr (C::kTr) {
+                    const float mq = ctrl->m[tt];
+                    const float mk = (mq == -INFINITY) ? 0.f : mq;
+                    float ls = 0.f;
 #pragma unroll
-                for (int u = 0; u < NH / 4; ++u) {
-                    const float4 mv = m4p[u];
-                    const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+                    for (int c = 0; c < NH; ++c) {
+                        x[c] = ex2(x[c] - mk);
+                        ls += x[c];
+                    }
+                    l[0] += ls;
+                } else {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = 4 * u + k;
-                        const float mk = (mm[k] == -INFINITY) ? 0.f : mm[k];
-                        const float pc = ex2(x[c] - mk);
-                        l[c] += pc;
-                        x[c] = pc;
+                    for (int u = 0; u < NH / 4; ++u) {
+                        const float4 mv = m4p[u];
+                        const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int c = 4 * u + k;
+                            const float mk = (mm[k] == -INFINITY) ? 0.f : mm[k];
+                            const float pc = ex2(x[c] - mk);
+                            l[c] += pc;
+                            x[c] = pc;
+                        }
                     }
                 }
                 if (lead) MLA_TRACE_POINT(i, kTrSmExpLoop);
@@ -2496,7 +2632,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     if (!okp && lane == 0) fail(p, ctrl, kErrWaitTimeout, kSiteOPbuf, i);
                 }
                 if (lead) MLA_TRACE_POINT(i, kTrSmExp);
-                // P row tt, columns [own0, own0 + NH): NH / 8 16-byte units
+                // P row tt, columns [own0, own0 + NH): NH / 8 16-byte units (kTr: row
+                // = query tt, columns = tokens: the K-major P the value product reads)
                 const int pb = i % C::kPBufs;
                 uint8_t* prow = pbufs + pb * C::kPBytes + tt * NP * 2;
                 const int sz = swz_p(tt, C::kPSwizzle);
@@ -2522,8 +2659,16 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 if (lead) MLA_TRACE_POINT(i, kTrSmPStore);
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_sync(bsync, 128);
-                if (!finish(i)) {
+                // kTr: the groups meet at barriers of all 256 threads, so they must
+                // leave together: the abort flag is read in one reduction
+                bool aborted;
+                if constexpr (C::kTr) {
+                    aborted = named_bar_or(kBarAllOr, 256, ctrl->abort != 0) != 0;
+                } else {
+                    named_bar_sync(bsync, 128);
+                    aborted = ctrl->abort != 0;
+                }
+                if (!finish(i, aborted)) {
                     alive = false;
                     break;
                 }
@@ -2533,6 +2678,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     seg_start_j = 0;
                 }
                 it.next(p.seq_lens, p.B);
+                // S(i), the request's last score product, has read Q: the next one's
+                if (C::kTr && last_of_seg && i + 1 < ntiles) write_q(it.b);
             }
             if (alive) {
                 // the last segment: finish the older drain, capture, wait for its

@@ -2,7 +2,8 @@
 
 The actors are the roles of one CTA:
 - the load producers, one warp, or two that split each tile's blocks;
-- the S (score) issuer;
+- the S (score) issuer, into SB score buffers (one with the transposed
+  64-row product);
 - the softmax warps, as one actor because named barriers keep them in step;
 - the two PV issuers.
 Each actor takes one step at a time, in a random order weighted per actor,
@@ -67,7 +68,7 @@ class Bar:
 
 
 def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int, N: int = 40,
-        weights: dict | None = None, rope_first: bool = False, expand: bool = False) -> list[str]:
+        weights: dict | None = None, rope_first: bool = False, expand: bool = False, SB: int = 2) -> list[str]:
     """One random schedule; returns the problems found (empty when none)."""
     rnd = random.Random(seed)
     blk_full = [Bar(1) for _ in range(R)]
@@ -79,7 +80,7 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
     blk_empty = [Bar(1) for _ in range(R)]
     rope_full = [Bar(producers) for _ in range(RR)]
     rope_empty = [Bar(1) for _ in range(RR)]
-    s_full, s_free = [Bar(1), Bar(1)], [Bar(1), Bar(1)]
+    s_full, s_free = [Bar(1) for _ in range(SB)], [Bar(1) for _ in range(SB)]
     o_done = [Bar(2), Bar(2)]
     handoff = [Bar(1) for _ in range(H)]
     slot_data, slot_held = [None] * R, [None] * R
@@ -164,8 +165,8 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
 
     def s_issuer():
         for i in range(N):
-            if i >= 2:
-                yield lambda i=i: s_free[i & 1].passes(((i - 2) >> 1) & 1)
+            if i >= SB:
+                yield lambda i=i: s_free[i % SB].passes(((i // SB) - 1) & 1)
             rr = i % RR
             if rope_first:
                 # the rope's products first; its slot is released once they are done
@@ -185,8 +186,8 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
                     errors.append(f"S({i}) rope read tile {rope_data[rr]}")
 
             def done(i=i, rr=rr):
-                s_buf[i & 1] = i
-                s_full[i & 1].arrive_expect()
+                s_buf[i % SB] = i
+                s_full[i % SB].arrive_expect()
                 if not rope_first:
                     rope_empty[rr].arrive_expect()
             commits["S"].append(done)
@@ -194,10 +195,10 @@ def run(seed: int, *, KB: int, R: int, RR: int, producers: int, PB: int, H: int,
 
     def softmax():
         for i in range(N):
-            yield lambda i=i: s_full[i & 1].passes((i >> 1) & 1)
-            if s_buf[i & 1] != i:
-                errors.append(f"softmax({i}) read S of tile {s_buf[i & 1]}")
-            s_free[i & 1].arrive_expect()
+            yield lambda i=i: s_full[i % SB].passes((i // SB) & 1)
+            if s_buf[i % SB] != i:
+                errors.append(f"softmax({i}) read S of tile {s_buf[i % SB]}")
+            s_free[i % SB].arrive_expect()
             yield None
             if i > 0 and rnd.random() < 0.3:
                 yield lambda i=i: o_done[(i - 1) & 1].passes(((i - 1) >> 1) & 1)

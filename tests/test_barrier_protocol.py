@@ -25,7 +25,7 @@ SKEWS = [None, {"PV0": 0.02}, {"PV1": 0.02}, {"PV0": 0.01, "LD1": 0.2}, {"PV1": 
 SHAPES = [
     ("folded 16 rows", 4, 11, 2, 2, 2, True, False),
     ("folded 32 rows", 4, 10, 1, 2, 2, True, False),
-    ("folded 64 rows", 4, 8, 1, 2, 1, True, False),
+    ("folded 64 rows (two score buffers)", 4, 8, 1, 2, 1, True, False),
     ("folded latent 256, 16 rows", 2, 11, 2, 2, 2, True, False),
     ("folded latent 256, 32 rows", 2, 10, 2, 2, 2, True, False),
     ("folded latent 768, 16 rows", 6, 10, 2, 2, 2, True, False),
@@ -50,6 +50,19 @@ def failures(seeds, **shape):
             if e:
                 out.append((w, seed, e[0]))
     return out
+
+
+# the transposed 64-row kernels: twelve K-block slots, one score buffer
+SHAPES_ONE_S = [
+    ("folded 64 rows, transposed scores", 4, 12, 1, 2, 1, True, False),
+    ("folded fp8 64 rows, transposed scores", 4, 12, 1, 1, 1, True, True),
+]
+
+
+@pytest.mark.parametrize("name,KB,R,RR,producers,PB,rope_first,expand", SHAPES_ONE_S, ids=[s[0] for s in SHAPES_ONE_S])
+def test_one_score_buffer_shapes_survive_skew(name, KB, R, RR, producers, PB, rope_first, expand):
+    bad = failures(40, KB=KB, R=R, RR=RR, producers=producers, PB=PB, H=2, rope_first=rope_first, expand=expand, SB=1)
+    assert not bad, bad[:3]
 
 
 @pytest.mark.parametrize("name,KB,R,RR,producers,PB,rope_first,expand", SHAPES, ids=[s[0] for s in SHAPES])
