@@ -1470,8 +1470,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // Query rows: NP = 16, 32 or 64 a CTA. At 32 and 64 rows two softmax groups of
 // four warps each own half of the columns (at 64 rows: half of the tile's
 // tokens, for every query). At 64 rows the score product is transposed, with
-// Q's latent part in TMEM as its A operand; the ring has twelve K-block slots
-// (three tiles), one S buffer, one P buffer and one O accumulator (a finished
+// Q's latent part in TMEM as its A operand; the ring has eleven K-block slots
+// and two rope slots, one S buffer, one P buffer and one O accumulator (a finished
 // segment is written out before the next segment's first value product).
 // 65..128 rows: the two 64-row groups of a worker run
 // as a cluster of two CTAs that share each tile through multicast TMA (each
@@ -1498,20 +1498,21 @@ struct FoldCfg {
     // K-block slots (4 per tile) and rope slots (1 per tile, freed right after
     // S): at 32 rows a tenth K-block slot is worth more than a second rope slot
     // (the rope reload waits for one S, well inside a tile's time; 3% faster)
-    // At 64 query rows only Q's rope part (8 KB) stays in shared memory: twelve
-    // K-block slots (three tiles, so that tile i's loads wait for PV(i - 3))
-    // and one rope slot fit beside one P buffer and a quarter-width exchange
-    // buffer.
+    // At 64 query rows only Q's rope part (8 KB) stays in shared memory: eleven
+    // K-block slots (almost three tiles) and two rope slots fit beside one P
+    // buffer and a quarter-width exchange buffer. With one rope slot, each
+    // tile's rope copy would wait for the previous tile's score product, a
+    // chain as long as a tile (twelve K-block slots and one rope slot: 2% slower).
     // kTr: at 64 rows the score product runs transposed, S^T = Q K^T, with the
     // latent part of Q as the A operand in TMEM (lanes 0..63: the queries'
     // first latent halves, 64..127: their second halves) and the tile as B, so
-    // that Q's 64 KB leave shared memory for four more K-block slots (three
-    // tiles in flight). TMEM: O in columns [0, 256), Q in [256, 384), one S
+    // that Q's 64 KB leave shared memory for three more K-block slots and a
+    // second rope slot. TMEM: O in columns [0, 256), Q in [256, 384), one S
     // buffer in [384, 512).
     static constexpr bool kTr = NP == 64;
-    static constexpr int kRL = PAIR ? 9 : (KB == 4) ? ((NP == 16) ? 11 : NP == 32 ? 10 : 12)
+    static constexpr int kRL = PAIR ? 9 : (KB == 4) ? ((NP == 16) ? 11 : NP == 32 ? 10 : 11)
                                                     : (KB == 2 ? ((NP == 16) ? 11 : 10) : 10);
-    static constexpr int kRR = (KB == 4) ? ((NP == 16) ? 2 : 1) : 2;
+    static constexpr int kRR = (KB == 4) ? ((NP == 32) ? 1 : 2) : 2;
     // K-blocks [kb_lo(pp), kb_hi(pp)) of each tile belong to producer pp and PV issuer pp
     static __host__ __device__ constexpr int kb_lo(int pp) { return pp ? (KB + 1) / 2 : 0; }
     static __host__ __device__ constexpr int kb_hi(int pp) { return pp ? KB : (KB + 1) / 2; }
