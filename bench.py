@@ -282,16 +282,16 @@ def config_dict(name, ctx_tokens, cache_bytes, row_bytes, ws_):
 
 def build_workload(name, dev, rank=0, requests=None):
     """The named workload on `dev` (verify: the mtp workload's pool and
-    requests), seeded per rank. `requests` (long and fp8 only) keeps that
-    many of their equal-length requests: a cut-down copy for profiling."""
+    requests), seeded per rank. `requests` (long, fp8 and mtp only) keeps
+    that many of their requests: a cut-down copy for profiling."""
     from mla_latent_kv_cache_gb300 import workloads as W
     if name.startswith("latent"):
         return W.latent(int(name[len("latent"):]), device=dev, seed=WORKLOAD_SEED["batched"] + 1000 * rank)
     base = "mtp" if name.startswith("verify") else name
     kw = {"Qt": 8} if name == "verify8" else {}
     if requests is not None:
-        if base not in ("long", "fp8"):
-            raise SystemExit("--requests applies to the long and fp8 workloads only")
+        if name not in ("long", "fp8", "mtp"):
+            raise SystemExit("--requests applies to the long, fp8 and mtp workloads only")
         kw["B"] = int(requests)
     return W.CONFIGS[base](device=dev, seed=WORKLOAD_SEED[base] + 1000 * rank, **kw)
 
@@ -896,7 +896,7 @@ def main():
                          "'workloads' in its line ('none' to skip)")
     ap.add_argument("--clock-csv", default=None, help="write the headline run's nvidia-smi clock samples here")
     ap.add_argument("--requests", type=int, default=None,
-                    help="long / fp8 headline only: keep this many requests (a cut-down case for profiling; "
+                    help="long / fp8 / mtp headline only: keep this many requests (a cut-down case for profiling; "
                          "the line then describes that case, not the named workload)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")

@@ -1723,6 +1723,12 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
     if constexpr (PAIR || MC) cluster_sync_all();  // the peer's barriers exist before any remote traffic
     if (threadIdx.x == 0) {
         MLA_KTRACE(1);
+#ifdef MLA_TRACE
+        unsigned sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        MLA_KSM(0, sm);
+        MLA_KSM(1, ctrl->t_end - ctrl->t_begin);
+#endif
         griddep_launch_dependents();  // the merge grid may be scheduled as CTAs retire
     }
     tc_fence_after();

@@ -242,9 +242,14 @@ def mtp_seq_lens(seed: int = 4) -> np.ndarray:
             return sl
 
 
-def mtp(device="cpu", seed: int = 4, Qt: int = 4) -> Workload:
+def mtp(device="cpu", seed: int = 4, Qt: int = 4, B: int = 128) -> Workload:
     """The large-pool verify workload; Qt = 4 (1 + 3 drafts) as named, or a
-    longer step (1 + 7 drafts: Qt = 8) on the same pool and requests."""
+    longer step (1 + 7 drafts: Qt = 8) on the same pool and requests. B < 128
+    keeps the first B requests in a pool of their own size (a cut-down copy of
+    the same row shape for profiling; no slot past the int32 wrap)."""
+    if B < 128:
+        return make(f"mtp_b{B}", B=B, Hq=16, Qt=Qt, page_size=MTP_PAGE, seq_lens=mtp_seq_lens(seed)[:B], seed=seed,
+                    device=device)
     nb = MTP_POOL_SLOTS // MTP_PAGE            # 612,500 pages
     first = -(-INT32_WRAP_SLOT // MTP_PAGE)    # 233,017: first page wholly above the wrap slot
     return make("mtp" if Qt == 4 else f"mtp_q{Qt}", B=128, Hq=16, Qt=Qt, page_size=MTP_PAGE,
