@@ -140,7 +140,8 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  * sees itself and its past, as in the multi-token verify step of "qwen-mla-vllm"
  * README, "Speculative decoding (MTP)", which reads the latent once per
  * request). With c_j = row[0:512], k_pe_j = row[512:576] (fp8 rows:
- * c_j[d] = e4m3(code) * scale_{d/128}):
+ * c_j[d] = e4m3(code) * scale_{d/128}, widened in the kernel to bf16, or at
+ * 33..64 rows to f16 with the latent queries and probabilities in f16 too):
  *   s_j      = scale * (q_lat[r] . c_j + q_pe[r] . k_pe_j)
  *   out[r]   = sum_j softmax_j(s) c_j          (softmax over the tokens)
  *   lse[r]   = ln sum_j exp(s_j)
@@ -164,7 +165,11 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *                device-side status bits: 1 = a bounded internal wait gave up
  *                (the kernel returned early, outputs are invalid), 2 = a
  *                block-table entry pointed outside the pool (page 0 was read
- *                instead). Words 1..3: wait site, tile and CTA of the lowest
+ *                instead), 4 = fp8 pools at 33..64 rows, which compute in f16:
+ *                a block scale above 146 or a query value above 65504 in
+ *                magnitude was met (outputs may hold inf or NaN; the cache
+ *                writer's scales stay below 146 for latents under 65,000 in
+ *                magnitude). Words 1..3: wait site, tile and CTA of the lowest
  *                failing CTA; words 4..11 where each of its roles gave up.
  *                Calls sharing a workspace must be ordered on one stream.
  *   num_ctas     CTAs sharing the token stream (0 = as many as fit on the
@@ -310,7 +315,8 @@ MLA_API int mla_decode_static_scratch(const void* q_lat, const void* q_pe, const
  * mla_decode_static_scratch call on this device they are the words
  * mla_decode documents for its workspace header (word 0: bit 1 = a bounded
  * wait gave up and the outputs are invalid, bit 2 = a block-table entry
- * outside the pool; words 1..11 where). dst is device memory or pinned host
+ * outside the pool, bit 4 = an fp8 value past the f16 range; words 1..11
+ * where). dst is device memory or pinned host
  * memory (one cudaMemcpyAsync, direction inferred); it allocates nothing.
  * Before any static-scratch call on the device the words are undefined.
  * Returns MLA_ERR_INVALID_ARG for a null dst or n outside 1..12.

@@ -319,5 +319,6 @@ def test_slow_pv_next_decode() -> None:
 
 def device_status(workspace: torch.Tensor) -> int:
     """Device-side status word of the last mla_decode that used `workspace`
-    (0 = ok; bit 1 = a bounded wait gave up; bit 2 = bad block id)."""
+    (0 = ok; bit 1 = a bounded wait gave up; bit 2 = bad block id; bit 4 =
+    an fp8 value past the f16 range of the 64-row fp8 path)."""
     return int(workspace[:4].view(torch.int32).item())

@@ -122,6 +122,9 @@ __device__ unsigned long long g_mtrace[512][2];
 #endif
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// fp8 rows widened to f16: |code| <= 448, so a block scale up to this keeps
+// every widened value (and its product with the scale) within the f16 range
+constexpr float kMaxF16Scale = 146.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kPrefetchTiles = 2;          // L2 lookahead of the load/convert producers
 constexpr int kRawSlots = 3;               // fp8 tiles in flight between TMA and the expand warps
@@ -1752,6 +1755,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             It it;
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             const uint32_t idS = idesc_bf16(128, 2 * NP, false, false);
+            // fp8 rows: the latent products are f16 (the widened cache, Q in TMEM)
+            const uint32_t idSlat = idesc_bf16(128, 2 * NP, false, false, KIND == 1);
             const uint64_t dq = smem_desc(smem_u32(qs), 16, 1024, kSw128);
             const uint64_t dqr = smem_desc(smem_u32(qs) + (C::kTr ? 0 : 2 * KB * NP * 128), 16, 512, kSw64);
             int seg = 0;
@@ -1807,7 +1812,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         if constexpr (C::kTr)
-                            umma_bf16_ta(tS, tmem + C::kColQ + kb * 32 + kk * 8, da + ((kk * 32) >> 4), idS, 1u);
+                            umma_bf16_ta(tS, tmem + C::kColQ + kb * 32 + kk * 8, da + ((kk * 32) >> 4), idSlat, 1u);
                         else
                             umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4), idS,
                                       (has_rope || (kb | kk) != 0) ? 1u : 0u);
@@ -1836,7 +1841,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             // P: [64 tokens][NP] (MN-major), or with kTr [NP queries][64 tokens]
             // (K-major, a 128-byte row per query)
-            const uint32_t idPV = idesc_bf16(128, NP, true, !C::kTr);
+            const uint32_t idPV = idesc_bf16(128, NP, true, !C::kTr, KIND == 1);
             constexpr uint32_t p_sbo = 8 * NP * 2;
 
             int seg = -1;
@@ -2066,16 +2071,24 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             // ------------------------------------------- expand warps (fp8 rows)
             // Warp e widens K-block e of every tile: the codes TMA
             // landed in the upper half of the slot (first-half rows at 8 KB + 64 t,
-            // second-half rows at 12 KB + 64 t for token t) become bf16 rows of the
-            // 128-byte-swizzled layout S and PV read, each code times its token's
-            // scale of the 128-value block it belongs to (one fp32 multiply, bf16
-            // round to nearest even). A second-half row overwrites codes, so every
-            // lane holds its codes in registers before any row is written.
+            // second-half rows at 12 KB + 64 t for token t) become f16 rows of the
+            // 128-byte-swizzled layout S and PV read, each code (exact in f16)
+            // times its token's scale of the 128-value block it belongs to, one
+            // f16 multiply rounded to nearest even: two instructions for two
+            // values, where a bf16 result would take six (f16 holds every such
+            // product more precisely than bf16; a scale above kMaxF16Scale, which
+            // could overflow it, is reported in the status word). The queries'
+            // latent part and P are f16 as well; the rope stays bf16. A
+            // second-half row overwrites codes, so every lane holds its codes in
+            // registers before any row is written.
             const int e = warp == 8 ? 0 : warp - kExp0 + 1;  // K-block e of every tile
             bool ok = true;
             int fsite = 0, ftile = 0;
+            It it;  // the tile's request: rows past its end hold stale bytes, not checked
+            it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             for (int i = 0; i < ntiles && ok; ++i) {
                 const int sb = i & 1;
+                const int valid = min(kT, it.T - it.j * kT);
                 if (!mbar_wait(&ctrl->scale_full[sb], (i >> 1) & 1, &ctrl->abort)) {
                     ok = false;
                     fsite = kSiteRawFull;
@@ -2099,6 +2112,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     // contiguous code bytes (no bank conflicts), and the two stores of
                     // a step hit every bank group once.
                     const int uq = lane & 3;
+                    bool wide = false;  // a scale past the f16 range
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint4 cd[8];
@@ -2110,19 +2124,22 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                         for (int it = 0; it < 8; ++it) {
                             const int t = 8 * it + (lane >> 2), r = 64 * h + t;
                             const float scale = *reinterpret_cast<const float*>(sc + t * 16 + 4 * (2 * h + (kb >> 1)));
+                            wide |= t < valid && !(scale <= kMaxF16Scale);
                             uint4 lo, hi;
-                            dequant16(cd[it], scale, lo, hi);
+                            dequant16_h(cd[it], __float2half2_rn(scale), lo, hi);
                             uint8_t* row = blk + r * 128;
                             *reinterpret_cast<uint4*>(row + (((2 * uq) ^ (r & 7)) << 4)) = lo;
                             *reinterpret_cast<uint4*>(row + (((2 * uq + 1) ^ (r & 7)) << 4)) = hi;
                         }
                         __syncwarp();  // the first halves' codes are consumed before h = 1 writes over them
                     }
+                    if (__any_sync(0xffffffffu, wide) && lane == 0) atomicOr(status_rec(p), kErrF16Range);
                     fence_proxy_async_smem();  // the products read these rows through the async proxy
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctrl->blk_full[slot]);
                 }
                 if (!ok) break;
+                it.next(p.seq_lens, p.B);
                 if (lane == 0) mbar_arrive(&ctrl->scale_empty[sb]);
                 if (lane == 0) MLA_TRACE_POINT(i, e == 0 ? kTrEpiEnd : kTrEpiHalf);  // expander e done with tile i
             }
@@ -2243,6 +2260,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 const bool v = tt < req_rows_in_group(p, bq, gy);
                 const __nv_bfloat16* src =
                     p.q_lat + (req_row0(p, bq) + gy * 64 + (v ? tt : 0)) * static_cast<int64_t>(C::kD) + 256 * hf + 128 * grp;
+                bool wide = false;  // fp8 rows: a value past the f16 range
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t r[16];
@@ -2254,8 +2272,19 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                         r[4 * u + 2] = w.z;
                         r[4 * u + 3] = w.w;
                     }
+                    if constexpr (KIND == 1) {
+                        // the cache side is f16 here, so Q's latent part is too (every
+                        // bf16 value in the f16 range converts exactly)
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r[k]));
+                            wide |= !(fabsf(f.x) <= 65504.f) || !(fabsf(f.y) <= 65504.f);
+                            r[k] = pack_half2(f.x, f.y);
+                        }
+                    }
                     tmem_st_x16(tmem + lane_base + C::kColQ + 64 * grp + 16 * q4, r);
                 }
+                if (KIND == 1 && __any_sync(0xffffffffu, wide) && lane == 0) atomicOr(status_rec(p), kErrF16Range);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -2647,8 +2676,10 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < NH / 8; ++u) {
                     const int un = own0 / 8 + u;
-                    const uint4 v = make_uint4(pack_bf16x2(x[8 * u + 0], x[8 * u + 1]), pack_bf16x2(x[8 * u + 2], x[8 * u + 3]),
-                                               pack_bf16x2(x[8 * u + 4], x[8 * u + 5]), pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
+                    const uint4 v = KIND == 1 ? make_uint4(pack_half2(x[8 * u + 0], x[8 * u + 1]), pack_half2(x[8 * u + 2], x[8 * u + 3]),
+                                                           pack_half2(x[8 * u + 4], x[8 * u + 5]), pack_half2(x[8 * u + 6], x[8 * u + 7]))
+                                              : make_uint4(pack_bf16x2(x[8 * u + 0], x[8 * u + 1]), pack_bf16x2(x[8 * u + 2], x[8 * u + 3]),
+                                                           pack_bf16x2(x[8 * u + 4], x[8 * u + 5]), pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
                     *reinterpret_cast<uint4*>(prow + ((un ^ sz) << 4)) = v;
                 }
                 if (grp == 0 && j * kT + tt >= T) {

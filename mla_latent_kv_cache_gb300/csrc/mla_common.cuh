@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -19,6 +20,7 @@ constexpr int kTile = 128;       // tokens per decode tile (UMMA M)
 // Device-side status bits written to the first word of the decode workspace.
 constexpr int kErrWaitTimeout = 1;   // a bounded wait gave up
 constexpr int kErrBadBlock = 2;      // a block-table entry pointed outside the pool
+constexpr int kErrF16Range = 4;      // fp8 rows: a block scale or query value beyond the f16 range
 
 // A wait that never ends would hold the GPU; every spin gives up after this.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
@@ -359,12 +361,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
-//   [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format,
-//   bit 15 A major (1 = MN), bit 16 B major, [17,23) N >> 3, [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor for kind::f16 with bf16 (or f16) A/B and fp32 D.
+//   [4,6) D format (1 = f32), [7,10) A format (0 = f16, 1 = bf16), [10,13) B
+//   format, bit 15 A major (1 = MN), bit 16 B major, [17,23) N >> 3, [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major, bool f16 = false) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -376,6 +378,31 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// e4m3 x16 (one uint4) times a scale -> 16 f16 (two uint4): each code widens
+// exactly to f16, one f16 multiply (round to nearest even) by the scale
+// rounded to f16. |code| <= 448, so a scale up to 146 keeps every product
+// finite.
+__device__ __forceinline__ void dequant16_h(uint4 codes, __half2 sc, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
+        const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
+        const __half2 p01 = __hmul2(*reinterpret_cast<const __half2*>(&h01), sc);
+        const __half2 p23 = __hmul2(*reinterpret_cast<const __half2*>(&h23), sc);
+        o[2 * i] = *reinterpret_cast<const uint32_t*>(&p01);
+        o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&p23);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 // e4m3 x16 (one uint4) times scale -> 16 bf16 (two uint4): each code widens

@@ -41,8 +41,9 @@ def check_decode(out, lse, ref_o, ref_l, rows, kind=0, what=""):
     ninf = np.isneginf(ref_l)
     assert np.array_equal(np.isneginf(l), ninf), f"{what}: -inf pattern of lse"
     if (~ninf).any():
-        # fp8 pools: the dequantised rows reach the MMA rounded to bf16, which
-        # moves every score (and so the LSE) by up to ~1e-2 on short requests
+        # fp8 pools: the dequantised rows reach the MMA rounded to bf16 (f16 at
+        # 33..64 rows), which moves every score (and so the LSE) by up to ~1e-2
+        # on short requests
         lse_tol = 1e-3 if kind == 0 else 5e-2
         assert np.abs(l[~ninf] - ref_l[~ninf]).max() <= lse_tol, \
             f"{what}: lse off by {np.abs(l[~ninf] - ref_l[~ninf]).max():.3e}"
@@ -238,6 +239,23 @@ def test_fp8_64_rows_boundaries(num_ctas, page_size, Hq, Qt):
     o, l, rr = oracle_step(wl, range(wl.B))
     out, lse = run_step(wl, num_ctas=num_ctas)
     check_decode(out, lse, o, l, rr, kind=1, what=f"fp8 ctas={num_ctas}")
+
+
+def test_fp8_64_rows_f16_range_flag():
+    """The 64-row fp8 path widens codes to f16: a block whose scale passes 146
+    (a latent value above ~65,400 in magnitude) sets status bit 4, and the
+    same pool without it leaves the word clear."""
+    sl = [300, 700]
+    for big, want in ((1.0e5, 4), (3.0e4, 0)):
+        wl = W.make("fp8r", B=2, Hq=64, Qt=1, page_size=64, seq_lens=sl, kind=W.KIND_FP8, write_all=True, seed=81,
+                    device=DEV)
+        wl.w_latent[5, 130] = big
+        m.mla_cache_write(wl.w_latent, wl.w_k_pe, wl.w_slots, wl.pool, wl.kind)
+        out, lse, ws = m.decode(wl.q_lat, wl.q_pe, wl.pool, wl.kind, wl.page_size, wl.block_table, wl.seq_lens,
+                                wl.Qt, wl.scale, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert m.device_status(ws) & 4 == want, (big, m.device_status(ws))
+        assert m.device_status(ws) & 3 == 0
 
 
 def test_single_token_is_bit_exact():
