@@ -1535,9 +1535,10 @@ struct FoldCfg {
     static constexpr int kSG = (NP == 64 || (NP == 32 && KB == 4 && !PAIR)) ? 2 : 1;
     static constexpr int kGW = NP / kSG;               // columns per group
     static constexpr int kNH = kGW / 2;                // softmax columns per thread
-    // the partner lane's half scores, kXR columns at a time (at 64 rows four
-    // rounds of 4 per group, so the two groups' buffers take 4 KB)
-    static constexpr int kXR = NP == 64 ? 4 : kNH;
+    // the partner lane's half scores, kXR columns at a time (at 64 rows two
+    // rounds of 8 per group, so the two groups' buffers take 8 KB; fp8 rows
+    // four rounds of 4, measured faster there: the expand warps' registers)
+    static constexpr int kXR = NP == 64 ? (KIND == 1 ? 4 : 8) : kNH;
     static constexpr int kXBytes = kSG * 128 * kXR * 4;
     // 9 warps, plus the second softmax group's 4
     // fp8 rows: four expand warps (one per K-block of a tile) widen the e4m3
@@ -2115,18 +2116,23 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     bool wide = false;  // a scale past the f16 range
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
+                        // the step's codes and scales all in flight at once (a scale
+                        // read after the previous step's stores would wait for them:
+                        // the compiler cannot tell the two regions apart)
                         uint4 cd[8];
+                        float scl[8];
 #pragma unroll
-                        for (int it = 0; it < 8; ++it)
+                        for (int it = 0; it < 8; ++it) {
                             cd[it] = *reinterpret_cast<const uint4*>(blk + 8192 + h * 4096 + it * 512 + lane * 16);
+                            scl[it] = *reinterpret_cast<const float*>(sc + (8 * it + (lane >> 2)) * 16 + 4 * (2 * h + (kb >> 1)));
+                        }
                         __syncwarp();  // every lane's codes are in registers
 #pragma unroll
                         for (int it = 0; it < 8; ++it) {
                             const int t = 8 * it + (lane >> 2), r = 64 * h + t;
-                            const float scale = *reinterpret_cast<const float*>(sc + t * 16 + 4 * (2 * h + (kb >> 1)));
-                            wide |= t < valid && !(scale <= kMaxF16Scale);
+                            wide |= t < valid && !(scl[it] <= kMaxF16Scale);
                             uint4 lo, hi;
-                            dequant16_h(cd[it], __float2half2_rn(scale), lo, hi);
+                            dequant16_h(cd[it], __float2half2_rn(scl[it]), lo, hi);
                             uint8_t* row = blk + r * 128;
                             *reinterpret_cast<uint4*>(row + (((2 * uq) ^ (r & 7)) << 4)) = lo;
                             *reinterpret_cast<uint4*>(row + (((2 * uq + 1) ^ (r & 7)) << 4)) = hi;
