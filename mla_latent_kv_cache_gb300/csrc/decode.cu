@@ -2347,27 +2347,59 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             };
 
             // One drain step: kDC columns of one M-tile, O / l, into the output
-            // rows (a whole request) or this worker's partial slot.
+            // rows (a whole request) or this worker's partial slot. A thread's TMEM
+            // lane is one latent dim; each quad of lanes transposes 4 x 4 blocks so
+            // that a lane stores 4 consecutive dims of one row in one 16-byte store
+            // (one-value stores made the drain ~6x slower).
             auto drain_step = [&]() {
                 const int m4 = dr_step / dr_per_mt;
                 const int c0 = cg0 + (dr_step - m4 * dr_per_mt) * kDC;
                 uint32_t o[kDC];
                 tmem_ld_x8(tmem + lane_base + dr_obuf + m4 * NP + c0, o);
-                // M-tile m4, lane st: latent dim 64 m4 + st (first half) or 256 + 64 m4 + st - 64
-                const int64_t d = dbase + (st < 64 ? 0 : C::kHalf - 64) + 64 * m4 + st;
+                // M-tile m4, lane st: latent dim 64 m4 + st (first half) or 256 + 64 m4 + st - 64;
+                // the quad's first dim
+                const int64_t dq = dbase + (st < 64 ? 0 : C::kHalf - 64) + 64 * m4 + (st & ~3);
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + dr_b;
+                if constexpr (KIND == 1) {
+                    // fp8 rows: one value a store (the transpose's registers cost the
+                    // expand-warp kernel more than the stores, measured 2%)
+                    const int64_t d = dq + (st & 3);
 #pragma unroll
-                for (int cc = 0; cc < kDC; ++cc) {
-                    const int c = c0 + cc;
-                    if (c < dr_hq) {
-                        const float lt = ctrl->dlt[dr_sg & 1][c];
-                        const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
-                        if (dr_final) {
-                            const int64_t idx = (dr_row0 + c) * C::kD + d;
-                            if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
-                            else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
-                        } else {
-                            p.part_o[(pslot * 64 + c) * C::kD + d] = v;
+                    for (int cc = 0; cc < kDC; ++cc) {
+                        const int c = c0 + cc;
+                        if (c < dr_hq) {
+                            const float lt = ctrl->dlt[dr_sg & 1][c];
+                            const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
+                            if (dr_final) {
+                                const int64_t idx = (dr_row0 + c) * C::kD + d;
+                                if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
+                                else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+                            } else {
+                                p.part_o[(pslot * 64 + c) * C::kD + d] = v;
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int cb = 0; cb < kDC; cb += 4) {
+                        float x[4] = {__uint_as_float(o[cb]), __uint_as_float(o[cb + 1]), __uint_as_float(o[cb + 2]),
+                                      __uint_as_float(o[cb + 3])};
+                        quad_transpose(x, lane);
+                        const int c = c0 + cb + (lane & 3);  // this lane's row now
+                        if (c < dr_hq) {
+                            const float lt = ctrl->dlt[dr_sg & 1][c];
+                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (lt > 0.f) v = make_float4(x[0] / lt, x[1] / lt, x[2] / lt, x[3] / lt);
+                            if (dr_final) {
+                                const int64_t idx = (dr_row0 + c) * C::kD + dq;
+                                if (p.out_f32)
+                                    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + idx) = v;
+                                else
+                                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + idx) =
+                                        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+                            } else {
+                                *reinterpret_cast<float4*>(p.part_o + (pslot * 64 + c) * C::kD + dq) = v;
+                            }
                         }
                     }
                 }

@@ -380,6 +380,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 4 x 4 transpose inside each quad of lanes: lane 4j + k holds in x[c]
+// column c of row k; afterwards it holds column k of rows 0..3 (x[r] = row r).
+// Two butterfly stages of two shuffles each, then a reorder by the lane bits.
+__device__ __forceinline__ void quad_transpose(float (&x)[4], int lane) {
+    const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
+    // rows k and k ^ 2 trade the column pair the other keeps
+    const float s0 = b1 ? x[0] : x[2], s1 = b1 ? x[1] : x[3];
+    const float k0 = b1 ? x[2] : x[0], k1 = b1 ? x[3] : x[1];
+    const float r0 = __shfl_xor_sync(0xffffffffu, s0, 2), r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+    // rows k and k ^ 1 trade the column the other keeps
+    const float t0 = b0 ? k0 : k1, t1 = b0 ? r0 : r1;
+    const float m0 = b0 ? k1 : k0, m1 = b0 ? r1 : r0;
+    const float u0 = __shfl_xor_sync(0xffffffffu, t0, 1), u1 = __shfl_xor_sync(0xffffffffu, t1, 1);
+    // column k of rows k, k ^ 1, k ^ 2, k ^ 3 is m0, u0, m1, u1: put row r at x[r]
+    const float w0 = b0 ? u0 : m0, w1 = b0 ? m0 : u0, w2 = b0 ? u1 : m1, w3 = b0 ? m1 : u1;
+    x[0] = b1 ? w2 : w0;
+    x[1] = b1 ? w3 : w1;
+    x[2] = b1 ? w0 : w2;
+    x[3] = b1 ? w1 : w3;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
