@@ -2477,13 +2477,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 };
                 put_x(0);
                 if (lead) MLA_TRACE_POINT(i, kTrSmTmemLd);
-                if (lead && (i == 0 || j == 0) && !last_of_seg) {
-                    // warm L2 with the next request's queries and page list
-                    It nx = it;
-                    nx.j = nx.tiles - 1;
-                    nx.next(p.seq_lens, p.B);
-                    if (nx.b < p.B) prefetch_request(p, nx.b, gy);
-                }
+
                 if (lead) MLA_TRACE_POINT(i, kTrSmSent);
                 if (i > 0 && j == 0) {
                     // the previous segment ended with tile i-1: finish the older
