@@ -1512,10 +1512,12 @@ struct FoldCfg {
     // that Q's 64 KB leave shared memory for three more K-block slots and a
     // second rope slot. TMEM: O in columns [0, 256), Q in [256, 384), one S
     // buffer in [384, 512).
+    // Latent width 768 (six K-blocks a tile, 16 rows): eleven K-block slots and
+    // one rope slot (ten and two: 5% slower).
     static constexpr bool kTr = NP == 64;
     static constexpr int kRL = PAIR ? 9 : (KB == 4) ? ((NP == 16) ? 11 : NP == 32 ? 10 : 11)
-                                                    : (KB == 2 ? ((NP == 16) ? 11 : 10) : 10);
-    static constexpr int kRR = (KB == 4) ? ((NP == 32) ? 1 : 2) : 2;
+                                                    : (KB == 2 ? ((NP == 16) ? 11 : 10) : (KB == 6 ? 11 : 10));
+    static constexpr int kRR = (KB == 4) ? ((NP == 32) ? 1 : 2) : (KB == 6 ? 1 : 2);
     // K-blocks [kb_lo(pp), kb_hi(pp)) of each tile belong to producer pp and PV issuer pp
     static __host__ __device__ constexpr int kb_lo(int pp) { return pp ? (KB + 1) / 2 : 0; }
     static __host__ __device__ constexpr int kb_hi(int pp) { return pp ? KB : (KB + 1) / 2; }
