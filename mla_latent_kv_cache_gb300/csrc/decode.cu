@@ -1088,20 +1088,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
                 const int c0 = (dr_step - mt * dr_per_half) * kDC;
                 uint32_t o[kDC];
                 tmem_ld_x8(tmem + lane_base + dr_obuf + mt * NP + c0, o);
-                const int64_t d = 256 * rank + 128 * mt + st;
+                // lane st holds dim 256 rank + 128 mt + st; each quad of lanes
+                // transposes 4 x 4 blocks so that a lane stores 4 consecutive dims
+                // of one row in one 16-byte store
+                const int64_t dq = 256 * rank + 128 * mt + (st & ~3);
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + dr_b;
 #pragma unroll
-                for (int cc = 0; cc < kDC; ++cc) {
-                    const int c = c0 + cc;
+                for (int cb = 0; cb < kDC; cb += 4) {
+                    float x[4] = {__uint_as_float(o[cb]), __uint_as_float(o[cb + 1]), __uint_as_float(o[cb + 2]),
+                                  __uint_as_float(o[cb + 3])};
+                    quad_transpose(x, lane);
+                    const int c = c0 + cb + (lane & 3);
                     if (c < dr_hq) {
                         const float lt = ctrl->dlt[dr_sg & 1][c];
-                        const float v = lt > 0.f ? __uint_as_float(o[cc]) / lt : 0.f;
+                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (lt > 0.f) v = make_float4(x[0] / lt, x[1] / lt, x[2] / lt, x[3] / lt);
                         if (dr_final) {
-                            const int64_t idx = (req_row0(p, dr_b) + gy * 64 + c) * kD + d;
-                            if (p.out_f32) static_cast<float*>(p.out)[idx] = v;
-                            else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+                            const int64_t idx = (req_row0(p, dr_b) + gy * 64 + c) * kD + dq;
+                            if (p.out_f32)
+                                *reinterpret_cast<float4*>(static_cast<float*>(p.out) + idx) = v;
+                            else
+                                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + idx) =
+                                    make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
                         } else {
-                            p.part_o[(pslot * 64 + c) * kD + d] = v;
+                            *reinterpret_cast<float4*>(p.part_o + (pslot * 64 + c) * kD + dq) = v;
                         }
                     }
                 }
