@@ -1581,8 +1581,9 @@ struct FoldCfg {
     static constexpr int kSmemBytes = kOffCtrl + 3584 + 1024;  // + control block, alignment slack
     // TMEM: two O accumulators of KB x NP columns (M-tile m at m * NP; one at
     // 64 rows, where two would leave no room for S), then two S buffers of
-    // 2 x NP columns. With one accumulator a finished segment is drained
-    // before the next segment's first value product.
+    // 2 x NP columns (at 64 rows: Q's latent part, then one S buffer). With
+    // one accumulator a finished segment is drained before the next segment's
+    // first value product.
     static constexpr bool kOneO = NP == 64;
     static constexpr int kColQ = KB * NP;               // kTr: Q's latent values, 2 a column
     static constexpr int kColS = kTr ? kColQ + 64 * KB / 2 : (kOneO ? 1 : 2) * KB * NP;
