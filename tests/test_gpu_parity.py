@@ -200,6 +200,29 @@ def test_decode_page_sizes_ragged(page_size):
     check_decode(out, lse, o, l, rows, what=f"page_size={page_size}")
 
 
+@pytest.mark.parametrize("Hq,Qt,num_ctas", [(32, 1, 0), (16, 4, 0), (48, 3, 9), (16, 8, 5), (64, 1, 3)])
+def test_bf16_outputs_at_32_to_128_rows(Hq, Qt, num_ctas):
+    """bf16 outputs through the drain's paired stores, for whole requests and
+    for split ones (partials then the merge), at 32, 64, 48 and 128 rows."""
+    sl = [Qt, 64 + Qt, 999, 4096, 130]
+    wl = W.make("b16", B=len(sl), Hq=Hq, Qt=Qt, page_size=16, seq_lens=sl, seed=40 + Hq + Qt, device=DEV)
+    o, l, rows = oracle_step(wl, range(wl.B))
+    out, lse = run_step(wl, out_dtype=torch.bfloat16, num_ctas=num_ctas)
+    check_decode(out, lse, o, l, rows, what=f"bf16 out Hq={Hq} Qt={Qt} ctas={num_ctas}")
+
+
+@pytest.mark.parametrize("kind,Hq,Qt,page_size", [(1, 16, 1, 64), (1, 32, 4, 64), (0, 16, 1, 5), (0, 32, 1, 7)])
+def test_bf16_outputs_on_the_cluster_kernel(kind, Hq, Qt, page_size):
+    """The same for the cluster kernel's paths: fp8 pools at 16 and 128 rows,
+    page sizes that are not a multiple of 8 (load/convert warps)."""
+    sl = [Qt, 300, 2500, 70]
+    wl = W.make("cb16", B=len(sl), Hq=Hq, Qt=Qt, page_size=page_size, seq_lens=sl, kind=kind, write_all=(kind == 1),
+                seed=60 + Hq + page_size, device=DEV)
+    o, l, rows = oracle_step(wl, range(wl.B))
+    out, lse = run_step(wl, out_dtype=torch.bfloat16, num_ctas=6)
+    check_decode(out, lse, o, l, rows, kind=kind, what=f"cluster bf16 out kind={kind} Hq={Hq} ps={page_size}")
+
+
 @pytest.mark.parametrize("Hq,Qt", [(16, 4), (8, 3), (32, 1), (64, 1), (80, 1), (20, 4), (16, 8), (32, 3), (128, 1),
                                    (48, 3)])
 def test_decode_row_shapes_and_causal(Hq, Qt):
