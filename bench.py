@@ -6,8 +6,9 @@ One step = the hot path over one batch: write the step's new cache rows
 (sum of context tokens x row bytes) / step time, each request's rows counted
 once; also decode steps/s and context tokens/s.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mtp|batched|long|fp8|tiny|verify]
-                  [--side long,fp8,...|none] [--clock-csv PATH]
+  python bench.py [--gpus N] [--steps K] [--warmup W]
+                  [--config mtp|batched|long|fp8|tiny|verify|verify8|latent768]
+                  [--side long,fp8,...|none] [--clock-csv PATH] [--requests N]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
   python bench.py --config gather        # the fp8_ds_mla prefill-context gather (mla_gather_upconvert)
 
