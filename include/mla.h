@@ -174,12 +174,12 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *                Calls sharing a workspace must be ordered on one stream.
  *   num_ctas     CTAs sharing the token stream (0 = as many as fit on the
  *                device, one per SM). Pools whose page_size is a multiple of
- *                8 (bf16 at any row count, fp8 at 33..64 rows): each CTA is a
+ *                8 (bf16 at any row count, fp8 up to 64 rows): each CTA is a
  *                worker on 64-token tiles of whole rows, except at 65..128
  *                rows (Hq * q_len), where the two 64-row groups of a worker
  *                are a cluster of two CTAs sharing each tile (num_ctas / 2
- *                workers). fp8 pools at other row counts and page sizes that
- *                are not a multiple of 8: clusters of two CTAs that split each
+ *                workers). fp8 pools above 64 rows and page sizes that are
+ *                not a multiple of 8: clusters of two CTAs that split each
  *                token's 576 dims between them, num_ctas / 2 workers on
  *                128-token tiles. The tiles of all requests are dealt out as
  *                equal contiguous ranges, one per worker; requests cut across

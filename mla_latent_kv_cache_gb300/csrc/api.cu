@@ -223,10 +223,10 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     // pages whose rows cannot be fetched as 8-row TMA boxes go through the
     // load/convert warps
     const bool lsu = (page_size % 8) != 0;
-    // bf16 pools, and fp8 pools at 33..64 query rows: folded 64-token tiles,
-    // one CTA per worker (or a CTA pair, see decode_fold_ctas); other fp8
-    // pools and odd page sizes: 128-token tiles split over clusters of two
-    // CTAs
+    // bf16 pools, and fp8 pools up to 64 query rows: folded 64-token tiles,
+    // one CTA per worker (or a CTA pair, see decode_fold_ctas); fp8 pools
+    // above 64 rows and odd page sizes: 128-token tiles split over clusters
+    // of two CTAs
     const bool fold = !lsu && (cache_kind == MLA_CACHE_BF16_576 || mla::fold_supported(NP, D, cache_kind, GY));
     // other latent widths: bf16 rows of D + 64 values, folded tiles only
     if (D != 512 && (!fold || !mla::fold_supported(NP, D, cache_kind, GY))) return MLA_ERR_UNSUPPORTED;

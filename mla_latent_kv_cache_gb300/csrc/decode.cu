@@ -1458,7 +1458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // ---------------------------------------------------------------- folded tiles
 //
 // Pools whose page size is a multiple of 8 rows: bf16 at 1..128 query rows,
-// fp8_ds_mla at 33..64 (and bf16 rows of other latent widths). One CTA per
+// fp8_ds_mla at 1..64 (and bf16 rows of other latent widths). One CTA per
 // worker, except the two cases below that pair two CTAs in a cluster. A tile
 // is 64 tokens of whole rows,
 // held as the 128-row A operand of one UMMA: row t (t < 64) carries token t's
@@ -1489,16 +1489,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // 65..128 rows: the two 64-row groups of a worker run
 // as a cluster of two CTAs that share each tile through multicast TMA (each
 // issues half of the boxes into both), so the cache is read once per request.
-// fp8_ds_mla rows at 64 rows: TMA lands each K-block's e4m3 codes in the upper
-// half of its slot, four expand warps widen them into the bf16 layout in
-// place. Latent width 1792: the two latent halves of every row in the two
+// fp8_ds_mla rows: TMA lands each K-block's e4m3 codes in the upper half of
+// its slot, four expand warps widen them in place (to f16 at 64 rows, where
+// the queries sit in TMEM as f16; to bf16 at 16 and 32 rows, beside the bf16
+// queries in shared memory). Latent width 1792: the two latent halves of every row in the two
 // CTAs of a cluster, which add their partial scores.
 
 template <int NP, int KB, bool PAIR = false, int KIND = 0>
 struct FoldCfg {
     static_assert(NP == 16 || NP == 32 || (NP == 64 && KB == 4 && !PAIR), "NP");
-    // KIND 1: fp8_ds_mla rows (656 bytes), at 64 query rows of the 576-wide row
-    static_assert(KIND == 0 || (NP == 64 && KB == 4 && !PAIR), "fp8 rows");
+    // KIND 1: fp8_ds_mla rows (656 bytes) of the 576-wide row
+    static_assert(KIND == 0 || (KB == 4 && !PAIR), "fp8 rows");
     // KB K-blocks per tile and CTA: 128 KB latent values in two halves of 64 KB.
     // PAIR: the two CTAs of a cluster take the latent's two halves (1792 = 2 x 896)
     static_assert(PAIR ? (KB == 7 && NP == 16) : (KB == 2 || KB == 4 || (KB == 6 && NP == 16)), "latent width");
@@ -1855,7 +1856,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             // P: [64 tokens][NP] (MN-major), or with kTr [NP queries][64 tokens]
             // (K-major, a 128-byte row per query)
-            const uint32_t idPV = idesc_bf16(128, NP, true, !C::kTr, KIND == 1);
+            const uint32_t idPV = idesc_bf16(128, NP, true, !C::kTr, KIND == 1 && C::kTr);
             constexpr uint32_t p_sbo = 8 * NP * 2;
 
             int seg = -1;
@@ -2143,9 +2144,13 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
 #pragma unroll
                         for (int it = 0; it < 8; ++it) {
                             const int t = 8 * it + (lane >> 2), r = 64 * h + t;
-                            wide |= t < valid && !(scl[it] <= kMaxF16Scale);
                             uint4 lo, hi;
-                            dequant16_h(cd[it], __float2half2_rn(scl[it]), lo, hi);
+                            if constexpr (C::kTr) {
+                                wide |= t < valid && !(scl[it] <= kMaxF16Scale);
+                                dequant16_h(cd[it], __float2half2_rn(scl[it]), lo, hi);
+                            } else {
+                                dequant16(cd[it], scl[it], lo, hi);  // bf16, as the queries in shared memory
+                            }
                             uint8_t* row = blk + r * 128;
                             *reinterpret_cast<uint4*>(row + (((2 * uq) ^ (r & 7)) << 4)) = lo;
                             *reinterpret_cast<uint4*>(row + (((2 * uq + 1) ^ (r & 7)) << 4)) = hi;
@@ -2373,9 +2378,9 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 // the quad's first dim
                 const int64_t dq = dbase + (st < 64 ? 0 : C::kHalf - 64) + 64 * m4 + (st & ~3);
                 const int64_t pslot = static_cast<int64_t>(gy) * p.SPG + g + dr_b;
-                if constexpr (KIND == 1) {
-                    // fp8 rows: one value a store (the transpose's registers cost the
-                    // expand-warp kernel more than the stores, measured 2%)
+                if constexpr (KIND == 1 && C::kTr) {
+                    // fp8 rows at 64 rows: one value a store (the transpose's registers
+                    // cost that kernel more than the stores, measured 2%)
                     const int64_t d = dq + (st & 3);
 #pragma unroll
                     for (int cc = 0; cc < kDC; ++cc) {
@@ -2729,7 +2734,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < NH / 8; ++u) {
                     const int un = own0 / 8 + u;
-                    const uint4 v = KIND == 1 ? make_uint4(pack_half2(x[8 * u + 0], x[8 * u + 1]), pack_half2(x[8 * u + 2], x[8 * u + 3]),
+                    const uint4 v = (KIND == 1 && C::kTr)
+                                        ? make_uint4(pack_half2(x[8 * u + 0], x[8 * u + 1]), pack_half2(x[8 * u + 2], x[8 * u + 3]),
                                                            pack_half2(x[8 * u + 4], x[8 * u + 5]), pack_half2(x[8 * u + 6], x[8 * u + 7]))
                                               : make_uint4(pack_bf16x2(x[8 * u + 0], x[8 * u + 1]), pack_bf16x2(x[8 * u + 2], x[8 * u + 3]),
                                                            pack_bf16x2(x[8 * u + 4], x[8 * u + 5]), pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
@@ -3213,15 +3219,15 @@ struct FoldVariant {
 // query rows of the 576-wide row the two row groups share each tile (MC);
 // fp8_ds_mla rows (KINDV 1) at 64 rows.
 #define MLA_FOLD(NPV, DV, MCV, KINDV, EXPR)                                                                   \
-    (DV == 512 ? (NPV == 16 ? EXPR(16, 4, false, false, 0)                                                     \
-                            : NPV == 32 ? EXPR(32, 4, false, false, 0)                                         \
+    (DV == 512 ? (NPV == 16 ? (KINDV ? EXPR(16, 4, false, false, 1) : EXPR(16, 4, false, false, 0))             \
+                            : NPV == 32 ? (KINDV ? EXPR(32, 4, false, false, 1) : EXPR(32, 4, false, false, 0)) \
                                         : (MCV ? EXPR(64, 4, false, true, 0)                                   \
                                                : KINDV ? EXPR(64, 4, false, false, 1) : EXPR(64, 4, false, false, 0))) \
                : DV == 256 ? (NPV == 16 ? EXPR(16, 2, false, false, 0) : EXPR(32, 2, false, false, 0))        \
                            : DV == 768 ? EXPR(16, 6, false, false, 0) : EXPR(16, 7, true, false, 0))
 
 bool fold_supported(int NP, int lat_dim, int kind, int GY) {
-    if (kind == 1) return lat_dim == 512 && NP == 64 && GY == 1;
+    if (kind == 1) return lat_dim == 512 && (NP == 16 || NP == 32 || NP == 64) && GY == 1;
     return lat_dim == 512   ? (NP == 16 || NP == 32 || NP == 64)
            : lat_dim == 256 ? (NP == 16 || NP == 32)
                             : ((lat_dim == 768 || lat_dim == 1792) && NP == 16);

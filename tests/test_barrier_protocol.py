@@ -30,7 +30,9 @@ SHAPES = [
     ("folded latent 256, 32 rows", 2, 10, 2, 2, 2, True, False),
     ("folded latent 768, 16 rows", 6, 11, 1, 2, 2, True, False),
     ("folded latent 1792 (one CTA of a pair), 16 rows", 7, 9, 2, 2, 2, True, False),
-    ("folded fp8 64 rows", 4, 8, 1, 1, 1, True, True),
+    ("folded fp8 64 rows (two score buffers)", 4, 8, 1, 1, 1, True, True),
+    ("folded fp8 16 rows", 4, 11, 2, 1, 2, True, True),
+    ("folded fp8 32 rows", 4, 10, 1, 1, 2, True, True),
     ("folded 64 rows, rope read last", 4, 8, 1, 2, 1, False, False),
     ("folded fp8 64 rows, rope read last", 4, 8, 1, 1, 1, False, True),
     ("cluster TMA 16 rows", 2, 5, 3, 1, 2, False, False),
