@@ -1514,7 +1514,7 @@ struct FoldCfg {
     // (the rope reload waits for one S, well inside a tile's time; 3% faster)
     // At 64 query rows only Q's rope part (8 KB) stays in shared memory: eleven
     // K-block slots (almost three tiles) and two rope slots fit beside one P
-    // buffer and a quarter-width exchange buffer. With one rope slot, each
+    // buffer and a half-width exchange buffer. With one rope slot, each
     // tile's rope copy would wait for the previous tile's score product, a
     // chain as long as a tile (twelve K-block slots and one rope slot: 2% slower).
     // kTr: at 64 rows the score product runs transposed, S^T = Q K^T, with the
