@@ -2086,14 +2086,16 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             // ------------------------------------------- expand warps (fp8 rows)
             // Warp e widens K-block e of every tile: the codes TMA
             // landed in the upper half of the slot (first-half rows at 8 KB + 64 t,
-            // second-half rows at 12 KB + 64 t for token t) become f16 rows of the
-            // 128-byte-swizzled layout S and PV read, each code (exact in f16)
-            // times its token's scale of the 128-value block it belongs to, one
-            // f16 multiply rounded to nearest even: two instructions for two
-            // values, where a bf16 result would take six (f16 holds every such
-            // product more precisely than bf16; a scale above kMaxF16Scale, which
-            // could overflow it, is reported in the status word). The queries'
-            // latent part and P are f16 as well; the rope stays bf16. A
+            // second-half rows at 12 KB + 64 t for token t) become rows of the
+            // 128-byte-swizzled layout S and PV read, each code times its token's
+            // scale of the 128-value block it belongs to. At 64 rows in f16: the
+            // code exact in f16, one f16 multiply rounded to nearest even, two
+            // instructions for two values where a bf16 result takes six (f16
+            // holds every such product more precisely than bf16; a scale above
+            // kMaxF16Scale, which could overflow it, is reported in the status
+            // word); the queries' latent part and P are f16 as well, the rope
+            // stays bf16. At 16 and 32 rows, beside bf16 queries in shared
+            // memory, in bf16: one fp32 multiply, rounded to nearest even. A
             // second-half row overwrites codes, so every lane holds its codes in
             // registers before any row is written.
             const int e = warp == 8 ? 0 : warp - kExp0 + 1;  // K-block e of every tile
