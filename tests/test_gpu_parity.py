@@ -250,6 +250,19 @@ def test_many_request_boundaries(rows, num_ctas):
     check_decode(out, lse, o, l, rr, what=f"rows={rows} ctas={num_ctas}")
 
 
+@pytest.mark.parametrize("num_ctas,page_size,Hq,Qt", [(5, 64, 16, 1), (0, 16, 32, 1), (9, 8, 8, 3), (3, 32, 16, 2)])
+def test_fp8_16_and_32_rows_folded(num_ctas, page_size, Hq, Qt):
+    """fp8 pools at 1..32 query rows on the folded kernel (codes widened to bf16
+    beside the bf16 queries in shared memory), ragged requests, tile and page
+    boundaries, requests cut across workers."""
+    sl = [0, 1, 64, 65, 127, 300, 900, 2049, 5]
+    wl = W.make("fp8s", B=len(sl), Hq=Hq, Qt=Qt, page_size=page_size, seq_lens=sl, kind=W.KIND_FP8, write_all=True,
+                seed=91 + num_ctas + page_size + Hq, device=DEV)
+    o, l, rr = oracle_step(wl, range(wl.B))
+    out, lse = run_step(wl, num_ctas=num_ctas)
+    check_decode(out, lse, o, l, rr, kind=1, what=f"fp8 {Hq * Qt} rows ctas={num_ctas}")
+
+
 @pytest.mark.parametrize("num_ctas,page_size,Hq,Qt", [(4, 64, 64, 1), (0, 64, 64, 1), (7, 16, 16, 4), (40, 8, 64, 1),
                                                      (3, 32, 16, 3)])
 def test_fp8_64_rows_boundaries(num_ctas, page_size, Hq, Qt):
