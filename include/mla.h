@@ -140,8 +140,8 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  * sees itself and its past, as in the multi-token verify step of "qwen-mla-vllm"
  * README, "Speculative decoding (MTP)", which reads the latent once per
  * request). With c_j = row[0:512], k_pe_j = row[512:576] (fp8 rows:
- * c_j[d] = e4m3(code) * scale_{d/128}, widened in the kernel to bf16, or at
- * 33..64 rows to f16 with the latent queries and probabilities in f16 too):
+ * c_j[d] = e4m3(code) * scale_{d/128}, widened in the kernel to f16 with the
+ * latent queries and probabilities in f16 too up to 64 rows, to bf16 above):
  *   s_j      = scale * (q_lat[r] . c_j + q_pe[r] . k_pe_j)
  *   out[r]   = sum_j softmax_j(s) c_j          (softmax over the tokens)
  *   lse[r]   = ln sum_j exp(s_j)
@@ -165,7 +165,7 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *                device-side status bits: 1 = a bounded internal wait gave up
  *                (the kernel returned early, outputs are invalid), 2 = a
  *                block-table entry pointed outside the pool (page 0 was read
- *                instead), 4 = fp8 pools at 33..64 rows, which compute in f16:
+ *                instead), 4 = fp8 pools up to 64 rows, which compute in f16:
  *                a block scale above 146 or a query value above 65504 in
  *                magnitude was met (outputs may hold inf or NaN; the cache
  *                writer's scales stay below 146 for latents under 65,000 in

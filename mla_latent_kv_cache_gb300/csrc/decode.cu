@@ -1490,9 +1490,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(decode_threads<LSU, 
 // as a cluster of two CTAs that share each tile through multicast TMA (each
 // issues half of the boxes into both), so the cache is read once per request.
 // fp8_ds_mla rows: TMA lands each K-block's e4m3 codes in the upper half of
-// its slot, four expand warps widen them in place (to f16 at 64 rows, where
-// the queries sit in TMEM as f16; to bf16 at 16 and 32 rows, beside the bf16
-// queries in shared memory). Latent width 1792: the two latent halves of every row in the two
+// its slot, four expand warps widen them in place to f16 (the queries' latent
+// part and P are f16 too). Latent width 1792: the two latent halves of every row in the two
 // CTAs of a cluster, which add their partial scores.
 
 template <int NP, int KB, bool PAIR = false, int KIND = 0>
@@ -1780,7 +1779,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                     // a new request: its Q (with kTr, the rope part here and the
                     // latent part in TMEM, written by the softmax warps)
                     if (!mbar_wait(&ctrl->q_full, seg & 1, &ctrl->abort) ||
-                        (C::kTr && !mbar_wait(&ctrl->q_tmem, seg & 1, &ctrl->abort))) {
+                        ((C::kTr || KIND == 1) && !mbar_wait(&ctrl->q_tmem, seg & 1, &ctrl->abort))) {
                         fail(p, ctrl, kErrWaitTimeout, kSiteQFull, i);
                         report(p, kRoleS, kSiteQFull, i);
                         break;
@@ -1829,8 +1828,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                         if constexpr (C::kTr)
                             umma_bf16_ta(tS, tmem + C::kColQ + kb * 32 + kk * 8, da + ((kk * 32) >> 4), idSlat, 1u);
                         else
-                            umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4), idS,
-                                      (has_rope || (kb | kk) != 0) ? 1u : 0u);
+                            umma_bf16(tS, da + ((kk * 32) >> 4), dq + ((kb * 2 * NP * 128 + kk * 32) >> 4),
+                                      KIND == 1 ? idSlat : idS, (has_rope || (kb | kk) != 0) ? 1u : 0u);
                     }
                 }
                 if (!ok) {
@@ -1856,7 +1855,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             it.init(p.seq_lens, ctrl->b0, ctrl->j0);
             // P: [64 tokens][NP] (MN-major), or with kTr [NP queries][64 tokens]
             // (K-major, a 128-byte row per query)
-            const uint32_t idPV = idesc_bf16(128, NP, true, !C::kTr, KIND == 1 && C::kTr);
+            const uint32_t idPV = idesc_bf16(128, NP, true, !C::kTr, KIND == 1);
             constexpr uint32_t p_sbo = 8 * NP * 2;
 
             int seg = -1;
@@ -2088,14 +2087,13 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
             // landed in the upper half of the slot (first-half rows at 8 KB + 64 t,
             // second-half rows at 12 KB + 64 t for token t) become rows of the
             // 128-byte-swizzled layout S and PV read, each code times its token's
-            // scale of the 128-value block it belongs to. At 64 rows in f16: the
-            // code exact in f16, one f16 multiply rounded to nearest even, two
-            // instructions for two values where a bf16 result takes six (f16
-            // holds every such product more precisely than bf16; a scale above
-            // kMaxF16Scale, which could overflow it, is reported in the status
-            // word); the queries' latent part and P are f16 as well, the rope
-            // stays bf16. At 16 and 32 rows, beside bf16 queries in shared
-            // memory, in bf16: one fp32 multiply, rounded to nearest even. A
+            // scale of the 128-value block it belongs to, in f16: the code exact
+            // in f16, one f16 multiply rounded to nearest even, two instructions
+            // for two values where a bf16 result takes six (f16 holds every such
+            // product more precisely than bf16; a scale above kMaxF16Scale, which
+            // could overflow it, is reported in the status word). The queries'
+            // latent part (in TMEM at 64 rows, converted in place in shared
+            // memory at 16 and 32) and P are f16 as well; the rope stays bf16. A
             // second-half row overwrites codes, so every lane holds its codes in
             // registers before any row is written.
             const int e = warp == 8 ? 0 : warp - kExp0 + 1;  // K-block e of every tile
@@ -2147,12 +2145,8 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                         for (int it = 0; it < 8; ++it) {
                             const int t = 8 * it + (lane >> 2), r = 64 * h + t;
                             uint4 lo, hi;
-                            if constexpr (C::kTr) {
-                                wide |= t < valid && !(scl[it] <= kMaxF16Scale);
-                                dequant16_h(cd[it], __float2half2_rn(scl[it]), lo, hi);
-                            } else {
-                                dequant16(cd[it], scl[it], lo, hi);  // bf16, as the queries in shared memory
-                            }
+                            wide |= t < valid && !(scl[it] <= kMaxF16Scale);
+                            dequant16_h(cd[it], __float2half2_rn(scl[it]), lo, hi);
                             uint8_t* row = blk + r * 128;
                             *reinterpret_cast<uint4*>(row + (((2 * uq) ^ (r & 7)) << 4)) = lo;
                             *reinterpret_cast<uint4*>(row + (((2 * uq + 1) ^ (r & 7)) << 4)) = hi;
@@ -2317,6 +2311,33 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 if (lane == 0) mbar_arrive(&ctrl->q_tmem);
             };
 
+            // fp8 rows at 16 and 32 rows: once the request's queries have landed
+            // in shared memory (bf16), their latent part becomes f16 in place, the
+            // type of the widened cache; the rope part stays bf16.
+            int qseg = 0;
+            auto convert_q = [&]() {
+                group_wait(&ctrl->q_full, qseg & 1, p, ctrl, kSiteQFull, 0);
+                ++qseg;
+                constexpr int kUnits = 2 * NP * KB * 128 / 16;  // 16-byte units of the latent part
+                bool wide = false;
+                for (int u = grp * 128 + st; u < kUnits; u += 128 * C::kSG) {
+                    uint4* q = reinterpret_cast<uint4*>(qs) + u;
+                    uint4 w = *q;
+                    uint32_t* e = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&e[k]));
+                        wide |= !(fabsf(f.x) <= 65504.f) || !(fabsf(f.y) <= 65504.f);
+                        e[k] = pack_half2(f.x, f.y);
+                    }
+                    *q = w;
+                }
+                if (__any_sync(0xffffffffu, wide) && lane == 0) atomicOr(status_rec(p), kErrF16Range);
+                fence_proxy_async_smem();  // the score product reads them through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->q_tmem);
+            };
+
             // Row sums and maxima of segment sg, which just ended, into
             // dlt / dm [sg & 1]; fresh softmax state for the next segment.
             auto capture = [&](int sg) {
@@ -2460,6 +2481,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
 
             if (lead) issue_q(it.b);
             if constexpr (C::kTr) write_q(it.b);
+            else if constexpr (KIND == 1) convert_q();
             bool alive = true;
             for (int i = 0; i < ntiles; ++i) {
                 const int b = it.b, j = it.j, T = it.T;
@@ -2736,7 +2758,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < NH / 8; ++u) {
                     const int un = own0 / 8 + u;
-                    const uint4 v = (KIND == 1 && C::kTr)
+                    const uint4 v = KIND == 1
                                         ? make_uint4(pack_half2(x[8 * u + 0], x[8 * u + 1]), pack_half2(x[8 * u + 2], x[8 * u + 3]),
                                                            pack_half2(x[8 * u + 4], x[8 * u + 5]), pack_half2(x[8 * u + 6], x[8 * u + 7]))
                                               : make_uint4(pack_bf16x2(x[8 * u + 0], x[8 * u + 1]), pack_bf16x2(x[8 * u + 2], x[8 * u + 3]),
@@ -2779,6 +2801,7 @@ __global__ void __launch_bounds__(FoldCfg<NP, KB, PAIR, KIND>::kThreads, 1)
                 it.next(p.seq_lens, p.B);
                 // S(i), the request's last score product, has read Q: the next one's
                 if (C::kTr && last_of_seg && i + 1 < ntiles) write_q(it.b);
+                if (!C::kTr && KIND == 1 && last_of_seg && i + 1 < ntiles) convert_q();
             }
             if (alive) {
                 // the last segment: finish the older drain, capture, wait for its

@@ -41,8 +41,8 @@ def check_decode(out, lse, ref_o, ref_l, rows, kind=0, what=""):
     ninf = np.isneginf(ref_l)
     assert np.array_equal(np.isneginf(l), ninf), f"{what}: -inf pattern of lse"
     if (~ninf).any():
-        # fp8 pools: the dequantised rows reach the MMA rounded to bf16 (f16 at
-        # 33..64 rows), which moves every score (and so the LSE) by up to ~1e-2
+        # fp8 pools: the dequantised rows reach the MMA rounded to bf16 (f16 up
+        # to 64 rows), which moves every score (and so the LSE) by up to ~1e-2
         # on short requests
         lse_tol = 1e-3 if kind == 0 else 5e-2
         assert np.abs(l[~ninf] - ref_l[~ninf]).max() <= lse_tol, \
@@ -252,9 +252,9 @@ def test_many_request_boundaries(rows, num_ctas):
 
 @pytest.mark.parametrize("num_ctas,page_size,Hq,Qt", [(5, 64, 16, 1), (0, 16, 32, 1), (9, 8, 8, 3), (3, 32, 16, 2)])
 def test_fp8_16_and_32_rows_folded(num_ctas, page_size, Hq, Qt):
-    """fp8 pools at 1..32 query rows on the folded kernel (codes widened to bf16
-    beside the bf16 queries in shared memory), ragged requests, tile and page
-    boundaries, requests cut across workers."""
+    """fp8 pools at 1..32 query rows on the folded kernel (codes widened to f16,
+    the queries converted to f16 in shared memory), ragged requests, tile and
+    page boundaries, requests cut across workers."""
     sl = [0, 1, 64, 65, 127, 300, 900, 2049, 5]
     wl = W.make("fp8s", B=len(sl), Hq=Hq, Qt=Qt, page_size=page_size, seq_lens=sl, kind=W.KIND_FP8, write_all=True,
                 seed=91 + num_ctas + page_size + Hq, device=DEV)
