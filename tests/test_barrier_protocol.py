@@ -1,6 +1,8 @@
 """The decode kernels' mbarrier hand-offs on random-schedule models
 (tests/barrier_model.py for one CTA, tests/barrier_model_pair.py for the
-cluster kernel's CTA pair), with the shapes the kernels use.
+cluster kernel's CTA pair, tests/barrier_model_mc.py for the 65..128-row
+pair of 64-row CTAs that share tiles through multicast copies), with the
+shapes the kernels use.
 
 Every shape must finish every schedule with no problem. The schedules include
 ones where a PV issuer, a producer or one CTA's softmax runs far behind the
@@ -10,10 +12,13 @@ other roles. Controls show that the models catch each kind of fault:
 - an odd pair ring fed by per-pair producers, which the kernels also used to
   have: a slot is reloaded before its PV has freed it;
 - the cluster kernel without the wait that protects its score staging: P
-  overwrites the staged scores before the bulk copy has read them."""
+  overwrites the staged scores before the bulk copy has read them;
+- a multicast pair whose slots are released by one CTA's products only: a
+  copy lands in the peer's slot while the peer still reads it."""
 import pytest
 
 from barrier_model import run
+from barrier_model_mc import run_mc
 from barrier_model_pair import run_pair
 
 SKEWS = [None, {"PV0": 0.02}, {"PV1": 0.02}, {"PV0": 0.01, "LD1": 0.2}, {"PV1": 0.01, "LD0": 0.2},
@@ -141,3 +146,36 @@ def test_score_staging_needs_the_peer_to_have_read_it():
     staging before the bulk copy has read it."""
     bad = pair_failures(20, R=5, RR=2, PB=2, split=True, send_in_p=True, skip_xfree_before_p=True)
     assert any("source changed" in e for _, _, e in bad)
+
+
+MC_SKEWS = [None, {"PV00": 0.02}, {"PV11": 0.02}, {"SM1": 0.05}, {"S0": 0.02, "LD11": 3.0},
+            {"LD00": 0.05, "PV10": 0.1}, {"PV01": 0.01, "LD10": 0.2}]
+
+
+def mc_failures(seeds, **shape):
+    out = []
+    for w in MC_SKEWS:
+        for seed in range(seeds):
+            e = run_mc(seed, weights=w, **shape)
+            if e:
+                out.append((w, seed, e[0]))
+    return out
+
+
+def test_multicast_pair_at_128_rows_survives_skew():
+    """The 65..128-row pair: eleven K-block slots and two rope slots per CTA
+    (the 64-row transposed kernel's ring), each CTA copying its half of every
+    block and its rope half into both CTAs, both CTAs' products releasing
+    each slot."""
+    bad = mc_failures(30, KB=4, R=11, RR=2)
+    assert not bad, bad[:3]
+
+
+def test_multicast_slot_released_by_one_cta_reloads_early():
+    bad = mc_failures(20, KB=4, R=11, RR=2, empty_count=1)
+    assert any("still in use" in e for _, _, e in bad)
+
+
+def test_multicast_rope_released_by_one_cta_reloads_early():
+    bad = mc_failures(20, KB=4, R=11, RR=2, rope_count=1)
+    assert any("unconsumed rope slot" in e for _, _, e in bad)
