@@ -104,7 +104,9 @@ MLA_API int mla_cache_write(const void* latent, int64_t latent_stride, const voi
  *                num_slots rows of 656 bytes, 16-byte aligned.
  *   page_size    tokens per page, >= 1.
  *   block_table  device, int32 [B, block_table_stride]; entries past
- *                ceil(len_b / page_size) are never read.
+ *                ceil(len_b / page_size) are never read, and a page index
+ *                >= block_table_stride (a request longer than its row) counts
+ *                as an entry outside the pool.
  *   cu_seq_lens  device, int32 [B + 1], non-decreasing, cu_seq_lens[0] = 0
  *                (read on the device only).
  *   num_rows     rows of dst the call may write (normally cu_seq_lens[B]);
@@ -153,7 +155,10 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *                num_slots rows of mla_row_bytes(cache_kind) bytes.
  *   page_size    tokens per page, >= 1.
  *   block_table  device, int32 [B, block_table_stride]; entries past
- *                ceil(seq_lens[b] / page_size) are never read.
+ *                ceil(seq_lens[b] / page_size) are never read. A request
+ *                longer than its row (page index >= block_table_stride)
+ *                reads nothing past the row: those page indices count as
+ *                entries outside the pool.
  *   seq_lens     device, int32 [B], each >= 0; read on the device only, so the
  *                call does not synchronise.
  *   scale        softmax scale applied to the dot products.
@@ -164,8 +169,8 @@ MLA_API size_t mla_decode_workspace_bytes(int B, int q_len, int Hq, int num_ctas
  *                Once the call's work has run, its first int32 holds
  *                device-side status bits: 1 = a bounded internal wait gave up
  *                (the kernel returned early, outputs are invalid), 2 = a
- *                block-table entry pointed outside the pool (page 0 was read
- *                instead), 4 = fp8 pools up to 64 rows, which compute in f16:
+ *                block-table entry pointed outside the pool, or a page index
+ *                was past the table row (page 0 was read instead), 4 = fp8 pools up to 64 rows, which compute in f16:
  *                a block scale above 146 or a query value above 65504 in
  *                magnitude was met (outputs may hold inf or NaN; the cache
  *                writer's scales stay below 146 for latents under 65,000 in
@@ -219,9 +224,10 @@ MLA_API int mla_decode(const void* q_lat, const void* q_pe, const void* cache, i
  * 64-token tiles whose rows are folded into two halves (as mla_decode's bf16
  * path at up to 32 query rows); at lat_dim 1792 the two CTAs of a cluster
  * each hold one 896-value half of every row and exchange partial scores.
- * Supported: lat_dim 256 or 512 with Hq * q_len <= 32, lat_dim 768 or 1792
- * with Hq * q_len <= 16, page_size a multiple of 8; otherwise
- * MLA_ERR_UNSUPPORTED before any launch.
+ * Supported: lat_dim 512 wherever mla_decode takes a bf16 pool (it is that
+ * call); lat_dim 256 with Hq * q_len <= 32 and lat_dim 768 or 1792 with
+ * Hq * q_len <= 16, page_size a multiple of 8; otherwise MLA_ERR_UNSUPPORTED
+ * before any launch.
  */
 MLA_API int mla_cache_write_latent(const void* latent, int64_t latent_stride, const void* k_pe, int64_t k_pe_stride,
                                    const int64_t* slot_mapping, int64_t num_tokens, void* cache, int64_t num_slots,
@@ -250,7 +256,11 @@ MLA_API int mla_decode_latent(const void* q_lat, const void* q_pe, const void* c
  *                   is mla_decode_workspace_bytes(B, max_q_len, Hq, num_ctas).
  * While max_q_len * Hq <= 64, and up to 128 for bf16 pools whose page_size
  * is a multiple of 8 (two row groups sharing each tile), every request's
- * cache is read once.
+ * cache is read once. The kernels clamp every cu_q_lens entry to
+ * [0, total_q_tokens], so no row at or past total_q_tokens * Hq of q_lat,
+ * q_pe, out or lse is read or written whatever the prefix sums hold: a
+ * request whose sums run past total_q_tokens verifies only its tokens below
+ * it, with the length the clamped sums give (nothing flags this).
  */
 MLA_API int mla_decode_varlen(const void* q_lat, const void* q_pe, int64_t total_q_tokens, const void* cache,
                               int cache_kind, int64_t num_slots, int page_size, const int32_t* block_table,

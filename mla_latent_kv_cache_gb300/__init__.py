@@ -319,6 +319,7 @@ def test_slow_pv_next_decode() -> None:
 
 def device_status(workspace: torch.Tensor) -> int:
     """Device-side status word of the last mla_decode that used `workspace`
-    (0 = ok; bit 1 = a bounded wait gave up; bit 2 = bad block id; bit 4 =
-    an fp8 value past the f16 range of the 64-row fp8 path)."""
+    (0 = ok; bit 1 = a bounded wait gave up; bit 2 = a block id outside the
+    pool or a page index past the table row; bit 4 = an fp8 value past the
+    f16 range of the fp8 path up to 64 rows)."""
     return int(workspace[:4].view(torch.int32).item())

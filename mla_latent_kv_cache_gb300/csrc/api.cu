@@ -346,6 +346,7 @@ int decode_impl(const void* q_lat, const void* q_pe, int64_t total_q, const void
     p.wseg = fold ? (NP == 16 ? 4 : NP == 32 ? 8 : 4) : (NP == 16 ? 2 : NP == 32 ? 4 : 8);
     p.test_hold = g_test_hold.exchange(0);
     p.cu_q = cu_q;
+    p.total_q = static_cast<int>(total_q);  // total_q * Hq < 2^31 (checked above)
     p.lat_dim = D;
     p.rope_dim = mla::kP;
     cudaError_t e = fold ? mla::launch_decode_fold(maps, p, NP, cache_kind, W, GY, s)

@@ -159,7 +159,9 @@ __global__ void __launch_bounds__(256) gather_upconvert_fp8_kernel(const uint8_t
         slot[k] = 0;
         if (have[k]) {
             const int64_t j = r - c0;
-            const int64_t page = __ldg(block_table + static_cast<int64_t>(b) * bt_stride + j / page_size);
+            // a page index past the block-table row reads as an entry outside the pool
+            const int64_t pi = j / page_size;
+            const int64_t page = pi < bt_stride ? __ldg(block_table + static_cast<int64_t>(b) * bt_stride + pi) : -1;
             const int64_t s = page * page_size + j % page_size;
             ok[k] = page >= 0 && s < num_slots;
             slot[k] = ok[k] ? s : 0;

@@ -238,12 +238,18 @@ using TileIt = TileItT<7>;
 
 // Query rows of request b: the first row of its verify step and the step's
 // length in tokens (Qt for every request unless per-request lengths are given),
-// and how many of its rows fall in row group gy (0 .. 64).
+// and how many of its rows fall in row group gy (0 .. 64). Per-request prefix
+// sums are clamped to [0, total_q], so whatever they hold no row past the
+// query, output and LSE buffers is touched (a request whose sums run past
+// total_q keeps its tokens below it).
+__device__ __forceinline__ int cu_clamped(const DecodeParams& p, int b) {
+    return min(max(__ldg(p.cu_q + b), 0), p.total_q);
+}
 __device__ __forceinline__ int64_t req_row0(const DecodeParams& p, int b) {
-    return p.cu_q ? static_cast<int64_t>(__ldg(p.cu_q + b)) * p.Hq : static_cast<int64_t>(b) * p.HQ;
+    return p.cu_q ? static_cast<int64_t>(cu_clamped(p, b)) * p.Hq : static_cast<int64_t>(b) * p.HQ;
 }
 __device__ __forceinline__ int req_qt(const DecodeParams& p, int b) {
-    return p.cu_q ? __ldg(p.cu_q + b + 1) - __ldg(p.cu_q + b) : p.Qt;
+    return p.cu_q ? cu_clamped(p, b + 1) - cu_clamped(p, b) : p.Qt;
 }
 __device__ __forceinline__ int req_rows_in_group(const DecodeParams& p, int b, int gy) {
     return min(64, max(0, req_qt(p, b) * p.Hq - gy * 64));
@@ -260,7 +266,7 @@ __device__ __forceinline__ void prefetch_request(const DecodeParams& p, int b, i
         prefetch_l2_bulk(p.q_pe + row0 * p.rope_dim, static_cast<uint32_t>(HQg * p.rope_dim * 2));
     }
     const int T = max(__ldg(p.seq_lens + b), 0);
-    const int64_t pages = (static_cast<int64_t>(T) + p.page_size - 1) / p.page_size;
+    const int64_t pages = min((static_cast<int64_t>(T) + p.page_size - 1) / p.page_size, p.bt_stride);
     uintptr_t a0 = reinterpret_cast<uintptr_t>(p.block_table + static_cast<int64_t>(b) * p.bt_stride);
     uintptr_t a1 = a0 + static_cast<uintptr_t>(pages) * 4;
     a0 = (a0 + 15) & ~static_cast<uintptr_t>(15);
@@ -440,7 +446,10 @@ __device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, const
 
 // 64-bit slot of token `tok` of the request whose block-table row is `btr`.
 __device__ __forceinline__ int64_t token_slot(const DecodeParams& p, const int32_t* btr, int tok, bool& bad) {
-    const int64_t page = __ldg(btr + tok / p.page_size);
+    const int pi = tok / p.page_size;
+    // a page index past the block-table row (a sequence longer than the table)
+    // counts as an entry outside the pool
+    const int64_t page = pi < p.bt_stride ? __ldg(btr + pi) : -1;
     const int64_t ps = p.page_size;
     if (page < 0 || (page + 1) * ps > p.num_slots) {
         bad = true;

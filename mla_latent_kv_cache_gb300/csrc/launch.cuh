@@ -37,6 +37,7 @@ struct DecodeParams {
     int test_hold;     // test hooks: 1 = withhold the first hand-off to the PV issuers,
                        // 2 = hold one PV issuer ~20 us after each of its first 32 tiles
     const int32_t* cu_q;  // [B + 1] prefix sums of query tokens per request, or null: Qt each
+    int total_q;          // query tokens in q_lat, q_pe, out and lse; cu_q is clamped to [0, total_q]
     int lat_dim;       // latent width D: 512 (576-value rows), or 256 / 768 / 1792 (folded tiles, bf16)
     int rope_dim;      // rotary width P: 64
 };
