@@ -3,8 +3,11 @@
 The compute path lives in ``_lib/libmla_gb300.so`` (built from ``csrc/`` by
 ``mla_latent_kv_cache_gb300.build``). This module only marshals arguments:
 torch tensors -> device pointers, the current CUDA stream, and status codes ->
-exceptions. There is no fallback: if the library is missing, every call
-raises.
+exceptions. Before a call it checks what the library cannot see (that every
+tensor is a CUDA tensor on one device, and the dtypes, layouts and sizes of
+the buffers the call reads and writes) and raises MlaError with
+MLA_ERR_INVALID_ARG otherwise. There is no fallback: if the library is
+missing, every call raises.
 
 Entry points mirror ``include/mla.h``:
   mla_cache_write, mla_decode_workspace_bytes, mla_decode, mla_decode_varlen,
@@ -36,9 +39,9 @@ _lib = None
 
 
 class MlaError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{where}: {mla_status_string(status)} ({status})")
+        super().__init__(f"{where}: {mla_status_string(status)} ({status})" + (f": {detail}" if detail else ""))
 
 
 def load() -> ctypes.CDLL:
@@ -105,6 +108,79 @@ def _check(status: int, where: str) -> None:
         raise MlaError(status, where)
 
 
+# Argument checks of the binding. The library validates sizes, pointers and
+# alignment on the host, but it cannot tell a host pointer from a device one
+# or how large a caller's buffer is: a host tensor handed to a kernel is an
+# illegal address (or, where the GPU reaches host memory, a silent slow
+# path), and an output smaller than the call writes is overrun. These checks
+# run before the library is called and raise MlaError(MLA_ERR_INVALID_ARG).
+
+def _is_cuda(t) -> bool:
+    return isinstance(t, torch.Tensor) and t.is_cuda
+
+
+def _need(ok: bool, where: str, detail: str) -> None:
+    if not ok:
+        raise MlaError(MLA_ERR_INVALID_ARG, where, detail)
+
+
+def _on_device(where: str, **tensors) -> None:
+    """Every tensor passed as a device pointer is a CUDA tensor, all on one device."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        _need(_is_cuda(t), where, f"{name} must be a CUDA tensor")
+        if dev is None:
+            dev = t.device
+        _need(t.device == dev, where, f"{name} is on {t.device}, the other arguments on {dev}")
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _decode_args(where, q_lat, q_pe, cache, block_table, seq_lens, out, lse, workspace, rows, width):
+    """Checks shared by the decode entry points: `rows` query rows of `width`
+    latent values (query tokens x heads)."""
+    _on_device(where, q_lat=q_lat, q_pe=q_pe, cache=cache, block_table=block_table, seq_lens=seq_lens, out=out,
+               lse=lse, workspace=workspace)
+    _need(q_lat.dtype == torch.bfloat16 and q_pe.dtype == torch.bfloat16, where, "q_lat and q_pe must be bf16")
+    _need(q_lat.is_contiguous() and q_pe.is_contiguous(), where, "q_lat and q_pe must be contiguous")
+    _need(q_lat.numel() == rows * width and q_pe.numel() == rows * 64, where,
+          f"q_lat / q_pe hold {q_lat.numel()} / {q_pe.numel()} values, {rows} rows of {width} / 64 expected")
+    _need(out.dtype in (torch.bfloat16, torch.float32) and out.is_contiguous(), where,
+          "out must be a contiguous bf16 or fp32 tensor")
+    _need(out.numel() >= rows * width, where, f"out holds {out.numel()} values, the call writes {rows * width}")
+    _need(lse.dtype == torch.float32 and lse.is_contiguous() and lse.numel() >= rows, where,
+          f"lse must be a contiguous fp32 tensor of at least {rows} values")
+    _need(cache.is_contiguous(), where, "cache must be contiguous")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.stride(1) == 1, where,
+          "block_table must be a 2-D int32 tensor with contiguous rows")
+    B = seq_lens.numel()
+    _need(block_table.shape[0] >= B, where, f"block_table has {block_table.shape[0]} rows for {B} requests")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.is_contiguous(), where, "seq_lens must be contiguous int32")
+    if workspace is not None:
+        _need(workspace.is_contiguous(), where, "workspace must be contiguous")
+
+
+def _write_args(where, latent, k_pe, slot_mapping, cache, status, width):
+    """Checks shared by the cache writes: rows of `width` latent values."""
+    _on_device(where, latent=latent, k_pe=k_pe, slot_mapping=slot_mapping, cache=cache, status=status)
+    _need(latent.dtype == torch.bfloat16 and k_pe.dtype == torch.bfloat16, where, "latent and k_pe must be bf16")
+    _need(latent.dim() in (1, 2) and k_pe.dim() in (1, 2) and latent.shape[-1] == width and k_pe.shape[-1] == 64,
+          where, f"latent must be [T, {width}] and k_pe [T, 64]")
+    _need(latent.stride(-1) == 1 and k_pe.stride(-1) == 1, where, "latent and k_pe rows must be contiguous")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(), where,
+          "slot_mapping must be contiguous int64")
+    T = slot_mapping.numel()
+    rows = lambda t: t.shape[0] if t.dim() == 2 else 1
+    _need(rows(latent) >= T and rows(k_pe) >= T, where, f"latent / k_pe have fewer than the {T} rows slot_mapping names")
+    _need(cache.is_contiguous(), where, "cache must be contiguous")
+    _need(status is None or (status.dtype == torch.int32 and status.numel() >= 1), where,
+          "status must be an int32 tensor")
+
+
 def mla_status_string(status: int) -> str:
     try:
         return load().mla_status_string(status).decode()
@@ -127,12 +203,11 @@ def mla_cache_write(latent: torch.Tensor, k_pe: torch.Tensor, slot_mapping: torc
     viewable as bytes). Scatters rows in place; slots >= num_slots are skipped
     and, when `status` (a device int32 tensor) is given, OR bit 2 into its
     first element."""
-    assert latent.dtype == torch.bfloat16 and k_pe.dtype == torch.bfloat16
-    assert latent.stride(-1) == 1 and k_pe.stride(-1) == 1 and slot_mapping.dtype == torch.int64
-    assert status is None or status.dtype == torch.int32
+    _write_args("mla_cache_write", latent, k_pe, slot_mapping, cache, status, 512)
     T = slot_mapping.numel()
     nbytes = cache.numel() * cache.element_size()
     rb = mla_row_bytes(cache_kind)
+    _need(rb > 0, "mla_cache_write", f"unknown cache kind {cache_kind}")
     _check(load().mla_cache_write(latent.data_ptr(), latent.stride(0) if latent.dim() == 2 else 512,
                                   k_pe.data_ptr(), k_pe.stride(0) if k_pe.dim() == 2 else 64,
                                   slot_mapping.data_ptr(), T, cache.data_ptr(), nbytes // rb, cache_kind,
@@ -144,31 +219,43 @@ def mla_decode_varlen(q_lat, q_pe, cache, cache_kind, page_size, block_table, se
                       scale, out, lse, workspace, num_ctas: int = 0, stream=None) -> None:
     """Decode with per-request verify lengths (include/mla.h): q_lat [total_q, Hq, 512],
     cu_q_lens int32 [B+1] on the device."""
+    where = "mla_decode_varlen"
+    _need(isinstance(q_lat, torch.Tensor) and q_lat.dim() == 3, where, "q_lat must be [total_q, Hq, 512]")
     total_q, Hq = q_lat.shape[0], q_lat.shape[1]
-    assert q_lat.shape == (total_q, Hq, 512) and q_pe.shape == (total_q, Hq, 64)
-    assert q_lat.is_contiguous() and q_pe.is_contiguous() and out.is_contiguous() and lse.is_contiguous()
-    assert cu_q_lens.dtype == torch.int32 and cu_q_lens.is_contiguous()
-    assert block_table.dtype == torch.int32 and block_table.stride(1) == 1 and seq_lens.dtype == torch.int32
-    B = seq_lens.shape[0]
-    assert cu_q_lens.shape[0] == B + 1
+    _need(q_lat.shape == (total_q, Hq, 512) and tuple(q_pe.shape) == (total_q, Hq, 64), where,
+          "q_lat must be [total_q, Hq, 512] and q_pe [total_q, Hq, 64]")
+    _decode_args(where, q_lat, q_pe, cache, block_table, seq_lens, out, lse, workspace, total_q * Hq, 512)
+    _on_device(where, q_lat=q_lat, cu_q_lens=cu_q_lens)
+    B = seq_lens.numel()
+    _need(cu_q_lens.dtype == torch.int32 and cu_q_lens.is_contiguous() and cu_q_lens.numel() == B + 1, where,
+          f"cu_q_lens must be contiguous int32 with {B + 1} entries")
+    rb = mla_row_bytes(cache_kind)
+    _need(rb > 0, where, f"unknown cache kind {cache_kind}")
     odt = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
     st = load().mla_decode_varlen(q_lat.data_ptr(), q_pe.data_ptr(), total_q, cache.data_ptr(), int(cache_kind),
-                                  cache.shape[0], int(page_size), block_table.data_ptr(), block_table.stride(0),
-                                  seq_lens.data_ptr(), cu_q_lens.data_ptr(), B, int(max_q_len), Hq, float(scale),
-                                  out.data_ptr(), odt, lse.data_ptr(), workspace.data_ptr(), workspace.numel(),
-                                  int(num_ctas), _stream(stream))
+                                  _nbytes(cache) // rb, int(page_size), block_table.data_ptr(),
+                                  block_table.stride(0), seq_lens.data_ptr(), cu_q_lens.data_ptr(), B,
+                                  int(max_q_len), Hq, float(scale), out.data_ptr(), odt, lse.data_ptr(),
+                                  workspace.data_ptr(), _nbytes(workspace), int(num_ctas), _stream(stream))
     _check(st, "mla_decode_varlen")
 
 
 def mla_gather_upconvert(cache: torch.Tensor, page_size: int, block_table: torch.Tensor, cu_seq_lens: torch.Tensor,
                          dst: torch.Tensor, num_rows: int = None, stream=None) -> None:
     """Context gather of an fp8_ds_mla pool into bf16 rows (include/mla.h)."""
-    assert cache.dtype == torch.uint8 and cache.dim() == 2 and cache.shape[1] == 656 and cache.is_contiguous()
-    assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.stride(1) == 1
-    assert cu_seq_lens.dtype == torch.int32 and cu_seq_lens.is_contiguous()
-    assert dst.dtype == torch.bfloat16 and dst.dim() == 2 and dst.stride(1) == 1
+    where = "mla_gather_upconvert"
+    _on_device(where, cache=cache, block_table=block_table, cu_seq_lens=cu_seq_lens, dst=dst)
+    _need(cache.dtype == torch.uint8 and cache.dim() == 2 and cache.shape[1] == 656 and cache.is_contiguous(), where,
+          "cache must be a contiguous uint8 [num_slots, 656] tensor")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.stride(1) == 1, where,
+          "block_table must be a 2-D int32 tensor with contiguous rows")
+    _need(cu_seq_lens.dtype == torch.int32 and cu_seq_lens.is_contiguous() and cu_seq_lens.numel() >= 1, where,
+          "cu_seq_lens must be contiguous int32 with B + 1 entries")
+    _need(block_table.shape[0] >= cu_seq_lens.numel() - 1, where, "block_table has fewer rows than requests")
+    _need(dst.dtype == torch.bfloat16 and dst.dim() == 2 and dst.stride(1) == 1 and dst.shape[1] >= 576, where,
+          "dst must be a bf16 [rows, >= 576] tensor with contiguous rows")
     rows = dst.shape[0] if num_rows is None else int(num_rows)
-    assert rows <= dst.shape[0]
+    _need(0 <= rows <= dst.shape[0], where, f"num_rows {rows} outside [0, {dst.shape[0]}]")
     st = load().mla_gather_upconvert(cache.data_ptr(), cache.shape[0], int(page_size), block_table.data_ptr(),
                                      block_table.stride(0), cu_seq_lens.data_ptr(), cu_seq_lens.shape[0] - 1, rows,
                                      dst.data_ptr(), dst.stride(0), _stream(stream))
@@ -179,10 +266,8 @@ def mla_cache_write_latent(latent, k_pe, slot_mapping, cache, lat_dim, stream=No
     """bf16 rows [latent lat_dim | rope 64] (include/mla.h): latent
     [T, lat_dim] bf16, k_pe [T, 64] bf16, slot_mapping [T] int64, cache
     [num_slots, 2 (lat_dim + 64)] bytes."""
+    _write_args("mla_cache_write_latent", latent, k_pe, slot_mapping, cache, status, int(lat_dim))
     T = slot_mapping.numel()
-    assert latent.dtype == torch.bfloat16 and k_pe.dtype == torch.bfloat16 and slot_mapping.dtype == torch.int64
-    assert latent.stride(-1) == 1 and k_pe.stride(-1) == 1
-    assert status is None or status.dtype == torch.int32
     row_bytes = 2 * (lat_dim + 64)
     nbytes = cache.numel() * cache.element_size()
     _check(load().mla_cache_write_latent(latent.data_ptr(), latent.stride(0), k_pe.data_ptr(), k_pe.stride(0),
@@ -204,9 +289,11 @@ def mla_decode_latent(q_lat, q_pe, cache, lat_dim, page_size, block_table, seq_l
     q_lat [B*q_len, Hq, lat_dim], out [B*q_len, Hq, lat_dim]."""
     B = seq_lens.numel()
     Hq = q_lat.shape[-2]
-    assert q_lat.shape[-1] == lat_dim and q_pe.shape[-1] == 64 and out.shape[-1] == lat_dim
-    assert q_lat.is_contiguous() and q_pe.is_contiguous() and out.is_contiguous() and lse.is_contiguous()
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1 and seq_lens.dtype == torch.int32
+    where = "mla_decode_latent"
+    _need(q_lat.shape[-1] == lat_dim and q_pe.shape[-1] == 64 and out.shape[-1] == lat_dim, where,
+          f"q_lat and out must end in {lat_dim} values, q_pe in 64")
+    _decode_args(where, q_lat, q_pe, cache, block_table, seq_lens, out, lse, workspace, B * int(q_len) * Hq,
+                 int(lat_dim))
     out_dtype = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
     row_bytes = 2 * (lat_dim + 64)
     nbytes = cache.numel() * cache.element_size()
@@ -230,11 +317,12 @@ def mla_decode(q_lat, q_pe, cache, cache_kind, page_size, block_table, seq_lens,
     """Raw entry point: every buffer is caller-allocated (see include/mla.h)."""
     B = seq_lens.numel()
     Hq = q_lat.shape[-2]
-    assert q_lat.is_contiguous() and q_pe.is_contiguous() and block_table.dtype == torch.int32
-    assert seq_lens.dtype == torch.int32 and lse.dtype == torch.float32
+    _decode_args("mla_decode", q_lat, q_pe, cache, block_table, seq_lens, out, lse, workspace, B * int(q_len) * Hq,
+                 512)
     out_dtype = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
     nbytes = cache.numel() * cache.element_size()
     rb = mla_row_bytes(cache_kind)
+    _need(rb > 0, "mla_decode", f"unknown cache kind {cache_kind}")
     _check(load().mla_decode(q_lat.data_ptr(), q_pe.data_ptr(), cache.data_ptr(), cache_kind, nbytes // rb,
                              page_size, block_table.data_ptr(), block_table.stride(0), seq_lens.data_ptr(), B, q_len,
                              Hq, float(scale), out.data_ptr(), out_dtype, lse.data_ptr(), workspace.data_ptr(),
@@ -249,11 +337,12 @@ def mla_decode_static_scratch(q_lat, q_pe, cache, cache_kind, page_size, block_t
     device must be ordered on one stream)."""
     B = seq_lens.numel()
     Hq = q_lat.shape[-2]
-    assert q_lat.is_contiguous() and q_pe.is_contiguous() and block_table.dtype == torch.int32
-    assert seq_lens.dtype == torch.int32 and lse.dtype == torch.float32
+    _decode_args("mla_decode_static_scratch", q_lat, q_pe, cache, block_table, seq_lens, out, lse, None,
+                 B * int(q_len) * Hq, 512)
     out_dtype = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
     nbytes = cache.numel() * cache.element_size()
     rb = mla_row_bytes(cache_kind)
+    _need(rb > 0, "mla_decode_static_scratch", f"unknown cache kind {cache_kind}")
     _check(load().mla_decode_static_scratch(q_lat.data_ptr(), q_pe.data_ptr(), cache.data_ptr(), cache_kind,
                                             nbytes // rb, page_size, block_table.data_ptr(), block_table.stride(0),
                                             seq_lens.data_ptr(), B, q_len, Hq, float(scale), out.data_ptr(),
@@ -273,8 +362,17 @@ def static_scratch_status_words(n: int = 12, stream=None) -> list:
 
 def mla_merge_lse(part_out: torch.Tensor, part_lse: torch.Tensor, out: torch.Tensor, lse=None, stream=None) -> None:
     """part_out [S,N,512] fp32, part_lse [S,N] fp32 -> out [N,512] (bf16/fp32), lse [N]."""
+    where = "mla_merge_lse"
+    _on_device(where, part_out=part_out, part_lse=part_lse, out=out, lse=lse)
+    _need(part_lse.dim() == 2, where, "part_lse must be [S, N]")
     S, N = part_lse.shape
-    assert part_out.is_contiguous() and part_lse.is_contiguous() and part_out.dtype == torch.float32
+    _need(part_out.dtype == torch.float32 and part_lse.dtype == torch.float32, where, "partials must be fp32")
+    _need(part_out.is_contiguous() and part_lse.is_contiguous() and part_out.numel() == S * N * 512, where,
+          f"part_out must be a contiguous [{S}, {N}, 512] tensor")
+    _need(out.dtype in (torch.bfloat16, torch.float32) and out.is_contiguous() and out.numel() >= N * 512, where,
+          f"out must be a contiguous bf16 or fp32 tensor of at least {N} x 512 values")
+    _need(lse is None or (lse.dtype == torch.float32 and lse.is_contiguous() and lse.numel() >= N), where,
+          f"lse must be a contiguous fp32 tensor of at least {N} values")
     out_dtype = MLA_OUT_F32 if out.dtype == torch.float32 else MLA_OUT_BF16
     _check(load().mla_merge_lse(part_out.data_ptr(), part_lse.data_ptr(), S, N, out.data_ptr(), out_dtype,
                                 lse.data_ptr() if lse is not None else None, _stream(stream)), "mla_merge_lse")
