@@ -95,3 +95,18 @@ def test_queries_with_nothing_visible_are_zero_and_minus_inf():
                                 np.array(seq_lens, dtype=np.int32), cu, Hq, 0.1)
     assert np.all(o[0:2] == 0) and np.all(l[0:2] == -np.inf)
     assert np.all(np.isfinite(l[2:]))
+
+
+def test_a_request_that_verifies_no_token_adds_no_rows():
+    # the verify step of request 1 is empty (cu_q_lens repeats a value): the
+    # other requests' rows are those of a batch without it
+    seq_lens, q_lens, Hq, ps = [30, 50, 17], [2, 0, 3], 2, 8
+    pool, _, bt, q, cu = _tiny(5, seq_lens, q_lens, Hq, ps)
+    ql, qp = q[:, :, :D].contiguous(), q[:, :, D:].contiguous()
+    sl = np.array(seq_lens, dtype=np.int32)
+    o, l = oracle.decode_varlen(ql, qp, pool, 0, ps, bt, sl, cu, Hq, 0.08)
+    assert o.shape[0] == 5 and l.shape[0] == 5
+    keep = [0, 2]
+    cu2 = np.array([0, 2, 5], dtype=np.int32)
+    o2, l2 = oracle.decode_varlen(ql, qp, pool, 0, ps, bt[keep], sl[keep], cu2, Hq, 0.08)
+    assert np.array_equal(o, o2) and np.array_equal(l, l2)
